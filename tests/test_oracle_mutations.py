@@ -1,0 +1,108 @@
+"""Plant plausible mistakes in a copy of the C oracle and check the pins catch every one (CPU).
+
+Each mutant is compiled from a modified copy of oracle/gdr_oracle.c into a temporary library and
+swapped in for the real one while the pin tests of test_oracle_pins.py run against it.  A mutant
+that passes every pin would mean the pins cannot tell that mistake from the method.
+"""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "gdr_oracle.c")
+
+PIN_TESTS = [
+    pins.test_interference_read_em02e,
+    pins.test_delta_overwrite_em03d,
+    pins.test_two_token_chunk_em04e,
+    lambda: pins.test_decay_survival_em05d(True),
+    lambda: pins.test_decay_survival_em05d(False),
+    pins.test_hand_2x2_steps,
+    pins.test_linear_attention_is_masked_qk_v,
+    pins.test_gdn_matrix_form,
+    pins.test_alpha_zero_resets_memory,
+    pins.test_beta_zero_is_pure_decay,
+    pins.test_read_back_after_write,
+    pins.test_orthonormal_keys_store_last_value,
+]
+
+
+def _block(src, start, end):
+    i, j = src.index(start), src.index(end)
+    return src[i:j]
+
+
+def _swap_fade_and_read(src):
+    fade = _block(src, "/* 1. fade", "/* 2. read")
+    read = _block(src, "/* 2. read", "/* 3. write")
+    return src.replace(fade + read, read + fade)
+
+
+def _fade_after_write(src):
+    fade = _block(src, "/* 1. fade", "/* 2. read")
+    write_end = src.index("    }\n    /* 4. read-out")
+    src2 = src[:write_end] + fade + src[write_end:]
+    return src2.replace(fade, "", 1)
+
+
+MUTANTS = {
+    "read the unfaded state": _swap_fade_and_read,
+    "erase before fade": _fade_after_write,
+    "dropped beta": lambda s: s.replace("vhat[j] = bt * (vt[j] - vhat[j])",
+                                        "vhat[j] = (vt[j] - vhat[j])"),
+    "wrong sign of the correction": lambda s: s.replace("bt * (vt[j] - vhat[j])",
+                                                        "bt * (vt[j] + vhat[j])"),
+    "gate on the wrong channel": lambda s: s.replace("Si[j] *= at[i]", "Si[j] *= at[dk - 1 - i]"),
+    "scalar gate ignored": lambda s: s.replace("S[e] *= at;", "S[e] *= 1.0;"),
+    "read-out with the key": lambda s: s.replace("ot[j] += Si[j] * qt[i]",
+                                                 "ot[j] += Si[j] * kt[i]"),
+    "transposed key read": lambda s: s.replace("vhat[j] += Si[j] * kt[i]",
+                                               "vhat[j] += Si[j] * kt[j % dk]"),
+    "transposed linear write": lambda s: s.replace("Si[j] += kt[i] * vt[j]",
+                                                   "Si[j] += kt[j % dk] * vt[i % dv]"),
+    "output before the write": lambda s: s.replace(
+        "    /* 4. read-out", "    /* 4. read-out").replace(
+        "if (J->mode == ORACLE_LINEAR) {\n      /* S <- S + k v^T */",
+        "for (int j = 0; j < dv; ++j) ot[j] = 0.0;\n    for (int i = 0; i < dk; ++i)"
+        " for (int j = 0; j < dv; ++j) ot[j] += S[(size_t)i * dv + j] * qt[i];\n"
+        "    if (J->mode == ORACLE_LINEAR) {\n      /* S <- S + k v^T */").replace(
+        "    /* 4. read-out of the updated state: o = S^T q */\n"
+        "    for (int j = 0; j < dv; ++j) ot[j] = 0.0;",
+        "    /* 4. (mutant: output already read) */\n    if (0)"),
+}
+
+
+@pytest.fixture(scope="module")
+def original_source():
+    with open(SRC) as f:
+        return f.read()
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, original_source, tmp_path):
+    src = MUTANTS[name](original_source)
+    assert src != original_source, "mutation did not apply"
+    c = tmp_path / "mutant.c"
+    so = tmp_path / "libmutant.so"
+    c.write_text(src)
+    subprocess.check_call(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-pthread", "-o",
+                           str(so), str(c)])
+    real = oracle._load()
+    lib = ctypes.CDLL(str(so))
+    lib.gdr_oracle_run.argtypes = real.gdr_oracle_run.argtypes
+    lib.gdr_oracle_run.restype = ctypes.c_int
+    caught = []
+    oracle._lib = lib
+    try:
+        for t in PIN_TESTS:
+            try:
+                t()
+            except AssertionError:
+                caught.append(getattr(t, "__name__", "lambda"))
+    finally:
+        oracle._lib = real
+    assert caught, "no pin caught the mutant '%s'" % name

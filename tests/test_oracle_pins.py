@@ -1,0 +1,345 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix (no GPU).
+
+Each test ties the oracle to something other than itself: a value printed on a page (fixtures
+under tests/golden/, each with its source), a closed form, a textbook routine it reduces to, an
+invariant stated on a page, or brute force.  test_oracle_mutations.py then plants plausible
+mistakes in a copy of the oracle and checks that these pins catch them.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import chunked
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def one_head(*arrs):
+    """[L, d] per-head arrays -> token-major [L, 1, d] (or [L] -> [L, 1])."""
+    return [np.asarray(a, dtype=np.float64)[:, None] for a in arrs]
+
+
+def rand_inputs(rng, T, H, dk, dv, channel=True, unit_k=True):
+    q = rng.standard_normal((T, H, dk))
+    k = rng.standard_normal((T, H, dk))
+    if unit_k:
+        k /= np.linalg.norm(k, axis=-1, keepdims=True)
+        q /= np.linalg.norm(q, axis=-1, keepdims=True)
+    v = rng.standard_normal((T, H, dv))
+    alpha = rng.uniform(0.3, 1.0, (T, H, dk) if channel else (T, H))
+    beta = rng.uniform(0.0, 1.0, (T, H))
+    return q, k, v, alpha, beta
+
+
+# ------------------------------------------------------------------------------------------
+# values printed on the pages
+# ------------------------------------------------------------------------------------------
+def test_interference_read_em02e():
+    g = golden("em_02e_interference_read.json")
+    k = np.array(g["k"], float)
+    v = np.array(g["v"], float)
+    q = np.stack([g["q_read"], g["q_read"]]).astype(float)
+    out, S = oracle.linear_attn(*one_head(q, k, v))
+    np.testing.assert_allclose(out[1, 0], g["expected_read"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(S[0, 0, 1], g["expected_row1"], rtol=0, atol=1e-12)
+    # the error is exactly the interference law's crosstalk (k_cat . k_dog) v_rex
+    np.testing.assert_allclose(out[1, 0] - v[0], (k[0] @ k[1]) * v[1], atol=1e-12)
+
+
+def test_delta_overwrite_em03d():
+    g = golden("em_03d_delta_overwrite.json")
+    S0 = np.zeros((1, 1, 4, 4))
+    S0[0, 0, 0] = g["row0_before"]
+    S0[0, 0, 2] = [0.0, 0.0, 3.0, 1.0]  # another fact on a row the key does not touch
+    S0[0, 0, 3] = [0.5, -1.0, 0.0, 2.0]
+    k = np.array([g["k"]], float)
+    v = np.array([g["v"]], float)
+    a = np.ones((1, 4))
+    b = np.array([g["beta"]])
+    out, S = oracle.gated_delta(*one_head(k, k, v, a, b), S0=S0)
+    np.testing.assert_allclose(S[0, 0, 0], g["expected_row0_after"], atol=1e-12)
+    np.testing.assert_allclose(S[0, 0, 0] - S0[0, 0, 0], g["expected_u"], atol=1e-12)
+    np.testing.assert_allclose(S[0, 0, 1:], S0[0, 0, 1:], atol=0)
+    np.testing.assert_allclose(out[0, 0], g["v"], atol=1e-12)  # read-back is exact
+
+
+def test_two_token_chunk_em04e():
+    g = golden("em_04e_two_token_chunk.json")
+    k = np.array(g["k"], float)
+    v = np.array(g["v"], float)
+    b = np.array(g["beta"], float)
+    a = np.ones((2, 4))
+    for qrow, key in ((k[1], "derived_read_k2"), (k[0], "derived_read_k1")):
+        q = np.stack([k[0], qrow])
+        out, S = oracle.gated_delta(*one_head(q, k, v, a, b))
+        np.testing.assert_allclose(out[1, 0], g[key], atol=1e-12)
+    # S2 = k1 u1^T + k2 u2^T with the printed corrections
+    expect = np.outer(k[0], g["expected_u1"]) + np.outer(k[1], g["expected_u2"])
+    np.testing.assert_allclose(S[0, 0], expect, atol=1e-12)
+    # and the chunked (triangular solve) form reproduces the printed u2
+    _, _, Us = chunked.gated_delta_seq(k, k, v, a, b, np.zeros((4, 4)), C=2)
+    np.testing.assert_allclose(Us[0][0], g["expected_u1"], atol=1e-12)
+    np.testing.assert_allclose(Us[0][1], g["expected_u2"], atol=1e-12)
+
+
+@pytest.mark.parametrize("channel", [True, False])
+def test_decay_survival_em05d(channel):
+    g = golden("em_05d_decay_survival.json")
+    d = 4
+    L = g["write_step"] + len(g["gates_after_write"])
+    rng = np.random.default_rng(0)
+    k = np.zeros((L, d))
+    q = np.zeros((L, d))
+    v = rng.standard_normal((L, d))
+    k[g["write_step"] - 1, 0] = 1.0
+    q[-1, 0] = 1.0
+    b = np.zeros(L)
+    b[g["write_step"] - 1] = 1.0
+    gates = np.ones(L)
+    gates[g["write_step"]:] = g["gates_after_write"]
+    if channel:
+        a = np.ones((L, d))
+        a[:, 0] = gates  # only channel 0 carries the fact
+        a[:, 1:] = 0.3
+    else:
+        a = gates
+    out, _ = oracle.gated_delta(*one_head(q, k, v, a, b))
+    np.testing.assert_allclose(out[-1, 0], g["expected_strength"] * v[g["write_step"] - 1],
+                               atol=1e-12)
+
+
+def test_hand_2x2_steps():
+    g = golden("hand_2x2_steps.json")
+    for c in g["cases"]:
+        S0 = np.array(c["S0"], float)[None, None]
+        k = np.array([c["k"]], float)
+        q = np.array([c["q"]], float)
+        v = np.array([c["v"]], float)
+        a = np.array([c["alpha"]], float) if np.ndim(c["alpha"]) else np.array([c["alpha"]])
+        b = np.array([c["beta"]], float)
+        out, S = oracle.gated_delta(*one_head(q, k, v, a, b), S0=S0)
+        np.testing.assert_allclose(S[0, 0], c["expected_S1"], atol=1e-12)
+        np.testing.assert_allclose(out[0, 0], c["expected_o"], atol=1e-12)
+        # the read of the faded state that the correction was computed from
+        np.testing.assert_allclose(S[0, 0].T @ k[0], (1 - c["beta"]) * np.array(c["v_hat"])
+                                   + c["beta"] * np.array(c["v"]), atol=1e-12)
+
+
+# ------------------------------------------------------------------------------------------
+# closed forms and textbook reductions
+# ------------------------------------------------------------------------------------------
+def test_linear_attention_is_masked_qk_v():
+    """alpha = 1 and no erase: O = tril(Q K^T) V (+ Q S0) per sequence, by brute force."""
+    rng = np.random.default_rng(1)
+    lens = [1, 17, 0, 40]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    T, H, dk, dv = cu[-1], 3, 8, 5
+    q, k, v, _, _ = rand_inputs(rng, T, H, dk, dv, unit_k=False)
+    S0 = rng.standard_normal((len(lens), H, dk, dv))
+    out, Sf = oracle.linear_attn(q, k, v, S0=S0, cu_seqlens=cu)
+    for n in range(len(lens)):
+        t0, t1 = cu[n], cu[n + 1]
+        for h in range(H):
+            Q, K, V = q[t0:t1, h], k[t0:t1, h], v[t0:t1, h]
+            ref = np.tril(Q @ K.T) @ V + Q @ S0[n, h]
+            np.testing.assert_allclose(out[t0:t1, h], ref, atol=1e-10)
+            np.testing.assert_allclose(Sf[n, h], S0[n, h] + K.T @ V, atol=1e-10)
+
+
+def test_gdn_matrix_form():
+    """Scalar gate: S_t = alpha (I - beta k k^T) S_{t-1} + beta k v^T (Gated DeltaNet form)."""
+    rng = np.random.default_rng(2)
+    T, dk, dv = 9, 6, 4
+    q, k, v, a, b = rand_inputs(rng, T, 1, dk, dv, channel=False)
+    S0 = rng.standard_normal((1, 1, dk, dv))
+    out, Sf = oracle.gated_delta(q, k, v, a, b, S0=S0)
+    S = S0[0, 0].copy()
+    for t in range(T):
+        kt = k[t, 0]
+        S = a[t, 0] * (np.eye(dk) - b[t, 0] * np.outer(kt, kt)) @ S + b[t, 0] * np.outer(kt, v[t, 0])
+        np.testing.assert_allclose(out[t, 0], S.T @ q[t, 0], atol=1e-12)
+    np.testing.assert_allclose(Sf[0, 0], S, atol=1e-12)
+
+
+def test_scalar_gate_equals_uniform_channel_gate():
+    rng = np.random.default_rng(3)
+    q, k, v, a, b = rand_inputs(rng, 20, 2, 8, 8, channel=False)
+    S0 = rng.standard_normal((1, 2, 8, 8))
+    o1, s1 = oracle.gated_delta(q, k, v, a, b, S0=S0)
+    o2, s2 = oracle.gated_delta(q, k, v, np.repeat(a[:, :, None], 8, axis=2), b, S0=S0)
+    np.testing.assert_allclose(o1, o2, atol=1e-13)
+    np.testing.assert_allclose(s1, s2, atol=1e-13)
+
+
+def test_alpha_zero_resets_memory():
+    """alpha = 0: amnesia, the new state is exactly beta k v^T whatever came before."""
+    rng = np.random.default_rng(4)
+    q, k, v, a, b = rand_inputs(rng, 1, 1, 8, 6)
+    S0 = rng.standard_normal((1, 1, 8, 6))
+    _, Sf = oracle.gated_delta(q, k, v, np.zeros_like(a), b, S0=S0)
+    np.testing.assert_allclose(Sf[0, 0], b[0, 0] * np.outer(k[0, 0], v[0, 0]), atol=1e-14)
+
+
+def test_beta_zero_is_pure_decay():
+    """beta = 0: no write at all; S_t = Diag(prod alpha) S0 and o_t reads that state."""
+    rng = np.random.default_rng(5)
+    T, dk, dv = 12, 8, 5
+    q, k, v, a, _ = rand_inputs(rng, T, 1, dk, dv)
+    S0 = rng.standard_normal((1, 1, dk, dv))
+    out, Sf = oracle.gated_delta(q, k, v, a, np.zeros((T, 1)), S0=S0)
+    P = np.cumprod(a[:, 0], axis=0)
+    for t in range(T):
+        np.testing.assert_allclose(out[t, 0], (P[t][:, None] * S0[0, 0]).T @ q[t, 0], atol=1e-12)
+    np.testing.assert_allclose(Sf[0, 0], P[-1][:, None] * S0[0, 0], atol=1e-12)
+
+
+def test_idle_gates_coast():
+    """alpha = 1, beta = 0: the memory coasts untouched."""
+    rng = np.random.default_rng(6)
+    q, k, v, a, _ = rand_inputs(rng, 7, 2, 4, 4)
+    S0 = rng.standard_normal((1, 2, 4, 4))
+    out, Sf = oracle.gated_delta(q, k, v, np.ones_like(a), np.zeros((7, 2)), S0=S0)
+    np.testing.assert_array_equal(Sf, S0)
+    np.testing.assert_allclose(out, np.einsum("thc,hcd->thd", q, S0[0]), atol=1e-12)
+
+
+def test_orthonormal_keys_store_last_value():
+    """Keys cycling through e_0..e_{d-1} with beta = alpha = 1: row c = last value at key c."""
+    rng = np.random.default_rng(7)
+    d, T = 6, 20
+    k = np.zeros((T, 1, d))
+    for t in range(T):
+        k[t, 0, t % d] = 1.0
+    v = rng.standard_normal((T, 1, d))
+    q = rng.standard_normal((T, 1, d))
+    S0 = rng.standard_normal((1, 1, d, d))
+    _, Sf = oracle.gated_delta(q, k, v, np.ones((T, 1, d)), np.ones((T, 1)), S0=S0)
+    for c in range(d):
+        last = max(t for t in range(T) if t % d == c)
+        np.testing.assert_allclose(Sf[0, 0, c], v[last, 0], atol=1e-13)
+
+
+def test_deltanet_householder_geometry():
+    """alpha = 1, unit k: beta = 2 with v = 0 is a reflection (norm kept); beta = 1 with v = 0
+    projects the k-direction out (k^T S = 0)."""
+    rng = np.random.default_rng(8)
+    T, d = 10, 7
+    q, k, _, _, _ = rand_inputs(rng, T, 1, d, d)
+    S0 = rng.standard_normal((1, 1, d, d))
+    zero_v = np.zeros((T, 1, d))
+    ones = np.ones((T, 1, d))
+    _, Sf = oracle.gated_delta(q, k, zero_v, ones, 2 * np.ones((T, 1)), S0=S0)
+    assert abs(np.linalg.norm(Sf) - np.linalg.norm(S0)) < 1e-12
+    _, Sf = oracle.gated_delta(q[:1], k[:1], zero_v[:1], ones[:1], np.ones((1, 1)), S0=S0)
+    np.testing.assert_allclose(k[0, 0] @ Sf[0, 0], 0, atol=1e-13)
+
+
+# ------------------------------------------------------------------------------------------
+# invariants stated on the pages
+# ------------------------------------------------------------------------------------------
+def _prefix_states(q, k, v, a, b, S0):
+    """State before each token (the oracle's own S_final of each prefix)."""
+    T = q.shape[0]
+    states = [S0[0, 0]]
+    for t in range(1, T):
+        _, s = oracle.gated_delta(q[:t], k[:t], v[:t], a[:t], b[:t], S0=S0)
+        states.append(s[0, 0])
+    return states
+
+
+def test_read_back_after_write():
+    """Unit k: k_t^T S_t = (1 - beta) v_hat + beta v with v_hat the read of the faded state; the
+    SGD view: ||S_t^T k - v|| = (1 - beta) ||v_hat - v||.  beta = 1 returns v exactly."""
+    rng = np.random.default_rng(9)
+    T, dk, dv = 8, 6, 5
+    q, k, v, a, b = rand_inputs(rng, T, 1, dk, dv)
+    S0 = rng.standard_normal((1, 1, dk, dv))
+    out, _ = oracle.gated_delta(k, k, v, a, b, S0=S0)  # read-out with q = k
+    for t, S in enumerate(_prefix_states(k, k, v, a, b, S0)):
+        vhat = (a[t, 0][:, None] * S).T @ k[t, 0]
+        expect = (1 - b[t, 0]) * vhat + b[t, 0] * v[t, 0]
+        np.testing.assert_allclose(out[t, 0], expect, atol=1e-12)
+        np.testing.assert_allclose(np.linalg.norm(out[t, 0] - v[t, 0]),
+                                   (1 - b[t, 0]) * np.linalg.norm(vhat - v[t, 0]), atol=1e-12)
+    out1, _ = oracle.gated_delta(k, k, v, a, np.ones((T, 1)), S0=S0)
+    np.testing.assert_allclose(out1[:, 0], v[:, 0], atol=1e-12)
+
+
+def test_causality():
+    """Changing tokens after t leaves every output up to t unchanged."""
+    rng = np.random.default_rng(10)
+    q, k, v, a, b = rand_inputs(rng, 30, 2, 8, 8)
+    out, _ = oracle.gated_delta(q, k, v, a, b)
+    q2, k2, v2, a2, b2 = (x.copy() for x in (q, k, v, a, b))
+    t = 13
+    for x in (q2, k2, v2, a2, b2):
+        x[t + 1:] = rng.uniform(0.1, 0.9, x[t + 1:].shape)
+    out2, _ = oracle.gated_delta(q2, k2, v2, a2, b2)
+    np.testing.assert_array_equal(out[:t + 1], out2[:t + 1])
+    assert not np.allclose(out[t + 1:], out2[t + 1:])
+
+
+def test_continuation_and_varlen_and_decode():
+    """prefill(T1) -> S; prefill(T2, S0=S) == prefill(T1+T2); packed == per-sequence;
+    n decode steps == a prefill of n tokens; a (seq, head) subset == the full run."""
+    rng = np.random.default_rng(11)
+    H, dk, dv = 2, 8, 6
+    lens = [23, 5, 0, 31]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    q, k, v, a, b = rand_inputs(rng, cu[-1], H, dk, dv)
+    S0 = rng.standard_normal((len(lens), H, dk, dv))
+    out, Sf = oracle.gated_delta(q, k, v, a, b, S0=S0, cu_seqlens=cu)
+    for n in range(len(lens)):
+        t0, t1 = cu[n], cu[n + 1]
+        o1, s1 = oracle.gated_delta(q[t0:t1], k[t0:t1], v[t0:t1], a[t0:t1], b[t0:t1],
+                                    S0=S0[n:n + 1])
+        np.testing.assert_array_equal(out[t0:t1], o1)
+        np.testing.assert_array_equal(Sf[n], s1[0])
+    # continuation of sequence 0 split at token 9
+    t0, cut, t1 = cu[0], cu[0] + 9, cu[1]
+    oa, sa = oracle.gated_delta(q[t0:cut], k[t0:cut], v[t0:cut], a[t0:cut], b[t0:cut], S0=S0[:1])
+    ob, sb = oracle.gated_delta(q[cut:t1], k[cut:t1], v[cut:t1], a[cut:t1], b[cut:t1], S0=sa)
+    np.testing.assert_allclose(np.concatenate([oa, ob]), out[t0:t1], atol=1e-13)
+    np.testing.assert_allclose(sb[0], Sf[0], atol=1e-13)
+    # decode steps (sequence 3, all heads, token by token)
+    S = S0[3:4]
+    for t in range(cu[3], cu[4]):
+        o, S = oracle.decode_step(q[t:t + 1], k[t:t + 1], v[t:t + 1], a[t:t + 1], b[t:t + 1], S)
+        np.testing.assert_allclose(o[0], out[t], atol=1e-13)
+    np.testing.assert_allclose(S[0], Sf[3], atol=1e-13)
+    # subset of pairs
+    o_sub, s_sub = oracle.gated_delta(q, k, v, a, b, S0=S0, cu_seqlens=cu, pairs=[(3, 1), (0, 0)])
+    np.testing.assert_array_equal(o_sub[cu[3]:cu[4], 1], out[cu[3]:cu[4], 1])
+    np.testing.assert_array_equal(s_sub[0, 0], Sf[0, 0])
+    assert np.all(o_sub[cu[3]:cu[4], 0] == 0)
+
+
+# ------------------------------------------------------------------------------------------
+# the chunk algebra (derivation check), against the token loop
+# ------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("C", [1, 2, 3, 16, 64, 200])
+@pytest.mark.parametrize("channel", [True, False])
+def test_chunked_equals_recurrence(C, channel):
+    rng = np.random.default_rng(12 + C)
+    lens = [70, 1, 0, 45]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    H, dk, dv = 2, 8, 6
+    q, k, v, a, b = rand_inputs(rng, cu[-1], H, dk, dv, channel=channel)
+    a[5] = 0.0  # a full reset inside a chunk
+    S0 = rng.standard_normal((len(lens), H, dk, dv))
+    ref_o, ref_s = oracle.gated_delta(q, k, v, a, b, S0=S0, cu_seqlens=cu)
+    o, s = chunked.run_packed(q, k, v, a, b, S0, cu, C)
+    np.testing.assert_allclose(o, ref_o, atol=1e-10, rtol=1e-10)
+    np.testing.assert_allclose(s, ref_s, atol=1e-10, rtol=1e-10)
+    lo, ls = oracle.linear_attn(q, k, v, S0=S0, cu_seqlens=cu)
+    o, s = chunked.run_packed(q, k, v, None, None, S0, cu, C, linear=True)
+    np.testing.assert_allclose(o, lo, atol=1e-10, rtol=1e-10)
+    np.testing.assert_allclose(s, ls, atol=1e-10, rtol=1e-10)
