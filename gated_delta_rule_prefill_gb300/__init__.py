@@ -1,0 +1,151 @@
+"""gated_delta_rule_prefill_gb300 -- Python binding of libgdr (the gated delta rule on GB300).
+
+Same names as the C ABI (include/gdr.h); this layer only marshals torch CUDA tensors into
+pointers and sizes and raises on a non-zero status.  Every step of the computation runs in the
+library's CUDA kernels; there is no Python or CPU fallback.
+
+    gdr_prefill(q, k, v, alpha, beta, S0=None, cu_seqlens=None, out=None, S_final=None, ...)
+    gdr_decode_step(q, k, v, alpha, beta, S_inout, out=None)
+    gdr_linear_attn(q, k, v, S0=None, cu_seqlens=None, out=None, S_final=None, ...)
+    gdr_prefill_workspace_size(n_seqs)  /  gdr_workspace_status(workspace)
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _abi
+from ._abi import (GDR_BF16, GDR_F32, GDR_FLAG_FORCE_SIMT, GDR_GATE_CHANNEL, GDR_GATE_SCALAR,
+                   GdrError, GdrShape)
+
+__all__ = ["gdr_prefill", "gdr_decode_step", "gdr_linear_attn", "gdr_prefill_workspace_size",
+           "gdr_workspace_status", "make_shape", "GdrError"]
+
+_DT = {torch.float32: GDR_F32, torch.bfloat16: GDR_BF16}
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(t, name, dtype=None):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+
+
+def make_shape(n_seqs, H, total_tokens, d_k, d_v, dtype, gate=GDR_GATE_CHANNEL, chunk_size=0,
+               flags=0) -> GdrShape:
+    return GdrShape(n_seqs, H, total_tokens, d_k, d_v, dtype, gate, chunk_size, flags)
+
+
+def gdr_prefill_workspace_size(n_seqs: int) -> int:
+    sh = make_shape(n_seqs, 1, 0, 128, 128, GDR_BF16)
+    return int(_abi.load().gdr_prefill_workspace_size(ctypes.byref(sh)))
+
+
+def _workspace(n_seqs, device, workspace):
+    need = gdr_prefill_workspace_size(n_seqs)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    return workspace
+
+
+def _prefill_like(linear, q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, workspace,
+                  chunk_size, force_simt, stream, want_final):
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    dtype = _DT.get(q.dtype)
+    if dtype is None:
+        raise ValueError("q/k/v must be float32 or bfloat16")
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, q.dtype)
+    n_seqs = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    gate = GDR_GATE_CHANNEL
+    if not linear:
+        _check(alpha, "alpha", torch.float32)
+        _check(beta, "beta", torch.float32)
+        gate = GDR_GATE_CHANNEL if alpha.dim() == 3 else GDR_GATE_SCALAR
+    _check(S0, "S0", torch.float32)
+    _check(cu_seqlens, "cu_seqlens", torch.int32)
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=q.dtype, device=q.device)
+    _check(out, "out", q.dtype)
+    if S_final is None and want_final:
+        S_final = torch.empty((n_seqs, H, dk, dv), dtype=torch.float32, device=q.device)
+    _check(S_final, "S_final", torch.float32)
+    ws = _workspace(n_seqs, q.device, workspace)
+    sh = make_shape(n_seqs, H, T, dk, dv, dtype, gate, chunk_size,
+                    GDR_FLAG_FORCE_SIMT if force_simt else 0)
+    lib = _abi.load()
+    if linear:
+        rc = lib.gdr_linear_attn(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(S0),
+                                 _ptr(cu_seqlens), _ptr(out), _ptr(S_final), _ptr(ws),
+                                 ws.numel(), _stream(stream))
+    else:
+        rc = lib.gdr_prefill(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
+                             _ptr(beta), _ptr(S0), _ptr(cu_seqlens), _ptr(out), _ptr(S_final),
+                             _ptr(ws), ws.numel(), _stream(stream))
+    if rc != 0:
+        raise GdrError(rc, "gdr_linear_attn" if linear else "gdr_prefill")
+    return out, S_final
+
+
+def gdr_prefill(q, k, v, alpha, beta, S0=None, cu_seqlens=None, out=None, S_final=None,
+                workspace=None, chunk_size=0, force_simt=False, stream=None, want_final=True):
+    """Chunked packed-varlen prefill.  q,k [T,H,d_k], v [T,H,d_v] (fp32 or bf16); alpha
+    [T,H,d_k] or [T,H] fp32; beta [T,H] fp32; S0 [N,H,d_k,d_v] fp32 or None; cu_seqlens int32
+    [N+1] or None.  Returns (out [T,H,d_v], S_final [N,H,d_k,d_v] or None)."""
+    return _prefill_like(False, q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, workspace,
+                         chunk_size, force_simt, stream, want_final)
+
+
+def gdr_linear_attn(q, k, v, S0=None, cu_seqlens=None, out=None, S_final=None, workspace=None,
+                    chunk_size=0, force_simt=False, stream=None, want_final=True):
+    """Plain linear attention (alpha = 1, no erase).  Returns (out, S_final)."""
+    return _prefill_like(True, q, k, v, None, None, S0, cu_seqlens, out, S_final, workspace,
+                         chunk_size, force_simt, stream, want_final)
+
+
+def gdr_decode_step(q, k, v, alpha, beta, S_inout, out=None, stream=None):
+    """One token per sequence; S_inout [N,H,d_k,d_v] fp32 is updated in place.  Returns out."""
+    N, H, dk = q.shape
+    dv = v.shape[2]
+    dtype = _DT.get(q.dtype)
+    if dtype is None:
+        raise ValueError("q/k/v must be float32 or bfloat16")
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, q.dtype)
+    _check(alpha, "alpha", torch.float32)
+    _check(beta, "beta", torch.float32)
+    _check(S_inout, "S_inout", torch.float32)
+    if out is None:
+        out = torch.empty((N, H, dv), dtype=q.dtype, device=q.device)
+    _check(out, "out", q.dtype)
+    gate = GDR_GATE_CHANNEL if alpha.dim() == 3 else GDR_GATE_SCALAR
+    sh = make_shape(N, H, N, dk, dv, dtype, gate)
+    rc = _abi.load().gdr_decode_step(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
+                                     _ptr(beta), _ptr(S_inout), _ptr(out), _stream(stream))
+    if rc != 0:
+        raise GdrError(rc, "gdr_decode_step")
+    return out
+
+
+def gdr_workspace_status(workspace, stream=None) -> int:
+    """Synchronise and return (then clear) the device-check code of a workspace."""
+    code = ctypes.c_int32(0)
+    rc = _abi.load().gdr_workspace_status(_ptr(workspace), _stream(stream), ctypes.byref(code))
+    if rc != 0:
+        raise GdrError(rc, "gdr_workspace_status")
+    return int(code.value)

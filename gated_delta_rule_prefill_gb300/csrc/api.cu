@@ -1,0 +1,167 @@
+// api.cu -- the C ABI of libgdr (declared in include/gdr.h): argument validation, the sequence
+// pre-pass, kernel selection and launch on the caller's stream.
+#include <string.h>
+
+#include "gdr_internal.cuh"
+
+namespace gdr {
+namespace {
+
+constexpr int kPrepThreads = 1024;
+constexpr int kSortMax = 8192;  // longest-first ordering up to this many sequences
+
+// One CTA: clears the status word, checks cu_seqlens, and writes the visiting order of the
+// sequences (longest first, ties by index) so that long sequences start first.
+__global__ void __launch_bounds__(kPrepThreads)
+    prep_kernel(const int32_t* __restrict__ cu, int n_seqs, int64_t total, int32_t* order,
+                int32_t* status) {
+  __shared__ int32_t s_len[kSortMax];
+  __shared__ int s_bad;
+  if (threadIdx.x == 0) {
+    *status = 0;
+    s_bad = 0;
+  }
+  __syncthreads();
+  const bool sort = n_seqs <= kSortMax;
+  for (int i = threadIdx.x; i < n_seqs; i += blockDim.x) {
+    int64_t a = cu ? cu[i] : 0, b = cu ? cu[i + 1] : total;
+    int32_t len = (int32_t)(b - a);
+    if (a < 0 || b < a || b > total) {
+      s_bad = 1;
+      len = 0;
+    }
+    if (sort) s_len[i] = len;
+  }
+  __syncthreads();
+  if (s_bad && threadIdx.x == 0) atomicCAS(status, 0, GDR_DEVCHECK_SEQLENS);
+  for (int i = threadIdx.x; i < n_seqs; i += blockDim.x) {
+    if (!sort) {
+      order[i] = i;
+      continue;
+    }
+    const int32_t li = s_len[i];
+    int rank = 0;
+    for (int j = 0; j < n_seqs; ++j) {
+      const int32_t lj = s_len[j];
+      rank += (lj > li) || (lj == li && j < i);
+    }
+    order[rank] = i;
+  }
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+gdr_status check_shape(const gdr_shape* sh, bool need_gate) {
+  if (!sh) return GDR_ERR_INVALID_ARG;
+  if (sh->n_seqs < 1 || sh->H < 1 || sh->total_tokens < 0 || sh->d_k < 1 || sh->d_v < 1)
+    return GDR_ERR_INVALID_ARG;
+  if (sh->dtype != GDR_F32 && sh->dtype != GDR_BF16) return GDR_ERR_INVALID_ARG;
+  if (need_gate && sh->gate != GDR_GATE_SCALAR && sh->gate != GDR_GATE_CHANNEL)
+    return GDR_ERR_INVALID_ARG;
+  if (sh->chunk_size < 0 || (sh->flags & ~GDR_FLAG_FORCE_SIMT)) return GDR_ERR_INVALID_ARG;
+  if (sh->d_k != sh->d_v || (sh->d_k != 64 && sh->d_k != 128)) return GDR_ERR_UNSUPPORTED;
+  // grid sizes stay within 32-bit block counts
+  if ((int64_t)sh->n_seqs * sh->H * 4 > (int64_t)INT32_MAX) return GDR_ERR_UNSUPPORTED;
+  return GDR_OK;
+}
+
+gdr_status prefill_common(const gdr_shape* sh, const void* q, const void* k, const void* v,
+                          const float* alpha, const float* beta, const float* S0,
+                          const int32_t* cu, void* out, float* S_final, void* ws,
+                          size_t ws_bytes, void* stream, bool linear) {
+  gdr_status st = check_shape(sh, !linear);
+  if (st != GDR_OK) return st;
+  if (!cu && sh->n_seqs != 1) return GDR_ERR_INVALID_ARG;
+  if (sh->total_tokens > 0) {
+    if (!q || !k || !v || !out) return GDR_ERR_INVALID_ARG;
+    if (!linear && (!alpha || !beta)) return GDR_ERR_INVALID_ARG;
+  }
+  const void* ptrs[] = {q, k, v, alpha, beta, S0, cu, out, S_final};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return GDR_ERR_INVALID_ARG;
+  if (!ws || ((uintptr_t)ws & 255u) || ws_bytes < WorkspaceLayout::total(sh->n_seqs))
+    return GDR_ERR_INVALID_ARG;
+  if (out && (out == q || out == k || out == v)) return GDR_ERR_INVALID_ARG;
+  if (sh->chunk_size != 0 && sh->chunk_size != 64) return GDR_ERR_UNSUPPORTED;
+
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t* status = (int32_t*)ws;
+  int32_t* order = (int32_t*)((char*)ws + WorkspaceLayout::kHeaderBytes);
+  PrefillArgs a{sh->n_seqs, sh->H, sh->total_tokens, q, k, v, alpha, beta, S0, cu,
+                out, S_final, order, status};
+  prep_kernel<<<1, kPrepThreads, 0, s>>>(cu, sh->n_seqs, sh->total_tokens, order, status);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = launch_prefill_simt(*sh, a, linear, s);
+  return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace gdr
+
+extern "C" {
+
+size_t gdr_prefill_workspace_size(const gdr_shape* shape) {
+  if (!shape || shape->n_seqs < 1) return 0;
+  return gdr::WorkspaceLayout::total(shape->n_seqs);
+}
+
+gdr_status gdr_prefill(const gdr_shape* shape, const void* q, const void* k, const void* v,
+                       const float* alpha, const float* beta, const float* S0,
+                       const int32_t* cu_seqlens, void* out, float* S_final, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  return gdr::prefill_common(shape, q, k, v, alpha, beta, S0, cu_seqlens, out, S_final,
+                             workspace, workspace_bytes, stream, false);
+}
+
+gdr_status gdr_linear_attn(const gdr_shape* shape, const void* q, const void* k, const void* v,
+                           const float* S0, const int32_t* cu_seqlens, void* out, float* S_final,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  return gdr::prefill_common(shape, q, k, v, nullptr, nullptr, S0, cu_seqlens, out, S_final,
+                             workspace, workspace_bytes, stream, true);
+}
+
+gdr_status gdr_decode_step(const gdr_shape* shape, const void* q, const void* k, const void* v,
+                           const float* alpha, const float* beta, float* S_inout, void* out,
+                           void* stream) {
+  gdr_status st = gdr::check_shape(shape, true);
+  if (st != GDR_OK) return st;
+  if (shape->total_tokens != shape->n_seqs) return GDR_ERR_INVALID_ARG;
+  if (!q || !k || !v || !alpha || !beta || !S_inout || !out) return GDR_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, alpha, beta, S_inout, out};
+  for (const void* p : ptrs)
+    if (!gdr::aligned16(p)) return GDR_ERR_INVALID_ARG;
+  if (out == q || out == k || out == v || (const void*)S_inout == out) return GDR_ERR_INVALID_ARG;
+  cudaError_t e = gdr::launch_decode(*shape, q, k, v, alpha, beta, S_inout, out,
+                                     (cudaStream_t)stream);
+  return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+}
+
+gdr_status gdr_workspace_status(void* workspace, void* stream, int32_t* code) {
+  if (!workspace || !code) return GDR_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t h = 0;
+  if (cudaMemcpyAsync(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return GDR_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return GDR_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), s) != cudaSuccess) return GDR_ERR_CUDA;
+  *code = h;
+  return GDR_OK;
+}
+
+const char* gdr_status_string(gdr_status status) {
+  switch (status) {
+    case GDR_OK:
+      return "GDR_OK";
+    case GDR_ERR_INVALID_ARG:
+      return "GDR_ERR_INVALID_ARG";
+    case GDR_ERR_UNSUPPORTED:
+      return "GDR_ERR_UNSUPPORTED";
+    case GDR_ERR_CUDA:
+      return "GDR_ERR_CUDA";
+    case GDR_ERR_DEVICE_CHECK:
+      return "GDR_ERR_DEVICE_CHECK";
+  }
+  return "GDR_ERR_UNKNOWN";
+}
+
+}  // extern "C"

@@ -1,0 +1,155 @@
+// decode.cu -- one-token decode step of the gated delta rule, fused in one pass over the state.
+//
+// Per (sequence, head), from engineermaxxing "From GPT-2 to Kimi K3: one memory, seven eviction
+// policies" §06b (decay per row of S, read, correct) and dev.to "From GPT-2 to Kimi K3: How
+// Language Models Learned to Manage Memory" §4-§5 (fade, then read the faded state, then
+// correct):
+//     S_a   = Diag(alpha) S                    (the faded state, never written to memory)
+//     y_k   = S_a^T k          y_q = S_a^T q   (one read pass computes both)
+//     delta = beta (v - y_k)
+//     o     = S'^T q = y_q + (q . k) delta     (S' = S_a + k delta^T)
+//     S'    = S_a + k delta^T                  (written back in place)
+// Each element of S is read once and written once: the kernel is bound by HBM bandwidth
+// (2 * d_k * d_v * 4 bytes per head per step).
+//
+// Mapping: one CTA (8 warps) per (sequence, head).  Lane l owns d_v columns [l*CPL, l*CPL+CPL)
+// (CPL = d_v / 32, one 16-byte load for d = 128); warp w owns d_k rows [w*RPW, w*RPW+RPW).  The
+// whole d_k x d_v slab is held in registers between the read and the write, so the state is
+// streamed exactly once in each direction.  Column sums over rows are per-thread FMAs, then one
+// cross-warp reduction through shared memory; q . k is a warp-shuffle reduction.
+#include "gdr_internal.cuh"
+
+namespace gdr {
+namespace {
+
+__device__ __forceinline__ void vload(float (&x)[4], const float* p) {
+  float4 t = __ldcs(reinterpret_cast<const float4*>(p));
+  x[0] = t.x, x[1] = t.y, x[2] = t.z, x[3] = t.w;
+}
+__device__ __forceinline__ void vload(float (&x)[2], const float* p) {
+  float2 t = __ldcs(reinterpret_cast<const float2*>(p));
+  x[0] = t.x, x[1] = t.y;
+}
+__device__ __forceinline__ void vstore(float* p, const float (&x)[4]) {
+  __stcs(reinterpret_cast<float4*>(p), make_float4(x[0], x[1], x[2], x[3]));
+}
+__device__ __forceinline__ void vstore(float* p, const float (&x)[2]) {
+  __stcs(reinterpret_cast<float2*>(p), make_float2(x[0], x[1]));
+}
+
+constexpr int kDecodeWarps = 8;
+
+template <int D, typename T, bool CHANNEL>
+__global__ void __launch_bounds__(kDecodeWarps * 32, 2)
+    decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                  const float* __restrict__ alpha, const float* __restrict__ beta,
+                  float* __restrict__ S, T* __restrict__ out) {
+  constexpr int CPL = D / 32;           // columns per lane
+  constexpr int RPW = D / kDecodeWarps;  // rows per warp
+  __shared__ float s_q[D], s_k[D], s_a[D], s_v[D], s_delta[D];
+  __shared__ float s_red_k[kDecodeWarps][D], s_red_q[kDecodeWarps][D];
+
+  const int pair = blockIdx.x;  // n * H + h
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float* Sp = S + (size_t)pair * D * D;
+  const int col0 = lane * CPL;
+
+  // 1. issue the whole slab of state loads first (the only large stream)
+  float x[RPW][CPL];
+#pragma unroll
+  for (int r = 0; r < RPW; ++r) vload(x[r], Sp + (size_t)(warp * RPW + r) * D + col0);
+
+  // 2. the token's vectors
+  if (tid < D) {
+    const size_t o = (size_t)pair * D + tid;
+    s_q[tid] = to_f32(q[o]);
+    s_k[tid] = to_f32(k[o]);
+    s_v[tid] = to_f32(v[o]);
+    s_a[tid] = CHANNEL ? alpha[o] : alpha[pair];
+  }
+  __syncthreads();
+
+  // 3. fade the rows and accumulate the two column reads
+  float yk[CPL], yq[CPL];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) yk[c] = yq[c] = 0.f;
+#pragma unroll
+  for (int r = 0; r < RPW; ++r) {
+    const int row = warp * RPW + r;
+    const float a = s_a[row], kr = s_k[row], qr = s_q[row];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) {
+      x[r][c] *= a;
+      yk[c] = fmaf(kr, x[r][c], yk[c]);
+      yq[c] = fmaf(qr, x[r][c], yq[c]);
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) {
+    s_red_k[warp][col0 + c] = yk[c];
+    s_red_q[warp][col0 + c] = yq[c];
+  }
+  // q . k (every warp computes it; it is needed by the threads that finish the columns)
+  float qk = 0.f;
+#pragma unroll
+  for (int c = lane; c < D; c += 32) qk = fmaf(s_q[c], s_k[c], qk);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) qk += __shfl_xor_sync(0xffffffffu, qk, off);
+  __syncthreads();
+
+  // 4. finish the columns: delta and the read-out
+  if (tid < D) {
+    float tk = 0.f, tq = 0.f;
+#pragma unroll
+    for (int w = 0; w < kDecodeWarps; ++w) {
+      tk += s_red_k[w][tid];
+      tq += s_red_q[w][tid];
+    }
+    const float d = beta[pair] * (s_v[tid] - tk);
+    s_delta[tid] = d;
+    out[(size_t)pair * D + tid] = from_f32<T>(fmaf(qk, d, tq));
+  }
+  __syncthreads();
+
+  // 5. write back S' = S_a + k delta^T
+  float dl[CPL];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) dl[c] = s_delta[col0 + c];
+#pragma unroll
+  for (int r = 0; r < RPW; ++r) {
+    const float kr = s_k[warp * RPW + r];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) x[r][c] = fmaf(kr, dl[c], x[r][c]);
+    vstore(Sp + (size_t)(warp * RPW + r) * D + col0, x[r]);
+  }
+}
+
+template <int D, typename T>
+cudaError_t launch_typed(const gdr_shape& sh, const void* q, const void* k, const void* v,
+                         const float* alpha, const float* beta, float* S, void* out,
+                         cudaStream_t s) {
+  const unsigned grid = (unsigned)sh.n_seqs * (unsigned)sh.H;
+  if (sh.gate == GDR_GATE_CHANNEL)
+    decode_kernel<D, T, true><<<grid, kDecodeWarps * 32, 0, s>>>(
+        (const T*)q, (const T*)k, (const T*)v, alpha, beta, S, (T*)out);
+  else
+    decode_kernel<D, T, false><<<grid, kDecodeWarps * 32, 0, s>>>(
+        (const T*)q, (const T*)k, (const T*)v, alpha, beta, S, (T*)out);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const gdr_shape& sh, const void* q, const void* k, const void* v,
+                          const float* alpha, const float* beta, float* S, void* out,
+                          cudaStream_t s) {
+  if (sh.d_k == 128)
+    return sh.dtype == GDR_BF16
+               ? launch_typed<128, __nv_bfloat16>(sh, q, k, v, alpha, beta, S, out, s)
+               : launch_typed<128, float>(sh, q, k, v, alpha, beta, S, out, s);
+  return sh.dtype == GDR_BF16
+             ? launch_typed<64, __nv_bfloat16>(sh, q, k, v, alpha, beta, S, out, s)
+             : launch_typed<64, float>(sh, q, k, v, alpha, beta, S, out, s);
+}
+
+}  // namespace gdr

@@ -1,0 +1,267 @@
+// prefill_simt.cu -- chunked prefill of the gated delta rule (and of plain linear attention) in
+// fp32 FFMA.  This is the exact-arithmetic path: fp32 inputs, d = 64, and the cross-check of the
+// tensor-core path.
+//
+// Chunk algebra (derived from the recurrence; the alpha = 1 case is the per-chunk triangular
+// solve of engineermaxxing "From GPT-2 to Kimi K3: one memory, seven eviction policies" §04e-§04f
+// and heqinghuang "gpt2-to-kimi" §10; the decay products folded through it are the survival
+// products of engineermaxxing §05d / heqinghuang §11, one per key channel as in dev.to "From
+// GPT-2 to Kimi K3: How Language Models Learned to Manage Memory" §5).  For a chunk of n <= C
+// tokens, local index r, entering state S (d_k x d_v), with G_r = sum_{m <= r} log(alpha_m)
+// (per key channel, clamped at -60 per token):
+//   A[r][j] = beta_r sum_c k_r[c] k_j[c] e^{G_r[c] - G_j[c]}   (j < r)
+//   M[r][j] =        sum_c q_r[c] k_j[c] e^{G_r[c] - G_j[c]}   (j <= r)
+//   (I + A) [W | U~] = diag(beta) [K * e^G | V]                (forward substitution)
+//   U = U~ - W S;   O = (Q * e^G) S + M U;   S <- Diag(e^{G_n}) S + (K * e^{G_n - G})^T U
+// Plain linear attention: O = Q S + tril(Q K^T) V;  S <- S + K^T V.
+//
+// Mapping: one CTA (256 threads) per (sequence, head, block of DVB value columns); the columns
+// of S are independent (v and U enter column-wise), so the value dimension splits across CTAs
+// with no communication.  Each CTA walks its sequence's chunks in order; the state block lives
+// in shared memory for the whole walk.  All pair decays e^{G_r - G_j} are formed directly (no
+// factorisation), so any alpha in [0, 1] is exact to fp32 rounding.
+#include "gdr_internal.cuh"
+
+namespace gdr {
+namespace {
+
+constexpr int kSimtThreads = 256;
+constexpr int kDVB = 32;  // value columns per CTA
+
+template <int D, int C>
+struct SimtSmem {
+  static constexpr int LD = D + 1;      // row stride of [C][D] tiles (conflict-free columns)
+  static constexpr int LX = D + kDVB + 1;
+  static constexpr int LC = C + 1;
+  static constexpr int LV = kDVB + 1;
+  static constexpr int off_Q = 0;
+  static constexpr int off_K = off_Q + C * LD;
+  static constexpr int off_Kh = off_K + C * LD;
+  static constexpr int off_G = off_Kh + C * LD;
+  static constexpr int off_X = off_G + C * LD;
+  static constexpr int off_A = off_X + C * LX;
+  static constexpr int off_M = off_A + C * LC;
+  static constexpr int off_S = off_M + C * LC;
+  static constexpr int off_V = off_S + D * LV;
+  static constexpr int off_U = off_V + C * LV;
+  static constexpr int off_B = off_U + C * LV;
+  static constexpr int off_Gam = off_B + C;
+  static constexpr int total_floats = off_Gam + D;
+  static constexpr size_t bytes = (size_t)total_floats * 4;
+};
+
+template <int D, int C, typename T, bool CHANNEL, bool LINEAR>
+__global__ void __launch_bounds__(kSimtThreads) prefill_simt_kernel(PrefillArgs a) {
+  using L = SimtSmem<D, C>;
+  constexpr int NB = D / kDVB;
+  extern __shared__ float sm[];
+  float* sQ = sm + L::off_Q;
+  float* sK = sm + L::off_K;
+  float* sKh = sm + L::off_Kh;
+  float* sG = sm + L::off_G;
+  float* sX = sm + L::off_X;
+  float* sA = sm + L::off_A;
+  float* sM = sm + L::off_M;
+  float* sS = sm + L::off_S;
+  float* sV = sm + L::off_V;
+  float* sU = sm + L::off_U;
+  float* sB = sm + L::off_B;
+  float* sGam = sm + L::off_Gam;
+
+  const int tid = threadIdx.x;
+  const int H = a.H;
+  const int rank = blockIdx.x / (H * NB);
+  const int rem = blockIdx.x % (H * NB);
+  const int h = rem / NB, vb = rem % NB;
+  const int seq = a.order ? a.order[rank] : rank;
+  int64_t t0, t1;
+  if (!seq_range(a, seq, t0, t1)) return;
+
+  const T* q = static_cast<const T*>(a.q);
+  const T* k = static_cast<const T*>(a.k);
+  const T* v = static_cast<const T*>(a.v);
+  T* out = static_cast<T*>(a.out);
+  const int vc0 = vb * kDVB;
+  const size_t sidx = ((size_t)seq * H + h) * D * D;
+
+  // entering state block [D][DVB]
+  for (int i = tid; i < D * kDVB; i += kSimtThreads) {
+    const int r = i / kDVB, c = i % kDVB;
+    sS[r * L::LV + c] = a.S0 ? a.S0[sidx + (size_t)r * D + vc0 + c] : 0.f;
+  }
+
+  for (int64_t tc = t0; tc < t1; tc += C) {
+    const int n = (int)(t1 - tc < (int64_t)C ? t1 - tc : (int64_t)C);
+    __syncthreads();  // previous chunk fully consumed
+    // ---- 1. load the chunk (rows >= n: q = k = v = 0, alpha = 1, beta = 0)
+    for (int i = tid; i < C * D; i += kSimtThreads) {
+      const int r = i / D, c = i % D;
+      const bool ok = r < n;
+      const size_t o = ((size_t)(tc + r) * H + h) * D + c;
+      sQ[r * L::LD + c] = ok ? to_f32(q[o]) : 0.f;
+      sK[r * L::LD + c] = ok ? to_f32(k[o]) : 0.f;
+      if (!LINEAR) {
+        float g = 0.f;
+        if (ok) g = log_gate(CHANNEL ? a.alpha[o] : a.alpha[(size_t)(tc + r) * H + h]);
+        sG[r * L::LD + c] = g;
+      }
+    }
+    for (int i = tid; i < C * kDVB; i += kSimtThreads) {
+      const int r = i / kDVB, c = i % kDVB;
+      sV[r * L::LV + c] = r < n ? to_f32(v[((size_t)(tc + r) * H + h) * D + vc0 + c]) : 0.f;
+    }
+    if (!LINEAR && tid < C) sB[tid] = tid < n ? a.beta[(size_t)(tc + tid) * H + h] : 0.f;
+    __syncthreads();
+
+    if (!LINEAR) {
+      // ---- 2. in-chunk inclusive prefix sums of the log-gates, per key channel
+      for (int c = tid; c < D; c += kSimtThreads) {
+        float acc = 0.f;
+        for (int r = 0; r < C; ++r) {
+          acc += sG[r * L::LD + c];
+          sG[r * L::LD + c] = acc;
+        }
+      }
+      __syncthreads();
+    }
+
+    // ---- 3. pair matrices over the lower triangle (decay-weighted for the gated rule)
+    for (int p = tid; p < C * (C + 1) / 2; p += kSimtThreads) {
+      int r = (int)((sqrtf(8.f * p + 1.f) - 1.f) * 0.5f);
+      while (r * (r + 1) / 2 > p) --r;
+      while ((r + 1) * (r + 2) / 2 <= p) ++r;
+      const int j = p - r * (r + 1) / 2;
+      float acc_a = 0.f, acc_m = 0.f;
+      const float* kr = sK + r * L::LD;
+      const float* kj = sK + j * L::LD;
+      const float* qr = sQ + r * L::LD;
+      if (LINEAR) {
+        for (int c = 0; c < D; ++c) acc_m = fmaf(qr[c], kj[c], acc_m);
+      } else {
+        const float* gr = sG + r * L::LD;
+        const float* gj = sG + j * L::LD;
+        for (int c = 0; c < D; ++c) {
+          const float w = kj[c] * __expf(gr[c] - gj[c]);
+          acc_a = fmaf(kr[c], w, acc_a);
+          acc_m = fmaf(qr[c], w, acc_m);
+        }
+        sA[r * L::LC + j] = (j < r) ? sB[r] * acc_a : 0.f;
+      }
+      sM[r * L::LC + j] = acc_m;
+    }
+    __syncthreads();
+
+    if (!LINEAR) {
+      // ---- 4. gate-scaled operands and the right-hand sides of the solve
+      for (int i = tid; i < C * D; i += kSimtThreads) {
+        const int r = i / D, c = i % D;
+        const float g = sG[r * L::LD + c];
+        const float gam = __expf(g);
+        const float kv = sK[r * L::LD + c];
+        sX[r * L::LX + c] = sB[r] * kv * gam;                               // beta K~
+        sKh[r * L::LD + c] = kv * __expf(sG[(C - 1) * L::LD + c] - g);      // K^
+        sQ[r * L::LD + c] *= gam;                                           // Q~
+      }
+      for (int i = tid; i < C * kDVB; i += kSimtThreads) {
+        const int r = i / kDVB, c = i % kDVB;
+        sX[r * L::LX + D + c] = sB[r] * sV[r * L::LV + c];  // beta V
+      }
+      for (int c = tid; c < D; c += kSimtThreads) sGam[c] = __expf(sG[(C - 1) * L::LD + c]);
+      __syncthreads();
+
+      // ---- 5. forward substitution (I + A) X = rhs; each thread owns whole columns of X
+      for (int col = tid; col < D + kDVB; col += kSimtThreads) {
+        for (int r = 1; r < n; ++r) {
+          float acc0 = sX[r * L::LX + col], acc1 = 0.f;
+          const float* ar = sA + r * L::LC;
+          int j = 0;
+          for (; j + 1 < r; j += 2) {
+            acc0 = fmaf(-ar[j], sX[j * L::LX + col], acc0);
+            acc1 = fmaf(-ar[j + 1], sX[(j + 1) * L::LX + col], acc1);
+          }
+          if (j < r) acc0 = fmaf(-ar[j], sX[j * L::LX + col], acc0);
+          sX[r * L::LX + col] = acc0 + acc1;
+        }
+      }
+      __syncthreads();
+
+      // ---- 6. U = U~ - W S
+      for (int i = tid; i < C * kDVB; i += kSimtThreads) {
+        const int r = i / kDVB, c = i % kDVB;
+        const float* wr = sX + r * L::LX;
+        float acc0 = wr[D + c], acc1 = 0.f;
+        for (int m = 0; m < D; m += 2) {
+          acc0 = fmaf(-wr[m], sS[m * L::LV + c], acc0);
+          acc1 = fmaf(-wr[m + 1], sS[(m + 1) * L::LV + c], acc1);
+        }
+        sU[r * L::LV + c] = acc0 + acc1;
+      }
+      __syncthreads();
+    }
+    const float* sUse = LINEAR ? sV : sU;  // the values the chunk writes
+
+    // ---- 7. O = Q~ S + M U
+    for (int i = tid; i < C * kDVB; i += kSimtThreads) {
+      const int r = i / kDVB, c = i % kDVB;
+      if (r >= n) continue;
+      const float* qr = sQ + r * L::LD;
+      float acc0 = 0.f, acc1 = 0.f;
+      for (int m = 0; m < D; m += 2) {
+        acc0 = fmaf(qr[m], sS[m * L::LV + c], acc0);
+        acc1 = fmaf(qr[m + 1], sS[(m + 1) * L::LV + c], acc1);
+      }
+      const float* mr = sM + r * L::LC;
+      for (int j = 0; j <= r; ++j) acc0 = fmaf(mr[j], sUse[j * L::LV + c], acc0);
+      out[((size_t)(tc + r) * H + h) * D + vc0 + c] = from_f32<T>(acc0 + acc1);
+    }
+    __syncthreads();
+
+    // ---- 8. S <- Diag(e^{G_n}) S + K^T U
+    const float* kh = LINEAR ? sK : sKh;
+    for (int i = tid; i < D * kDVB; i += kSimtThreads) {
+      const int m = i / kDVB, c = i % kDVB;
+      float acc = LINEAR ? sS[m * L::LV + c] : sGam[m] * sS[m * L::LV + c];
+      for (int j = 0; j < n; ++j) acc = fmaf(kh[j * L::LD + m], sUse[j * L::LV + c], acc);
+      sS[m * L::LV + c] = acc;
+    }
+  }
+  __syncthreads();
+  if (a.S_final) {
+    for (int i = tid; i < D * kDVB; i += kSimtThreads) {
+      const int r = i / kDVB, c = i % kDVB;
+      a.S_final[sidx + (size_t)r * D + vc0 + c] = sS[r * L::LV + c];
+    }
+  }
+}
+
+template <int D, int C, typename T, bool CHANNEL, bool LINEAR>
+cudaError_t launch_one(const gdr_shape& sh, const PrefillArgs& a, cudaStream_t s) {
+  auto kern = prefill_simt_kernel<D, C, T, CHANNEL, LINEAR>;
+  const size_t smem = SimtSmem<D, C>::bytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = (unsigned)sh.n_seqs * (unsigned)sh.H * (unsigned)(D / kDVB);
+  kern<<<grid, kSimtThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int D, int C, typename T>
+cudaError_t launch_t(const gdr_shape& sh, const PrefillArgs& a, bool linear, cudaStream_t s) {
+  if (linear) return launch_one<D, C, T, true, true>(sh, a, s);
+  if (sh.gate == GDR_GATE_CHANNEL) return launch_one<D, C, T, true, false>(sh, a, s);
+  return launch_one<D, C, T, false, false>(sh, a, s);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_simt(const gdr_shape& sh, const PrefillArgs& a, bool linear,
+                                cudaStream_t s) {
+  if (sh.d_k == 128)
+    return sh.dtype == GDR_BF16 ? launch_t<128, 32, __nv_bfloat16>(sh, a, linear, s)
+                                : launch_t<128, 32, float>(sh, a, linear, s);
+  return sh.dtype == GDR_BF16 ? launch_t<64, 64, __nv_bfloat16>(sh, a, linear, s)
+                              : launch_t<64, 64, float>(sh, a, linear, s);
+}
+
+}  // namespace gdr

@@ -1,0 +1,145 @@
+/*
+ * gdr.h -- C ABI of libgdr: the gated delta rule (Kimi Delta Attention / Gated DeltaNet /
+ * DeltaNet / linear attention) on one GB300 GPU (sm_103a).
+ *
+ * The update, per (sequence, head), token t, with state S (d_k x d_v, fp32, row i = key
+ * channel i; read of a key is S^T k):
+ *
+ *     S_t = Diag(alpha_t) S_{t-1} + beta_t k_t (v_t - (Diag(alpha_t) S_{t-1})^T k_t)^T
+ *     o_t = S_t^T q_t
+ *
+ * Sources (web pages; sections as numbered on each page):
+ *   dev.to "From GPT-2 to Kimi K3: How Language Models Learned to Manage Memory", §3 (delta
+ *     rule), §4 (Gated DeltaNet: fade, then read, then correct), §5 (one retention factor per
+ *     key channel, i.e. per row of S);
+ *   engineermaxxing "From GPT-2 to Kimi K3: one memory, seven eviction policies", §03b
+ *     (read / subtract / write; state convention), §04b-§04f (chunked form and the triangular
+ *     solve), §05c-§05d (gate, survival products), §06b (per-channel gate);
+ *   heqinghuang "gpt2-to-kimi", §09-§11 (recurrent form, chunked DeltaNet, Gated DeltaNet);
+ *   kylehh "Kimi K3: From KV Cache to Selective Memory", §5-§8.
+ * The decay is applied before the read (the per-channel code of engineermaxxing §06b, dev.to
+ * §4-§5); with a scalar gate the two orders coincide.
+ *
+ * Conventions shared by every call
+ *   - Pointers are DEVICE pointers unless stated otherwise; the caller owns every buffer.  The
+ *     library allocates nothing, keeps no state between calls and never frees caller memory.
+ *   - Layouts are packed and token-major, row-major, no padding:
+ *       q, k            [T_total, H, d_k]   dtype = shape->dtype
+ *       v, out          [T_total, H, d_v]   dtype = shape->dtype
+ *       alpha           [T_total, H, d_k] fp32 (GDR_GATE_CHANNEL) or [T_total, H] fp32 (SCALAR)
+ *       beta            [T_total, H] fp32
+ *       S0, S_final     [n_seqs, H, d_k, d_v] fp32 (row = key channel)
+ *       cu_seqlens      [n_seqs + 1] int32 offsets into the token axis (device memory)
+ *   - alpha is the retention factor in [0, 1] (0 = reset); the kernels clamp log(alpha) at -60
+ *     per token, which is a reset to within fp32.  beta is the write strength (any real value;
+ *     (0, 1) in the method).  q and k are used as given (no normalisation, no 1/sqrt(d) scale).
+ *   - Supported: d_k = d_v in {64, 128}; dtype GDR_F32 (fp32 FFMA path) or GDR_BF16 (tensor-core
+ *     path for d = 128, fp32 FFMA otherwise).  Other shapes return GDR_ERR_UNSUPPORTED.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL = the legacy
+ *     default stream).  Argument errors are returned synchronously, before any launch.  Launch
+ *     failures return GDR_ERR_CUDA.  Checks that need device data (cu_seqlens monotone and within
+ *     total_tokens) run on the device and record the first failure in the workspace status word,
+ *     read with gdr_workspace_status(); sequences that fail the check are skipped.
+ *   - 16-byte alignment is required for every pointer (GDR_ERR_INVALID_ARG otherwise).
+ */
+#ifndef GDR_H_
+#define GDR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GDR_OK = 0,
+  GDR_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, bad size, bad enum, workspace too small */
+  GDR_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. d_k != d_v, d not 64/128) */
+  GDR_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
+  GDR_ERR_DEVICE_CHECK = 4  /* a device-side check failed (see gdr_workspace_status) */
+} gdr_status;
+
+typedef enum { GDR_F32 = 0, GDR_BF16 = 1 } gdr_dtype; /* dtype of q, k, v and out */
+typedef enum { GDR_GATE_SCALAR = 0, GDR_GATE_CHANNEL = 1 } gdr_gate;
+
+/* Device-side check codes written to the workspace status word (0 = no failure). */
+enum {
+  GDR_DEVCHECK_OK = 0,
+  GDR_DEVCHECK_SEQLENS = 1 /* cu_seqlens not monotone, negative, or beyond total_tokens */
+};
+
+typedef struct {
+  int32_t n_seqs;       /* number of sequences (>= 1) */
+  int32_t H;            /* heads (>= 1) */
+  int64_t total_tokens; /* T_total = length of the packed token axis (>= 0) */
+  int32_t d_k;          /* key / query channels = rows of S */
+  int32_t d_v;          /* value channels = columns of S */
+  int32_t dtype;        /* gdr_dtype of q, k, v, out */
+  int32_t gate;         /* gdr_gate layout of alpha (ignored by gdr_linear_attn) */
+  int32_t chunk_size;   /* 0 = the kernel's choice; otherwise must equal a supported size */
+  int32_t flags;        /* GDR_FLAG_* (0 = default) */
+} gdr_shape;
+
+/* Force the fp32 FFMA chunked path even where a tensor-core path exists (for cross-checks). */
+#define GDR_FLAG_FORCE_SIMT 1
+
+/*
+ * gdr_prefill -- chunked, packed variable-length prefill of the gated delta rule.
+ * engineermaxxing §04e-§04f (per-chunk triangular solve), heqinghuang §10-§11 (chunked DeltaNet
+ * with the running decay products folded in), dev.to §5 (per-channel gate).
+ *   q, k, v, alpha, beta, out: as above (out must not alias an input).
+ *   S0:         initial states, or NULL for zeros.
+ *   cu_seqlens: NULL means one sequence of total_tokens tokens (then n_seqs must be 1).
+ *   S_final:    final states, or NULL.  S_final may equal S0 (in-place hand-off).
+ *   workspace:  device scratch of at least gdr_prefill_workspace_size(shape) bytes, 256-byte
+ *               aligned; its contents need not be initialised; calls that overlap on the GPU
+ *               must use different workspaces.
+ * Empty sequences (length 0) produce no output and S_final = S0 (or zeros).
+ */
+gdr_status gdr_prefill(const gdr_shape* shape, const void* q, const void* k, const void* v,
+                       const float* alpha, const float* beta, const float* S0,
+                       const int32_t* cu_seqlens, void* out, float* S_final, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/* Workspace bytes gdr_prefill / gdr_linear_attn need for this shape (0 if the shape is invalid). */
+size_t gdr_prefill_workspace_size(const gdr_shape* shape);
+
+/*
+ * gdr_decode_step -- one token per sequence, state updated in place.
+ * engineermaxxing §06b (the per-channel code: decay per row, read, correct), heqinghuang §09.
+ * shape->total_tokens must equal shape->n_seqs; cu_seqlens is implied (token n = sequence n).
+ *   q, k [N, H, d_k]; v, out [N, H, d_v]; alpha [N, H, d_k] or [N, H]; beta [N, H];
+ *   S_inout [N, H, d_k, d_v] fp32, read and overwritten with the new state.
+ * One fused pass per state: the read of the faded state, the correction, the read-out and the
+ * write-back use each element of S once.  No workspace is needed.
+ */
+gdr_status gdr_decode_step(const gdr_shape* shape, const void* q, const void* k, const void* v,
+                           const float* alpha, const float* beta, float* S_inout, void* out,
+                           void* stream);
+
+/*
+ * gdr_linear_attn -- plain (unnormalised) linear attention, the alpha = 1, no-erase case:
+ * S_t = S_{t-1} + k_t v_t^T, o_t = S_t^T q_t; chunked as O = Q S + tril(Q K^T) V, S += K^T V.
+ * engineermaxxing §03b (identity transition) and §04b (chunked form); heqinghuang §10.
+ * No feature map, no normaliser, no beta.  Arguments as gdr_prefill (shape->gate ignored).
+ */
+gdr_status gdr_linear_attn(const gdr_shape* shape, const void* q, const void* k, const void* v,
+                           const float* S0, const int32_t* cu_seqlens, void* out, float* S_final,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * gdr_workspace_status -- synchronise `stream`, read the device-check word of a workspace used
+ * by gdr_prefill / gdr_linear_attn into *code (a GDR_DEVCHECK_* value) and clear it.
+ * Returns GDR_OK, or GDR_ERR_CUDA if the copy or the synchronisation failed.
+ */
+gdr_status gdr_workspace_status(void* workspace, void* stream, int32_t* code);
+
+/* Static, human-readable name of a status. */
+const char* gdr_status_string(gdr_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDR_H_ */

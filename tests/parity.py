@@ -1,0 +1,51 @@
+"""Helpers of the GPU parity tests: move generator inputs to the device, run the library through
+the binding, run the oracle on the same numbers, and measure the error.
+
+Error metric (the tolerances are the ones stated for this method: 1e-4 for fp32 inputs, 2e-2 for
+bf16 inputs with an fp32 state):
+  outputs: max over (token, head) of ||o_gpu - o_ref||_2 / max(||o_ref||_2, floor)
+  states:  max over (seq, head)  of ||S_gpu - S_ref||_F / max(||S_ref||_F, floor)
+with floor = 1e-3 x the RMS of the reference row (or state) norms, so that rows whose reference
+is nearly zero are judged against the typical magnitude instead of blowing up.
+"""
+import numpy as np
+import torch
+
+import gdr_inputs as gi
+
+TOL = {"f32": 1e-4, "bf16": 2e-2}
+
+
+def to_dev(x: np.ndarray, dtype: str, device="cuda"):
+    if dtype == "bf16":
+        bits = gi.bf16_bits(x)
+        return torch.from_numpy(bits.view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(device)
+
+
+def dev_inputs(a: dict, dtype: str, device="cuda"):
+    d = dict(q=to_dev(a["q"], dtype, device), k=to_dev(a["k"], dtype, device),
+             v=to_dev(a["v"], dtype, device), alpha=to_dev(a["alpha"], "f32", device),
+             beta=to_dev(a["beta"], "f32", device), S0=to_dev(a["S0"], "f32", device))
+    d["cu_seqlens"] = torch.from_numpy(a["cu_seqlens"].astype(np.int32)).to(device)
+    return d
+
+
+def rel_rows(got: np.ndarray, ref: np.ndarray) -> float:
+    """Largest row-normwise relative error over the leading axes (last axis = the row)."""
+    got = got.reshape(-1, got.shape[-1]).astype(np.float64)
+    ref = ref.reshape(-1, ref.shape[-1]).astype(np.float64)
+    if ref.size == 0:
+        return 0.0
+    rn = np.linalg.norm(ref, axis=1)
+    floor = max(1e-3 * np.sqrt(np.mean(rn ** 2)), 1e-30)
+    return float(np.max(np.linalg.norm(got - ref, axis=1) / np.maximum(rn, floor)))
+
+
+def rel_states(got: np.ndarray, ref: np.ndarray) -> float:
+    d = got.shape[-1] * got.shape[-2]
+    return rel_rows(got.reshape(-1, d), ref.reshape(-1, d))
+
+
+def host(t: torch.Tensor) -> np.ndarray:
+    return t.float().cpu().numpy()

@@ -1,0 +1,95 @@
+"""The C ABI on the CPU (no GPU needed): the library builds, loads, exports every symbol that
+include/gdr.h declares, and rejects bad arguments synchronously, before any CUDA work."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gated_delta_rule_prefill_gb300 import _abi, build
+    build.build_library()
+    return _abi.load()
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(gdr_[a-z0-9_]+)\s*\(", src))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    from gated_delta_rule_prefill_gb300 import _abi
+    names = declared_functions()
+    assert names and names == set(_abi.EXPORTS), names
+    for n in names:
+        assert getattr(lib, n) is not None
+
+
+def test_status_strings(lib):
+    from gated_delta_rule_prefill_gb300 import _abi
+    assert _abi.status_string(0) == "GDR_OK"
+    assert _abi.status_string(2) == "GDR_ERR_UNSUPPORTED"
+    assert _abi.status_string(99) == "GDR_ERR_UNKNOWN"
+
+
+def _shape(**kw):
+    from gated_delta_rule_prefill_gb300 import make_shape
+    base = dict(n_seqs=2, H=4, total_tokens=100, d_k=128, d_v=128, dtype=1, gate=1)
+    base.update(kw)
+    return make_shape(**base)
+
+
+FAKE = 1 << 20  # 16-byte aligned, never dereferenced: every case below fails validation first
+
+
+def _prefill(lib, sh, ws_bytes=1 << 16, **over):
+    p = dict(q=FAKE, k=FAKE + 4096, v=FAKE + 8192, alpha=FAKE, beta=FAKE, S0=None, cu=FAKE,
+             out=FAKE + 65536, Sf=None, ws=FAKE * 2)
+    p.update(over)
+    P = ctypes.c_void_p
+    return lib.gdr_prefill(ctypes.byref(sh), P(p["q"]), P(p["k"]), P(p["v"]), P(p["alpha"]),
+                           P(p["beta"]), P(p["S0"]), P(p["cu"]), P(p["out"]), P(p["Sf"]),
+                           P(p["ws"]), ws_bytes, None)
+
+
+def test_argument_errors(lib):
+    INV, UNS = 1, 2
+    assert lib.gdr_prefill(None, *([None] * 10), 0, None) == INV
+    assert _prefill(lib, _shape(d_k=96, d_v=96)) == UNS
+    assert _prefill(lib, _shape(d_k=128, d_v=64)) == UNS
+    assert _prefill(lib, _shape(dtype=7)) == INV
+    assert _prefill(lib, _shape(gate=5)) == INV
+    assert _prefill(lib, _shape(n_seqs=0)) == INV
+    assert _prefill(lib, _shape(total_tokens=-1)) == INV
+    assert _prefill(lib, _shape(), q=FAKE + 2) == INV           # misaligned
+    assert _prefill(lib, _shape(), q=None) == INV               # null input
+    assert _prefill(lib, _shape(), alpha=None) == INV           # gated rule needs alpha
+    assert _prefill(lib, _shape(), ws=None) == INV              # no workspace
+    assert _prefill(lib, _shape(), ws=FAKE * 2 + 16) == INV     # workspace not 256-aligned
+    assert _prefill(lib, _shape(), ws_bytes=8) == INV           # workspace too small
+    assert _prefill(lib, _shape(), cu=None) == INV              # n_seqs > 1 needs cu_seqlens
+    assert _prefill(lib, _shape(), out=FAKE) == INV             # out aliases q
+    assert _prefill(lib, _shape(chunk_size=48)) == UNS
+    assert _prefill(lib, _shape(flags=8)) == INV
+    # decode: total_tokens must equal n_seqs
+    P = ctypes.c_void_p
+    sh = _shape(total_tokens=3)
+    assert lib.gdr_decode_step(ctypes.byref(sh), *[P(FAKE + 4096 * i) for i in range(7)],
+                               None) == INV
+
+
+def test_workspace_size(lib):
+    from gated_delta_rule_prefill_gb300 import _abi
+    sh = _shape(n_seqs=64)
+    n = lib.gdr_prefill_workspace_size(ctypes.byref(sh))
+    assert n >= 256 + 64 * 4 and n % 256 == 0
+    assert lib.gdr_prefill_workspace_size(None) == 0
