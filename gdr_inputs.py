@@ -235,3 +235,47 @@ def random_state(seed: int, N: int, H: int, d_k: int, d_v: int, std: float = 0.1
     """A synthetic fp32 state [N,H,d_k,d_v] ~ N(0, std^2) (decode parity from a given state)."""
     return (std * _rng(seed, _S0, 99991).standard_normal((N, H, d_k, d_v), dtype=np.float32)
             ).astype(np.float32)
+
+
+# ----------------------------------------------------------------------------------------------
+# device-side drawing (timing only)
+# ----------------------------------------------------------------------------------------------
+def device_full(wl: Workload, device, seed_offset: int = 0):
+    """The same distributions drawn on the device with torch's seeded generator (different
+    numbers from the host streams above).  Used where only the shape and distribution of the
+    inputs matter (throughput runs); parity always uses the host streams."""
+    import torch
+
+    g = torch.Generator(device=device)
+    g.manual_seed(wl.seed * 1000003 + seed_offset)
+    T, H, dk, dv = wl.total_tokens, wl.H, wl.d_k, wl.d_v
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+
+    def unit(shape):
+        x = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+        return (x / x.norm(dim=-1, keepdim=True).clamp_min(1e-30)).to(tdt)
+
+    q = unit((T, H, dk))
+    k = unit((T, H, dk))
+    v = torch.randn((T, H, dv), generator=g, device=device, dtype=torch.float32).to(tdt)
+    ashape = (T, H, dk) if wl.gate == "channel" else (T, H)
+    alpha = torch.exp(-torch.nn.functional.softplus(
+        torch.randn(ashape, generator=g, device=device) - 4.0))
+    beta = torch.sigmoid(torch.randn((T, H), generator=g, device=device))
+    if wl.s0 == "normal":
+        S0 = 0.1 * torch.randn((wl.n_seqs, H, dk, dv), generator=g, device=device)
+    else:
+        S0 = torch.zeros((wl.n_seqs, H, dk, dv), device=device)
+    cu = torch.from_numpy(wl.cu_seqlens.astype(np.int32)).to(device)
+    return dict(q=q, k=k, v=v, alpha=alpha.contiguous(), beta=beta.contiguous(), S0=S0,
+                cu_seqlens=cu)
+
+
+def device_decode_steps(wl: Workload, n_sets: int, device):
+    """n_sets distinct decode-step input sets drawn on the device (throughput runs)."""
+    one = dataclasses.replace(wl, seqlens=np.ones(wl.n_seqs, dtype=np.int64), s0="zeros")
+    sets = []
+    for i in range(n_sets):
+        d = device_full(one, device, seed_offset=1 + i)
+        sets.append({k: d[k] for k in ("q", "k", "v", "alpha", "beta")})
+    return sets
