@@ -152,5 +152,7 @@ def gdr_workspace_status(workspace, stream=None) -> int:
 
 
 def compute_dtype(dtype: str, d: int, force_simt: bool = False) -> str:
-    """Arithmetic type of the prefill kernel the library selects for these inputs."""
-    return "f32"
+    """Arithmetic type of the prefill kernel the library selects for these inputs: bf16
+    tensor-core operands with fp32 accumulation and state for bf16 inputs at d = 128, fp32
+    FFMA otherwise."""
+    return "bf16" if (dtype == "bf16" and d == 128 and not force_simt) else "f32"

@@ -91,7 +91,9 @@ gdr_status prefill_common(const gdr_shape* sh, const void* q, const void* k, con
                 out, S_final, order, status};
   prep_kernel<<<1, kPrepThreads, 0, s>>>(cu, sh->n_seqs, sh->total_tokens, order, status);
   cudaError_t e = cudaGetLastError();
-  if (e == cudaSuccess) e = launch_prefill_simt(*sh, a, linear, s);
+  if (e == cudaSuccess)
+    e = prefill_tc_supported(*sh) ? launch_prefill_tc(*sh, a, linear, s)
+                                  : launch_prefill_simt(*sh, a, linear, s);
   return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }
 

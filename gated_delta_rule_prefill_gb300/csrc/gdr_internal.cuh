@@ -77,6 +77,9 @@ __device__ __forceinline__ bool seq_range(const PrefillArgs& a, int seq, int64_t
 cudaError_t launch_prep(const PrefillArgs& a, int32_t* order, cudaStream_t s);
 cudaError_t launch_prefill_simt(const gdr_shape& sh, const PrefillArgs& a, bool linear,
                                 cudaStream_t s);
+bool prefill_tc_supported(const gdr_shape& sh);
+cudaError_t launch_prefill_tc(const gdr_shape& sh, const PrefillArgs& a, bool linear,
+                              cudaStream_t s);
 cudaError_t launch_decode(const gdr_shape& sh, const void* q, const void* k, const void* v,
                           const float* alpha, const float* beta, float* S, void* out,
                           cudaStream_t s);

@@ -66,7 +66,8 @@ typedef enum { GDR_GATE_SCALAR = 0, GDR_GATE_CHANNEL = 1 } gdr_gate;
 /* Device-side check codes written to the workspace status word (0 = no failure). */
 enum {
   GDR_DEVCHECK_OK = 0,
-  GDR_DEVCHECK_SEQLENS = 1 /* cu_seqlens not monotone, negative, or beyond total_tokens */
+  GDR_DEVCHECK_SEQLENS = 1, /* cu_seqlens not monotone, negative, or beyond total_tokens */
+  GDR_DEVCHECK_TIMEOUT = 2  /* a tensor-core wait gave up (the kernel unwound; results invalid) */
 };
 
 typedef struct {
