@@ -22,11 +22,12 @@
 // G = sum max(log alpha, -60) and form A' and M from direct pairwise exponentials (exact,
 // slower).  Linear attention: no gates (K~ = Kr = K^ = K, Q~ = Q), U = V, no solve.
 //
-// Mapping: one CTA (4 warps) per (sequence, head, block of DV value columns); columns of S are
-// independent, so the value dimension splits across CTAs.  Thread t owns TMEM lane t: key
-// channel t of the state, or token row t of the M = 128 Gram accumulator; M = 64 accumulators
-// (token rows) occupy lanes 32w + [0, 16) for rows 16w + [0, 16).  q, k, alpha and v tiles of
-// the next chunk are fetched by TMA while the current chunk computes.
+// Mapping: one CTA (8 warps) per (sequence, head, block of DV value columns); columns of S are
+// independent, so the value dimension splits across CTAs.  Warp w reads TMEM lane quarter w & 3
+// and the column half w >> 2 of every accumulator: thread t owns lane t & 127, i.e. key channel
+// t & 127 of the state or token row t & 127 of the M = 128 Gram accumulator; M = 64
+// accumulators (token rows) occupy lanes 32q + [0, 16) for rows 16q + [0, 16).  q, k, alpha and
+// v tiles of the next chunk are fetched by TMA while the current chunk computes.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -42,7 +43,7 @@ using namespace umma;
 
 constexpr int kD = 128;          // d_k = d_v
 constexpr int kC = 64;           // chunk
-constexpr int kThreads = 128;    // 4 warps, one per TMEM lane quarter
+constexpr int kThreads = 256;    // 8 warps: two per TMEM lane quarter
 constexpr float kSafeGamma = 4.2483543e-18f;  // e^-40
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s: a copy or MMA not done by then is a fault
 
@@ -72,16 +73,16 @@ struct TcSmem {
   static constexpr uint32_t BETA = SS + DV * 256;   // beta [64]
   static constexpr uint32_t ALPHA = BETA + 256;     // scalar gates [64]
   static constexpr uint32_t GAM = ALPHA + 256;      // gamma [128]
-  static constexpr uint32_t RED = GAM + 512;        // reductions
+  static constexpr uint32_t RED = GAM + 512;        // reductions [8]
   static constexpr uint32_t BARS = RED + 64;        // 4 mbarriers + TMEM slot
   static constexpr uint32_t END = BARS + 64;
   static constexpr size_t bytes = END + 1024;       // + alignment slack
   // fp32 scratch of the solve, in tiles that are dead while it runs
   static constexpr uint32_t SA = KR;                // A [64][64]  (Kr is consumed by then)
   static constexpr uint32_t ST32 = WW;              // T [64][64]  (W is written later)
-  static constexpr uint32_t SX = UU;                // 3 x [16][16] (U is written later)
+  static constexpr uint32_t SX = UU;                // [32][32] (U is written later)
   static_assert(bytes <= 232448, "shared memory per CTA");
-  static_assert(DV * 128 >= 3 * 256 * 4, "block scratch fits in U");
+  static_assert(DV * 128 >= 32 * 32 * 4, "block scratch fits in U");
 };
 
 // 8 consecutive bf16 elements (one 16-byte chunk) at (row, k0) of a 128B-swizzled tile.
@@ -112,54 +113,107 @@ __device__ __forceinline__ void cta_sync_tc() {
   fence_after_sync();
 }
 
-// Blockwise inverse of the unit lower-triangular I + A (A strictly lower, 64 x 64 fp32, row
-// stride 64) into sT: 16 x 16 diagonal blocks by forward substitution, then the off-diagonal
-// blocks by block diagonals, T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj.
+// fp32 64 x 64 scratch matrices (A, T) keep their 16-byte column groups XOR-swizzled by the
+// row (group g of row r stored at position g ^ (r & 7)), so eight consecutive rows touching the
+// same column group hit eight different bank groups.
+__device__ __forceinline__ int f32x(int r, int j) {
+  return r * kC + ((((j >> 2) ^ (r & 7))) << 2) + (j & 3);
+}
+__device__ __forceinline__ float4 ld4x(const float* m, int r, int grp) {
+  return *reinterpret_cast<const float4*>(m + r * kC + ((grp ^ (r & 7)) << 2));
+}
+__device__ __forceinline__ void st4x(float* m, int r, int grp, float4 v) {
+  *reinterpret_cast<float4*>(m + r * kC + ((grp ^ (r & 7)) << 2)) = v;
+}
+__device__ __forceinline__ void fma4(float4& acc, float a, float4 b) {
+  acc.x = fmaf(a, b.x, acc.x);
+  acc.y = fmaf(a, b.y, acc.y);
+  acc.z = fmaf(a, b.z, acc.z);
+  acc.w = fmaf(a, b.w, acc.w);
+}
+
+// T = (I + A)^-1 for A strictly lower (64 x 64, fp32, swizzled layout above), by doubling the
+// inverted block size: the four 16 x 16 diagonal blocks by right-looking forward substitution
+// (one column per thread, held in registers); then both 32 x 32 diagonal blocks at once,
+// T_ba = -T_bb (A_ba T_aa) for (a, b) = (0, 1) and (2, 3); then the 64 x 64 inverse,
+// T_[23][01] = -T_[23][23] (A_[23][01] T_[01][01]).  sX holds the 32 x 32 intermediate.
 __device__ void unit_lower_inverse(const float* sA, float* sT, float* sX, int tid) {
-  constexpr int LD = kC;
-  for (int i = tid; i < kC * kC; i += kThreads) {
-    const int r = i / kC, c = i % kC;
-    if ((c >> 4) > (r >> 4)) sT[r * LD + c] = 0.f;
-  }
   if (tid < 64) {
     const int b = tid >> 4, c = tid & 15, o = 16 * b;
-    float x[16];
+    float acc[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float acc = (i == c) ? 1.f : 0.f;
+    for (int i = 0; i < 16; ++i) acc[i] = (i == c) ? 1.f : 0.f;
 #pragma unroll
-      for (int j = 0; j < i; ++j) acc = fmaf(-sA[(o + i) * LD + o + j], x[j], acc);
-      x[i] = (i < c) ? 0.f : acc;
+    for (int j = 0; j < 15; ++j) {
+      const float xj = acc[j];
+#pragma unroll
+      for (int i = j + 1; i < 16; ++i) acc[i] = fmaf(-sA[f32x(o + i, o + j)], xj, acc[i]);
     }
 #pragma unroll
-    for (int i = 0; i < 16; ++i) sT[(o + i) * LD + o + c] = x[i];
+    for (int i = 0; i < 16; ++i) sT[f32x(o + i, o + c)] = acc[i];
+  } else {
+    // strictly-upper blocks of T are zero: rows 0-31 from column 32, and the 16 x 16 blocks
+    // (0, 1) and (2, 3)
+    for (int e = tid - 64; e < kC * 16; e += kThreads - 64) {
+      const int r = e >> 4, grp = e & 15;
+      if (grp >= 4 * ((r >> 4) + 1)) st4x(sT, r, grp, make_float4(0.f, 0.f, 0.f, 0.f));
+    }
   }
   __syncthreads();
-#pragma unroll 1
-  for (int dist = 1; dist < 4; ++dist) {
-    const int nblk = 4 - dist;  // blocks (i, j = i - dist), i = dist..3
-    for (int e = tid; e < nblk * 256; e += kThreads) {
-      const int bi = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-      const int i = bi + dist, j = bi;
-      float acc = 0.f;
-      for (int kb = j; kb < i; ++kb) {
-        const float* arow = sA + (16 * i + rr) * LD + 16 * kb;
+  // ---- level 32: blocks (1, 0) and (3, 2); 2 x 256 outputs, 2 per thread
+  {
+    const int blk = tid >> 7, e = tid & 127;       // blk 0: (1,0); blk 1: (3,2)
+    const int rr = e >> 3, c2 = (e & 7) * 2;       // row in the block, column pair
+    const int ra = 32 * blk, rb = ra + 16;         // first rows of block rows a and b
+    float x0 = 0.f, x1 = 0.f;
 #pragma unroll
-        for (int m = 0; m < 16; ++m) acc = fmaf(arow[m], sT[(16 * kb + m) * LD + 16 * j + cc], acc);
-      }
-      sX[bi * 256 + rr * 16 + cc] = acc;
+    for (int m = 0; m < 16; ++m) {
+      const float am = sA[f32x(rb + rr, ra + m)];
+      x0 = fmaf(am, sT[f32x(ra + m, ra + c2)], x0);
+      x1 = fmaf(am, sT[f32x(ra + m, ra + c2 + 1)], x1);
     }
+    sX[blk * 256 + rr * 16 + c2] = x0;
+    sX[blk * 256 + rr * 16 + c2 + 1] = x1;
     __syncthreads();
-    for (int e = tid; e < nblk * 256; e += kThreads) {
-      const int bi = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-      const int i = bi + dist, j = bi;
-      const float* trow = sT + (16 * i + rr) * LD + 16 * i;
-      float acc = 0.f;
+    float y0 = 0.f, y1 = 0.f;
 #pragma unroll
-      for (int m = 0; m < 16; ++m) acc = fmaf(trow[m], sX[bi * 256 + m * 16 + cc], acc);
-      sT[(16 * i + rr) * LD + 16 * j + cc] = -acc;
+    for (int m = 0; m < 16; ++m) {
+      const float tm = m <= rr ? sT[f32x(rb + rr, rb + m)] : 0.f;
+      y0 = fmaf(tm, sX[blk * 256 + m * 16 + c2], y0);
+      y1 = fmaf(tm, sX[blk * 256 + m * 16 + c2 + 1], y1);
     }
+    sT[f32x(rb + rr, ra + c2)] = -y0;
+    sT[f32x(rb + rr, ra + c2 + 1)] = -y1;
     __syncthreads();
+  }
+  // ---- level 64: block [23][01] (32 x 32); 1024 outputs, 4 per thread (one float4 group)
+  {
+    const int rr = tid >> 3, grp = tid & 7;  // row 0..31 of the block, float4 group 0..7
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int m = 0; m < 32; ++m) fma4(x, sA[f32x(32 + rr, m)], ld4x(sT, m, grp));
+    *reinterpret_cast<float4*>(sX + rr * 32 + 4 * grp) = x;
+    __syncthreads();
+    float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int m = 0; m < 32; ++m) {
+      const float tm = m <= rr ? sT[f32x(32 + rr, 32 + m)] : 0.f;
+      fma4(y, tm, *reinterpret_cast<const float4*>(sX + m * 32 + 4 * grp));
+    }
+    st4x(sT, 32 + rr, grp, make_float4(-y.x, -y.y, -y.z, -y.w));
+    __syncthreads();
+  }
+}
+
+// 8 bf16 values (one 16-byte chunk) -> fp32
+__device__ __forceinline__ void ld_bf16x8(const __nv_bfloat16* p, float* x) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(h[i]);
+    x[2 * i] = f.x;
+    x[2 * i + 1] = f.y;
   }
 }
 
@@ -172,6 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ TcMaps maps, const PrefillArgs a) {
   using L = TcSmem<DV>;
   constexpr int NB = kD / DV;
+  constexpr int DH = DV / 2;  // accumulator columns per warp half
   constexpr bool kAlphaTile = CHANNEL && !LINEAR;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm =
@@ -196,6 +251,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int lrow = tid & 127;      // TMEM lane of this thread
+  const int wh = warp >> 2;        // column half of the accumulators
   const int H = a.H;
   const int rank = blockIdx.x / (H * NB);
   const int rem = blockIdx.x % (H * NB);
@@ -218,7 +275,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   cta_sync_tc();
   const uint32_t tm = *tslot;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;  // this warp's TMEM lane quarter
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;  // TMEM lane quarter
+  const int m64row = 16 * (warp & 3) + (lane & 15);  // token row of M = 64 accumulators
+  const bool m64ok = lane < 16;
   uint32_t ph_mma = 0, ph_qk = 0, ph_a = 0, ph_v = 0;
   bool failed = false;
 
@@ -272,15 +331,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- entering state: fp32 master in TMEM (lane = key channel), bf16 S operand row-wise
   {
-    const float* s0 = a.S0 ? a.S0 + sidx + (size_t)tid * kD + vc0 : nullptr;
+    const float* s0 = a.S0 ? a.S0 + sidx + (size_t)lrow * kD + vc0 : nullptr;
 #pragma unroll
-    for (int c0 = 0; c0 < DV; c0 += 32) {
+    for (int c0 = wh * DH; c0 < wh * DH + DH; c0 += 32) {
       float x[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) x[j] = s0 ? s0[c0 + j] : 0.f;
       tmem_st32(tm + lane_base + kColS + c0, x);
 #pragma unroll
-      for (int j = 0; j < 32; j += 8) st_chunk8(sm + L::SS, 16384, tid, c0 + j, x + j);
+      for (int j = 0; j < 32; j += 8) st_chunk8(sm + L::SS, 16384, lrow, c0 + j, x + j);
     }
     tmem_wait_st();
   }
@@ -307,7 +366,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int64_t tc = t0; tc < t1 && !failed; tc += kC) {
     const int n = (int)((t1 - tc) < (int64_t)kC ? (t1 - tc) : (int64_t)kC);
     const int64_t tn = tc + kC;  // next chunk
-    const int c = tid;           // key channel owned in the gate pass
 
     if (tid < kC) {
       sBeta[tid] = nb_beta;
@@ -317,43 +375,108 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!wait_bar(bar_qk, ph_qk)) { failed = true; break; }
     if (kAlphaTile && !wait_bar(bar_a, ph_a)) { failed = true; break; }
 
-    // ================= 1. gates and operand tiles (thread = key channel)
-    float gam = 1.f;
-    if (!LINEAR) {
-#pragma unroll 8
-      for (int r = 0; r < kC; ++r)
-        if (r < n) gam *= kAlphaTile ? sAin[r * kD + c] : sAlpha[r];
-      sGam[c] = gam;
+    // ================= 1. gates and operand tiles
+    // thread = 8 key channels (group g8) x 4 tokens (row block rb): running products of the
+    // gates down its own rows, then the carry of the earlier row blocks through shared memory.
+    const int g8 = tid & 15, rb = tid >> 4;
+    float p[4][8];  // prefix products Gam[4 rb + rr][8 g8 + cc]
+    float gn[8];    // Gam_n (= gamma) of the 8 channels
+    {
+      float run[8];
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) run[cc] = 1.f;
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        const int r = 4 * rb + rr;
+        float a8[8];
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) a8[cc] = 1.f;
+        if (!LINEAR && r < n) {
+          if (kAlphaTile) {
+            const float4 u0 = *reinterpret_cast<const float4*>(sAin + r * kD + 8 * g8);
+            const float4 u1 = *reinterpret_cast<const float4*>(sAin + r * kD + 8 * g8 + 4);
+            a8[0] = u0.x, a8[1] = u0.y, a8[2] = u0.z, a8[3] = u0.w;
+            a8[4] = u1.x, a8[5] = u1.y, a8[6] = u1.z, a8[7] = u1.w;
+          } else {
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) a8[cc] = sAlpha[r];
+          }
+        }
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          run[cc] *= a8[cc];
+          p[rr][cc] = run[cc];
+        }
+      }
+      float* sTot = reinterpret_cast<float*>(sm + L::WW);  // [16 row blocks][128 channels]
+      *reinterpret_cast<float4*>(sTot + rb * kD + 8 * g8) = make_float4(run[0], run[1], run[2], run[3]);
+      *reinterpret_cast<float4*>(sTot + rb * kD + 8 * g8 + 4) = make_float4(run[4], run[5], run[6], run[7]);
+      __syncthreads();
+      float carry[8];
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) carry[cc] = gn[cc] = 1.f;
+#pragma unroll
+      for (int b2 = 0; b2 < 16; ++b2) {
+        const float4 u0 = *reinterpret_cast<const float4*>(sTot + b2 * kD + 8 * g8);
+        const float4 u1 = *reinterpret_cast<const float4*>(sTot + b2 * kD + 8 * g8 + 4);
+        const float t8[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          if (b2 < rb) carry[cc] *= t8[cc];
+          gn[cc] *= t8[cc];
+        }
+      }
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) p[rr][cc] *= carry[cc];
     }
-    float mn = gam;
+    float mn = gn[0];
+#pragma unroll
+    for (int cc = 1; cc < 8; ++cc) mn = fminf(mn, gn[cc]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
     if (lane == 0) sRed[warp] = mn;
+    if (!LINEAR && rb == 0) {
+      *reinterpret_cast<float4*>(sGam + 8 * g8) = make_float4(gn[0], gn[1], gn[2], gn[3]);
+      *reinterpret_cast<float4*>(sGam + 8 * g8 + 4) = make_float4(gn[4], gn[5], gn[6], gn[7]);
+    }
     __syncthreads();
-    const bool safe =
-        LINEAR || fminf(fminf(sRed[0], sRed[1]), fminf(sRed[2], sRed[3])) > kSafeGamma;
+    float mall = sRed[0];
+#pragma unroll
+    for (int w = 1; w < kThreads / 32; ++w) mall = fminf(mall, sRed[w]);
+    const bool safe = LINEAR || mall > kSafeGamma;
 
     if (safe) {
-      float G = 1.f;  // running product of the gates
-#pragma unroll 4
-      for (int r = 0; r < kC; ++r) {
-        const bool ok = r < n;
-        const float kv = ok ? __bfloat162float(sKin[r * kD + c]) : 0.f;
-        const float qv = ok ? __bfloat162float(sQin[r * kD + c]) : 0.f;
-        float e = 1.f, ei = 1.f;
-        if (!LINEAR && ok) {
-          G *= kAlphaTile ? sAin[r * kD + c] : sAlpha[r];
-          e = G;
-          ei = __frcp_rn(G);
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        const int r = 4 * rb + rr;
+        float k8[8], q8[8];
+        if (r < n) {
+          ld_bf16x8(sKin + r * kD + 8 * g8, k8);
+          ld_bf16x8(sQin + r * kD + 8 * g8, q8);
+        } else {
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) k8[cc] = q8[cc] = 0.f;
         }
-        const float ke = kv * e, ki = kv * ei;
-        st_bf16(sm + L::KQ, sw128_offset(r, c, 16384), ke);              // K~
-        st_bf16(sm + L::KQ, sw128_offset(64 + r, c, 16384), qv * e);     // Q~
-        st_bf16(sm + L::KR, sw128_offset(r, c, 8192), ki);               // Kr
-        st_bf16(sm + L::KH, sw128_offset(r, c, 8192), ki * gam);         // K^
+        float ke[8], qe[8], ki[8], kh[8];
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          const float G = p[rr][cc];
+          const float inv = LINEAR ? 1.f : __fdividef(1.f, G);
+          ke[cc] = k8[cc] * G;
+          qe[cc] = q8[cc] * G;
+          ki[cc] = k8[cc] * inv;
+          kh[cc] = ki[cc] * gn[cc];
+        }
+        st_chunk8(sm + L::KQ, 16384, r, 8 * g8, ke);       // K~
+        st_chunk8(sm + L::KQ, 16384, 64 + r, 8 * g8, qe);  // Q~
+        st_chunk8(sm + L::KR, 8192, r, 8 * g8, ki);        // Kr
+        st_chunk8(sm + L::KH, 8192, r, 8 * g8, kh);        // K^
       }
-    } else {
-      // strong decay: log-gate prefix sums, in place of the staged gates
+    } else if (tid < kD) {
+      // strong decay: log-gate prefix sums in place of the staged gates (thread = channel)
+      const int c = tid;
       float G = 0.f;
 #pragma unroll 4
       for (int r = 0; r < kC; ++r) {
@@ -374,14 +497,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         st_bf16(sm + L::KQ, sw128_offset(64 + r, c, 16384), qv * e);
         st_bf16(sm + L::KH, sw128_offset(r, c, 8192), kv * __expf(Gn - G));
       }
-      if (!kAlphaTile) {  // scalar gates: keep the per-token prefix sums for the pair decays
-        __syncthreads();
-        if (tid == 0) {
-          float g = 0.f;
-          for (int r = 0; r < kC; ++r) {
-            if (r < n) g += log_gate(sAlpha[r]);
-            sAlpha[r] = g;
-          }
+    }
+    if (!safe && !kAlphaTile) {  // scalar gates: per-token prefix sums for the pair decays
+      __syncthreads();
+      if (tid == 0) {
+        float g = 0.f;
+        for (int r = 0; r < kC; ++r) {
+          if (r < n) g += log_gate(sAlpha[r]);
+          sAlpha[r] = g;
         }
       }
     }
@@ -399,31 +522,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar_mma);
       }
       if (!wait_bar(bar_mma, ph_mma)) { failed = true; break; }
-      const int r = tid & 63;
+      const int r = lrow & 63;
+      const int c0 = 32 * wh;
+      float x[32];
+      tmem_ld32(tm + lane_base + kColAM + c0, x);
+      if (lrow < 64) {
+        if (!LINEAR) {
+          const float b = sBeta[r];
 #pragma unroll
-      for (int c0 = 0; c0 < kC; c0 += 32) {
-        float x[32];
-        tmem_ld32(tm + lane_base + kColAM + c0, x);
-        if (tid < 64) {
-          if (!LINEAR) {
-            const float b = sBeta[r];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) sA[r * kC + c0 + j] = (c0 + j < r) ? b * x[j] : 0.f;
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) x[j] = (c0 + j <= r) ? x[j] : 0.f;
-#pragma unroll
-          for (int j = 0; j < 32; j += 8) st_chunk8(sm + L::MM, 8192, r, c0 + j, x + j);
+          for (int j = 0; j < 32; j += 4)
+            st4x(sA, r, (c0 + j) >> 2,
+                 make_float4((c0 + j < r) ? b * x[j] : 0.f, (c0 + j + 1 < r) ? b * x[j + 1] : 0.f,
+                             (c0 + j + 2 < r) ? b * x[j + 2] : 0.f,
+                             (c0 + j + 3 < r) ? b * x[j + 3] : 0.f));
         }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = (c0 + j <= r) ? x[j] : 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) st_chunk8(sm + L::MM, 8192, r, c0 + j, x + j);
       }
     } else {
       // direct pairwise decays over the lower triangle
-      for (int p = tid; p < kC * (kC + 1) / 2; p += kThreads) {
-        int r = (int)((sqrtf(8.f * p + 1.f) - 1.f) * 0.5f);
-        while (r * (r + 1) / 2 > p) --r;
-        while ((r + 1) * (r + 2) / 2 <= p) ++r;
-        const int j = p - r * (r + 1) / 2;
+      for (int p2 = tid; p2 < kC * (kC + 1) / 2; p2 += kThreads) {
+        int r = (int)((sqrtf(8.f * p2 + 1.f) - 1.f) * 0.5f);
+        while (r * (r + 1) / 2 > p2) --r;
+        while ((r + 1) * (r + 2) / 2 <= p2) ++r;
+        const int j = p2 - r * (r + 1) / 2;
         float acc_a = 0.f, acc_m = 0.f;
         if (r < n) {
           for (int cc = 0; cc < kD; ++cc) {
@@ -434,13 +559,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             acc_m = fmaf(__bfloat162float(sQin[r * kD + cc]), w, acc_m);
           }
         }
-        sA[r * kC + j] = (j < r) ? sBeta[r] * acc_a : 0.f;
+        sA[f32x(r, j)] = (j < r) ? sBeta[r] * acc_a : 0.f;
         st_bf16(sm + L::MM, sw128_offset(r, j, 8192), acc_m);
       }
-      for (int p = tid; p < kC * kC; p += kThreads) {
-        const int r = p / kC, j = p % kC;
+      for (int p2 = tid; p2 < kC * kC; p2 += kThreads) {
+        const int r = p2 / kC, j = p2 % kC;
         if (j > r) {
-          sA[r * kC + j] = 0.f;
+          sA[f32x(r, j)] = 0.f;
           st_bf16(sm + L::MM, sw128_offset(r, j, 8192), 0.f);
         }
       }
@@ -470,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = e >> 3, j0 = (e & 7) * 8;
         float x[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) x[i] = sT32[r * kC + j0 + i] * sBeta[j0 + i];
+        for (int i = 0; i < 8; ++i) x[i] = sT32[f32x(r, j0 + i)] * sBeta[j0 + i];
         st_chunk8(sm + L::TT, 8192, r, j0, x);
       }
       fence_async_smem();
@@ -484,16 +609,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!wait_bar(bar_mma, ph_mma)) { failed = true; break; }
       if (tn < t1) issue_v(tn);  // V is consumed
-      {
+#pragma unroll
+      for (int c0 = wh * 64; c0 < wh * 64 + 64; c0 += 32) {
         float x[32];
-        const int r = warp * 16 + (lane & 15);
+        tmem_ld32(tm + lane_base + kColWO + c0, x);
+        if (m64ok) {
 #pragma unroll
-        for (int c0 = 0; c0 < kD; c0 += 32) {
-          tmem_ld32(tm + lane_base + kColWO + c0, x);
-          if (lane < 16) {
-#pragma unroll
-            for (int j = 0; j < 32; j += 8) st_chunk8(sm + L::WW, 8192, r, c0 + j, x + j);
-          }
+          for (int j = 0; j < 32; j += 8) st_chunk8(sm + L::WW, 8192, m64row, c0 + j, x + j);
         }
       }
       fence_async_smem();
@@ -508,9 +630,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!LINEAR) {
       // meanwhile: fade the state master, S <- Diag(gamma) S (lane = key channel)
-      const float gm = sGam[tid];
+      const float gm = sGam[lrow];
 #pragma unroll
-      for (int c0 = 0; c0 < DV; c0 += 32) {
+      for (int c0 = wh * DH; c0 < wh * DH + DH; c0 += 32) {
         float x[32];
         tmem_ld32(tm + lane_base + kColS + c0, x);
 #pragma unroll
@@ -521,14 +643,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!wait_bar(bar_mma, ph_mma)) { failed = true; break; }
     if (!LINEAR) {
-      float x[32];
-      const int r = warp * 16 + (lane & 15);
 #pragma unroll
-      for (int c0 = 0; c0 < DV; c0 += 32) {
+      for (int c0 = wh * DH; c0 < wh * DH + DH; c0 += 32) {
+        float x[32];
         tmem_ld32(tm + lane_base + kColU + c0, x);
-        if (lane < 16) {
+        if (m64ok) {
 #pragma unroll
-          for (int j = 0; j < 32; j += 8) st_chunk8(sm + L::UU, 8192, r, c0 + j, x + j);
+          for (int j = 0; j < 32; j += 8) st_chunk8(sm + L::UU, 8192, m64row, c0 + j, x + j);
         }
       }
       fence_async_smem();
@@ -545,31 +666,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!wait_bar(bar_mma, ph_mma)) { failed = true; break; }
     if (LINEAR && tn < t1) issue_v(tn);
     // O (M = 64 layout) -> out, rows < n
-    {
+#pragma unroll
+    for (int c0 = wh * DH; c0 < wh * DH + DH; c0 += 32) {
       float x[32];
-      const int r = warp * 16 + (lane & 15);
+      tmem_ld32(tm + lane_base + kColWO + c0, x);
+      if (m64ok && m64row < n) {
+        __nv_bfloat16* dst = out + ((size_t)(tc + m64row) * H + h) * kD + vc0 + c0;
 #pragma unroll
-      for (int c0 = 0; c0 < DV; c0 += 32) {
-        tmem_ld32(tm + lane_base + kColWO + c0, x);
-        if (lane < 16 && r < n) {
-          __nv_bfloat16* dst = out + ((size_t)(tc + r) * H + h) * kD + vc0 + c0;
+        for (int j = 0; j < 32; j += 8) {
+          __align__(16) __nv_bfloat162 hv[4];
 #pragma unroll
-          for (int j = 0; j < 32; j += 8) {
-            __align__(16) __nv_bfloat162 hv[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) hv[i] = __floats2bfloat162_rn(x[j + 2 * i], x[j + 2 * i + 1]);
-            *reinterpret_cast<uint4*>(dst + j) = *reinterpret_cast<const uint4*>(hv);
-          }
+          for (int i = 0; i < 4; ++i) hv[i] = __floats2bfloat162_rn(x[j + 2 * i], x[j + 2 * i + 1]);
+          *reinterpret_cast<uint4*>(dst + j) = *reinterpret_cast<const uint4*>(hv);
         }
       }
     }
     // new state -> bf16 S operand for the next chunk (lane = key channel)
 #pragma unroll
-    for (int c0 = 0; c0 < DV; c0 += 32) {
+    for (int c0 = wh * DH; c0 < wh * DH + DH; c0 += 32) {
       float x[32];
       tmem_ld32(tm + lane_base + kColS + c0, x);
 #pragma unroll
-      for (int j = 0; j < 32; j += 8) st_chunk8(sm + L::SS, 16384, tid, c0 + j, x + j);
+      for (int j = 0; j < 32; j += 8) st_chunk8(sm + L::SS, 16384, lrow, c0 + j, x + j);
     }
     fence_async_smem();
     cta_sync_tc();
@@ -582,9 +700,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (kAlphaTile) mbar_wait(bar_a, ph_a, kWaitNs);
     mbar_wait(bar_v, ph_v, kWaitNs);
   } else if (a.S_final) {
-    float* sf = a.S_final + sidx + (size_t)tid * kD + vc0;
+    float* sf = a.S_final + sidx + (size_t)lrow * kD + vc0;
 #pragma unroll
-    for (int c0 = 0; c0 < DV; c0 += 32) {
+    for (int c0 = wh * DH; c0 < wh * DH + DH; c0 += 32) {
       float x[32];
       tmem_ld32(tm + lane_base + kColS + c0, x);
 #pragma unroll
