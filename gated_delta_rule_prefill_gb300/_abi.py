@@ -15,7 +15,8 @@ GDR_DEVCHECK_OK, GDR_DEVCHECK_SEQLENS, GDR_DEVCHECK_TIMEOUT = 0, 1, 2
 
 # every symbol include/gdr.h declares
 EXPORTS = ("gdr_prefill", "gdr_prefill_workspace_size", "gdr_decode_step", "gdr_linear_attn",
-           "gdr_workspace_status", "gdr_status_string")
+           "gdr_workspace_status", "gdr_status_string", "gdr_prefill_noalloc")
+GDR_NOALLOC_MAX_SEQS = 4096
 
 
 class GdrShape(ctypes.Structure):
@@ -48,6 +49,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.gdr_prefill_workspace_size.restype = ctypes.c_size_t
     lib.gdr_workspace_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
     lib.gdr_workspace_status.restype = ctypes.c_int
+    lib.gdr_prefill_noalloc.argtypes = [S, P, P, P, P, P, P, P, P, P, P]
+    lib.gdr_prefill_noalloc.restype = ctypes.c_int
     lib.gdr_status_string.argtypes = [ctypes.c_int]
     lib.gdr_status_string.restype = ctypes.c_char_p
     _lib = lib

@@ -98,6 +98,15 @@ gdr_status prefill_common(const gdr_shape* sh, const void* q, const void* k, con
 }
 
 }  // namespace
+
+gdr_status prefill_launch(const gdr_shape* sh, const void* q, const void* k, const void* v,
+                          const float* alpha, const float* beta, const float* S0,
+                          const int32_t* cu, void* out, float* S_final, void* ws,
+                          size_t ws_bytes, void* stream) {
+  return prefill_common(sh, q, k, v, alpha, beta, S0, cu, out, S_final, ws, ws_bytes, stream,
+                        false);
+}
+
 }  // namespace gdr
 
 extern "C" {

@@ -73,6 +73,12 @@ __device__ __forceinline__ bool seq_range(const PrefillArgs& a, int seq, int64_t
   return true;
 }
 
+// gdr_prefill with an explicit workspace (validation, pre-pass and launch).
+gdr_status prefill_launch(const gdr_shape* sh, const void* q, const void* k, const void* v,
+                          const float* alpha, const float* beta, const float* S0,
+                          const int32_t* cu, void* out, float* S_final, void* ws,
+                          size_t ws_bytes, void* stream);
+
 // Host-side launchers (each returns cudaSuccess or the launch error).
 cudaError_t launch_prep(const PrefillArgs& a, int32_t* order, cudaStream_t s);
 cudaError_t launch_prefill_simt(const gdr_shape& sh, const PrefillArgs& a, bool linear,

@@ -136,6 +136,31 @@ gdr_status gdr_linear_attn(const gdr_shape* shape, const void* q, const void* k,
  */
 gdr_status gdr_workspace_status(void* workspace, void* stream, int32_t* code);
 
+/*
+ * gdr_prefill_noalloc -- gdr_prefill for callers that cannot provide a workspace.  (The pages
+ * have no counterpart: this is a property of the library interface, not of the method.)
+ *
+ * For callers whose device memory is fully budgeted (by a host framework's allocator or a
+ * static memory plan), so that they have no scratch buffer to pass and may not call cudaMalloc
+ * (which can also synchronise the device).  Arguments and results are those of gdr_prefill
+ * without the workspace; the call allocates and frees nothing.  Its scratch is a fixed array in
+ * the library's device memory, sized for at most GDR_NOALLOC_MAX_SEQS sequences (larger n_seqs
+ * returns GDR_ERR_UNSUPPORTED), held on every GPU that loads the library until the process
+ * exits.
+ *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress)
+ *     with that device current; make that first call before any stream capture.
+ *   - Every call shares the array and leaves its contents behind; each call rewrites what it
+ *     uses, but calls that overlap on the GPU (other streams, other host threads) race on it:
+ *     serialise them.
+ *   - The device-check word of this entry point is internal: cu_seqlens failures skip the
+ *     offending sequences but cannot be read back; validate cu_seqlens before the call.
+ */
+#define GDR_NOALLOC_MAX_SEQS 4096
+gdr_status gdr_prefill_noalloc(const gdr_shape* shape, const void* q, const void* k,
+                               const void* v, const float* alpha, const float* beta,
+                               const float* S0, const int32_t* cu_seqlens, void* out,
+                               float* S_final, void* stream);
+
 /* Static, human-readable name of a status. */
 const char* gdr_status_string(gdr_status status);
 
