@@ -74,7 +74,9 @@ struct TcSmem {
   static constexpr uint32_t ALPHA = BETA + 256;     // scalar gates [64]
   static constexpr uint32_t GAM = ALPHA + 256;      // gamma [128]
   static constexpr uint32_t RED = GAM + 512;        // reductions [8]
-  static constexpr uint32_t BARS = RED + 64;        // 4 mbarriers + TMEM slot
+  static constexpr uint32_t DIAG = RED + 64;        // q_r . k_r [64]
+  static constexpr uint32_t GS = DIAG + 256;        // scalar gates: log prefix sums [64]
+  static constexpr uint32_t BARS = GS + 256;        // 4 mbarriers + TMEM slot
   static constexpr uint32_t END = BARS + 64;
   static constexpr size_t bytes = END + 1024;       // + alignment slack
   // fp32 scratch of the solve, in tiles that are dead while it runs
@@ -228,6 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int NB = kD / DV;
   constexpr int DH = DV / 2;  // accumulator columns per warp half
   constexpr bool kAlphaTile = CHANNEL && !LINEAR;
+  constexpr bool kScalar = !CHANNEL && !LINEAR;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -243,6 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* sAlpha = reinterpret_cast<float*>(sm + L::ALPHA);
   float* sGam = reinterpret_cast<float*>(sm + L::GAM);
   float* sRed = reinterpret_cast<float*>(sm + L::RED);
+  float* sDiag = reinterpret_cast<float*>(sm + L::DIAG);
+  float* sGs = reinterpret_cast<float*>(sm + L::GS);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);
   uint64_t* bar_mma = bars + 0;
   uint64_t* bar_qk = bars + 1;
@@ -376,82 +381,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (kAlphaTile && !wait_bar(bar_a, ph_a)) { failed = true; break; }
 
     // ================= 1. gates and operand tiles
-    // thread = 8 key channels (group g8) x 4 tokens (row block rb): running products of the
-    // gates down its own rows, then the carry of the earlier row blocks through shared memory.
+    // thread = 8 key channels (group g8) x 4 tokens (row block rb)
     const int g8 = tid & 15, rb = tid >> 4;
-    float p[4][8];  // prefix products Gam[4 rb + rr][8 g8 + cc]
-    float gn[8];    // Gam_n (= gamma) of the 8 channels
-    {
-      float run[8];
+    bool safe = true;
+    if constexpr (kScalar) {
+      // Scalar gates: the pair decay e^(G_r - G_j) is a per-token factor, applied in fp32 after
+      // the Gram products of the raw (exact bf16) q and k; G = prefix sums of the clamped log
+      // gates, two tokens per lane of warp 0.
+      if (warp == 0) {
+        const int r0 = 2 * lane;
+        const float g0 = r0 < n ? log_gate(sAlpha[r0]) : 0.f;
+        const float g1 = r0 + 1 < n ? log_gate(sAlpha[r0 + 1]) : 0.f;
+        float sc = g0 + g1;
 #pragma unroll
-      for (int cc = 0; cc < 8; ++cc) run[cc] = 1.f;
-#pragma unroll
-      for (int rr = 0; rr < 4; ++rr) {
-        const int r = 4 * rb + rr;
-        float a8[8];
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) a8[cc] = 1.f;
-        if (!LINEAR && r < n) {
-          if (kAlphaTile) {
-            const float4 u0 = *reinterpret_cast<const float4*>(sAin + r * kD + 8 * g8);
-            const float4 u1 = *reinterpret_cast<const float4*>(sAin + r * kD + 8 * g8 + 4);
-            a8[0] = u0.x, a8[1] = u0.y, a8[2] = u0.z, a8[3] = u0.w;
-            a8[4] = u1.x, a8[5] = u1.y, a8[6] = u1.z, a8[7] = u1.w;
-          } else {
-#pragma unroll
-            for (int cc = 0; cc < 8; ++cc) a8[cc] = sAlpha[r];
-          }
+        for (int off = 1; off < 32; off <<= 1) {
+          const float t = __shfl_up_sync(0xffffffffu, sc, off);
+          if (lane >= off) sc += t;
         }
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          run[cc] *= a8[cc];
-          p[rr][cc] = run[cc];
-        }
+        sGs[r0] = sc - g1;
+        sGs[r0 + 1] = sc;
       }
-      float* sTot = reinterpret_cast<float*>(sm + L::WW);  // [16 row blocks][128 channels]
-      *reinterpret_cast<float4*>(sTot + rb * kD + 8 * g8) = make_float4(run[0], run[1], run[2], run[3]);
-      *reinterpret_cast<float4*>(sTot + rb * kD + 8 * g8 + 4) = make_float4(run[4], run[5], run[6], run[7]);
       __syncthreads();
-      float carry[8];
-#pragma unroll
-      for (int cc = 0; cc < 8; ++cc) carry[cc] = gn[cc] = 1.f;
-#pragma unroll
-      for (int b2 = 0; b2 < 16; ++b2) {
-        const float4 u0 = *reinterpret_cast<const float4*>(sTot + b2 * kD + 8 * g8);
-        const float4 u1 = *reinterpret_cast<const float4*>(sTot + b2 * kD + 8 * g8 + 4);
-        const float t8[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          if (b2 < rb) carry[cc] *= t8[cc];
-          gn[cc] *= t8[cc];
-        }
-      }
-#pragma unroll
-      for (int rr = 0; rr < 4; ++rr)
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) p[rr][cc] *= carry[cc];
-    }
-    float mn = gn[0];
-#pragma unroll
-    for (int cc = 1; cc < 8; ++cc) mn = fminf(mn, gn[cc]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
-    if (lane == 0) sRed[warp] = mn;
-    if (!LINEAR && rb == 0) {
-      *reinterpret_cast<float4*>(sGam + 8 * g8) = make_float4(gn[0], gn[1], gn[2], gn[3]);
-      *reinterpret_cast<float4*>(sGam + 8 * g8 + 4) = make_float4(gn[4], gn[5], gn[6], gn[7]);
-    }
-    __syncthreads();
-    float mall = sRed[0];
-#pragma unroll
-    for (int w = 1; w < kThreads / 32; ++w) mall = fminf(mall, sRed[w]);
-    const bool safe = LINEAR || mall > kSafeGamma;
-
-    if (safe) {
+      const float Gn = sGs[kC - 1];
 #pragma unroll
       for (int rr = 0; rr < 4; ++rr) {
         const int r = 4 * rb + rr;
-        float k8[8], q8[8];
+        float k8[8], q8[8], kh[8];
         if (r < n) {
           ld_bf16x8(sKin + r * kD + 8 * g8, k8);
           ld_bf16x8(sQin + r * kD + 8 * g8, q8);
@@ -459,52 +414,151 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int cc = 0; cc < 8; ++cc) k8[cc] = q8[cc] = 0.f;
         }
-        float ke[8], qe[8], ki[8], kh[8];
+        const float eh = __expf(Gn - sGs[r]);
+        float dq = 0.f;
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) {
-          const float G = p[rr][cc];
-          const float inv = LINEAR ? 1.f : __fdividef(1.f, G);
-          ke[cc] = k8[cc] * G;
-          qe[cc] = q8[cc] * G;
-          ki[cc] = k8[cc] * inv;
-          kh[cc] = ki[cc] * gn[cc];
+          kh[cc] = k8[cc] * eh;
+          dq = fmaf(q8[cc], k8[cc], dq);
         }
-        st_chunk8(sm + L::KQ, 16384, r, 8 * g8, ke);       // K~
-        st_chunk8(sm + L::KQ, 16384, 64 + r, 8 * g8, qe);  // Q~
-        st_chunk8(sm + L::KR, 8192, r, 8 * g8, ki);        // Kr
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) dq += __shfl_xor_sync(0xffffffffu, dq, off);
+        if (g8 == 0) sDiag[r] = dq;
+        st_chunk8(sm + L::KQ, 16384, r, 8 * g8, k8);       // K (scaled to K~ after the Gram MMA)
+        st_chunk8(sm + L::KQ, 16384, 64 + r, 8 * g8, q8);  // Q (scaled to Q~ likewise)
+        st_chunk8(sm + L::KR, 8192, r, 8 * g8, k8);        // K
         st_chunk8(sm + L::KH, 8192, r, 8 * g8, kh);        // K^
       }
-    } else if (tid < kD) {
-      // strong decay: log-gate prefix sums in place of the staged gates (thread = channel)
-      const int c = tid;
-      float G = 0.f;
-#pragma unroll 4
-      for (int r = 0; r < kC; ++r) {
-        if (r < n) G += log_gate(kAlphaTile ? sAin[r * kD + c] : sAlpha[r]);
-        if (kAlphaTile) sAin[r * kD + c] = G;
+      if (rb == 0) {
+        const float gm = __expf(Gn);
+        *reinterpret_cast<float4*>(sGam + 8 * g8) = make_float4(gm, gm, gm, gm);
+        *reinterpret_cast<float4*>(sGam + 8 * g8 + 4) = make_float4(gm, gm, gm, gm);
       }
-      const float Gn = G;
-      G = 0.f;
-#pragma unroll 4
-      for (int r = 0; r < kC; ++r) {
-        const bool ok = r < n;
-        const float kv = ok ? __bfloat162float(sKin[r * kD + c]) : 0.f;
-        const float qv = ok ? __bfloat162float(sQin[r * kD + c]) : 0.f;
-        if (kAlphaTile) G = sAin[r * kD + c];
-        else if (ok) G += log_gate(sAlpha[r]);
-        const float e = __expf(G);
-        st_bf16(sm + L::KQ, sw128_offset(r, c, 16384), kv * e);
-        st_bf16(sm + L::KQ, sw128_offset(64 + r, c, 16384), qv * e);
-        st_bf16(sm + L::KH, sw128_offset(r, c, 8192), kv * __expf(Gn - G));
+    } else {
+      // Per-channel gates (and linear attention): running products of the gates down the
+      // thread's rows, then the carry of the earlier row blocks through shared memory.
+      float p[4][8];  // prefix products Gam[4 rb + rr][8 g8 + cc]
+      float gn[8];    // Gam_n (= gamma) of the 8 channels
+      {
+        float run[8];
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) run[cc] = 1.f;
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+          const int r = 4 * rb + rr;
+          float a8[8];
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) a8[cc] = 1.f;
+          if (!LINEAR && r < n) {
+            const float4 u0 = *reinterpret_cast<const float4*>(sAin + r * kD + 8 * g8);
+            const float4 u1 = *reinterpret_cast<const float4*>(sAin + r * kD + 8 * g8 + 4);
+            a8[0] = u0.x, a8[1] = u0.y, a8[2] = u0.z, a8[3] = u0.w;
+            a8[4] = u1.x, a8[5] = u1.y, a8[6] = u1.z, a8[7] = u1.w;
+          }
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) {
+            run[cc] *= a8[cc];
+            p[rr][cc] = run[cc];
+          }
+        }
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) gn[cc] = 1.f;
+        if (!LINEAR) {
+          float* sTot = reinterpret_cast<float*>(sm + L::WW);  // [16 row blocks][128 channels]
+          *reinterpret_cast<float4*>(sTot + rb * kD + 8 * g8) = make_float4(run[0], run[1], run[2], run[3]);
+          *reinterpret_cast<float4*>(sTot + rb * kD + 8 * g8 + 4) = make_float4(run[4], run[5], run[6], run[7]);
+          __syncthreads();
+          float carry[8];
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) carry[cc] = 1.f;
+#pragma unroll
+          for (int b2 = 0; b2 < 16; ++b2) {
+            const float4 u0 = *reinterpret_cast<const float4*>(sTot + b2 * kD + 8 * g8);
+            const float4 u1 = *reinterpret_cast<const float4*>(sTot + b2 * kD + 8 * g8 + 4);
+            const float t8[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) {
+              if (b2 < rb) carry[cc] *= t8[cc];
+              gn[cc] *= t8[cc];
+            }
+          }
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) p[rr][cc] *= carry[cc];
+        }
       }
-    }
-    if (!safe && !kAlphaTile) {  // scalar gates: per-token prefix sums for the pair decays
-      __syncthreads();
-      if (tid == 0) {
-        float g = 0.f;
+      if (!LINEAR) {
+        float mn = gn[0];
+#pragma unroll
+        for (int cc = 1; cc < 8; ++cc) mn = fminf(mn, gn[cc]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+        if (lane == 0) sRed[warp] = mn;
+        if (rb == 0) {
+          *reinterpret_cast<float4*>(sGam + 8 * g8) = make_float4(gn[0], gn[1], gn[2], gn[3]);
+          *reinterpret_cast<float4*>(sGam + 8 * g8 + 4) = make_float4(gn[4], gn[5], gn[6], gn[7]);
+        }
+        __syncthreads();
+        float mall = sRed[0];
+#pragma unroll
+        for (int w = 1; w < kThreads / 32; ++w) mall = fminf(mall, sRed[w]);
+        safe = mall > kSafeGamma;
+      }
+
+      if (safe) {
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+          const int r = 4 * rb + rr;
+          float k8[8], q8[8];
+          if (r < n) {
+            ld_bf16x8(sKin + r * kD + 8 * g8, k8);
+            ld_bf16x8(sQin + r * kD + 8 * g8, q8);
+          } else {
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) k8[cc] = q8[cc] = 0.f;
+          }
+          float ke[8], qe[8], ki[8], kh[8], dq = 0.f;
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) {
+            const float G = p[rr][cc];
+            const float inv = LINEAR ? 1.f : __fdividef(1.f, G);
+            ke[cc] = k8[cc] * G;
+            qe[cc] = q8[cc] * G;
+            ki[cc] = k8[cc] * inv;
+            kh[cc] = ki[cc] * gn[cc];
+            dq = fmaf(q8[cc], k8[cc], dq);
+          }
+          if (!LINEAR) {  // the diagonal of M carries no decay: q_r . k_r in fp32
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) dq += __shfl_xor_sync(0xffffffffu, dq, off);
+            if (g8 == 0) sDiag[r] = dq;
+          }
+          st_chunk8(sm + L::KQ, 16384, r, 8 * g8, ke);       // K~
+          st_chunk8(sm + L::KQ, 16384, 64 + r, 8 * g8, qe);  // Q~
+          st_chunk8(sm + L::KR, 8192, r, 8 * g8, ki);        // Kr
+          st_chunk8(sm + L::KH, 8192, r, 8 * g8, kh);        // K^
+        }
+      } else if (tid < kD) {
+        // strong decay: log-gate prefix sums in place of the staged gates (thread = channel)
+        const int c = tid;
+        float G = 0.f;
+#pragma unroll 4
         for (int r = 0; r < kC; ++r) {
-          if (r < n) g += log_gate(sAlpha[r]);
-          sAlpha[r] = g;
+          if (r < n) G += log_gate(sAin[r * kD + c]);
+          sAin[r * kD + c] = G;
+        }
+        const float Gn = G;
+#pragma unroll 4
+        for (int r = 0; r < kC; ++r) {
+          const bool ok = r < n;
+          const float kv = ok ? __bfloat162float(sKin[r * kD + c]) : 0.f;
+          const float qv = ok ? __bfloat162float(sQin[r * kD + c]) : 0.f;
+          G = sAin[r * kD + c];
+          const float e = __expf(G);
+          st_bf16(sm + L::KQ, sw128_offset(r, c, 16384), kv * e);
+          st_bf16(sm + L::KQ, sw128_offset(64 + r, c, 16384), qv * e);
+          st_bf16(sm + L::KH, sw128_offset(r, c, 8192), kv * __expf(Gn - G));
         }
       }
     }
@@ -526,6 +580,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int c0 = 32 * wh;
       float x[32];
       tmem_ld32(tm + lane_base + kColAM + c0, x);
+      if constexpr (kScalar) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          x[j] = (c0 + j <= r) ? x[j] * __expf(sGs[r] - sGs[c0 + j]) : 0.f;
+      }
       if (lrow < 64) {
         if (!LINEAR) {
           const float b = sBeta[r];
@@ -538,12 +597,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = (c0 + j <= r) ? x[j] : 0.f;
+        for (int j = 0; j < 32; ++j) {
+          x[j] = (c0 + j <= r) ? x[j] : 0.f;
+          if (!LINEAR && c0 + j == r) x[j] = sDiag[r];
+        }
 #pragma unroll
         for (int j = 0; j < 32; j += 8) st_chunk8(sm + L::MM, 8192, r, c0 + j, x + j);
       }
+      if constexpr (kScalar) {
+        // the raw K and Q rows of the Gram operand become K~ = K e^G and Q~ = Q e^G in place
+        __syncthreads();
+        for (int e = tid; e < 2 * 128 * 8; e += kThreads) {
+          const int slab = e >> 10, row = (e >> 3) & 127, ch = e & 7;
+          uint4* pch = reinterpret_cast<uint4*>(sm + L::KQ + slab * 16384 + row * 128 + ch * 16);
+          const float f = __expf(sGs[row & 63]);
+          uint4 u = *pch;
+          __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 v2 = __bfloat1622float2(hv[i]);
+            hv[i] = __floats2bfloat162_rn(v2.x * f, v2.y * f);
+          }
+          *pch = u;
+        }
+        fence_async_smem();
+      }
     } else {
-      // direct pairwise decays over the lower triangle
+      // direct pairwise decays over the lower triangle (per-channel gates only)
       for (int p2 = tid; p2 < kC * (kC + 1) / 2; p2 += kThreads) {
         int r = (int)((sqrtf(8.f * p2 + 1.f) - 1.f) * 0.5f);
         while (r * (r + 1) / 2 > p2) --r;
@@ -552,9 +632,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float acc_a = 0.f, acc_m = 0.f;
         if (r < n) {
           for (int cc = 0; cc < kD; ++cc) {
-            const float dg = kAlphaTile ? sAin[r * kD + cc] - sAin[j * kD + cc]
-                                        : sAlpha[r] - sAlpha[j];
-            const float w = __bfloat162float(sKin[j * kD + cc]) * __expf(dg);
+            const float w = __bfloat162float(sKin[j * kD + cc]) *
+                            __expf(sAin[r * kD + cc] - sAin[j * kD + cc]);
             acc_a = fmaf(__bfloat162float(sKin[r * kD + cc]), w, acc_a);
             acc_m = fmaf(__bfloat162float(sQin[r * kD + cc]), w, acc_m);
           }

@@ -1,0 +1,140 @@
+"""GPU parity at the full sizes of the five named workloads (the launch configurations the
+benchmark uses), against the CPU oracle.  Small workloads are compared on every output; the
+0.65M-token varlen workload is compared on a seeded sample of (sequence, head) pairs that covers
+every sequence (including the longest), regenerated on the host from the same per-block streams.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gdr_inputs as gi
+import oracle
+from tests.parity import TOL, dev_inputs, host, rel_rows, rel_states, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def _prefill(d, linear=False):
+    import gated_delta_rule_prefill_gb300 as g
+    if linear:
+        out, Sf = g.gdr_linear_attn(d["q"], d["k"], d["v"], S0=d["S0"],
+                                    cu_seqlens=d["cu_seqlens"])
+    else:
+        out, Sf = g.gdr_prefill(d["q"], d["k"], d["v"], d["alpha"], d["beta"], S0=d["S0"],
+                                cu_seqlens=d["cu_seqlens"])
+    torch.cuda.synchronize()
+    return out, Sf
+
+
+def _check(name, got_o, got_s, ref_o, ref_s, tol):
+    eo, es = rel_rows(got_o, ref_o), rel_states(got_s, ref_s)
+    print("%s: output err %.3g, state err %.3g" % (name, eo, es))
+    assert eo <= tol and es <= tol, (name, eo, es)
+
+
+@pytest.mark.parametrize("name", ["kda_t256_d64_f32", "gdn_b4_h16_t4096", "kda_b1_h32_t32768"])
+def test_prefill_full(name):
+    wl = gi.workload(name)
+    a = gi.gen_full(wl, threads=16)
+    d = dev_inputs(a, wl.dtype)
+    out, Sf = _prefill(d)
+    ro, rs = oracle.gated_delta(a["q"], a["k"], a["v"], a["alpha"], a["beta"], S0=a["S0"],
+                                cu_seqlens=a["cu_seqlens"])
+    _check(name, host(out), host(Sf), ro, rs, TOL[wl.dtype])
+
+
+def test_decode_full_size():
+    """256 sequences x 32 heads, d = 128 (the benchmark's decode launch), three steps from a
+    seeded fp32 state, every output and state compared."""
+    import gated_delta_rule_prefill_gb300 as g
+    wl = gi.workload("decode_n256_h32")
+    S = gi.random_state(1003, wl.n_seqs, wl.H, wl.d_k, wl.d_v, std=0.3)
+    S_dev = torch.from_numpy(S).cuda()
+    S_ref = S.astype(np.float64)
+    for step in range(3):
+        x = gi.gen_decode_step(wl, step)
+        out = g.gdr_decode_step(to_dev(x["q"], "bf16"), to_dev(x["k"], "bf16"),
+                                to_dev(x["v"], "bf16"), to_dev(x["alpha"], "f32"),
+                                to_dev(x["beta"], "f32"), S_dev)
+        ro, S_ref = oracle.decode_step(x["q"], x["k"], x["v"], x["alpha"], x["beta"], S_ref)
+        torch.cuda.synchronize()
+        _check("decode step %d" % step, host(out), host(S_dev), ro, S_ref, TOL["bf16"])
+
+
+def test_decode_after_2048_token_prefill():
+    """The serving pipeline of the decode workload on 8 of its 256 sequences (all 32 heads):
+    a 2048-token prefill from S0 = 0, then decode steps, each against the oracle run from
+    scratch on the same inputs."""
+    import gated_delta_rule_prefill_gb300 as g
+    wl = gi.workload("decode_n256_h32")
+    seqs = [0, 37, 101, 255, 128, 7, 64, 200]
+    a = gi.gen_full(wl, seqs=seqs, threads=16)
+    d = dev_inputs(a, "bf16")
+    _, S = _prefill(d)
+    _, S_ref = oracle.gated_delta(a["q"], a["k"], a["v"], a["alpha"], a["beta"], S0=None,
+                                  cu_seqlens=a["cu_seqlens"])
+    es = rel_states(host(S), S_ref)
+    print("2048-token prefill states: err %.3g" % es)
+    assert es <= TOL["bf16"], es
+    for step in range(2):
+        x = gi.gen_decode_step(wl, step)
+        xs = {k: v[seqs] for k, v in x.items()}
+        out = g.gdr_decode_step(to_dev(xs["q"], "bf16"), to_dev(xs["k"], "bf16"),
+                                to_dev(xs["v"], "bf16"), to_dev(xs["alpha"], "f32"),
+                                to_dev(xs["beta"], "f32"), S)
+        ro, S_ref = oracle.decode_step(xs["q"], xs["k"], xs["v"], xs["alpha"], xs["beta"], S_ref)
+        torch.cuda.synchronize()
+        _check("decode %d after prefill" % step, host(out), host(S), ro, S_ref, TOL["bf16"])
+
+
+def test_varlen_full_sampled():
+    """64 sequences (about 0.65M tokens) x 16 heads, packed with cu_seqlens, per-sequence S0:
+    the gated rule and the linear-attention pass over the same inputs, on the GPU at full size;
+    one head of every sequence (64 pairs) checked against the oracle."""
+    wl = gi.workload("varlen_n64_h16")
+    T, H, d = wl.total_tokens, wl.H, wl.d_k
+    dev = {"q": torch.empty((T, H, d), dtype=torch.bfloat16, device="cuda"),
+           "k": torch.empty((T, H, d), dtype=torch.bfloat16, device="cuda"),
+           "v": torch.empty((T, H, d), dtype=torch.bfloat16, device="cuda"),
+           "alpha": torch.empty((T, H, d), dtype=torch.float32, device="cuda"),
+           "beta": torch.empty((T, H), dtype=torch.float32, device="cuda"),
+           "S0": torch.empty((wl.n_seqs, H, d, d), dtype=torch.float32, device="cuda")}
+    for h0 in range(0, H, 2):  # two heads at a time keeps host memory small
+        part = gi.gen_full(wl, heads=[h0, h0 + 1], threads=16)
+        for name in ("q", "k", "v"):
+            dev[name][:, h0:h0 + 2] = to_dev(part[name], "bf16")
+        dev["alpha"][:, h0:h0 + 2] = to_dev(part["alpha"], "f32")
+        dev["beta"][:, h0:h0 + 2] = to_dev(part["beta"], "f32")
+        dev["S0"][:, h0:h0 + 2] = to_dev(part["S0"], "f32")
+        del part
+    dev["cu_seqlens"] = torch.from_numpy(wl.cu_seqlens.astype(np.int32)).cuda()
+    out, Sf = _prefill(dev)
+    lout, lSf = _prefill(dev, linear=True)
+    cu = wl.cu_seqlens
+    got = {"o": [], "s": [], "lo": [], "ls": []}
+    ref = {"o": [], "s": [], "lo": [], "ls": []}
+    for n in range(wl.n_seqs):
+        h = (7 * n) % H
+        a = gi.gen_full(wl, heads=[h], seqs=[n], threads=4)
+        ro, rs = oracle.gated_delta(a["q"], a["k"], a["v"], a["alpha"], a["beta"], S0=a["S0"],
+                                    cu_seqlens=a["cu_seqlens"])
+        lo, ls = oracle.linear_attn(a["q"], a["k"], a["v"], S0=a["S0"], cu_seqlens=a["cu_seqlens"])
+        got["o"].append(host(out[cu[n]:cu[n + 1], h]))
+        got["s"].append(host(Sf[n, h]))
+        got["lo"].append(host(lout[cu[n]:cu[n + 1], h]))
+        got["ls"].append(host(lSf[n, h]))
+        ref["o"].append(ro[:, 0])
+        ref["s"].append(rs[0, 0])
+        ref["lo"].append(lo[:, 0])
+        ref["ls"].append(ls[0, 0])
+    cat = lambda xs: np.concatenate([x.reshape(-1, x.shape[-1]) for x in xs])  # noqa: E731
+    _check("varlen gated (64 pairs)", cat(got["o"]), np.stack(got["s"]), cat(ref["o"]),
+           np.stack(ref["s"]), TOL["bf16"])
+    _check("varlen linear (64 pairs)", cat(got["lo"]), np.stack(got["ls"]), cat(ref["lo"]),
+           np.stack(ref["ls"]), TOL["bf16"])
