@@ -85,9 +85,9 @@ def source_digest(files):
     return h.hexdigest()[:16]
 
 
-KERNEL_SOURCES = {"prefill": ["prefill_simt.cu", "api.cu", "gdr_internal.cuh"],
-                  "linear_attn": ["prefill_simt.cu", "api.cu", "gdr_internal.cuh"],
-                  "decode": ["decode.cu", "gdr_internal.cuh"]}
+KERNEL_SOURCES = {"prefill": ["prefill_tc.cu", "umma.cuh"],
+                  "linear_attn": ["prefill_tc.cu", "umma.cuh"],
+                  "decode": ["decode.cu"]}
 
 
 def ncu_traffic(kernel):
