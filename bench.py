@@ -103,6 +103,25 @@ def ncu_traffic(kernel):
 
 
 # ----------------------------------------------------------------------------------------------
+# ranks: every rank runs its own replica of the workload (independent problems, weak scaling);
+# the only cross-rank traffic is this max-reduction of the timings and the barriers around them
+# ----------------------------------------------------------------------------------------------
+def max_over_ranks(values, device, world):
+    """Element-wise maximum of per-rank float timings (no-op for one rank)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, device=device, dtype=torch.float64)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_tokens_per_s(world, tokens_per_rank, seconds_max):
+    """Whole-job throughput: the tokens all ranks processed over the slowest rank's time."""
+    return world * tokens_per_rank / seconds_max
+
+
+# ----------------------------------------------------------------------------------------------
 # clocks during the timed region
 # ----------------------------------------------------------------------------------------------
 class ClockSampler:
@@ -306,11 +325,8 @@ def run_gpu(args):
     pre_ms = [e[0].elapsed_time(e[1]) for e in evs]
     lin_ms = [e[1].elapsed_time(e[2]) for e in evs]
     dec_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    tm = torch.tensor([total_ms, sum(pre_ms), sum(lin_ms), sum(dec_ms)], device=dev,
-                      dtype=torch.float64)
-    if world > 1:
-        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
-    total_ms, pre_tot, lin_tot, dec_tot = tm.tolist()
+    total_ms, pre_tot, lin_tot, dec_tot = max_over_ranks(
+        [total_ms, sum(pre_ms), sum(lin_ms), sum(dec_ms)], dev, world)
 
     # ---- end to end through the public API with host buffers (prefill), rank-local
     host_in = {k: P[k].cpu().pin_memory() for k in ("q", "k", "v", "alpha", "beta", "S0")}
@@ -339,11 +355,9 @@ def run_gpu(args):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = torch.tensor([e0.elapsed_time(e1) / e2e_steps], device=dev, dtype=torch.float64)
+    e2e_ms = max_over_ranks([e0.elapsed_time(e1) / e2e_steps], dev, world)[0]
     if world > 1:
-        dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
         dist.barrier()
-    e2e_ms = e2e_ms.item()
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = host_out.numel() * host_out.element_size() + host_sf.numel() * host_sf.element_size()
 
@@ -356,9 +370,9 @@ def run_gpu(args):
     K = args.steps
     pre_s, lin_s, dec_s = pre_tot / K / 1e3, lin_tot / K / 1e3, dec_tot / K / 1e3
     n = world
-    prefill_tps = n * T / pre_s
-    decode_tps = n * wd.n_seqs / dec_s
-    linear_tps = n * T / lin_s
+    prefill_tps = job_tokens_per_s(n, T, pre_s)
+    decode_tps = job_tokens_per_s(n, wd.n_seqs, dec_s)
+    linear_tps = job_tokens_per_s(n, T, lin_s)
 
     def roof(name, bytes_, flops, secs):
         gbs = bytes_ / secs / 1e9
@@ -398,7 +412,7 @@ def run_gpu(args):
         "linear_attn_tokens_per_s": linear_tps,
         "roofline": main_roof,
         "kernels": kern,
-        "e2e": {"value": n * T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_tokens_per_s(n, T, e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "what": "gdr_prefill with pinned host inputs copied "
                 "in and out/S_final copied back, per step"},
         "gpu_launches": 5 * K,

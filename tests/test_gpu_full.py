@@ -1,6 +1,6 @@
 """GPU parity at the full sizes of the five named workloads (the launch configurations the
 benchmark uses), against the CPU oracle.  Small workloads are compared on every output; the
-0.65M-token varlen workload is compared on a seeded sample of (sequence, head) pairs that covers
+0.46M-token varlen workload is compared on a seeded sample of (sequence, head) pairs that covers
 every sequence (including the longest), regenerated on the host from the same per-block streams.
 """
 import numpy as np
@@ -94,7 +94,7 @@ def test_decode_after_2048_token_prefill():
 
 
 def test_varlen_full_sampled():
-    """64 sequences (about 0.65M tokens) x 16 heads, packed with cu_seqlens, per-sequence S0:
+    """64 sequences (about 0.46M tokens) x 16 heads, packed with cu_seqlens, per-sequence S0:
     the gated rule and the linear-attention pass over the same inputs, on the GPU at full size;
     one head of every sequence (64 pairs) checked against the oracle."""
     wl = gi.workload("varlen_n64_h16")
