@@ -16,7 +16,8 @@ import ctypes
 import torch
 
 from . import _abi
-from ._abi import (GDR_BF16, GDR_F32, GDR_FLAG_FORCE_SIMT, GDR_GATE_CHANNEL, GDR_GATE_SCALAR,
+from ._abi import (GDR_BF16, GDR_F32, GDR_FLAG_FORCE_SIMT, GDR_FLAG_NO_CLUSTER,
+                   GDR_GATE_CHANNEL, GDR_GATE_SCALAR,
                    GdrError, GdrShape)
 
 __all__ = ["gdr_prefill", "gdr_decode_step", "gdr_linear_attn", "gdr_prefill_workspace_size",
@@ -63,7 +64,7 @@ def _workspace(n_seqs, device, workspace):
 
 
 def _prefill_like(linear, q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, workspace,
-                  chunk_size, force_simt, stream, want_final):
+                  chunk_size, force_simt, stream, want_final, no_cluster=False):
     T, H, dk = q.shape
     dv = v.shape[2]
     dtype = _DT.get(q.dtype)
@@ -86,8 +87,8 @@ def _prefill_like(linear, q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, wo
         S_final = torch.empty((n_seqs, H, dk, dv), dtype=torch.float32, device=q.device)
     _check(S_final, "S_final", torch.float32)
     ws = _workspace(n_seqs, q.device, workspace)
-    sh = make_shape(n_seqs, H, T, dk, dv, dtype, gate, chunk_size,
-                    GDR_FLAG_FORCE_SIMT if force_simt else 0)
+    flags = (GDR_FLAG_FORCE_SIMT if force_simt else 0) | (GDR_FLAG_NO_CLUSTER if no_cluster else 0)
+    sh = make_shape(n_seqs, H, T, dk, dv, dtype, gate, chunk_size, flags)
     lib = _abi.load()
     if linear:
         rc = lib.gdr_linear_attn(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(S0),
@@ -103,12 +104,13 @@ def _prefill_like(linear, q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, wo
 
 
 def gdr_prefill(q, k, v, alpha, beta, S0=None, cu_seqlens=None, out=None, S_final=None,
-                workspace=None, chunk_size=0, force_simt=False, stream=None, want_final=True):
+                workspace=None, chunk_size=0, force_simt=False, stream=None, want_final=True,
+                no_cluster=False):
     """Chunked packed-varlen prefill.  q,k [T,H,d_k], v [T,H,d_v] (fp32 or bf16); alpha
     [T,H,d_k] or [T,H] fp32; beta [T,H] fp32; S0 [N,H,d_k,d_v] fp32 or None; cu_seqlens int32
     [N+1] or None.  Returns (out [T,H,d_v], S_final [N,H,d_k,d_v] or None)."""
     return _prefill_like(False, q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, workspace,
-                         chunk_size, force_simt, stream, want_final)
+                         chunk_size, force_simt, stream, want_final, no_cluster)
 
 
 def gdr_linear_attn(q, k, v, S0=None, cu_seqlens=None, out=None, S_final=None, workspace=None,

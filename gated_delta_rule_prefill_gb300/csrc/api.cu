@@ -58,7 +58,7 @@ gdr_status check_shape(const gdr_shape* sh, bool need_gate) {
   if (sh->dtype != GDR_F32 && sh->dtype != GDR_BF16) return GDR_ERR_INVALID_ARG;
   if (need_gate && sh->gate != GDR_GATE_SCALAR && sh->gate != GDR_GATE_CHANNEL)
     return GDR_ERR_INVALID_ARG;
-  if (sh->chunk_size < 0 || (sh->flags & ~GDR_FLAG_FORCE_SIMT)) return GDR_ERR_INVALID_ARG;
+  if (sh->chunk_size < 0 || (sh->flags & ~(GDR_FLAG_FORCE_SIMT | GDR_FLAG_NO_CLUSTER))) return GDR_ERR_INVALID_ARG;
   if (sh->d_k != sh->d_v || (sh->d_k != 64 && sh->d_k != 128)) return GDR_ERR_UNSUPPORTED;
   // grid sizes stay within 32-bit block counts
   if ((int64_t)sh->n_seqs * sh->H * 4 > (int64_t)INT32_MAX) return GDR_ERR_UNSUPPORTED;

@@ -1,15 +1,437 @@
-// prefill_cluster.cu -- thread-block-cluster variant of the tensor-core prefill (not yet enabled:
-// every workload runs the fused kernel of prefill_tc.cu).
+// prefill_cluster.cu -- the tensor-core prefill for workloads with few (sequence, head) chains,
+// as thread-block clusters of 1 + NH CTAs per chain.
+//
+// The chunk recurrence of a chain is sequential, but most of a chunk's work does not depend on
+// the state: the gate prologue, the decay-weighted Gram matrices, the triangular solve and
+// W = T' K~ (stages 1-4 of prefill_tc.cu).  In a cluster, CTA 0 (the chain CTA) runs only the
+// state pass of every chunk (U = T' V - W S, O = Q~ S + M U, S <- gamma S + K^^T U), while the NH
+// helper CTAs prepare the chunks round-robin (helper h takes chunks c with c mod NH = h) and copy
+// the operands the state pass needs -- Q~, K^, W, M, T' (bf16) and gamma -- into one of two slots
+// in the chain CTA's shared memory with bulk copies over distributed shared memory.  The copies
+// complete on the slot's mbarrier in the chain CTA; after consuming a slot the chain CTA re-arms
+// it and publishes its count of consumed chunks into every helper's shared memory, which a
+// helper waits on before it overwrites a slot.  Every wait is bounded; a timeout records
+// GDR_DEVCHECK_TIMEOUT and the CTA unwinds to the closing cluster barrier.
+#include <cuda.h>
+
+#include <atomic>
+#include <mutex>
+
 #include "tc_common.cuh"
 
 namespace gdr {
 namespace tc {
+namespace {
 
-int cluster_size_for(const gdr_shape&) { return 1; }
+using namespace umma;
 
-cudaError_t launch_prefill_cluster(const gdr_shape&, const PrefillArgs&, const TcMaps&, int,
-                                   cudaStream_t) {
-  return cudaErrorNotSupported;
+// slot layout (bytes from the slot base)
+constexpr uint32_t kSlotQ = 0;        // Q~  [64][128] K-major, slabs 8 KB apart
+constexpr uint32_t kSlotKH = 16384;   // K^  [tok][ch] (MN-major A), slabs 8 KB apart
+constexpr uint32_t kSlotW = 32768;    // W   [64][128] K-major, slabs 8 KB apart
+constexpr uint32_t kSlotM = 49152;    // M   [64][64] K-major
+constexpr uint32_t kSlotT = 57344;    // T'  [64][64] K-major
+constexpr uint32_t kSlotGam = 65536;  // gamma [128] fp32
+constexpr uint32_t kSlotPayload = 65536 + 512;
+constexpr uint32_t kSlotBytes = 66560;  // 1024-aligned
+
+struct ChainSmem {
+  static constexpr uint32_t SLOT = 0;                      // 2 slots
+  static constexpr uint32_t VIN = 2 * kSlotBytes;          // V [64 tok][128] SW128, 2 slabs
+  static constexpr uint32_t UU = VIN + 16384;              // U [tok][128] (MN-major B)
+  static constexpr uint32_t SS = UU + 16384;               // S [d_k][128] (MN-major B)
+  static constexpr uint32_t BARS = SS + 32768;             // full[2], v, mma, TMEM slot
+  static constexpr uint32_t END = BARS + 64;
+};
+
+struct HelperSmem {
+  static constexpr uint32_t QIN = 0;              // [64][128] bf16 row-major
+  static constexpr uint32_t KIN = QIN + 16384;
+  static constexpr uint32_t AIN = KIN + 16384;    // [64][128] fp32 row-major
+  static constexpr uint32_t KQ = AIN + 32768;     // [K~ ; Q~] 128 x 128 K-major
+  static constexpr uint32_t KR = KQ + 32768;      // Kr 64 x 128
+  static constexpr uint32_t KH = KR + 16384;      // K^ [tok][ch]
+  static constexpr uint32_t TT = KH + 16384;      // T' 64 x 64
+  static constexpr uint32_t MM = TT + 8192;       // M 64 x 64
+  static constexpr uint32_t WW = MM + 8192;       // W 64 x 128
+  static constexpr uint32_t SX = WW + 16384;      // solve scratch [32][32] fp32
+  static constexpr uint32_t BETA = SX + 4096;
+  static constexpr uint32_t ALPHA = BETA + 256;
+  static constexpr uint32_t GAM = ALPHA + 256;
+  static constexpr uint32_t RED = GAM + 512;
+  static constexpr uint32_t DIAG = RED + 64;
+  static constexpr uint32_t GS = DIAG + 256;
+  static constexpr uint32_t CONS = GS + 256;      // chunks consumed by the chain CTA (u32)
+  static constexpr uint32_t BARS = CONS + 64;     // qk, alpha, mma, TMEM slot
+  static constexpr uint32_t END = BARS + 64;
+  static constexpr uint32_t SA = KR;              // A [64][64] fp32 (Kr is consumed by then)
+  static constexpr uint32_t ST32 = WW;            // T [64][64] fp32 (W is written later)
+};
+
+constexpr size_t kClusterSmem =
+    (ChainSmem::END > HelperSmem::END ? ChainSmem::END : HelperSmem::END) + 1024;
+static_assert(kClusterSmem <= 232448, "shared memory per CTA");
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+// shared::cluster address of the same shared-memory offset in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t map_to(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+// bulk copy from this CTA's shared memory into another CTA's, completing on its mbarrier
+__device__ __forceinline__ void bulk_copy_to(uint32_t dst_cluster, uint32_t src_local,
+                                             uint32_t bytes, uint32_t mbar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(dst_cluster),
+      "r"(src_local), "r"(bytes), "r"(mbar_cluster)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void st_release_remote(uint32_t addr_cluster, uint32_t v) {
+  asm volatile("st.release.cluster.shared::cluster.u32 [%0], %1;" ::"r"(addr_cluster), "r"(v)
+               : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_local(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.cluster.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p))
+               : "memory");
+  return v;
+}
+
+// Waits until the chain CTA has consumed at least `need` chunks (bounded).
+__device__ bool wait_consumed(const uint32_t* cons, uint32_t need) {
+  bool ok = true;
+  if (threadIdx.x == 0) {
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+      if (ld_acquire_local(cons) >= need) break;
+      if (i == 0) {
+        t0 = globaltimer_ns();
+      } else if ((i & 63u) == 0 && globaltimer_ns() - t0 > kWaitNs) {
+        ok = false;
+        break;
+      }
+      __nanosleep(64);
+    }
+  }
+  return !__syncthreads_or(!ok);
+}
+
+template <bool CHANNEL>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_cluster_kernel(const __grid_constant__ TcMaps maps, const PrefillArgs a, int ncl) {
+  constexpr bool kAlphaTile = CHANNEL;
+  constexpr int DV = kD, DH = DV / 2;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                       ~(uintptr_t)1023);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const uint32_t crank = cluster_rank();
+  const int nh = ncl - 1;
+  const int H = a.H;
+  const int pair = blockIdx.x / ncl;
+  const int h = pair % H;
+  const int seq = a.order ? a.order[pair / H] : pair / H;
+  int64_t t0 = 0, t1 = 0;
+  const bool valid = seq_range(a, seq, t0, t1);
+  if (!valid) t1 = t0;  // skip the work but keep the cluster barriers
+  const int nch = (int)((t1 - t0 + kC - 1) / kC);
+  const size_t sidx = ((size_t)seq * H + h) * kD * kD;
+  bool failed = false;
+
+  if (crank == 0) {
+    // ===================================================================== chain CTA
+    using L = ChainSmem;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);
+    uint64_t* full = bars;  // [2]
+    uint64_t* bar_v = bars + 2;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 4);
+    if (warp == 0) tmem_alloc(tslot, kTmemCols);
+    if (tid == 0) {
+      for (int i = 0; i < 4; ++i) mbar_init(bars + i, 1);
+      fence_mbar_init();
+      prefetch_tmap(&maps.v);
+      for (int s = 0; s < 2 && s < nch; ++s) mbar_expect_tx(full + s, kSlotPayload);
+    }
+    cta_sync_tc();
+    cluster_sync();  // every CTA's barriers and counters are initialised
+    TcCtx x = make_ctx(sm, *tslot, bars + 3);
+    uint32_t ph_v = 0, ph_full[2] = {0, 0};
+    __nv_bfloat16* __restrict__ out = static_cast<__nv_bfloat16*>(a.out);
+    auto issue_v = [&](int64_t tc) {
+      if (tid == 0) {
+        mbar_expect_tx(bar_v, 16384);
+        tma_load_3d(sm + L::VIN, &maps.v, 0, h, (int)tc, bar_v);
+        tma_load_3d(sm + L::VIN + 8192, &maps.v, 64, h, (int)tc, bar_v);
+      }
+    };
+    if (nch > 0) issue_v(t0);
+    s_init<DH>(x, a.S0 ? a.S0 + sidx + (size_t)x.lrow * kD : nullptr, sm + L::SS);
+    const Opnd opV{x.sb + L::VIN, 8192, true};
+    const Opnd opU{x.sb + L::UU, 8192, true};
+    const Opnd opS{x.sb + L::SS, 16384, true};
+    const uint32_t id_v = idesc_bf16(64, DV, false, false, true);
+    const uint32_t id_negw = idesc_bf16(64, DV, true, false, true);
+    const uint32_t id_s = idesc_bf16(128, DV, false, true, true);
+    const uint32_t cons_local = smem_u32(sm + HelperSmem::CONS);
+
+#pragma unroll 1
+    for (int c = 0; c < nch && !failed; ++c) {
+      const int s = c & 1;
+      const int64_t tc = t0 + (int64_t)c * kC;
+      const int n = (int)((t1 - tc) < (int64_t)kC ? (t1 - tc) : (int64_t)kC);
+      const uint32_t slot = L::SLOT + s * kSlotBytes;
+      const Opnd opQ{x.sb + slot + kSlotQ, 8192, false};
+      const Opnd opKH{x.sb + slot + kSlotKH, 8192, true};
+      const Opnd opW{x.sb + slot + kSlotW, 8192, false};
+      const Opnd opM{x.sb + slot + kSlotM, 8192, false};
+      const Opnd opT{x.sb + slot + kSlotT, 8192, false};
+      if (!wait_bar(full + s, ph_full[s])) { failed = true; break; }
+      if (!wait_bar(bar_v, ph_v)) { failed = true; break; }
+      zero_v_tail<DV>(x, sm + L::VIN, n);
+      cta_sync_tc();
+      // U = T' V - W S (accumulated in TMEM) and O = Q~ S; the state master is faded meanwhile
+      if (tid == 0) {
+        mma_run(x.tm + kColU, opT, opV, kC, id_v, false);
+        mma_run(x.tm + kColU, opW, opS, kD, id_negw, true);
+        mma_run(x.tm + kColWO, opQ, opS, kD, id_v, false);
+        mma_commit(x.bar_mma);
+      }
+      gamma_fade<DH>(x, reinterpret_cast<const float*>(sm + slot + kSlotGam));
+      if (!wait_bar(x.bar_mma, x.ph_mma)) { failed = true; break; }
+      if (c + 1 < nch) issue_v(tc + kC);  // V is consumed
+      u_epilogue<DH>(x, sm + L::UU);
+      cta_sync_tc();
+      // O += M U and S += K^^T U
+      if (tid == 0) {
+        mma_run(x.tm + kColWO, opM, opU, kC, id_v, true);
+        mma_run(x.tm + kColS, opKH, opU, kC, id_s, true);
+        mma_commit(x.bar_mma);
+      }
+      if (!wait_bar(x.bar_mma, x.ph_mma)) { failed = true; break; }
+      // the slot is consumed: re-arm it for chunk c + 2 and tell the helpers
+      if (tid == 0) {
+        if (c + 2 < nch) mbar_expect_tx(full + s, kSlotPayload);
+        for (int r = 1; r < ncl; ++r) st_release_remote(map_to(cons_local, r), (uint32_t)(c + 1));
+      }
+      o_epilogue<DH>(x, out, tc, n, H, h, 0);
+      s_epilogue<DH>(x, sm + L::SS);
+      cta_sync_tc();
+    }
+    if (failed) {
+      if (tid == 0) report(a.status, GDR_DEVCHECK_TIMEOUT);
+      mbar_wait(bar_v, ph_v, kWaitNs);
+    } else if (valid && a.S_final) {
+      s_final<DH>(x, a.S_final + sidx + (size_t)x.lrow * kD);
+    }
+    cta_sync_tc();
+    if (warp == 0) tmem_dealloc(x.tm, kTmemCols);
+  } else {
+    // ===================================================================== helper CTA
+    using L = HelperSmem;
+    const int hid = (int)crank - 1;
+    float* sBeta = reinterpret_cast<float*>(sm + L::BETA);
+    float* sAlpha = reinterpret_cast<float*>(sm + L::ALPHA);
+    uint32_t* cons = reinterpret_cast<uint32_t*>(sm + L::CONS);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);
+    uint64_t* bar_qk = bars + 0;
+    uint64_t* bar_a = bars + 1;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3);
+    if (warp == 0) tmem_alloc(tslot, kTmemCols);
+    if (tid == 0) {
+      *cons = 0;
+      for (int i = 0; i < 3; ++i) mbar_init(bars + i, 1);
+      fence_mbar_init();
+      prefetch_tmap(&maps.q);
+      prefetch_tmap(&maps.k);
+      if (kAlphaTile) prefetch_tmap(&maps.alpha);
+    }
+    cta_sync_tc();
+    cluster_sync();
+    TcCtx x = make_ctx(sm, *tslot, bars + 2);
+    uint32_t ph_qk = 0, ph_a = 0;
+    const uint32_t chain_full = map_to(smem_u32(sm + ChainSmem::BARS), 0);
+    const uint32_t chain_slots = map_to(smem_u32(sm + ChainSmem::SLOT), 0);
+    auto issue_qk = [&](int64_t tc) {
+      if (tid == 0) {
+        mbar_expect_tx(bar_qk, 2 * 16384);
+        tma_load_3d(sm + L::QIN, &maps.q, 0, h, (int)tc, bar_qk);
+        tma_load_3d(sm + L::KIN, &maps.k, 0, h, (int)tc, bar_qk);
+      }
+    };
+    auto issue_a = [&](int64_t tc) {
+      if (kAlphaTile && tid == 0) {
+        mbar_expect_tx(bar_a, 32768);
+        tma_load_3d(sm + L::AIN, &maps.alpha, 0, h, (int)tc, bar_a);
+      }
+    };
+    auto load_scalars = [&](int64_t tc, float& b, float& al) {
+      b = 0.f;
+      al = 1.f;
+      if (tid < kC && tc + tid < t1) {
+        const size_t o = (size_t)(tc + tid) * H + h;
+        b = a.beta[o];
+        if (!CHANNEL) al = a.alpha[o];
+      }
+    };
+    float nb_beta = 0.f, nb_alpha = 1.f;
+    if (hid < nch) {
+      issue_qk(t0 + (int64_t)hid * kC);
+      issue_a(t0 + (int64_t)hid * kC);
+      load_scalars(t0 + (int64_t)hid * kC, nb_beta, nb_alpha);
+    }
+#pragma unroll 1
+    for (int c = hid; c < nch && !failed; c += nh) {
+      const int64_t tc = t0 + (int64_t)c * kC;
+      const int n = (int)((t1 - tc) < (int64_t)kC ? (t1 - tc) : (int64_t)kC);
+      const int cn = c + nh;  // this helper's next chunk
+      const int64_t tn = t0 + (int64_t)cn * kC;
+      if (tid < kC) {
+        sBeta[tid] = nb_beta;
+        sAlpha[tid] = nb_alpha;
+      }
+      if (cn < nch) load_scalars(tn, nb_beta, nb_alpha);
+      if (tid == 0) bulk_wait_read();  // the previous chunk's copies have read the tiles
+      if (!wait_bar(bar_qk, ph_qk)) { failed = true; break; }
+      if (kAlphaTile && !wait_bar(bar_a, ph_a)) { failed = true; break; }
+
+      const bool safe = gate_stage<L, CHANNEL, false>(x, n);
+      fence_async_smem();
+      cta_sync_tc();
+      if (safe && cn < nch) {
+        issue_qk(tn);
+        issue_a(tn);
+      }
+      if (!gram_stage<L, CHANNEL, false>(x, n, safe)) { failed = true; break; }
+      if (!safe && cn < nch) {
+        issue_qk(tn);
+        issue_a(tn);
+      }
+      solve_stage<L>(x);
+      if (!w_stage<L>(x, false, Opnd{0, 0, false}, 0)) { failed = true; break; }
+      w_epilogue<L>(x);
+      fence_async_smem();
+      cta_sync_tc();
+      // hand the operands over: slot c & 1 is free once chunk c - 2 has been consumed
+      if (c >= 2 && !wait_consumed(cons, (uint32_t)(c - 1))) { failed = true; break; }
+      if (tid == 0) {
+        const uint32_t dst = chain_slots + (uint32_t)(c & 1) * kSlotBytes;
+        const uint32_t mbar = chain_full + (uint32_t)(c & 1) * 8u;
+        const uint32_t src = x.sb;
+        bulk_copy_to(dst + kSlotQ, src + L::KQ + 8192, 8192, mbar);          // Q~ slab 0
+        bulk_copy_to(dst + kSlotQ + 8192, src + L::KQ + 24576, 8192, mbar);  // Q~ slab 1
+        bulk_copy_to(dst + kSlotKH, src + L::KH, 16384, mbar);
+        bulk_copy_to(dst + kSlotW, src + L::WW, 16384, mbar);
+        bulk_copy_to(dst + kSlotM, src + L::MM, 8192, mbar);
+        bulk_copy_to(dst + kSlotT, src + L::TT, 8192, mbar);
+        bulk_copy_to(dst + kSlotGam, src + L::GAM, 512, mbar);
+        bulk_commit();
+      }
+    }
+    if (tid == 0) bulk_wait_all();  // every copy into the chain CTA has landed
+    if (failed) {
+      if (tid == 0) report(a.status, GDR_DEVCHECK_TIMEOUT);
+      mbar_wait(bar_qk, ph_qk, kWaitNs);
+      if (kAlphaTile) mbar_wait(bar_a, ph_a, kWaitNs);
+    }
+    cta_sync_tc();
+    if (warp == 0) tmem_dealloc(x.tm, kTmemCols);
+  }
+  cluster_sync();  // no CTA leaves while the cluster may still address its shared memory
+}
+
+template <bool CHANNEL>
+cudaError_t launch_typed(const gdr_shape& sh, const PrefillArgs& a, const TcMaps& maps, int ncl,
+                         cudaStream_t s) {
+  auto kern = prefill_cluster_kernel<CHANNEL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kClusterSmem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)sh.n_seqs * (unsigned)sh.H * (unsigned)ncl, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kClusterSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)ncl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, maps, a, ncl);
+}
+
+// co-resident clusters of `ncl` CTAs of this kernel on the current device (0 if unknown)
+constexpr int kMaxDevices = 64;
+int max_active_clusters(int ncl) {
+  static std::atomic<int> cache[kMaxDevices][9];
+  static std::once_flag once;
+  std::call_once(once, [] {
+    for (auto& row : cache)
+      for (auto& v : row) v.store(-1);
+  });
+  int dev = 0;
+  if (ncl < 2 || ncl > 8 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return 0;
+  const int known = cache[dev][ncl].load();
+  if (known >= 0) return known;
+  auto kern = prefill_cluster_kernel<true>;
+  int n = 0;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kClusterSmem) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ncl, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kClusterSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)ncl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();
+  cache[dev][ncl].store(n);
+  return n;
+}
+
+}  // namespace
+
+// The largest cluster (1 chain CTA + up to 7 helpers) of which one per (sequence, head) chain
+// fits on the device at once; 1 (the one-CTA kernel) when even pairs of CTAs do not fit.
+int cluster_size_for(const gdr_shape& sh) {
+  const long pairs = (long)sh.n_seqs * sh.H;
+  for (int ncl = 8; ncl >= 2; --ncl)
+    if (pairs <= max_active_clusters(ncl)) return ncl;
+  return 1;
+}
+
+cudaError_t launch_prefill_cluster(const gdr_shape& sh, const PrefillArgs& a, const TcMaps& maps,
+                                   int ncl, cudaStream_t s) {
+  if (sh.gate == GDR_GATE_CHANNEL) return launch_typed<true>(sh, a, maps, ncl, s);
+  return launch_typed<false>(sh, a, maps, ncl, s);
 }
 
 }  // namespace tc

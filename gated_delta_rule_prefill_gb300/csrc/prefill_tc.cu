@@ -337,7 +337,7 @@ cudaError_t launch_prefill_tc(const gdr_shape& sh, const PrefillArgs& a, bool li
   TcMaps maps;
   if (!tc::make_tc_maps(sh, a, linear, &maps)) return cudaErrorInvalidValue;
   // few (sequence, head) chains: clusters whose helper CTAs prepare the chunks of a chain
-  if (!linear) {
+  if (!linear && !(sh.flags & GDR_FLAG_NO_CLUSTER)) {
     const int ncl = tc::cluster_size_for(sh);
     if (ncl > 1) return tc::launch_prefill_cluster(sh, a, maps, ncl, s);
   }

@@ -84,6 +84,9 @@ typedef struct {
 
 /* Force the fp32 FFMA chunked path even where a tensor-core path exists (for cross-checks). */
 #define GDR_FLAG_FORCE_SIMT 1
+/* On the tensor-core path, run the one-CTA-per-chain kernel even where the clustered kernel
+ * (one chain CTA plus helper CTAs that prepare its chunks) would be chosen (for cross-checks). */
+#define GDR_FLAG_NO_CLUSTER 2
 
 /*
  * gdr_prefill -- chunked, packed variable-length prefill of the gated delta rule.
