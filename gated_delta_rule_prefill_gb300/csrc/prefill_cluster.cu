@@ -61,7 +61,8 @@ struct HelperSmem {
   static constexpr uint32_t RED = GAM + 512;
   static constexpr uint32_t DIAG = RED + 64;
   static constexpr uint32_t GS = DIAG + 256;
-  static constexpr uint32_t CONS = GS + 256;      // chunks consumed by the chain CTA (u32)
+  static constexpr uint32_t TOT = GS + 256;       // gate carries [17][128] fp32
+  static constexpr uint32_t CONS = TOT + 8704;    // chunks consumed by the chain CTA (u32)
   static constexpr uint32_t BARS = CONS + 64;     // qk, alpha, mma, TMEM slot
   static constexpr uint32_t END = BARS + 64;
   static constexpr uint32_t SA = KR;              // A [64][64] fp32 (Kr is consumed by then)
@@ -99,14 +100,19 @@ __device__ __forceinline__ void bulk_copy_to(uint32_t dst_cluster, uint32_t src_
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
+template <int N>
 __device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
-__device__ __forceinline__ void st_release_remote(uint32_t addr_cluster, uint32_t v) {
-  asm volatile("st.release.cluster.shared::cluster.u32 [%0], %1;" ::"r"(addr_cluster), "r"(v)
+// A plain (relaxed) store suffices for the consumed-chunk counter: the chain CTA's reads of
+// the slot have completed before it is written (MMA completion observed on an mbarrier, and the
+// generic reads of gamma precede a CTA barrier), and a release would also wait for the chain
+// CTA's earlier output stores to global memory.
+__device__ __forceinline__ void st_relaxed_remote(uint32_t addr_cluster, uint32_t v) {
+  asm volatile("st.relaxed.cluster.shared::cluster.u32 [%0], %1;" ::"r"(addr_cluster), "r"(v)
                : "memory");
 }
 __device__ __forceinline__ uint32_t ld_acquire_local(const uint32_t* p) {
@@ -194,6 +200,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t id_s = idesc_bf16(128, DV, false, true, true);
     const uint32_t cons_local = smem_u32(sm + HelperSmem::CONS);
 
+    // O alternates between two accumulators, so a chunk's output rows are written out while
+    // the next chunk's first MMAs run.
+    auto o_col = [](int c) { return (c & 1) ? kColAM : kColWO; };
 #pragma unroll 1
     for (int c = 0; c < nch && !failed; ++c) {
       const int s = c & 1;
@@ -205,37 +214,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Opnd opW{x.sb + slot + kSlotW, 8192, false};
       const Opnd opM{x.sb + slot + kSlotM, 8192, false};
       const Opnd opT{x.sb + slot + kSlotT, 8192, false};
-      if (!wait_bar(full + s, ph_full[s])) { failed = true; break; }
-      if (!wait_bar(bar_v, ph_v)) { failed = true; break; }
-      zero_v_tail<DV>(x, sm + L::VIN, n);
-      cta_sync_tc();
-      // U = T' V - W S (accumulated in TMEM) and O = Q~ S; the state master is faded meanwhile
-      if (tid == 0) {
-        mma_run(x.tm + kColU, opT, opV, kC, id_v, false);
-        mma_run(x.tm + kColU, opW, opS, kD, id_negw, true);
-        mma_run(x.tm + kColWO, opQ, opS, kD, id_v, false);
-        mma_commit(x.bar_mma);
+      {  // the chunk's operands and V tile
+        bool ok = mbar_wait(full + s, ph_full[s], kWaitNs);
+        ok = ok && mbar_wait(bar_v, ph_v, kWaitNs);
+        ph_full[s] ^= 1u;
+        ph_v ^= 1u;
+        if (ok && n < kC) zero_v_tail<DV>(x, sm + L::VIN, n);
+        if (__syncthreads_or(!ok)) { failed = true; break; }
+        fence_after_sync();
+      }
+      // U = T' V - W S (accumulated in TMEM) and O = Q~ S; meanwhile the state master is faded
+      // and the previous chunk's output rows are stored
+      if (warp == 0) {
+        mma_run<kC>(x.tm + kColU, opT, opV, id_v, false);
+        mma_run<kD>(x.tm + kColU, opW, opS, id_negw, true);
+        mma_run<kD>(x.tm + o_col(c), opQ, opS, id_v, false);
+        mma_commit_elect(x.bar_mma);
       }
       gamma_fade<DH>(x, reinterpret_cast<const float*>(sm + slot + kSlotGam));
+      if (c > 0) o_epilogue<DH>(x, out, tc - kC, kC, H, h, 0, o_col(c - 1));
       if (!wait_bar(x.bar_mma, x.ph_mma)) { failed = true; break; }
       if (c + 1 < nch) issue_v(tc + kC);  // V is consumed
       u_epilogue<DH>(x, sm + L::UU);
       cta_sync_tc();
       // O += M U and S += K^^T U
-      if (tid == 0) {
-        mma_run(x.tm + kColWO, opM, opU, kC, id_v, true);
-        mma_run(x.tm + kColS, opKH, opU, kC, id_s, true);
-        mma_commit(x.bar_mma);
+      if (warp == 0) {
+        mma_run<kC>(x.tm + o_col(c), opM, opU, id_v, true);
+        mma_run<kC>(x.tm + kColS, opKH, opU, id_s, true);
+        mma_commit_elect(x.bar_mma);
       }
       if (!wait_bar(x.bar_mma, x.ph_mma)) { failed = true; break; }
-      // the slot is consumed: re-arm it for chunk c + 2 and tell the helpers
+      // the slot is consumed (its MMAs are complete and gamma was read before the barrier
+      // wait): re-arm it for chunk c + 2 and tell the helpers
       if (tid == 0) {
         if (c + 2 < nch) mbar_expect_tx(full + s, kSlotPayload);
-        for (int r = 1; r < ncl; ++r) st_release_remote(map_to(cons_local, r), (uint32_t)(c + 1));
+        for (int r = 1; r < ncl; ++r) st_relaxed_remote(map_to(cons_local, r), (uint32_t)(c + 1));
       }
-      o_epilogue<DH>(x, out, tc, n, H, h, 0);
       s_epilogue<DH>(x, sm + L::SS);
       cta_sync_tc();
+    }
+    if (!failed && nch > 0) {
+      const int64_t tl = t0 + (int64_t)(nch - 1) * kC;
+      o_epilogue<DH>(x, out, tl, (int)(t1 - tl), H, h, 0, o_col(nch - 1));
     }
     if (failed) {
       if (tid == 0) report(a.status, GDR_DEVCHECK_TIMEOUT);
@@ -310,11 +330,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         sAlpha[tid] = nb_alpha;
       }
       if (cn < nch) load_scalars(tn, nb_beta, nb_alpha);
-      if (tid == 0) bulk_wait_read();  // the previous chunk's copies have read the tiles
+      // the previous chunk's first copy group (Q~, K^, gamma) has read its tiles
+      if (tid == 0) bulk_wait_read<1>();
       if (!wait_bar(bar_qk, ph_qk)) { failed = true; break; }
       if (kAlphaTile && !wait_bar(bar_a, ph_a)) { failed = true; break; }
 
       const bool safe = gate_stage<L, CHANNEL, false>(x, n);
+      // ... and the second (W, M, T'), before the Gram epilogue rewrites M
+      if (tid == 0) bulk_wait_read<0>();
       fence_async_smem();
       cta_sync_tc();
       if (safe && cn < nch) {
@@ -340,10 +363,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         bulk_copy_to(dst + kSlotQ, src + L::KQ + 8192, 8192, mbar);          // Q~ slab 0
         bulk_copy_to(dst + kSlotQ + 8192, src + L::KQ + 24576, 8192, mbar);  // Q~ slab 1
         bulk_copy_to(dst + kSlotKH, src + L::KH, 16384, mbar);
+        bulk_copy_to(dst + kSlotGam, src + L::GAM, 512, mbar);
+        bulk_commit();
         bulk_copy_to(dst + kSlotW, src + L::WW, 16384, mbar);
         bulk_copy_to(dst + kSlotM, src + L::MM, 8192, mbar);
         bulk_copy_to(dst + kSlotT, src + L::TT, 8192, mbar);
-        bulk_copy_to(dst + kSlotGam, src + L::GAM, 512, mbar);
         bulk_commit();
       }
     }

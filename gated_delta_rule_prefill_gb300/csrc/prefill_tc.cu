@@ -70,6 +70,7 @@ struct TcSmem {
   static constexpr uint32_t SA = KR;                // A [64][64]  (Kr is consumed by then)
   static constexpr uint32_t ST32 = WW;              // T [64][64]  (W is written later)
   static constexpr uint32_t SX = UU;                // [32][32] (U is written later)
+  static constexpr uint32_t TOT = WW;               // gate carries [17][128] (W later)
   static_assert(bytes <= 232448, "shared memory per CTA");
   static_assert(DV * 128 >= 32 * 32 * 4, "block scratch fits in U");
 };
@@ -214,10 +215,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     cta_sync_tc();
 
     // 5. U = U~ - W S and O = Q~ S; the state master is faded meanwhile
-    if (tid == 0) {
-      if (!LINEAR) mma_run(x.tm + kColU, opW, opS, kD, id_negw, true);
-      mma_run(x.tm + kColWO, opQ, opS, kD, id_v, false);
-      mma_commit(x.bar_mma);
+    if (warp == 0) {
+      if (!LINEAR) mma_run<kD>(x.tm + kColU, opW, opS, id_negw, true);
+      mma_run<kD>(x.tm + kColWO, opQ, opS, id_v, false);
+      mma_commit_elect(x.bar_mma);
     }
     if (!LINEAR) gamma_fade<DH>(x, sGam);
     if (!wait_bar(x.bar_mma, x.ph_mma)) { failed = true; break; }
@@ -225,11 +226,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     cta_sync_tc();
 
     // 6. O += M U and S += K^^T U
-    if (tid == 0) {
+    if (warp == 0) {
       const Opnd opUse = LINEAR ? opV : opU;
-      mma_run(x.tm + kColWO, opM, opUse, kC, id_v, true);
-      mma_run(x.tm + kColS, opKH, opUse, kC, id_s, true);
-      mma_commit(x.bar_mma);
+      mma_run<kC>(x.tm + kColWO, opM, opUse, id_v, true);
+      mma_run<kC>(x.tm + kColS, opKH, opUse, id_s, true);
+      mma_commit_elect(x.bar_mma);
     }
     if (!wait_bar(x.bar_mma, x.ph_mma)) { failed = true; break; }
     if (LINEAR && tn < t1) issue_v(tn);

@@ -42,10 +42,13 @@ __device__ __forceinline__ void st_bf16(unsigned char* base, uint32_t off, float
 }
 
 // D (+)= A * B over K (multiple of 16).
-__device__ __forceinline__ void mma_run(uint32_t d, Opnd A, Opnd B, int K, uint32_t idesc,
+// K/16 MMA steps; called by all 32 lanes of one warp (one elected lane issues).
+template <int K>
+__device__ __forceinline__ void mma_run(uint32_t d, const Opnd& A, const Opnd& B, uint32_t idesc,
                                         bool acc) {
-#pragma unroll 1
-  for (int k = 0; k < K; k += 16) mma_bf16(d, A.at(k), B.at(k), idesc, (acc || k > 0) ? 1u : 0u);
+#pragma unroll
+  for (int k = 0; k < K; k += 16)
+    mma_bf16_elect(d, A.at(k), B.at(k), idesc, (acc || k > 0) ? 1u : 0u);
 }
 
 // CTA-wide barrier that also orders tcgen05 operations around it.
@@ -74,12 +77,44 @@ __device__ __forceinline__ void fma4(float4& acc, float a, float4 b) {
   acc.w = fmaf(a, b.w, acc.w);
 }
 
+// ---- warp-level tf32 products for the off-diagonal blocks of the triangular inverse.
+// mma.sync m16n8k8 (row.col) fragments, g = lane / 4, t = lane % 4:
+//   A (16 x 8): a0 (g, t), a1 (g + 8, t), a2 (g, t + 4), a3 (g + 8, t + 4)
+//   B (8 x 8):  b0 (t, g), b1 (t + 4, g)
+//   C (16 x 8): c0 (g, 2t), c1 (g, 2t + 1), c2 (g + 8, 2t), c3 (g + 8, 2t + 1)
+__device__ __forceinline__ uint32_t tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// A fragment of the 16 x 8 tile at (r0, k0) of a swizzled fp32 64 x 64 matrix
+__device__ __forceinline__ void frag_a(const float* m, int r0, int k0, int g, int t,
+                                       uint32_t (&a)[4]) {
+  a[0] = tf32(m[f32x(r0 + g, k0 + t)]);
+  a[1] = tf32(m[f32x(r0 + g + 8, k0 + t)]);
+  a[2] = tf32(m[f32x(r0 + g, k0 + t + 4)]);
+  a[3] = tf32(m[f32x(r0 + g + 8, k0 + t + 4)]);
+}
+// 32 x 32 fp32 scratch, columns XOR-swizzled by 8 * (row % 4) against bank conflicts
+__device__ __forceinline__ int x32(int r, int c) { return r * 32 + (c ^ ((r & 3) << 3)); }
+
 // T = (I + A)^-1 for A strictly lower (64 x 64, fp32, swizzled layout above), by doubling the
 // inverted block size: the four 16 x 16 diagonal blocks by right-looking forward substitution
 // (one column per thread, held in registers); then both 32 x 32 diagonal blocks at once,
 // T_ba = -T_bb (A_ba T_aa) for (a, b) = (0, 1) and (2, 3); then the 64 x 64 inverse,
-// T_[23][01] = -T_[23][23] (A_[23][01] T_[01][01]).  sX holds the 32 x 32 intermediate.
+// T_[23][01] = -T_[23][23] (A_[23][01] T_[01][01]).  The two products of each doubling step run
+// on the tensor cores as warp-level tf32 MMAs with fp32 accumulation (T' is rounded to bf16
+// afterwards, 4x coarser than tf32).  sX holds the intermediate (32 x 32 fp32).
 __device__ inline void unit_lower_inverse(const float* sA, float* sT, float* sX, int tid) {
+  const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
   if (tid < 64) {
     const int b = tid >> 4, c = tid & 15, o = 16 * b;
     float acc[16];
@@ -102,47 +137,65 @@ __device__ inline void unit_lower_inverse(const float* sA, float* sT, float* sX,
     }
   }
   __syncthreads();
-  // ---- level 32: blocks (1, 0) and (3, 2); 2 x 256 outputs, 2 per thread
-  {
-    const int blk = tid >> 7, e = tid & 127;       // blk 0: (1,0); blk 1: (3,2)
-    const int rr = e >> 3, c2 = (e & 7) * 2;       // row in the block, column pair
-    const int ra = 32 * blk, rb = ra + 16;         // first rows of block rows a and b
-    float x0 = 0.f, x1 = 0.f;
+  // ---- level 32: warp (p, j) of warps 0-3 computes the 8 columns 8j.. of pair p's blocks
+  if (warp < 4) {
+    const int p = warp >> 1, j = warp & 1;
+    const int ra = 32 * p, rb = ra + 16;
+    float* sXp = sX + p * 512;  // X_p as 16 x 32 rows of the x32 layout (columns 0-15 used)
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      const float am = sA[f32x(rb + rr, ra + m)];
-      x0 = fmaf(am, sT[f32x(ra + m, ra + c2)], x0);
-      x1 = fmaf(am, sT[f32x(ra + m, ra + c2 + 1)], x1);
+    for (int ks = 0; ks < 2; ++ks) {
+      if (ks < j) continue;  // T_aa rows above the column tile are zero
+      uint32_t a[4];
+      frag_a(sA, rb, ra + 8 * ks, g, t, a);
+      mma_tf32(c, a, tf32(sT[f32x(ra + 8 * ks + t, ra + 8 * j + g)]),
+               tf32(sT[f32x(ra + 8 * ks + t + 4, ra + 8 * j + g)]));
     }
-    sX[blk * 256 + rr * 16 + c2] = x0;
-    sX[blk * 256 + rr * 16 + c2 + 1] = x1;
-    __syncthreads();
-    float y0 = 0.f, y1 = 0.f;
+    *reinterpret_cast<float2*>(sXp + x32(g, 8 * j + 2 * t)) = make_float2(c[0], c[1]);
+    *reinterpret_cast<float2*>(sXp + x32(g + 8, 8 * j + 2 * t)) = make_float2(c[2], c[3]);
+    __syncwarp();
+    asm volatile("bar.sync 1, 128;" ::: "memory");  // warps 0-3 only
+    float y[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      const float tm = m <= rr ? sT[f32x(rb + rr, rb + m)] : 0.f;
-      y0 = fmaf(tm, sX[blk * 256 + m * 16 + c2], y0);
-      y1 = fmaf(tm, sX[blk * 256 + m * 16 + c2 + 1], y1);
+    for (int ks = 0; ks < 2; ++ks) {
+      uint32_t a[4];
+      frag_a(sT, rb, rb + 8 * ks, g, t, a);
+      mma_tf32(y, a, tf32(sXp[x32(8 * ks + t, 8 * j + g)]),
+               tf32(sXp[x32(8 * ks + t + 4, 8 * j + g)]));
     }
-    sT[f32x(rb + rr, ra + c2)] = -y0;
-    sT[f32x(rb + rr, ra + c2 + 1)] = -y1;
-    __syncthreads();
+    *reinterpret_cast<float2*>(sT + f32x(rb + g, ra + 8 * j + 2 * t)) = make_float2(-y[0], -y[1]);
+    *reinterpret_cast<float2*>(sT + f32x(rb + g + 8, ra + 8 * j + 2 * t)) =
+        make_float2(-y[2], -y[3]);
   }
-  // ---- level 64: block [23][01] (32 x 32); 1024 outputs, 4 per thread (one float4 group)
+  __syncthreads();
+  // ---- level 64: warp (mi, ni) computes the 16 x 8 tile (rows 16 mi.., columns 8 ni..)
   {
-    const int rr = tid >> 3, grp = tid & 7;  // row 0..31 of the block, float4 group 0..7
-    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-    for (int m = 0; m < 32; ++m) fma4(x, sA[f32x(32 + rr, m)], ld4x(sT, m, grp));
-    *reinterpret_cast<float4*>(sX + rr * 32 + 4 * grp) = x;
-    __syncthreads();
-    float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-    for (int m = 0; m < 32; ++m) {
-      const float tm = m <= rr ? sT[f32x(32 + rr, 32 + m)] : 0.f;
-      fma4(y, tm, *reinterpret_cast<const float4*>(sX + m * 32 + 4 * grp));
+    const int mi = warp >> 2, ni = warp & 3;
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      if (ks < ni) continue;  // rows of T_[01][01] above the column tile are zero
+      uint32_t a[4];
+      frag_a(sA, 32 + 16 * mi, 8 * ks, g, t, a);
+      mma_tf32(c, a, tf32(sT[f32x(8 * ks + t, 8 * ni + g)]),
+               tf32(sT[f32x(8 * ks + t + 4, 8 * ni + g)]));
     }
-    st4x(sT, 32 + rr, grp, make_float4(-y.x, -y.y, -y.z, -y.w));
+    *reinterpret_cast<float2*>(sX + x32(16 * mi + g, 8 * ni + 2 * t)) = make_float2(c[0], c[1]);
+    *reinterpret_cast<float2*>(sX + x32(16 * mi + g + 8, 8 * ni + 2 * t)) = make_float2(c[2], c[3]);
+    __syncthreads();
+    float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      if (ks > 2 * mi + 1) continue;  // T_[23][23] is zero right of the row tile's diagonal
+      uint32_t a[4];
+      frag_a(sT, 32 + 16 * mi, 32 + 8 * ks, g, t, a);
+      mma_tf32(y, a, tf32(sX[x32(8 * ks + t, 8 * ni + g)]),
+               tf32(sX[x32(8 * ks + t + 4, 8 * ni + g)]));
+    }
+    *reinterpret_cast<float2*>(sT + f32x(32 + 16 * mi + g, 8 * ni + 2 * t)) =
+        make_float2(-y[0], -y[1]);
+    *reinterpret_cast<float2*>(sT + f32x(32 + 16 * mi + g + 8, 8 * ni + 2 * t)) =
+        make_float2(-y[2], -y[3]);
     __syncthreads();
   }
 }
@@ -305,46 +358,43 @@ __device__ bool gate_stage(const TcCtx& x, int n) {
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) gn[cc] = 1.f;
         if (!LINEAR) {
-          float* sTot = reinterpret_cast<float*>(sm + L::WW);  // [16 row blocks][128 channels]
+          // row-block totals -> exclusive products down the 16 row blocks (one thread per
+          // channel; row 16 receives Gam_n) -> each thread's carry
+          float* sTot = reinterpret_cast<float*>(sm + L::TOT);  // [17][128 channels]
           *reinterpret_cast<float4*>(sTot + rb * kD + 8 * g8) = make_float4(run[0], run[1], run[2], run[3]);
           *reinterpret_cast<float4*>(sTot + rb * kD + 8 * g8 + 4) = make_float4(run[4], run[5], run[6], run[7]);
           __syncthreads();
-          float carry[8];
+          if (tid < kD) {
+            float t16[16];
 #pragma unroll
-          for (int cc = 0; cc < 8; ++cc) carry[cc] = 1.f;
+            for (int b2 = 0; b2 < 16; ++b2) t16[b2] = sTot[b2 * kD + tid];
+            float acc = 1.f;
 #pragma unroll
-          for (int b2 = 0; b2 < 16; ++b2) {
-            const float4 u0 = *reinterpret_cast<const float4*>(sTot + b2 * kD + 8 * g8);
-            const float4 u1 = *reinterpret_cast<const float4*>(sTot + b2 * kD + 8 * g8 + 4);
-            const float t8[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-#pragma unroll
-            for (int cc = 0; cc < 8; ++cc) {
-              if (b2 < rb) carry[cc] *= t8[cc];
-              gn[cc] *= t8[cc];
+            for (int b2 = 0; b2 < 16; ++b2) {
+              sTot[b2 * kD + tid] = acc;
+              acc *= t16[b2];
             }
+            sTot[16 * kD + tid] = acc;
+            sGam[tid] = acc;
+            float mn = acc;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+            if (lane == 0) sRed[warp] = mn;
           }
+          __syncthreads();
+          const float4 c0 = *reinterpret_cast<const float4*>(sTot + rb * kD + 8 * g8);
+          const float4 c1 = *reinterpret_cast<const float4*>(sTot + rb * kD + 8 * g8 + 4);
+          const float4 n0 = *reinterpret_cast<const float4*>(sTot + 16 * kD + 8 * g8);
+          const float4 n1 = *reinterpret_cast<const float4*>(sTot + 16 * kD + 8 * g8 + 4);
+          const float carry[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          gn[0] = n0.x, gn[1] = n0.y, gn[2] = n0.z, gn[3] = n0.w;
+          gn[4] = n1.x, gn[5] = n1.y, gn[6] = n1.z, gn[7] = n1.w;
 #pragma unroll
           for (int rr = 0; rr < 4; ++rr)
 #pragma unroll
             for (int cc = 0; cc < 8; ++cc) p[rr][cc] *= carry[cc];
+          safe = fminf(fminf(sRed[0], sRed[1]), fminf(sRed[2], sRed[3])) > kSafeGamma;
         }
-      }
-      if (!LINEAR) {
-        float mn = gn[0];
-#pragma unroll
-        for (int cc = 1; cc < 8; ++cc) mn = fminf(mn, gn[cc]);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
-        if (lane == 0) sRed[warp] = mn;
-        if (rb == 0) {
-          *reinterpret_cast<float4*>(sGam + 8 * g8) = make_float4(gn[0], gn[1], gn[2], gn[3]);
-          *reinterpret_cast<float4*>(sGam + 8 * g8 + 4) = make_float4(gn[4], gn[5], gn[6], gn[7]);
-        }
-        __syncthreads();
-        float mall = sRed[0];
-#pragma unroll
-        for (int w = 1; w < kThreads / 32; ++w) mall = fminf(mall, sRed[w]);
-        safe = mall > kSafeGamma;
       }
 
       if (safe) {
@@ -428,9 +478,9 @@ __device__ bool gram_stage(TcCtx& x, int n, bool safe) {
   const uint32_t id_am = idesc_bf16(128, kC);
     // ================= 2. decay-weighted Gram matrices [A'; M]
     if (safe) {
-      if (tid == 0) {
-        mma_run(tm + kColAM, opKQ, opKR, kD, id_am, false);
-        mma_commit(x.bar_mma);
+      if (x.warp == 0) {
+        mma_run<kD>(tm + kColAM, opKQ, opKR, id_am, false);
+        mma_commit_elect(x.bar_mma);
       }
       if (!wait_bar(x.bar_mma, x.ph_mma)) return false;
       const int r = lrow & 63;
@@ -537,114 +587,111 @@ template <class L>
 __device__ bool w_stage(TcCtx& x, bool with_v, Opnd opV, uint32_t id_v) {
   const Opnd opT{x.sb + L::TT, 8192, false};
   const Opnd opKt{x.sb + L::KQ, 16384, true};  // K~ rows as MN-major B (K = tokens)
-  if (x.tid == 0) {
-    mma_run(x.tm + kColWO, opT, opKt, kC, idesc_bf16(64, kD, false, false, true), false);
-    if (with_v) mma_run(x.tm + kColU, opT, opV, kC, id_v, false);
-    mma_commit(x.bar_mma);
+  if (x.warp == 0) {
+    mma_run<kC>(x.tm + kColWO, opT, opKt, idesc_bf16(64, kD, false, false, true), false);
+    if (with_v) mma_run<kC>(x.tm + kColU, opT, opV, id_v, false);
+    mma_commit_elect(x.bar_mma);
   }
   if (!wait_bar(x.bar_mma, x.ph_mma)) return false;
   return true;
 }
 template <class L>
 __device__ void w_epilogue(const TcCtx& x) {
+  float v[64];
+  tmem_ld64(x.tm + x.lane_base + kColWO + x.wh * 64, v);
+  if (x.m64ok) {
 #pragma unroll
-  for (int c0 = x.wh * 64; c0 < x.wh * 64 + 64; c0 += 32) {
-    float v[32];
-    tmem_ld32(x.tm + x.lane_base + kColWO + c0, v);
-    if (x.m64ok) {
-#pragma unroll
-      for (int j = 0; j < 32; j += 8) st_chunk8(x.sm + L::WW, 8192, x.m64row, c0 + j, v + j);
-    }
+    for (int j = 0; j < 64; j += 8) st_chunk8(x.sm + L::WW, 8192, x.m64row, x.wh * 64 + j, v + j);
   }
   fence_async_smem();
 }
 
 // ---- chain pieces (value-column width DV; DH = DV / 2 columns per warp half)
+// this warp half's DH columns of a TMEM region, one wait
+template <int DH>
+__device__ __forceinline__ void tmem_ld_half(uint32_t taddr, float (&v)[DH]) {
+  static_assert(DH == 32 || DH == 64, "warp-half width");
+  if constexpr (DH == 64) {
+    tmem_ld64(taddr, v);
+  } else {
+    tmem_ld32(taddr, v);
+  }
+}
+template <int DH>
+__device__ __forceinline__ void tmem_st_half(uint32_t taddr, const float (&v)[DH]) {
+#pragma unroll
+  for (int c = 0; c < DH; c += 32) tmem_st32(taddr + c, *reinterpret_cast<const float(*)[32]>(v + c));
+}
 // fade the fp32 state master: S <- Diag(gamma) S (lane = key channel)
 template <int DH>
 __device__ void gamma_fade(const TcCtx& x, const float* gam) {
   const float gm = gam[x.lrow];
+  const uint32_t t = x.tm + x.lane_base + kColS + x.wh * DH;
+  float v[DH];
+  tmem_ld_half<DH>(t, v);
 #pragma unroll
-  for (int c0 = x.wh * DH; c0 < x.wh * DH + DH; c0 += 32) {
-    float v[32];
-    tmem_ld32(x.tm + x.lane_base + kColS + c0, v);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] *= gm;
-    tmem_st32(x.tm + x.lane_base + kColS + c0, v);
-  }
+  for (int j = 0; j < DH; ++j) v[j] *= gm;
+  tmem_st_half<DH>(t, v);
   tmem_wait_st();
 }
 // U (M = 64 layout) -> bf16 [tok][DV] tile (MN-major B operand)
 template <int DH>
 __device__ void u_epilogue(const TcCtx& x, unsigned char* uu) {
+  float v[DH];
+  tmem_ld_half<DH>(x.tm + x.lane_base + kColU + x.wh * DH, v);
+  if (x.m64ok) {
 #pragma unroll
-  for (int c0 = x.wh * DH; c0 < x.wh * DH + DH; c0 += 32) {
-    float v[32];
-    tmem_ld32(x.tm + x.lane_base + kColU + c0, v);
-    if (x.m64ok) {
-#pragma unroll
-      for (int j = 0; j < 32; j += 8) st_chunk8(uu, 8192, x.m64row, c0 + j, v + j);
-    }
+    for (int j = 0; j < DH; j += 8) st_chunk8(uu, 8192, x.m64row, x.wh * DH + j, v + j);
   }
   fence_async_smem();
 }
-// O (M = 64 layout) -> out rows [tc, tc + n) of head h, value columns [vc0, vc0 + DV)
+// O (M = 64 layout, accumulator columns from `col`) -> out rows [tc, tc + n) of head h, value
+// columns [vc0, vc0 + DV)
 template <int DH>
 __device__ void o_epilogue(const TcCtx& x, __nv_bfloat16* out, int64_t tc, int n, int H, int h,
-                           int vc0) {
+                           int vc0, uint32_t col = kColWO) {
+  float v[DH];
+  tmem_ld_half<DH>(x.tm + x.lane_base + col + x.wh * DH, v);
+  if (x.m64ok && x.m64row < n) {
+    __nv_bfloat16* dst = out + ((size_t)(tc + x.m64row) * H + h) * kD + vc0 + x.wh * DH;
 #pragma unroll
-  for (int c0 = x.wh * DH; c0 < x.wh * DH + DH; c0 += 32) {
-    float v[32];
-    tmem_ld32(x.tm + x.lane_base + kColWO + c0, v);
-    if (x.m64ok && x.m64row < n) {
-      __nv_bfloat16* dst = out + ((size_t)(tc + x.m64row) * H + h) * kD + vc0 + c0;
+    for (int j = 0; j < DH; j += 8) {
+      __align__(16) __nv_bfloat162 hv[4];
 #pragma unroll
-      for (int j = 0; j < 32; j += 8) {
-        __align__(16) __nv_bfloat162 hv[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) hv[i] = __floats2bfloat162_rn(v[j + 2 * i], v[j + 2 * i + 1]);
-        *reinterpret_cast<uint4*>(dst + j) = *reinterpret_cast<const uint4*>(hv);
-      }
+      for (int i = 0; i < 4; ++i) hv[i] = __floats2bfloat162_rn(v[j + 2 * i], v[j + 2 * i + 1]);
+      *reinterpret_cast<uint4*>(dst + j) = *reinterpret_cast<const uint4*>(hv);
     }
   }
 }
 // state master -> bf16 [d_k][DV] tile (MN-major B operand of the next chunk)
 template <int DH>
 __device__ void s_epilogue(const TcCtx& x, unsigned char* ss) {
+  float v[DH];
+  tmem_ld_half<DH>(x.tm + x.lane_base + kColS + x.wh * DH, v);
 #pragma unroll
-  for (int c0 = x.wh * DH; c0 < x.wh * DH + DH; c0 += 32) {
-    float v[32];
-    tmem_ld32(x.tm + x.lane_base + kColS + c0, v);
-#pragma unroll
-    for (int j = 0; j < 32; j += 8) st_chunk8(ss, 16384, x.lrow, c0 + j, v + j);
-  }
+  for (int j = 0; j < DH; j += 8) st_chunk8(ss, 16384, x.lrow, x.wh * DH + j, v + j);
   fence_async_smem();
 }
 // entering state S0 (or zeros) -> fp32 master in TMEM and the bf16 operand tile
 template <int DH>
 __device__ void s_init(const TcCtx& x, const float* s0_row, unsigned char* ss) {
+  float v[DH];
 #pragma unroll
-  for (int c0 = x.wh * DH; c0 < x.wh * DH + DH; c0 += 32) {
-    float v[32];
+  for (int j = 0; j < DH; ++j) v[j] = s0_row ? s0_row[x.wh * DH + j] : 0.f;
+  tmem_st_half<DH>(x.tm + x.lane_base + kColS + x.wh * DH, v);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = s0_row ? s0_row[c0 + j] : 0.f;
-    tmem_st32(x.tm + x.lane_base + kColS + c0, v);
-#pragma unroll
-    for (int j = 0; j < 32; j += 8) st_chunk8(ss, 16384, x.lrow, c0 + j, v + j);
-  }
+  for (int j = 0; j < DH; j += 8) st_chunk8(ss, 16384, x.lrow, x.wh * DH + j, v + j);
   tmem_wait_st();
 }
 // state master -> S_final row (fp32)
 template <int DH>
 __device__ void s_final(const TcCtx& x, float* sf_row) {
+  float v[DH];
+  tmem_ld_half<DH>(x.tm + x.lane_base + kColS + x.wh * DH, v);
 #pragma unroll
-  for (int c0 = x.wh * DH; c0 < x.wh * DH + DH; c0 += 32) {
-    float v[32];
-    tmem_ld32(x.tm + x.lane_base + kColS + c0, v);
-#pragma unroll
-    for (int j = 0; j < 32; j += 4)
-      *reinterpret_cast<float4*>(sf_row + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-  }
+  for (int j = 0; j < DH; j += 4)
+    *reinterpret_cast<float4*>(sf_row + x.wh * DH + j) =
+        make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
 }
 // zero the V tile rows [n, 64) (SW128 [tok][DV] layout; a whole 128-byte row per slab)
 template <int DV>
