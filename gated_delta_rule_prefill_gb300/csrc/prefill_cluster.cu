@@ -6,12 +6,18 @@
 // W = T' K~ (stages 1-4 of prefill_tc.cu).  In a cluster, CTA 0 (the chain CTA) runs only the
 // state pass of every chunk (U = T' V - W S, O = Q~ S + M U, S <- gamma S + K^^T U), while the NH
 // helper CTAs prepare the chunks round-robin (helper h takes chunks c with c mod NH = h) and copy
-// the operands the state pass needs -- Q~, K^, W, M, T' (bf16) and gamma -- into one of two slots
+// the operands the state pass needs -- Q~, K^, -W, M, T' (bf16) and gamma -- into one of two slots
 // in the chain CTA's shared memory with bulk copies over distributed shared memory.  The copies
 // complete on the slot's mbarrier in the chain CTA; after consuming a slot the chain CTA re-arms
 // it and publishes its count of consumed chunks into every helper's shared memory, which a
 // helper waits on before it overwrites a slot.  Every wait is bounded; a timeout records
 // GDR_DEVCHECK_TIMEOUT and the CTA unwinds to the closing cluster barrier.
+//
+// The slot stacks the operands so that the chain's products are M = 128 MMAs (an M = 64 MMA takes
+// as long as an M = 128 one): with a zero tile Z between T' and M,
+//   D = [T'; Z] V + [-W; Q~] S   gives U in rows 0-63 and Q~ S in rows 64-127,
+//   D += [Z; M] U                completes O in rows 64-127 (rows 0-63 unchanged),
+// so U and O leave TMEM from different lane quarters at the same time.
 #include <cuda.h>
 
 #include <atomic>
@@ -25,22 +31,22 @@ namespace {
 
 using namespace umma;
 
-// slot layout (bytes from the slot base)
-constexpr uint32_t kSlotQ = 0;        // Q~  [64][128] K-major, slabs 8 KB apart
-constexpr uint32_t kSlotKH = 16384;   // K^  [tok][ch] (MN-major A), slabs 8 KB apart
-constexpr uint32_t kSlotW = 32768;    // W   [64][128] K-major, slabs 8 KB apart
-constexpr uint32_t kSlotM = 49152;    // M   [64][64] K-major
-constexpr uint32_t kSlotT = 57344;    // T'  [64][64] K-major
-constexpr uint32_t kSlotGam = 65536;  // gamma [128] fp32
-constexpr uint32_t kSlotPayload = 65536 + 512;
-constexpr uint32_t kSlotBytes = 66560;  // 1024-aligned
+// slot layout (bytes from the slot base); K-major tiles of 128 rows have 16 KB slabs
+constexpr uint32_t kSlotWQ = 0;       // [-W; Q~] 128 x 128: -W rows at +0 / +16K, Q~ at +8K / +24K
+constexpr uint32_t kSlotKH = 32768;   // K^  [tok][ch] (MN-major A), slabs 8 KB apart
+constexpr uint32_t kSlotT = 49152;    // T'  [64][64]   } [T'; Z] and [Z; M] are
+constexpr uint32_t kSlotZ = 57344;    // zeros [64][64] } 128 x 64 K-major tiles
+constexpr uint32_t kSlotM = 65536;    // M   [64][64]   }
+constexpr uint32_t kSlotGam = 73728;  // gamma [128] fp32
+constexpr uint32_t kSlotPayload = 65536 + 512;  // everything but Z
+constexpr uint32_t kSlotBytes = 74752;          // 1024-aligned
 
 struct ChainSmem {
   static constexpr uint32_t SLOT = 0;                      // 2 slots
   static constexpr uint32_t VIN = 2 * kSlotBytes;          // V [64 tok][128] SW128, 2 slabs
   static constexpr uint32_t UU = VIN + 16384;              // U [tok][128] (MN-major B)
   static constexpr uint32_t SS = UU + 16384;               // S [d_k][128] (MN-major B)
-  static constexpr uint32_t BARS = SS + 32768;             // full[2], v, mma, TMEM slot
+  static constexpr uint32_t BARS = SS + 32768;             // full[2], v, mma, o, TMEM slot
   static constexpr uint32_t END = BARS + 64;
 };
 
@@ -170,10 +176,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);
     uint64_t* full = bars;  // [2]
     uint64_t* bar_v = bars + 2;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 4);
+    uint64_t* bar_o = bars + 4;  // [Z; M] U of the chunk
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 5);
     if (warp == 0) tmem_alloc(tslot, kTmemCols);
+    for (int i = tid; i < 2 * 8192 / 16; i += kThreads) {  // the Z tiles of both slots
+      *reinterpret_cast<uint4*>(sm + L::SLOT + (i >> 9) * kSlotBytes + kSlotZ + (i & 511) * 16) =
+          make_uint4(0, 0, 0, 0);
+    }
+    fence_async_smem();
     if (tid == 0) {
-      for (int i = 0; i < 4; ++i) mbar_init(bars + i, 1);
+      for (int i = 0; i < 5; ++i) mbar_init(bars + i, 1);
       fence_mbar_init();
       prefetch_tmap(&maps.v);
       for (int s = 0; s < 2 && s < nch; ++s) mbar_expect_tx(full + s, kSlotPayload);
@@ -195,25 +207,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     const Opnd opV{x.sb + L::VIN, 8192, true};
     const Opnd opU{x.sb + L::UU, 8192, true};
     const Opnd opS{x.sb + L::SS, 16384, true};
-    const uint32_t id_v = idesc_bf16(64, DV, false, false, true);
-    const uint32_t id_negw = idesc_bf16(64, DV, true, false, true);
-    const uint32_t id_s = idesc_bf16(128, DV, false, true, true);
+    const uint32_t id_d = idesc_bf16(128, DV, false, false, true);  // K-major A, MN-major B
+    const uint32_t id_s = idesc_bf16(128, DV, false, true, true);   // K^ as MN-major A
     const uint32_t cons_local = smem_u32(sm + HelperSmem::CONS);
+    const bool u_rows = (warp & 3) < 2;  // TMEM lanes 0-63 (U) or 64-127 (O) of this warp
+    const int drow = (warp & 3) * 32 + (tid & 31) - (u_rows ? 0 : 64);
+    uint32_t ph_o = 0;
 
-    // O alternates between two accumulators, so a chunk's output rows are written out while
+    // D alternates between two accumulators, so a chunk's output rows are written out while
     // the next chunk's first MMAs run.
-    auto o_col = [](int c) { return (c & 1) ? kColAM : kColWO; };
+    auto d_col = [](int c) { return (c & 1) ? kColWO : kColU; };
+    // O rows (TMEM lanes 64-127 of D) -> out rows [tc, tc + n) of head h
+    auto o_store = [&](int c, int64_t tc, int n) {
+      float v[64];
+      tmem_ld64(x.tm + x.lane_base + d_col(c) + x.wh * 64, v);
+      if (drow < n) {
+        __nv_bfloat16* dst = out + ((size_t)(tc + drow) * H + h) * kD + x.wh * 64;
+#pragma unroll
+        for (int j = 0; j < 64; j += 8) {
+          __align__(16) __nv_bfloat162 hv[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) hv[i] = __floats2bfloat162_rn(v[j + 2 * i], v[j + 2 * i + 1]);
+          *reinterpret_cast<uint4*>(dst + j) = *reinterpret_cast<const uint4*>(hv);
+        }
+      }
+    };
 #pragma unroll 1
     for (int c = 0; c < nch && !failed; ++c) {
       const int s = c & 1;
       const int64_t tc = t0 + (int64_t)c * kC;
       const int n = (int)((t1 - tc) < (int64_t)kC ? (t1 - tc) : (int64_t)kC);
       const uint32_t slot = L::SLOT + s * kSlotBytes;
-      const Opnd opQ{x.sb + slot + kSlotQ, 8192, false};
+      const Opnd opTZ{x.sb + slot + kSlotT, 16384, false};
+      const Opnd opZM{x.sb + slot + kSlotZ, 16384, false};
+      const Opnd opWQ{x.sb + slot + kSlotWQ, 16384, false};
       const Opnd opKH{x.sb + slot + kSlotKH, 8192, true};
-      const Opnd opW{x.sb + slot + kSlotW, 8192, false};
-      const Opnd opM{x.sb + slot + kSlotM, 8192, false};
-      const Opnd opT{x.sb + slot + kSlotT, 8192, false};
       {  // the chunk's operands and V tile
         bool ok = mbar_wait(full + s, ph_full[s], kWaitNs);
         ok = ok && mbar_wait(bar_v, ph_v, kWaitNs);
@@ -223,39 +251,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (__syncthreads_or(!ok)) { failed = true; break; }
         fence_after_sync();
       }
-      // U = T' V - W S (accumulated in TMEM) and O = Q~ S; meanwhile the state master is faded
-      // and the previous chunk's output rows are stored
+      // D = [T'; Z] V + [-W; Q~] S; meanwhile the state master is faded and the previous
+      // chunk's output rows are stored
       if (warp == 0) {
-        mma_run<kC>(x.tm + kColU, opT, opV, id_v, false);
-        mma_run<kD>(x.tm + kColU, opW, opS, id_negw, true);
-        mma_run<kD>(x.tm + o_col(c), opQ, opS, id_v, false);
+        mma_run<kC>(x.tm + d_col(c), opTZ, opV, id_d, false);
+        mma_run<kD>(x.tm + d_col(c), opWQ, opS, id_d, true);
         mma_commit_elect(x.bar_mma);
       }
       gamma_fade<DH>(x, reinterpret_cast<const float*>(sm + slot + kSlotGam));
-      if (c > 0) o_epilogue<DH>(x, out, tc - kC, kC, H, h, 0, o_col(c - 1));
+      if (c > 0 && !u_rows) o_store(c - 1, tc - kC, kC);
       if (!wait_bar(x.bar_mma, x.ph_mma)) { failed = true; break; }
       if (c + 1 < nch) issue_v(tc + kC);  // V is consumed
-      u_epilogue<DH>(x, sm + L::UU);
+      if (u_rows) {  // U rows -> bf16 [tok][DV] tile (MN-major B operand)
+        float v[64];
+        tmem_ld64(x.tm + x.lane_base + d_col(c) + x.wh * 64, v);
+#pragma unroll
+        for (int j = 0; j < 64; j += 8) st_chunk8(sm + L::UU, 8192, drow, x.wh * 64 + j, v + j);
+        fence_async_smem();
+      }
       cta_sync_tc();
-      // O += M U and S += K^^T U
+      // S += K^^T U (on the chain's critical path), then O += M U
       if (warp == 0) {
-        mma_run<kC>(x.tm + o_col(c), opM, opU, id_v, true);
         mma_run<kC>(x.tm + kColS, opKH, opU, id_s, true);
         mma_commit_elect(x.bar_mma);
+        mma_run<kC>(x.tm + d_col(c), opZM, opU, id_d, true);
+        mma_commit_elect(bar_o);
       }
       if (!wait_bar(x.bar_mma, x.ph_mma)) { failed = true; break; }
-      // the slot is consumed (its MMAs are complete and gamma was read before the barrier
-      // wait): re-arm it for chunk c + 2 and tell the helpers
-      if (tid == 0) {
-        if (c + 2 < nch) mbar_expect_tx(full + s, kSlotPayload);
-        for (int r = 1; r < ncl; ++r) st_relaxed_remote(map_to(cons_local, r), (uint32_t)(c + 1));
-      }
       s_epilogue<DH>(x, sm + L::SS);
-      cta_sync_tc();
+      // the slot is consumed once O's MMA is complete (gamma was read before a barrier): re-arm
+      // it for chunk c + 2 and tell the helpers
+      bool ok_o = true;
+      if (tid == 0) {
+        ok_o = mbar_wait(bar_o, ph_o, kWaitNs);
+        if (ok_o) {
+          if (c + 2 < nch) mbar_expect_tx(full + s, kSlotPayload);
+          for (int r = 1; r < ncl; ++r) st_relaxed_remote(map_to(cons_local, r), (uint32_t)(c + 1));
+        }
+      }
+      ph_o ^= 1u;
+      fence_before_sync();
+      if (__syncthreads_or(!ok_o)) { failed = true; break; }
+      fence_after_sync();
     }
-    if (!failed && nch > 0) {
+    if (!failed && nch > 0 && !u_rows) {
       const int64_t tl = t0 + (int64_t)(nch - 1) * kC;
-      o_epilogue<DH>(x, out, tl, (int)(t1 - tl), H, h, 0, o_col(nch - 1));
+      o_store(nch - 1, tl, (int)(t1 - tl));
     }
     if (failed) {
       if (tid == 0) report(a.status, GDR_DEVCHECK_TIMEOUT);
@@ -336,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (kAlphaTile && !wait_bar(bar_a, ph_a)) { failed = true; break; }
 
       const bool safe = gate_stage<L, CHANNEL, false>(x, n);
-      // ... and the second (W, M, T'), before the Gram epilogue rewrites M
+      // ... and the second (-W, T', M), before the Gram epilogue rewrites M
       if (tid == 0) bulk_wait_read<0>();
       fence_async_smem();
       cta_sync_tc();
@@ -351,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       solve_stage<L>(x);
       if (!w_stage<L>(x, false, Opnd{0, 0, false}, 0)) { failed = true; break; }
-      w_epilogue<L>(x);
+      w_epilogue<L, true>(x);  // -W
       fence_async_smem();
       cta_sync_tc();
       // hand the operands over: slot c & 1 is free once chunk c - 2 has been consumed
@@ -360,14 +401,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t dst = chain_slots + (uint32_t)(c & 1) * kSlotBytes;
         const uint32_t mbar = chain_full + (uint32_t)(c & 1) * 8u;
         const uint32_t src = x.sb;
-        bulk_copy_to(dst + kSlotQ, src + L::KQ + 8192, 8192, mbar);          // Q~ slab 0
-        bulk_copy_to(dst + kSlotQ + 8192, src + L::KQ + 24576, 8192, mbar);  // Q~ slab 1
+        bulk_copy_to(dst + kSlotWQ + 8192, src + L::KQ + 8192, 8192, mbar);    // Q~, channels 0-63
+        bulk_copy_to(dst + kSlotWQ + 24576, src + L::KQ + 24576, 8192, mbar);  // Q~, 64-127
         bulk_copy_to(dst + kSlotKH, src + L::KH, 16384, mbar);
         bulk_copy_to(dst + kSlotGam, src + L::GAM, 512, mbar);
         bulk_commit();
-        bulk_copy_to(dst + kSlotW, src + L::WW, 16384, mbar);
-        bulk_copy_to(dst + kSlotM, src + L::MM, 8192, mbar);
+        bulk_copy_to(dst + kSlotWQ, src + L::WW, 8192, mbar);           // -W, channels 0-63
+        bulk_copy_to(dst + kSlotWQ + 16384, src + L::WW + 8192, 8192, mbar);  // -W, 64-127
         bulk_copy_to(dst + kSlotT, src + L::TT, 8192, mbar);
+        bulk_copy_to(dst + kSlotM, src + L::MM, 8192, mbar);
         bulk_commit();
       }
     }

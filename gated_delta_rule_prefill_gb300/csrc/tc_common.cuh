@@ -581,8 +581,8 @@ __device__ void solve_stage(const TcCtx& x) {
   cta_sync_tc();
 }
 
-// ---- Stage 4: W = T' K~ (and, with a V operand, U~ = T' V into the U accumulator), then W as
-// the bf16 K-major A operand WW.  Returns false if the MMA wait gave up.
+// ---- Stage 4: W = T' K~ (and, with a V operand, U~ = T' V into the U accumulator), then W (or
+// -W) as the bf16 K-major A operand WW.  Returns false if the MMA wait gave up.
 template <class L>
 __device__ bool w_stage(TcCtx& x, bool with_v, Opnd opV, uint32_t id_v) {
   const Opnd opT{x.sb + L::TT, 8192, false};
@@ -595,10 +595,14 @@ __device__ bool w_stage(TcCtx& x, bool with_v, Opnd opV, uint32_t id_v) {
   if (!wait_bar(x.bar_mma, x.ph_mma)) return false;
   return true;
 }
-template <class L>
+template <class L, bool NEG = false>
 __device__ void w_epilogue(const TcCtx& x) {
   float v[64];
   tmem_ld64(x.tm + x.lane_base + kColWO + x.wh * 64, v);
+  if constexpr (NEG) {
+#pragma unroll
+    for (int j = 0; j < 64; ++j) v[j] = -v[j];
+  }
   if (x.m64ok) {
 #pragma unroll
     for (int j = 0; j < 64; j += 8) st_chunk8(x.sm + L::WW, 8192, x.m64row, x.wh * 64 + j, v + j);
