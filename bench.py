@@ -85,8 +85,8 @@ def source_digest(files):
     return h.hexdigest()[:16]
 
 
-KERNEL_SOURCES = {"prefill": ["prefill_tc.cu", "umma.cuh"],
-                  "linear_attn": ["prefill_tc.cu", "umma.cuh"],
+KERNEL_SOURCES = {"prefill": ["prefill_cluster.cu", "prefill_tc.cu", "tc_common.cuh", "umma.cuh"],
+                  "linear_attn": ["prefill_tc.cu", "tc_common.cuh", "umma.cuh"],
                   "decode": ["decode.cu"]}
 
 

@@ -65,14 +65,14 @@ struct HelperSmem {
   static constexpr uint32_t ALPHA = BETA + 256;
   static constexpr uint32_t GAM = ALPHA + 256;
   static constexpr uint32_t RED = GAM + 512;
-  static constexpr uint32_t DIAG = RED + 64;
-  static constexpr uint32_t GS = DIAG + 256;
+  static constexpr uint32_t GS = RED + 64;
   static constexpr uint32_t TOT = GS + 256;       // gate carries [17][128] fp32
   static constexpr uint32_t CONS = TOT + 8704;    // chunks consumed by the chain CTA (u32)
   static constexpr uint32_t BARS = CONS + 64;     // qk, alpha, mma, TMEM slot
   static constexpr uint32_t END = BARS + 64;
   static constexpr uint32_t SA = KR;              // A [64][64] fp32 (Kr is consumed by then)
   static constexpr uint32_t ST32 = WW;            // T [64][64] fp32 (W is written later)
+  static constexpr uint32_t DIAGP = SX;           // q_r . k_r partials [64][16] (solve later)
 };
 
 constexpr size_t kClusterSmem =

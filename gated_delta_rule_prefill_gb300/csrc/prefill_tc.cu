@@ -61,23 +61,29 @@ struct TcSmem {
   static constexpr uint32_t ALPHA = BETA + 256;     // scalar gates [64]
   static constexpr uint32_t GAM = ALPHA + 256;      // gamma [128]
   static constexpr uint32_t RED = GAM + 512;        // reductions [8]
-  static constexpr uint32_t DIAG = RED + 64;        // q_r . k_r [64]
-  static constexpr uint32_t GS = DIAG + 256;        // scalar gates: log prefix sums [64]
-  static constexpr uint32_t BARS = GS + 256;        // 4 mbarriers + TMEM slot
-  static constexpr uint32_t END = BARS + 64;
+  static constexpr uint32_t GS = RED + 64;          // scalar gates: log prefix sums [64]
+  static constexpr uint32_t BARS = GS + 256;        // 12 mbarriers + TMEM slot
+  static constexpr uint32_t END = BARS + 128;
   static constexpr size_t bytes = END + 1024;       // + alignment slack
   // fp32 scratch of the solve, in tiles that are dead while it runs
   static constexpr uint32_t SA = KR;                // A [64][64]  (Kr is consumed by then)
   static constexpr uint32_t ST32 = WW;              // T [64][64]  (W is written later)
   static constexpr uint32_t SX = UU;                // [32][32] (U is written later)
   static constexpr uint32_t TOT = WW;               // gate carries [17][128] (W later)
+  static constexpr uint32_t DIAGP = UU;             // q_r . k_r partials [64][16] (U later)
+  // linear attention, segment prefix: 4 stages of [K tile 16 KB | V tile DV x 128 B] in tiles
+  // that are dead before the chunk loop starts (QIN+KIN, AIN, KQ, KR+KH)
+  __host__ __device__ static constexpr uint32_t pf(int st) {
+    return st == 0 ? QIN : st == 1 ? AIN : st == 2 ? KQ : KR;
+  }
   static_assert(bytes <= 232448, "shared memory per CTA");
   static_assert(DV * 128 >= 32 * 32 * 4, "block scratch fits in U");
+  static_assert(DV * 128 <= 16384 && KIN == QIN + 16384 && KH == KR + 16384, "prefix stages");
 };
 
 template <int DV, bool CHANNEL, bool LINEAR>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_tc_kernel(const __grid_constant__ TcMaps maps, const PrefillArgs a) {
+    prefill_tc_kernel(const __grid_constant__ TcMaps maps, const PrefillArgs a, int nseg) {
   using L = TcSmem<DV>;
   constexpr int NB = kD / DV;
   constexpr int DH = DV / 2;  // accumulator columns per warp half
@@ -93,28 +99,42 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_qk = bars + 1;
   uint64_t* bar_a = bars + 2;
   uint64_t* bar_v = bars + 3;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 4);
+  uint64_t* pf_full = bars + 4;  // [4] segment prefix: stage loaded
+  uint64_t* pf_mma = bars + 8;   // [4] segment prefix: stage consumed
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 12);
 
   const int tid = threadIdx.x, warp = tid >> 5;
   const int H = a.H;
-  const int rank = blockIdx.x / (H * NB);
-  const int rem = blockIdx.x % (H * NB);
-  const int h = rem / NB, vb = rem % NB;
+  // block -> (sequence rank, head, segment g of nseg, value-column block vb)
+  const int per_seq = H * nseg * NB;
+  const int rank = blockIdx.x / per_seq;
+  const int rem = blockIdx.x % per_seq;
+  const int h = rem / (nseg * NB);
+  const int g = (rem % (nseg * NB)) / NB, vb = rem % NB;
   const int seq = a.order ? a.order[rank] : rank;
   int64_t t0, t1;
   if (!seq_range(a, seq, t0, t1)) return;
+  // Linear attention splits a sequence into nseg runs of whole chunks; run g starts from
+  // S0 + sum over the earlier chunks of K^T V (its prefix, recomputed here).  nseg = 1 otherwise.
+  const int nch = (int)((t1 - t0 + kC - 1) / kC);
+  const int lseg = (nch + nseg - 1) / nseg;
+  const int c_begin = g * lseg, c_end = min(nch, c_begin + lseg);
+  if (g > 0 && c_begin >= c_end) return;
+  const int64_t ts = t0 + (int64_t)c_begin * kC;
+  const int64_t te = t0 + (int64_t)c_end * kC < t1 ? t0 + (int64_t)c_end * kC : t1;
   __nv_bfloat16* __restrict__ out = static_cast<__nv_bfloat16*>(a.out);
   const int vc0 = vb * DV;
   const size_t sidx = ((size_t)seq * H + h) * kD * kD;
 
   if (warp == 0) tmem_alloc(tslot, kTmemCols);
   if (tid == 0) {
-    for (int i = 0; i < 4; ++i) mbar_init(bars + i, 1);
+    for (int i = 0; i < 12; ++i) mbar_init(bars + i, 1);
     fence_mbar_init();
     prefetch_tmap(&maps.q);
     prefetch_tmap(&maps.k);
     prefetch_tmap(&maps.v);
     if (kAlphaTile) prefetch_tmap(&maps.alpha);
+    if (LINEAR && c_begin > 0) prefetch_tmap(&maps.k_sw);
   }
   cta_sync_tc();
   TcCtx x = make_ctx(sm, *tslot, bars + 0);
@@ -146,21 +166,79 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto load_scalars = [&](int64_t tc, float& b, float& al) {
     b = 0.f;
     al = 1.f;
-    if (tid < kC && tc + tid < t1) {
+    if (tid < kC && tc + tid < te) {
       const size_t o = (size_t)(tc + tid) * H + h;
       if (!LINEAR) b = a.beta[o];
       if (!CHANNEL && !LINEAR) al = a.alpha[o];
     }
   };
 
-  if (t0 < t1) {
-    issue_qk(t0);
-    issue_a(t0);
-    issue_v(t0);
+  s_init<DH>(x, a.S0 ? a.S0 + sidx + (size_t)x.lrow * kD + vc0 : nullptr, sm + L::SS);
+  if constexpr (LINEAR) {
+    if (c_begin > 0) {
+      // segment prefix: S += K_c^T V_c over chunks [0, c_begin) (all full), 4 TMA stages, one
+      // chunk's MMA per step; warp 0 drives it, the other warps wait at the barrier below
+      cta_sync_tc();  // S0 is in TMEM
+      bool pf_ok = true;
+      if (warp == 0) {
+        // lane 0 waits, the warp follows its verdict (the MMAs are issued warp-wide)
+        auto warp_wait = [&](uint64_t* bar, uint32_t parity) {
+          bool ok = true;
+          if ((tid & 31) == 0) ok = mbar_wait(bar, parity, kWaitNs);
+          return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        };
+        uint32_t ph_f = 0, ph_m = 0;  // per-stage phase bits
+        auto pf_issue = [&](int cp) {
+          if (tid == 0) {
+            const int st = cp & 3;
+            const int64_t tc = t0 + (int64_t)cp * kC;
+            mbar_expect_tx(pf_full + st, 16384 + DV * 128);
+            tma_load_3d(sm + L::pf(st), &maps.k_sw, 0, h, (int)tc, pf_full + st);
+            tma_load_3d(sm + L::pf(st) + 8192, &maps.k_sw, 64, h, (int)tc, pf_full + st);
+#pragma unroll
+            for (int s2 = 0; s2 < DV / 64; ++s2)
+              tma_load_3d(sm + L::pf(st) + 16384 + s2 * 8192, &maps.v, vc0 + 64 * s2, h, (int)tc,
+                          pf_full + st);
+          }
+        };
+        for (int cp = 0; cp < 3 && cp < c_begin; ++cp) pf_issue(cp);
+#pragma unroll 1
+        for (int cp = 0; cp < c_begin; ++cp) {
+          const int st = cp & 3;
+          if (!warp_wait(pf_full + st, (ph_f >> st) & 1u)) { pf_ok = false; break; }
+          ph_f ^= 1u << st;
+          const Opnd opKp{x.sb + L::pf(st), 8192, true};           // K as MN-major A
+          const Opnd opVp{x.sb + L::pf(st) + 16384, 8192, true};   // V as MN-major B
+          mma_run<kC>(x.tm + kColS, opKp, opVp, idesc_bf16(128, DV, false, true, true), true);
+          mma_commit_elect(pf_mma + st);
+          if (cp + 3 < c_begin) {  // stage (cp + 3) & 3 held chunk cp - 1: its MMA must be done
+            if (cp >= 1) {
+              const int sp = (cp - 1) & 3;
+              if (!warp_wait(pf_mma + sp, (ph_m >> sp) & 1u)) { pf_ok = false; break; }
+              ph_m ^= 1u << sp;
+            }
+            pf_issue(cp + 3);
+          }
+        }
+        mma_commit_elect(x.bar_mma);  // every prefix MMA complete
+      }
+      if (__syncthreads_or(!pf_ok)) {
+        failed = true;
+      } else if (!wait_bar(x.bar_mma, x.ph_mma)) {
+        failed = true;
+      } else {
+        s_epilogue<DH>(x, sm + L::SS);  // the bf16 operand copy of the segment's entering state
+        cta_sync_tc();
+      }
+    }
+  }
+  if (!failed && ts < te) {
+    issue_qk(ts);
+    issue_a(ts);
+    issue_v(ts);
   }
   float nb_beta, nb_alpha;
-  load_scalars(t0, nb_beta, nb_alpha);
-  s_init<DH>(x, a.S0 ? a.S0 + sidx + (size_t)x.lrow * kD + vc0 : nullptr, sm + L::SS);
+  load_scalars(ts, nb_beta, nb_alpha);
 
   // operand views of the state pass
   const Opnd opQ{x.sb + L::KQ + 8192, 16384, false};  // Q~ rows as K-major A (M = 64)
@@ -175,15 +253,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t id_s = idesc_bf16(128, DV, false, true, true);
 
 #pragma unroll 1
-  for (int64_t tc = t0; tc < t1 && !failed; tc += kC) {
-    const int n = (int)((t1 - tc) < (int64_t)kC ? (t1 - tc) : (int64_t)kC);
+  for (int64_t tc = ts; tc < te && !failed; tc += kC) {
+    const int n = (int)((te - tc) < (int64_t)kC ? (te - tc) : (int64_t)kC);
     const int64_t tn = tc + kC;  // next chunk
 
     if (tid < kC) {
       sBeta[tid] = nb_beta;
       sAlpha[tid] = nb_alpha;
     }
-    if (tn < t1) load_scalars(tn, nb_beta, nb_alpha);
+    if (tn < te) load_scalars(tn, nb_beta, nb_alpha);
     if (!wait_bar(bar_qk, ph_qk)) { failed = true; break; }
     if (kAlphaTile && !wait_bar(bar_a, ph_a)) { failed = true; break; }
 
@@ -191,13 +269,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool safe = gate_stage<L, CHANNEL, LINEAR>(x, n);
     fence_async_smem();
     cta_sync_tc();
-    if (safe && tn < t1) {  // q, k and alpha tiles are consumed: fetch the next chunk's
+    if (safe && tn < te) {  // q, k and alpha tiles are consumed: fetch the next chunk's
       issue_qk(tn);
       issue_a(tn);
     }
     // 2. decay-weighted Gram matrices [A'; M]
     if (!gram_stage<L, CHANNEL, LINEAR>(x, n, safe)) { failed = true; break; }
-    if (!safe && tn < t1) {
+    if (!safe && tn < te) {
       issue_qk(tn);
       issue_a(tn);
     }
@@ -209,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // 3. T' = (I + A)^-1 diag(beta);  4. W = T' K~ and U~ = T' V
       solve_stage<L>(x);
       if (!w_stage<L>(x, true, opV, id_v)) { failed = true; break; }
-      if (tn < t1) issue_v(tn);  // V is consumed
+      if (tn < te) issue_v(tn);  // V is consumed
       w_epilogue<L>(x);
     }
     cta_sync_tc();
@@ -233,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit_elect(x.bar_mma);
     }
     if (!wait_bar(x.bar_mma, x.ph_mma)) { failed = true; break; }
-    if (LINEAR && tn < t1) issue_v(tn);
+    if (LINEAR && tn < te) issue_v(tn);
     o_epilogue<DH>(x, out, tc, n, H, h, vc0);
     s_epilogue<DH>(x, sm + L::SS);
     cta_sync_tc();
@@ -245,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait(bar_qk, ph_qk, kWaitNs);
     if (kAlphaTile) mbar_wait(bar_a, ph_a, kWaitNs);
     mbar_wait(bar_v, ph_v, kWaitNs);
-  } else if (a.S_final) {
+  } else if (a.S_final && c_end == nch) {  // the last run of the sequence hands the state on
     s_final<DH>(x, a.S_final + sidx + (size_t)x.lrow * kD + vc0);
   }
   cta_sync_tc();
@@ -295,6 +373,9 @@ bool make_tc_maps(const gdr_shape& sh, const PrefillArgs& a, bool linear, TcMaps
                      CU_TENSOR_MAP_SWIZZLE_NONE) &&
             make_map(&maps->v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, T, 64,
                      CU_TENSOR_MAP_SWIZZLE_128B);
+  if (ok && linear)
+    ok = make_map(&maps->k_sw, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, T, 64,
+                  CU_TENSOR_MAP_SWIZZLE_128B);
   if (ok && !linear && sh.gate == GDR_GATE_CHANNEL)
     ok = make_map(&maps->alpha, a.alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, T, kD,
                   CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -305,24 +386,33 @@ bool make_tc_maps(const gdr_shape& sh, const PrefillArgs& a, bool linear, TcMaps
 namespace {
 
 template <int DV, bool CHANNEL, bool LINEAR>
-cudaError_t launch_one(const gdr_shape& sh, const PrefillArgs& a, const TcMaps& maps,
+cudaError_t launch_one(const gdr_shape& sh, const PrefillArgs& a, const TcMaps& maps, int nseg,
                        cudaStream_t s) {
   auto kern = prefill_tc_kernel<DV, CHANNEL, LINEAR>;
   const size_t smem = TcSmem<DV>::bytes;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)sh.n_seqs * (unsigned)sh.H * (unsigned)(kD / DV);
-  kern<<<grid, kThreads, smem, s>>>(maps, a);
+  const unsigned grid =
+      (unsigned)sh.n_seqs * (unsigned)sh.H * (unsigned)nseg * (unsigned)(kD / DV);
+  kern<<<grid, kThreads, smem, s>>>(maps, a, nseg);
   return cudaGetLastError();
 }
 
 template <int DV>
 cudaError_t launch_dv(const gdr_shape& sh, const PrefillArgs& a, const TcMaps& maps, bool linear,
-                      cudaStream_t s) {
-  if (linear) return launch_one<DV, true, true>(sh, a, maps, s);
-  if (sh.gate == GDR_GATE_CHANNEL) return launch_one<DV, true, false>(sh, a, maps, s);
-  return launch_one<DV, false, false>(sh, a, maps, s);
+                      int nseg, cudaStream_t s) {
+  if (linear) return launch_one<DV, true, true>(sh, a, maps, nseg, s);
+  if (sh.gate == GDR_GATE_CHANNEL) return launch_one<DV, true, false>(sh, a, maps, 1, s);
+  return launch_one<DV, false, false>(sh, a, maps, 1, s);
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return n;
 }
 
 }  // namespace
@@ -342,10 +432,20 @@ cudaError_t launch_prefill_tc(const gdr_shape& sh, const PrefillArgs& a, bool li
     const int ncl = tc::cluster_size_for(sh);
     if (ncl > 1) return tc::launch_prefill_cluster(sh, a, maps, ncl, s);
   }
-  // value-column split: enough CTAs to cover the SMs when there are few (sequence, head) pairs
   const long pairs = (long)sh.n_seqs * sh.H;
-  if (pairs >= 120) return launch_dv<128>(sh, a, maps, linear, s);
-  return launch_dv<64>(sh, a, maps, linear, s);
+  if (linear) {
+    // linear attention with few (sequence, head) pairs: runs of at least 16 chunks per CTA, as
+    // many as fill the SMs once (each run recomputes its entering state from the chunks before)
+    const long sms = sm_count();
+    const long avg_chunks = sh.total_tokens / ((long)sh.n_seqs * kC);
+    long nseg = pairs > 0 ? sms / pairs : 1;
+    if (nseg > avg_chunks / 16) nseg = avg_chunks / 16;
+    if (nseg > 8) nseg = 8;
+    if (nseg > 1) return launch_dv<128>(sh, a, maps, true, (int)nseg, s);
+  }
+  // value-column split: enough CTAs to cover the SMs when there are few (sequence, head) pairs
+  if (pairs >= 120) return launch_dv<128>(sh, a, maps, linear, 1, s);
+  return launch_dv<64>(sh, a, maps, linear, 1, s);
 }
 
 }  // namespace gdr

@@ -214,6 +214,7 @@ __device__ __forceinline__ void ld_bf16x8(const __nv_bfloat16* p, float* x) {
 
 struct TcMaps {
   CUtensorMap q, k, v, alpha;
+  CUtensorMap k_sw;  // k in 64-channel SW128 boxes (linear attention's segment prefix)
 };
 
 
@@ -272,7 +273,7 @@ __device__ bool gate_stage(const TcCtx& x, int n) {
   float* sAlpha = reinterpret_cast<float*>(sm + L::ALPHA);
   float* sGam = reinterpret_cast<float*>(sm + L::GAM);
   float* sRed = reinterpret_cast<float*>(sm + L::RED);
-  float* sDiag = reinterpret_cast<float*>(sm + L::DIAG);
+  float* sDiagP = reinterpret_cast<float*>(sm + L::DIAGP);  // [64 rows][16] partial q_r . k_r
   float* sGs = reinterpret_cast<float*>(sm + L::GS);
     // ================= 1. gates and operand tiles
     // thread = 8 key channels (group g8) x 4 tokens (row block rb)
@@ -315,9 +316,7 @@ __device__ bool gate_stage(const TcCtx& x, int n) {
           kh[cc] = k8[cc] * eh;
           dq = fmaf(q8[cc], k8[cc], dq);
         }
-#pragma unroll
-        for (int off = 8; off > 0; off >>= 1) dq += __shfl_xor_sync(0xffffffffu, dq, off);
-        if (g8 == 0) sDiag[r] = dq;
+        sDiagP[r * 16 + g8] = dq;
         st_chunk8(sm + L::KQ, 16384, r, 8 * g8, k8);       // K (scaled to K~ after the Gram MMA)
         st_chunk8(sm + L::KQ, 16384, 64 + r, 8 * g8, q8);  // Q (scaled to Q~ likewise)
         st_chunk8(sm + L::KR, 8192, r, 8 * g8, k8);        // K
@@ -420,11 +419,7 @@ __device__ bool gate_stage(const TcCtx& x, int n) {
             kh[cc] = ki[cc] * gn[cc];
             dq = fmaf(q8[cc], k8[cc], dq);
           }
-          if (!LINEAR) {  // the diagonal of M carries no decay: q_r . k_r in fp32
-#pragma unroll
-            for (int off = 8; off > 0; off >>= 1) dq += __shfl_xor_sync(0xffffffffu, dq, off);
-            if (g8 == 0) sDiag[r] = dq;
-          }
+          if (!LINEAR) sDiagP[r * 16 + g8] = dq;  // M's diagonal carries no decay: q_r . k_r
           st_chunk8(sm + L::KQ, 16384, r, 8 * g8, ke);       // K~
           st_chunk8(sm + L::KQ, 16384, 64 + r, 8 * g8, qe);  // Q~
           st_chunk8(sm + L::KR, 8192, r, 8 * g8, ki);        // Kr
@@ -471,7 +466,7 @@ __device__ bool gram_stage(TcCtx& x, int n, bool safe) {
   float* sAin = reinterpret_cast<float*>(sm + L::AIN);
   float* sA = reinterpret_cast<float*>(sm + L::SA);
   float* sBeta = reinterpret_cast<float*>(sm + L::BETA);
-  float* sDiag = reinterpret_cast<float*>(sm + L::DIAG);
+  const float* sDiagP = reinterpret_cast<const float*>(sm + L::DIAGP);
   float* sGs = reinterpret_cast<float*>(sm + L::GS);
   const Opnd opKQ{x.sb + L::KQ, 16384, false};  // [K~;Q~] as K-major A (M = 128)
   const Opnd opKR{x.sb + L::KR, 8192, false};   // Kr as K-major B (N = 64 tokens)
@@ -503,10 +498,18 @@ __device__ bool gram_stage(TcCtx& x, int n, bool safe) {
                              (c0 + j + 3 < r) ? b * xv[j + 3] : 0.f));
         }
       } else {
+        float dg = 0.f;  // q_r . k_r, summed from the gate stage's 16 partials
+        if (!LINEAR && r >= c0 && r < c0 + 32) {
+#pragma unroll
+          for (int i = 0; i < 16; i += 4) {
+            const float4 p4 = *reinterpret_cast<const float4*>(sDiagP + r * 16 + i);
+            dg += (p4.x + p4.y) + (p4.z + p4.w);
+          }
+        }
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           xv[j] = (c0 + j <= r) ? xv[j] : 0.f;
-          if (!LINEAR && c0 + j == r) xv[j] = sDiag[r];
+          if (!LINEAR && c0 + j == r) xv[j] = dg;
         }
 #pragma unroll
         for (int j = 0; j < 32; j += 8) st_chunk8(sm + L::MM, 8192, r, c0 + j, xv + j);

@@ -47,6 +47,11 @@ def test_prefill_full(name):
     ro, rs = oracle.gated_delta(a["q"], a["k"], a["v"], a["alpha"], a["beta"], S0=a["S0"],
                                 cu_seqlens=a["cu_seqlens"])
     _check(name, host(out), host(Sf), ro, rs, TOL[wl.dtype])
+    if name == "kda_b1_h32_t32768":  # the benchmark's linear-attention pass over the same inputs
+        del ro, rs
+        lout, lSf = _prefill(d, linear=True)
+        lo, ls = oracle.linear_attn(a["q"], a["k"], a["v"], S0=a["S0"], cu_seqlens=a["cu_seqlens"])
+        _check(name + " linear", host(lout), host(lSf), lo, ls, TOL[wl.dtype])
 
 
 def test_decode_full_size():

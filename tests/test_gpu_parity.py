@@ -83,6 +83,16 @@ def test_linear_attn_ragged(d, dtype):
           "linear d=%d %s" % (d, dtype))
 
 
+# few (sequence, head) pairs and long sequences: the linear pass splits each sequence into runs of
+# whole chunks, one CTA each, every run starting from the state its earlier chunks imply
+@pytest.mark.parametrize("lens,H", [([9000], 1), ([5000, 4000, 64], 2), ([3000, 2500], 3)])
+def test_linear_attn_segmented(lens, H):
+    wl = gi.custom(seed=23 + H, seqlens=lens, H=H, d_k=128, d_v=128, dtype="bf16", s0="normal")
+    a = gi.gen_full(wl)
+    check(run_prefill(a, "bf16", linear=True), ref_prefill(a, linear=True), TOL["bf16"],
+          "linear segmented %s H=%d" % (lens, H))
+
+
 @pytest.mark.parametrize("case", ["alpha0", "alpha1_beta0", "beta1", "tiny_alpha"])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_prefill_special_gates(case, dtype):
