@@ -132,17 +132,27 @@ class ClockSampler:
     def __init__(self):
         self.proc = None
         self.path = None
+        self.offset = 0
 
     def start(self):
+        """Start sampling every 20 ms and return once the first sample has been written."""
         try:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.Q,
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
+            t0 = time.time()
+            while os.path.getsize(self.path) == 0 and time.time() - t0 < 5:
+                time.sleep(0.01)
         except Exception:
             self.proc = None
+
+    def begin(self):
+        """Mark the start of the timed region: earlier samples are dropped (but one is kept)."""
+        if self.path:
+            self.offset = os.path.getsize(self.path)
 
     def stop(self):
         if not self.proc:
@@ -153,13 +163,17 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.f.close()
-        rows = []
+        rows, before = [], []
         with open(self.path) as f:
+            pos = 0
             for line in f:
                 parts = [x.strip() for x in line.split(",")]
                 if len(parts) >= 9:
-                    rows.append(parts)
+                    (rows if pos >= self.offset else before).append(parts)
+                pos += len(line)
         os.unlink(self.path)
+        if not rows and before:  # region shorter than the sampling interval: the last sample
+            rows = before[-1:]
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         dev = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0]
@@ -311,6 +325,7 @@ def run_gpu(args):
     clocks = ClockSampler()
     clocks.start()
     torch.cuda.synchronize()
+    clocks.begin()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
@@ -429,7 +444,7 @@ def run_gpu(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
