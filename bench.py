@@ -85,7 +85,7 @@ def source_digest(files):
     return h.hexdigest()[:16]
 
 
-KERNEL_SOURCES = {"prefill": ["prefill_cluster.cu", "prefill_tc.cu", "tc_common.cuh", "umma.cuh"],
+KERNEL_SOURCES = {"prefill": ["prefill_queue.cu", "prefill_tc.cu", "tc_common.cuh", "umma.cuh"],
                   "linear_attn": ["prefill_tc.cu", "tc_common.cuh", "umma.cuh"],
                   "decode": ["decode.cu"]}
 
@@ -281,14 +281,16 @@ def run_gpu(args):
     Sf = torch.empty_like(P["S0"])
     out_l = torch.empty_like(out)
     Sf_l = torch.empty_like(P["S0"])
-    ws = torch.empty(g.gdr_prefill_workspace_size(wp.n_seqs), dtype=torch.uint8, device=dev)
+    ws = torch.empty(g.gdr_prefill_workspace_size(wp.n_seqs, H, d, d), dtype=torch.uint8,
+                     device=dev)
 
     wd = gi.workload(DECODE)
     wd_pre = gi.Workload(wd.name, wd.seed, wd.H, wd.d_k, wd.d_v, wd.dtype, wd.gate,
                          np.full(wd.n_seqs, DECODE_PREFILL_LEN, dtype=np.int64), "zeros")
     S_dec = torch.empty((wd.n_seqs, wd.H, wd.d_k, wd.d_v), dtype=torch.float32, device=dev)
     # states pre-filled by a seeded 2048-token prefill, 32 sequences at a time
-    ws_d = torch.empty(g.gdr_prefill_workspace_size(32), dtype=torch.uint8, device=dev)
+    ws_d = torch.empty(g.gdr_prefill_workspace_size(32, wd.H, wd.d_k, wd.d_v), dtype=torch.uint8,
+                       device=dev)
     for s0 in range(0, wd.n_seqs, 32):
         part = gi.Workload(wd.name, wd.seed + s0, wd.H, wd.d_k, wd.d_v, wd.dtype, wd.gate,
                            wd_pre.seqlens[s0:s0 + 32], "zeros")

@@ -7,7 +7,7 @@ library's CUDA kernels; there is no Python or CPU fallback.
     gdr_prefill(q, k, v, alpha, beta, S0=None, cu_seqlens=None, out=None, S_final=None, ...)
     gdr_decode_step(q, k, v, alpha, beta, S_inout, out=None)
     gdr_linear_attn(q, k, v, S0=None, cu_seqlens=None, out=None, S_final=None, ...)
-    gdr_prefill_workspace_size(n_seqs)  /  gdr_workspace_status(workspace)
+    gdr_prefill_workspace_size(n_seqs, H, d_k, d_v, dtype)  /  gdr_workspace_status(workspace)
 """
 from __future__ import annotations
 
@@ -16,7 +16,7 @@ import ctypes
 import torch
 
 from . import _abi
-from ._abi import (GDR_BF16, GDR_F32, GDR_FLAG_FORCE_SIMT, GDR_FLAG_NO_CLUSTER,
+from ._abi import (GDR_BF16, GDR_F32, GDR_FLAG_FORCE_SIMT, GDR_FLAG_NO_CLUSTER, GDR_FLAG_PREFER_QUEUE,
                    GDR_GATE_CHANNEL, GDR_GATE_SCALAR,
                    GdrError, GdrShape)
 
@@ -51,20 +51,23 @@ def make_shape(n_seqs, H, total_tokens, d_k, d_v, dtype, gate=GDR_GATE_CHANNEL, 
     return GdrShape(n_seqs, H, total_tokens, d_k, d_v, dtype, gate, chunk_size, flags)
 
 
-def gdr_prefill_workspace_size(n_seqs: int) -> int:
-    sh = make_shape(n_seqs, 1, 0, 128, 128, GDR_BF16)
+def gdr_prefill_workspace_size(n_seqs: int, H: int = 1, d_k: int = 128, d_v: int = 128,
+                               dtype: str = "bf16") -> int:
+    """Bytes of the workspace gdr_prefill / gdr_linear_attn use for this shape."""
+    sh = make_shape(n_seqs, H, 0, d_k, d_v, GDR_BF16 if dtype == "bf16" else GDR_F32)
     return int(_abi.load().gdr_prefill_workspace_size(ctypes.byref(sh)))
 
 
-def _workspace(n_seqs, device, workspace):
-    need = gdr_prefill_workspace_size(n_seqs)
+def _workspace(n_seqs, H, d_k, d_v, dtype, device, workspace):
     if workspace is None:
+        need = gdr_prefill_workspace_size(n_seqs, H, d_k, d_v, dtype)
         workspace = torch.empty(need, dtype=torch.uint8, device=device)
     return workspace
 
 
 def _prefill_like(linear, q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, workspace,
-                  chunk_size, force_simt, stream, want_final, no_cluster=False):
+                  chunk_size, force_simt, stream, want_final, no_cluster=False,
+                  prefer_queue=False):
     T, H, dk = q.shape
     dv = v.shape[2]
     dtype = _DT.get(q.dtype)
@@ -86,8 +89,10 @@ def _prefill_like(linear, q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, wo
     if S_final is None and want_final:
         S_final = torch.empty((n_seqs, H, dk, dv), dtype=torch.float32, device=q.device)
     _check(S_final, "S_final", torch.float32)
-    ws = _workspace(n_seqs, q.device, workspace)
-    flags = (GDR_FLAG_FORCE_SIMT if force_simt else 0) | (GDR_FLAG_NO_CLUSTER if no_cluster else 0)
+    ws = _workspace(n_seqs, H, dk, dv, "bf16" if dtype == GDR_BF16 else "f32", q.device,
+                    workspace)
+    flags = ((GDR_FLAG_FORCE_SIMT if force_simt else 0) | (GDR_FLAG_NO_CLUSTER if no_cluster else 0)
+             | (GDR_FLAG_PREFER_QUEUE if prefer_queue else 0))
     sh = make_shape(n_seqs, H, T, dk, dv, dtype, gate, chunk_size, flags)
     lib = _abi.load()
     if linear:
@@ -105,12 +110,12 @@ def _prefill_like(linear, q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, wo
 
 def gdr_prefill(q, k, v, alpha, beta, S0=None, cu_seqlens=None, out=None, S_final=None,
                 workspace=None, chunk_size=0, force_simt=False, stream=None, want_final=True,
-                no_cluster=False):
+                no_cluster=False, prefer_queue=False):
     """Chunked packed-varlen prefill.  q,k [T,H,d_k], v [T,H,d_v] (fp32 or bf16); alpha
     [T,H,d_k] or [T,H] fp32; beta [T,H] fp32; S0 [N,H,d_k,d_v] fp32 or None; cu_seqlens int32
     [N+1] or None.  Returns (out [T,H,d_v], S_final [N,H,d_k,d_v] or None)."""
     return _prefill_like(False, q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, workspace,
-                         chunk_size, force_simt, stream, want_final, no_cluster)
+                         chunk_size, force_simt, stream, want_final, no_cluster, prefer_queue)
 
 
 def gdr_linear_attn(q, k, v, S0=None, cu_seqlens=None, out=None, S_final=None, workspace=None,

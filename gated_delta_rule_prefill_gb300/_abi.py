@@ -12,6 +12,7 @@ GDR_F32, GDR_BF16 = 0, 1
 GDR_GATE_SCALAR, GDR_GATE_CHANNEL = 0, 1
 GDR_FLAG_FORCE_SIMT = 1
 GDR_FLAG_NO_CLUSTER = 2
+GDR_FLAG_PREFER_QUEUE = 4
 GDR_DEVCHECK_OK, GDR_DEVCHECK_SEQLENS, GDR_DEVCHECK_TIMEOUT = 0, 1, 2
 
 # every symbol include/gdr.h declares

@@ -58,7 +58,7 @@ gdr_status check_shape(const gdr_shape* sh, bool need_gate) {
   if (sh->dtype != GDR_F32 && sh->dtype != GDR_BF16) return GDR_ERR_INVALID_ARG;
   if (need_gate && sh->gate != GDR_GATE_SCALAR && sh->gate != GDR_GATE_CHANNEL)
     return GDR_ERR_INVALID_ARG;
-  if (sh->chunk_size < 0 || (sh->flags & ~(GDR_FLAG_FORCE_SIMT | GDR_FLAG_NO_CLUSTER))) return GDR_ERR_INVALID_ARG;
+  if (sh->chunk_size < 0 || (sh->flags & ~(GDR_FLAG_FORCE_SIMT | GDR_FLAG_NO_CLUSTER | GDR_FLAG_PREFER_QUEUE))) return GDR_ERR_INVALID_ARG;
   if (sh->d_k != sh->d_v || (sh->d_k != 64 && sh->d_k != 128)) return GDR_ERR_UNSUPPORTED;
   // grid sizes stay within 32-bit block counts
   if ((int64_t)sh->n_seqs * sh->H * 4 > (int64_t)INT32_MAX) return GDR_ERR_UNSUPPORTED;
@@ -87,8 +87,15 @@ gdr_status prefill_common(const gdr_shape* sh, const void* q, const void* k, con
   cudaStream_t s = (cudaStream_t)stream;
   int32_t* status = (int32_t*)ws;
   int32_t* order = (int32_t*)((char*)ws + WorkspaceLayout::kHeaderBytes);
+  uint32_t* ring_flags = nullptr;
+  unsigned char* ring = nullptr;
+  if (WorkspaceLayout::ring_bytes(*sh) > 0 && ws_bytes >= WorkspaceLayout::full(*sh)) {
+    ring_flags = (uint32_t*)((char*)ws + WorkspaceLayout::total(sh->n_seqs));
+    ring = (unsigned char*)ring_flags +
+           WorkspaceLayout::flag_bytes(WorkspaceLayout::ring_pairs(*sh));
+  }
   PrefillArgs a{sh->n_seqs, sh->H, sh->total_tokens, q, k, v, alpha, beta, S0, cu,
-                out, S_final, order, status};
+                out, S_final, order, status, ring_flags, ring};
   prep_kernel<<<1, kPrepThreads, 0, s>>>(cu, sh->n_seqs, sh->total_tokens, order, status);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess)
@@ -112,8 +119,8 @@ gdr_status prefill_launch(const gdr_shape* sh, const void* q, const void* k, con
 extern "C" {
 
 size_t gdr_prefill_workspace_size(const gdr_shape* shape) {
-  if (!shape || shape->n_seqs < 1) return 0;
-  return gdr::WorkspaceLayout::total(shape->n_seqs);
+  if (!shape || shape->n_seqs < 1 || shape->H < 1) return 0;
+  return gdr::WorkspaceLayout::full(*shape);
 }
 
 gdr_status gdr_prefill(const gdr_shape* shape, const void* q, const void* k, const void* v,

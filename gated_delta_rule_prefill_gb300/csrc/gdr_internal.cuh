@@ -26,11 +26,33 @@ __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
 
 __device__ __forceinline__ float log_gate(float a) { return fmaxf(__logf(a), kLogAlphaMin); }
 
-// Workspace layout used by the prefill / linear-attention calls.
+// Workspace layout used by the prefill / linear-attention calls: the status word, the visiting
+// order, then (for shapes the work-queue tensor-core prefill may run) its flags and a ring of
+// operand slots per (sequence, head) chain, through which helper CTAs hand prepared chunks to
+// the chain's CTA.
 struct WorkspaceLayout {
-  static constexpr size_t kHeaderBytes = 256;  // int32 status word + reserved
+  static constexpr size_t kHeaderBytes = 256;      // int32 status word + reserved
+  static constexpr size_t kRingSlotBytes = 74752;  // one chunk's operand slot image
+  static constexpr int kRingSlots = 6;             // chunks in flight per chain
+  static constexpr long kRingMaxPairs = 76;        // chains of the largest work-queue launch
   static size_t order_bytes(int n_seqs) { return ((size_t)n_seqs * 4 + 255) / 256 * 256; }
+  // the minimum: enough for every path except the work-queue prefill
   static size_t total(int n_seqs) { return kHeaderBytes + order_bytes(n_seqs); }
+  static long ring_pairs(const gdr_shape& sh) {
+    const long pairs = (long)sh.n_seqs * sh.H;
+    return (sh.dtype == GDR_BF16 && sh.d_k == 128 && sh.d_v == 128 && pairs <= kRingMaxPairs)
+               ? pairs : 0;
+  }
+  // work-item counter, ready[pairs][slots], loaded[pairs] (uint32)
+  static size_t flag_bytes(long pairs) {
+    return ((size_t)(1 + pairs * kRingSlots + pairs) * 4 + 255) / 256 * 256;
+  }
+  static size_t ring_bytes(const gdr_shape& sh) {
+    const long p = ring_pairs(sh);
+    return p ? flag_bytes(p) + (size_t)p * kRingSlots * kRingSlotBytes : 0;
+  }
+  // the full size (gdr_prefill_workspace_size): also enables the work-queue prefill
+  static size_t full(const gdr_shape& sh) { return total(sh.n_seqs) + ring_bytes(sh); }
 };
 
 // Arguments of the chunked prefill kernels (device pointers; see gdr.h for layouts).
@@ -48,6 +70,8 @@ struct PrefillArgs {
   float* S_final;
   const int32_t* order;  // sequence visiting order (longest first)
   int32_t* status;       // device-check word
+  uint32_t* ring_flags;  // work-queue prefill: counter, ready, loaded (null: not available)
+  unsigned char* ring;   // work-queue prefill: operand slots
 };
 
 // Records the first device-check failure (0 -> code).

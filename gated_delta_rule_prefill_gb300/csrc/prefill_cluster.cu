@@ -31,16 +31,6 @@ namespace {
 
 using namespace umma;
 
-// slot layout (bytes from the slot base); K-major tiles of 128 rows have 16 KB slabs
-constexpr uint32_t kSlotWQ = 0;       // [-W; Q~] 128 x 128: -W rows at +0 / +16K, Q~ at +8K / +24K
-constexpr uint32_t kSlotKH = 32768;   // K^  [tok][ch] (MN-major A), slabs 8 KB apart
-constexpr uint32_t kSlotT = 49152;    // T'  [64][64]   } [T'; Z] and [Z; M] are
-constexpr uint32_t kSlotZ = 57344;    // zeros [64][64] } 128 x 64 K-major tiles
-constexpr uint32_t kSlotM = 65536;    // M   [64][64]   }
-constexpr uint32_t kSlotGam = 73728;  // gamma [128] fp32
-constexpr uint32_t kSlotPayload = 65536 + 512;  // everything but Z
-constexpr uint32_t kSlotBytes = 74752;          // 1024-aligned
-
 struct ChainSmem {
   static constexpr uint32_t SLOT = 0;                      // 2 slots
   static constexpr uint32_t VIN = 2 * kSlotBytes;          // V [64 tok][128] SW128, 2 slabs

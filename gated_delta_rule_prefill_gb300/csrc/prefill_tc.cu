@@ -427,9 +427,14 @@ cudaError_t launch_prefill_tc(const gdr_shape& sh, const PrefillArgs& a, bool li
                               cudaStream_t s) {
   TcMaps maps;
   if (!tc::make_tc_maps(sh, a, linear, &maps)) return cudaErrorInvalidValue;
-  // few (sequence, head) chains: clusters whose helper CTAs prepare the chunks of a chain
+  // few (sequence, head) chains: helper CTAs prepare the chunks of each chain, in clusters (the
+  // operands cross over DSMEM) or, when clusters would give a chain a single helper, from a
+  // work queue over every SM (the operands cross through L2 rings in the workspace)
   if (!linear && !(sh.flags & GDR_FLAG_NO_CLUSTER)) {
     const int ncl = tc::cluster_size_for(sh);
+    const int G = tc::queue_grid_for(sh, a);
+    if (G > 0 && (ncl <= 2 || (sh.flags & GDR_FLAG_PREFER_QUEUE)))
+      return tc::launch_prefill_queue(sh, a, maps, G, s);
     if (ncl > 1) return tc::launch_prefill_cluster(sh, a, maps, ncl, s);
   }
   const long pairs = (long)sh.n_seqs * sh.H;

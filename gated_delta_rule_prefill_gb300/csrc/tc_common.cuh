@@ -27,6 +27,18 @@ constexpr uint32_t kColWO = 256;  // W accumulator, then O accumulator (M = 64 l
 constexpr uint32_t kColAM = 384;  // [A'; M] accumulator (M = 128), 64 columns
 constexpr uint32_t kTmemCols = 512;
 
+// Operand slot of one chunk as a chain CTA consumes it (bytes from the slot base; K-major tiles
+// of 128 rows have 16 KB slabs).  With a zero tile Z between T' and M, [T'; Z] and [Z; M] are
+// 128 x 64 K-major tiles; [-W; Q~] is one 128 x 128 tile.
+constexpr uint32_t kSlotWQ = 0;       // [-W; Q~]: -W rows at +0 / +16K, Q~ rows at +8K / +24K
+constexpr uint32_t kSlotKH = 32768;   // K^  [tok][ch] (MN-major A), slabs 8 KB apart
+constexpr uint32_t kSlotT = 49152;    // T'  [64][64]
+constexpr uint32_t kSlotZ = 57344;    // zeros [64][64]
+constexpr uint32_t kSlotM = 65536;    // M   [64][64]
+constexpr uint32_t kSlotGam = 73728;  // gamma [128] fp32
+constexpr uint32_t kSlotPayload = 65536 + 512;  // everything but Z
+constexpr uint32_t kSlotBytes = 74752;          // 1024-aligned
+
 // 8 consecutive bf16 elements (one 16-byte chunk) at (row, k0) of a 128B-swizzled tile.
 __device__ __forceinline__ void st_chunk8(unsigned char* base, uint32_t slab_bytes, int row,
                                           int k0, const float* x) {
@@ -228,6 +240,10 @@ struct TcCtx {
   bool m64ok;
   uint64_t* bar_mma;
   uint32_t ph_mma;
+  // If set, the stages also write the chunk's hand-over operands (Q~, K^, gamma, M, T', -W) into
+  // this operand slot image in global memory, and skip the shared-memory copies only a chain
+  // CTA would read (K^, M, W).
+  unsigned char* gslot;
 };
 
 __device__ __forceinline__ TcCtx make_ctx(unsigned char* sm, uint32_t tm, uint64_t* bar_mma) {
@@ -245,6 +261,7 @@ __device__ __forceinline__ TcCtx make_ctx(unsigned char* sm, uint32_t tm, uint64
   x.m64ok = x.lane < 16;
   x.bar_mma = bar_mma;
   x.ph_mma = 0;
+  x.gslot = nullptr;
   return x;
 }
 
@@ -320,12 +337,21 @@ __device__ bool gate_stage(const TcCtx& x, int n) {
         st_chunk8(sm + L::KQ, 16384, r, 8 * g8, k8);       // K (scaled to K~ after the Gram MMA)
         st_chunk8(sm + L::KQ, 16384, 64 + r, 8 * g8, q8);  // Q (scaled to Q~ likewise)
         st_chunk8(sm + L::KR, 8192, r, 8 * g8, k8);        // K
-        st_chunk8(sm + L::KH, 8192, r, 8 * g8, kh);        // K^
+        if (x.gslot) {
+          st_chunk8(x.gslot + kSlotKH, 8192, r, 8 * g8, kh);  // K^ (hand-over only)
+        } else {
+          st_chunk8(sm + L::KH, 8192, r, 8 * g8, kh);        // K^
+        }
       }
       if (rb == 0) {
         const float gm = __expf(Gn);
         *reinterpret_cast<float4*>(sGam + 8 * g8) = make_float4(gm, gm, gm, gm);
         *reinterpret_cast<float4*>(sGam + 8 * g8 + 4) = make_float4(gm, gm, gm, gm);
+        if (x.gslot) {
+          float* gg = reinterpret_cast<float*>(x.gslot + kSlotGam);
+          *reinterpret_cast<float4*>(gg + 8 * g8) = make_float4(gm, gm, gm, gm);
+          *reinterpret_cast<float4*>(gg + 8 * g8 + 4) = make_float4(gm, gm, gm, gm);
+        }
       }
     } else {
       // Per-channel gates (and linear attention): running products of the gates down the
@@ -375,6 +401,7 @@ __device__ bool gate_stage(const TcCtx& x, int n) {
             }
             sTot[16 * kD + tid] = acc;
             sGam[tid] = acc;
+            if (x.gslot) reinterpret_cast<float*>(x.gslot + kSlotGam)[tid] = acc;
             float mn = acc;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
@@ -423,7 +450,12 @@ __device__ bool gate_stage(const TcCtx& x, int n) {
           st_chunk8(sm + L::KQ, 16384, r, 8 * g8, ke);       // K~
           st_chunk8(sm + L::KQ, 16384, 64 + r, 8 * g8, qe);  // Q~
           st_chunk8(sm + L::KR, 8192, r, 8 * g8, ki);        // Kr
-          st_chunk8(sm + L::KH, 8192, r, 8 * g8, kh);        // K^
+          if (x.gslot) {  // Q~ and K^ of the hand-over (K^ only there)
+            st_chunk8(x.gslot + kSlotWQ, 16384, 64 + r, 8 * g8, qe);
+            st_chunk8(x.gslot + kSlotKH, 8192, r, 8 * g8, kh);
+          } else {
+            st_chunk8(sm + L::KH, 8192, r, 8 * g8, kh);      // K^
+          }
         }
       } else if (tid < kD) {
         // strong decay: log-gate prefix sums in place of the staged gates (thread = channel)
@@ -444,7 +476,12 @@ __device__ bool gate_stage(const TcCtx& x, int n) {
           const float e = __expf(G);
           st_bf16(sm + L::KQ, sw128_offset(r, c, 16384), kv * e);
           st_bf16(sm + L::KQ, sw128_offset(64 + r, c, 16384), qv * e);
-          st_bf16(sm + L::KH, sw128_offset(r, c, 8192), kv * __expf(Gn - G));
+          if (x.gslot) {
+            st_bf16(x.gslot + kSlotWQ, sw128_offset(64 + r, c, 16384), qv * e);
+            st_bf16(x.gslot + kSlotKH, sw128_offset(r, c, 8192), kv * __expf(Gn - G));
+          } else {
+            st_bf16(sm + L::KH, sw128_offset(r, c, 8192), kv * __expf(Gn - G));
+          }
         }
       }
     }
@@ -511,8 +548,9 @@ __device__ bool gram_stage(TcCtx& x, int n, bool safe) {
           xv[j] = (c0 + j <= r) ? xv[j] : 0.f;
           if (!LINEAR && c0 + j == r) xv[j] = dg;
         }
+        unsigned char* mm = x.gslot ? x.gslot + kSlotM : sm + L::MM;  // M: hand-over only
 #pragma unroll
-        for (int j = 0; j < 32; j += 8) st_chunk8(sm + L::MM, 8192, r, c0 + j, xv + j);
+        for (int j = 0; j < 32; j += 8) st_chunk8(mm, 8192, r, c0 + j, xv + j);
       }
       if constexpr (kScalar) {
         // the raw K and Q rows of the Gram operand become K~ = K e^G and Q~ = Q e^G in place
@@ -529,6 +567,8 @@ __device__ bool gram_stage(TcCtx& x, int n, bool safe) {
             hv[i] = __floats2bfloat162_rn(v2.x * f, v2.y * f);
           }
           *pch = u;
+          if (x.gslot && row >= 64)  // Q~ rows of the hand-over
+            *reinterpret_cast<uint4*>(x.gslot + kSlotWQ + slab * 16384 + row * 128 + ch * 16) = u;
         }
         fence_async_smem();
       }
@@ -549,13 +589,13 @@ __device__ bool gram_stage(TcCtx& x, int n, bool safe) {
           }
         }
         sA[f32x(r, j)] = (j < r) ? sBeta[r] * acc_a : 0.f;
-        st_bf16(sm + L::MM, sw128_offset(r, j, 8192), acc_m);
+        st_bf16(x.gslot ? x.gslot + kSlotM : sm + L::MM, sw128_offset(r, j, 8192), acc_m);
       }
       for (int p2 = tid; p2 < kC * kC; p2 += kThreads) {
         const int r = p2 / kC, j = p2 % kC;
         if (j > r) {
           sA[f32x(r, j)] = 0.f;
-          st_bf16(sm + L::MM, sw128_offset(r, j, 8192), 0.f);
+          st_bf16(x.gslot ? x.gslot + kSlotM : sm + L::MM, sw128_offset(r, j, 8192), 0.f);
         }
       }
     }
@@ -579,6 +619,7 @@ __device__ void solve_stage(const TcCtx& x) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] = sT32[f32x(r, j0 + i)] * sBeta[j0 + i];
     st_chunk8(sm + L::TT, 8192, r, j0, v);
+    if (x.gslot) st_chunk8(x.gslot + kSlotT, 8192, r, j0, v);
   }
   fence_async_smem();
   cta_sync_tc();
@@ -608,7 +649,13 @@ __device__ void w_epilogue(const TcCtx& x) {
   }
   if (x.m64ok) {
 #pragma unroll
-    for (int j = 0; j < 64; j += 8) st_chunk8(x.sm + L::WW, 8192, x.m64row, x.wh * 64 + j, v + j);
+    for (int j = 0; j < 64; j += 8) {
+      if (x.gslot) {  // -W rows 0-63 of the hand-over's [-W; Q~] tile
+        st_chunk8(x.gslot + kSlotWQ, 16384, x.m64row, x.wh * 64 + j, v + j);
+      } else {
+        st_chunk8(x.sm + L::WW, 8192, x.m64row, x.wh * 64 + j, v + j);
+      }
+    }
   }
   fence_async_smem();
 }
@@ -714,6 +761,10 @@ __device__ void zero_v_tail(const TcCtx& x, unsigned char* vin, int n) {
 
 // host side: tensor maps of q, k, v and (per-channel gates) alpha; false if encoding failed
 bool make_tc_maps(const gdr_shape& sh, const PrefillArgs& a, bool linear, TcMaps* maps);
+// host side: CTAs of the work-queue prefill for this shape and workspace (0: use another kernel)
+int queue_grid_for(const gdr_shape& sh, const PrefillArgs& a);
+cudaError_t launch_prefill_queue(const gdr_shape& sh, const PrefillArgs& a, const TcMaps& maps,
+                                 int G, cudaStream_t s);
 // host side: CTAs per cluster of the clustered prefill for this shape (1: use the one-CTA kernel)
 int cluster_size_for(const gdr_shape& sh);
 cudaError_t launch_prefill_cluster(const gdr_shape& sh, const PrefillArgs& a, const TcMaps& maps,

@@ -84,9 +84,12 @@ typedef struct {
 
 /* Force the fp32 FFMA chunked path even where a tensor-core path exists (for cross-checks). */
 #define GDR_FLAG_FORCE_SIMT 1
-/* On the tensor-core path, run the one-CTA-per-chain kernel even where the clustered kernel
- * (one chain CTA plus helper CTAs that prepare its chunks) would be chosen (for cross-checks). */
+/* On the tensor-core path, run the one-CTA-per-chain kernel even where a kernel with helper CTAs
+ * that prepare each chain's chunks (work queue or clusters) would be chosen (for cross-checks). */
 #define GDR_FLAG_NO_CLUSTER 2
+/* Run the work-queue kernel wherever the workspace holds its operand rings, also where the
+ * clustered kernel would be chosen (for cross-checks). */
+#define GDR_FLAG_PREFER_QUEUE 4
 
 /*
  * gdr_prefill -- chunked, packed variable-length prefill of the gated delta rule.
@@ -96,9 +99,12 @@ typedef struct {
  *   S0:         initial states, or NULL for zeros.
  *   cu_seqlens: NULL means one sequence of total_tokens tokens (then n_seqs must be 1).
  *   S_final:    final states, or NULL.  S_final may equal S0 (in-place hand-off).
- *   workspace:  device scratch of at least gdr_prefill_workspace_size(shape) bytes, 256-byte
- *               aligned; its contents need not be initialised; calls that overlap on the GPU
- *               must use different workspaces.
+ *   workspace:  device scratch of gdr_prefill_workspace_size(shape) bytes, 256-byte aligned;
+ *               its contents need not be initialised; calls that overlap on the GPU must use
+ *               different workspaces.  A smaller workspace is accepted down to 256 bytes plus
+ *               4 * n_seqs rounded up to 256; it disables the work-queue tensor-core prefill
+ *               (at most 76 (sequence, head) chains, bf16, d = 128), and a slower kernel runs
+ *               instead with the same results.
  * Empty sequences (length 0) produce no output and S_final = S0 (or zeros).
  */
 gdr_status gdr_prefill(const gdr_shape* shape, const void* q, const void* k, const void* v,
@@ -106,7 +112,9 @@ gdr_status gdr_prefill(const gdr_shape* shape, const void* q, const void* k, con
                        const int32_t* cu_seqlens, void* out, float* S_final, void* workspace,
                        size_t workspace_bytes, void* stream);
 
-/* Workspace bytes gdr_prefill / gdr_linear_attn need for this shape (0 if the shape is invalid). */
+/* Workspace bytes gdr_prefill / gdr_linear_attn use for this shape (0 if n_seqs or H < 1): the
+ * status word, the visiting order and, for bf16 d = 128 shapes of at most 76 (sequence, head)
+ * chains, the work-queue prefill's flags and 6 operand slots of 74752 bytes per chain. */
 size_t gdr_prefill_workspace_size(const gdr_shape* shape);
 
 /*

@@ -1,10 +1,11 @@
-"""GPU parity of the clustered tensor-core prefill (one chain CTA plus helper CTAs per
-(sequence, head) chain), which the library picks for bf16, d = 128 workloads with few chains.
-
-The cluster size follows from the number of chains (the largest cluster of which one per chain
-fits on the device), so the pair counts below reach different helper counts; each case runs the
-default dispatch and the one-CTA kernel (GDR_FLAG_NO_CLUSTER) and checks both against the
-oracle."""
+"""GPU parity of the tensor-core prefill kernels with helper CTAs, which the library picks for
+bf16, d = 128 workloads with few (sequence, head) chains: the clustered kernel (one chain CTA plus
+1-7 helpers per cluster) and the work-queue kernel (one chain CTA per chain, every other SM a
+helper taking chunks from a shared queue; needs the full workspace, chosen where clusters would
+give a chain one helper).  Every case runs the default dispatch, the work-queue kernel
+(GDR_FLAG_PREFER_QUEUE), the clustered kernel (minimum workspace) and the one-CTA-per-chain kernel
+(GDR_FLAG_NO_CLUSTER), and checks each against the oracle.  The pair counts below reach different
+helper counts."""
 import numpy as np
 import pytest
 import torch
@@ -22,11 +23,19 @@ def _gpu():
         pytest.skip("no CUDA device")
 
 
-def _run(a, no_cluster):
+PATHS = ("default", "queue", "cluster", "one_cta")
+
+
+def _run(a, path="default"):
     import gated_delta_rule_prefill_gb300 as g
     d = dev_inputs(a, "bf16")
+    ws = None
+    if path == "cluster":  # the minimum workspace: no operand rings, so no work-queue kernel
+        n_seqs = d["cu_seqlens"].numel() - 1
+        ws = torch.empty(256 + (n_seqs * 4 + 255) // 256 * 256, dtype=torch.uint8, device="cuda")
     out, Sf = g.gdr_prefill(d["q"], d["k"], d["v"], d["alpha"], d["beta"], S0=d["S0"],
-                            cu_seqlens=d["cu_seqlens"], no_cluster=no_cluster)
+                            cu_seqlens=d["cu_seqlens"], workspace=ws,
+                            no_cluster=(path == "one_cta"), prefer_queue=(path == "queue"))
     torch.cuda.synchronize()
     return host(out), host(Sf)
 
@@ -34,11 +43,11 @@ def _run(a, no_cluster):
 def _check(a, what):
     ref = oracle.gated_delta(a["q"], a["k"], a["v"], a["alpha"], a["beta"], S0=a["S0"],
                              cu_seqlens=a["cu_seqlens"])
-    for no_cluster in (False, True):
-        o, s = _run(a, no_cluster)
+    for path in PATHS:
+        o, s = _run(a, path)
         eo, es = rel_rows(o, ref[0]), rel_states(s, ref[1])
-        print("%s no_cluster=%s: output err %.3g, state err %.3g" % (what, no_cluster, eo, es))
-        assert eo <= TOL["bf16"] and es <= TOL["bf16"], (what, no_cluster, eo, es)
+        print("%s %s: output err %.3g, state err %.3g" % (what, path, eo, es))
+        assert eo <= TOL["bf16"] and es <= TOL["bf16"], (what, path, eo, es)
         assert np.isfinite(o).all() and np.isfinite(s).all()
 
 
@@ -84,9 +93,9 @@ def test_cluster_two_calls_in_a_row():
     a = gi.gen_full(wl)
     b = gi.gen_full(gi.custom(seed=92, seqlens=[640, 100], H=4, d_k=128, d_v=128, dtype="bf16",
                               s0="normal"))
-    first = _run(a, False)
-    second = _run(b, False)
-    again = _run(a, False)
+    first = _run(a)
+    second = _run(b)
+    again = _run(a)
     np.testing.assert_array_equal(first[0], again[0])
     np.testing.assert_array_equal(first[1], again[1])
     ref = oracle.gated_delta(b["q"], b["k"], b["v"], b["alpha"], b["beta"], S0=b["S0"],
