@@ -119,34 +119,53 @@ __device__ __forceinline__ void frag_a(const float* m, int r0, int k0, int g, in
 __device__ __forceinline__ int x32(int r, int c) { return r * 32 + (c ^ ((r & 3) << 3)); }
 
 // T = (I + A)^-1 for A strictly lower (64 x 64, fp32, swizzled layout above), by doubling the
-// inverted block size: the four 16 x 16 diagonal blocks by right-looking forward substitution
-// (one column per thread, held in registers); then both 32 x 32 diagonal blocks at once,
-// T_ba = -T_bb (A_ba T_aa) for (a, b) = (0, 1) and (2, 3); then the 64 x 64 inverse,
-// T_[23][01] = -T_[23][23] (A_[23][01] T_[01][01]).  The two products of each doubling step run
+// inverted block size: the eight 8 x 8 diagonal blocks by right-looking forward substitution (one
+// column per thread, held in registers); then the 16, 32 and 64 levels, each
+// T_ba = -T_bb (A_ba T_aa) over the pairs of diagonal blocks (a, b) of the level below (level 64:
+// T_[23][01] = -T_[23][23] (A_[23][01] T_[01][01])).  The two products of each doubling step run
 // on the tensor cores as warp-level tf32 MMAs with fp32 accumulation (T' is rounded to bf16
-// afterwards, 4x coarser than tf32).  sX holds the intermediate (32 x 32 fp32).
+// afterwards, 4x coarser than tf32).  sX holds the intermediates (up to 32 x 32 fp32).
 __device__ inline void unit_lower_inverse(const float* sA, float* sT, float* sX, int tid) {
   const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
   if (tid < 64) {
-    const int b = tid >> 4, c = tid & 15, o = 16 * b;
-    float acc[16];
+    const int b = tid >> 3, c = tid & 7, o = 8 * b;
+    float acc[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) acc[i] = (i == c) ? 1.f : 0.f;
+    for (int i = 0; i < 8; ++i) acc[i] = (i == c) ? 1.f : 0.f;
 #pragma unroll
-    for (int j = 0; j < 15; ++j) {
+    for (int j = 0; j < 7; ++j) {
       const float xj = acc[j];
 #pragma unroll
-      for (int i = j + 1; i < 16; ++i) acc[i] = fmaf(-sA[f32x(o + i, o + j)], xj, acc[i]);
+      for (int i = j + 1; i < 8; ++i) acc[i] = fmaf(-sA[f32x(o + i, o + j)], xj, acc[i]);
     }
 #pragma unroll
-    for (int i = 0; i < 16; ++i) sT[f32x(o + i, o + c)] = acc[i];
+    for (int i = 0; i < 8; ++i) sT[f32x(o + i, o + c)] = acc[i];
   } else {
-    // strictly-upper blocks of T are zero: rows 0-31 from column 32, and the 16 x 16 blocks
-    // (0, 1) and (2, 3)
+    // everything right of the 8 x 8 diagonal blocks is zero
     for (int e = tid - 64; e < kC * 16; e += kThreads - 64) {
       const int r = e >> 4, grp = e & 15;
-      if (grp >= 4 * ((r >> 4) + 1)) st4x(sT, r, grp, make_float4(0.f, 0.f, 0.f, 0.f));
+      if (grp >= 2 * ((r >> 3) + 1)) st4x(sT, r, grp, make_float4(0.f, 0.f, 0.f, 0.f));
     }
+  }
+  __syncthreads();
+  // ---- level 16: warp p of warps 0-3 takes the 16 x 16 block p (8-blocks a = 2p, b = 2p + 1);
+  // the MMAs are 16 rows high, the 8 rows of the block padded with zeros
+  if (warp < 4) {
+    const int ra = 16 * warp, rb = ra + 8;
+    float* sXw = sX + warp * 64;  // X = A_ba T_aa, 8 x 8 row-major
+    uint32_t a[4];
+    a[0] = tf32(sA[f32x(rb + g, ra + t)]);
+    a[2] = tf32(sA[f32x(rb + g, ra + t + 4)]);
+    a[1] = a[3] = 0u;
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_tf32(c, a, tf32(sT[f32x(ra + t, ra + g)]), tf32(sT[f32x(ra + t + 4, ra + g)]));
+    *reinterpret_cast<float2*>(sXw + g * 8 + 2 * t) = make_float2(c[0], c[1]);
+    __syncwarp();
+    a[0] = tf32(sT[f32x(rb + g, rb + t)]);
+    a[2] = tf32(sT[f32x(rb + g, rb + t + 4)]);
+    float y[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_tf32(y, a, tf32(sXw[t * 8 + g]), tf32(sXw[(t + 4) * 8 + g]));
+    *reinterpret_cast<float2*>(sT + f32x(rb + g, ra + 2 * t)) = make_float2(-y[0], -y[1]);
   }
   __syncthreads();
   // ---- level 32: warp (p, j) of warps 0-3 computes the 8 columns 8j.. of pair p's blocks
@@ -615,9 +634,11 @@ __device__ void solve_stage(const TcCtx& x) {
   unit_lower_inverse(sA, sT32, sX, x.tid);
   for (int e = x.tid; e < kC * kC / 8; e += kThreads) {
     const int r = e >> 3, j0 = (e & 7) * 8;
-    float v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = sT32[f32x(r, j0 + i)] * sBeta[j0 + i];
+    const float4 t0 = ld4x(sT32, r, j0 >> 2), t1 = ld4x(sT32, r, (j0 >> 2) + 1);
+    const float4 b0 = *reinterpret_cast<const float4*>(sBeta + j0);
+    const float4 b1 = *reinterpret_cast<const float4*>(sBeta + j0 + 4);
+    const float v[8] = {t0.x * b0.x, t0.y * b0.y, t0.z * b0.z, t0.w * b0.w,
+                        t1.x * b1.x, t1.y * b1.y, t1.z * b1.z, t1.w * b1.w};
     st_chunk8(sm + L::TT, 8192, r, j0, v);
     if (x.gslot) st_chunk8(x.gslot + kSlotT, 8192, r, j0, v);
   }
