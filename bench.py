@@ -86,7 +86,7 @@ def source_digest(files):
 
 
 KERNEL_SOURCES = {"prefill": ["prefill_queue.cu", "prefill_tc.cu", "tc_common.cuh", "umma.cuh"],
-                  "linear_attn": ["prefill_tc.cu", "tc_common.cuh", "umma.cuh"],
+                  "linear_attn": ["linear_tc.cu", "tc_common.cuh", "umma.cuh"],
                   "decode": ["decode.cu"]}
 
 

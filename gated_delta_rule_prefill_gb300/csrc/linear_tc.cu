@@ -1,0 +1,277 @@
+// linear_tc.cu -- chunked linear attention (alpha = 1, no erase term) on the tensor cores,
+// d_k = d_v = 128, bf16 q/k/v, fp32 state.  Per chunk of C = 64 tokens entering with state S:
+//   O = Q S + lower(Q K^T) V,   S <- S + K^T V
+// (engineermaxxing "From GPT-2 to Kimi K3: one memory, seven eviction policies" §03b and §04b;
+// heqinghuang "gpt2-to-kimi" §10).  With no gates there is nothing to prepare per chunk: q and k
+// arrive by TMA directly as the 128B-swizzled [K; Q] operand tile (K rows 0-63, Q rows 64-127 of
+// each 64-channel slab), v as the MN-major B tile.  Per chunk (one CTA, 8 warps):
+//   S += K^T V                      (M = 128: K as MN-major A; fp32 state master in TMEM)
+//   D = [K; Q] S,  A = [K; Q] K^T   (M = 128 each; rows 64-127 are Q S and Q K^T)
+//   S master -> bf16 operand for the next chunk (double-buffered, so this waits only for the
+//   state MMA), lower(Q K^T) -> bf16 M,  then  D += [Z; M] V  (rows 64-127: O)
+// and the O rows leave TMEM while the next chunk's MMAs run.  q, k, v of the next chunk are
+// fetched one chunk ahead.  Like the one-CTA kernel, a sequence of few (sequence, head) pairs is
+// split into runs of whole chunks, run g starting from S0 + sum of K^T V over the chunks before it.
+#include <cuda.h>
+
+#include "tc_common.cuh"
+
+namespace gdr {
+namespace tc {
+namespace {
+
+using namespace umma;
+
+struct LinSmem {
+  static constexpr uint32_t KQ = 0;            // [K; Q] x 2 buffers, 32 KB each
+  static constexpr uint32_t VIN = 65536;       // V [64 tok][128] SW128 x 2 buffers, 16 KB each
+  static constexpr uint32_t ZM = VIN + 32768;  // [Z; M]: zeros 8 KB, then M [64][64] K-major
+  static constexpr uint32_t SS = ZM + 16384;   // S [d_k][128] (MN-major B) x 2 buffers, 32 KB each
+  static constexpr uint32_t BARS = SS + 65536;  // ld[2], s, q, m2, pf_full[4], pf_mma[4], TMEM
+  static constexpr uint32_t END = BARS + 128;
+  static constexpr size_t bytes = END + 1024;
+  // prefix stages (32 KB each, K at +0 / +16K, V at +8K / +24K): dead before the chunk loop
+  __host__ __device__ static constexpr uint32_t pf(int st) {
+    return st == 0 ? KQ : st == 1 ? KQ + 32768 : st == 2 ? VIN : SS;
+  }
+  static_assert(bytes <= 232448, "shared memory per CTA");
+};
+
+constexpr uint32_t kColD0 = 128, kColD1 = 256, kColA = 384;  // TMEM columns (S at 0)
+
+__global__ void __launch_bounds__(kThreads, 1)
+    linear_tc_kernel(const __grid_constant__ TcMaps maps, const PrefillArgs a, int nseg) {
+  using L = LinSmem;
+  constexpr int DH = kD / 2;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                       ~(uintptr_t)1023);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);
+  uint64_t* bar_ld = bars;        // [2] q, k, v of a chunk
+  uint64_t* bar_s = bars + 2;     // the state MMA
+  uint64_t* bar_q = bars + 3;     // the Q S and Q K^T MMAs
+  uint64_t* bar_m2 = bars + 4;    // the M V MMA
+  uint64_t* pf_full = bars + 5;   // [4] prefix stage loaded
+  uint64_t* pf_mma = bars + 9;    // [4] prefix stage consumed
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 13);
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int H = a.H;
+  const int per_seq = H * nseg;
+  const int rank = blockIdx.x / per_seq;
+  const int h = (blockIdx.x % per_seq) / nseg, g = blockIdx.x % nseg;
+  const int seq = a.order ? a.order[rank] : rank;
+  int64_t t0, t1;
+  if (!seq_range(a, seq, t0, t1)) return;
+  const int nch = (int)((t1 - t0 + kC - 1) / kC);
+  const int lseg = (nch + nseg - 1) / nseg;
+  const int c_begin = g * lseg, c_end = min(nch, c_begin + lseg);
+  if (g > 0 && c_begin >= c_end) return;
+  const size_t sidx = ((size_t)seq * H + h) * kD * kD;
+  __nv_bfloat16* __restrict__ out = static_cast<__nv_bfloat16*>(a.out);
+
+  if (warp == 0) tmem_alloc(tslot, kTmemCols);
+  for (int i = tid; i < 8192 / 16; i += kThreads)  // the zero half of [Z; M]
+    reinterpret_cast<uint4*>(sm + L::ZM)[i] = make_uint4(0, 0, 0, 0);
+  fence_async_smem();
+  if (tid == 0) {
+    for (int i = 0; i < 13; ++i) mbar_init(bars + i, 1);
+    fence_mbar_init();
+    prefetch_tmap(&maps.q_sw);
+    prefetch_tmap(&maps.k_sw);
+    prefetch_tmap(&maps.v);
+  }
+  cta_sync_tc();
+  TcCtx x = make_ctx(sm, *tslot, bar_s);
+  bool failed = false;
+  s_init<DH>(x, a.S0 ? a.S0 + sidx + (size_t)x.lrow * kD : nullptr, sm + L::SS);
+  const uint32_t id_s = idesc_bf16(128, kD, false, true, true);   // K as MN-major A, V MN-major B
+  const uint32_t id_d = idesc_bf16(128, kD, false, false, true);  // K-major A, MN-major B
+  const uint32_t id_a = idesc_bf16(128, kC, false, false, false);  // [K; Q] K^T (K-major B)
+
+  if (c_begin > 0) {
+    // run prefix: S += K_c^T V_c over chunks [0, c_begin) (all full), 4 TMA stages, one chunk's
+    // MMA per step; warp 0 drives it, the other warps wait at the barrier below
+    cta_sync_tc();  // S0 is in TMEM
+    bool pf_ok = true;
+    if (warp == 0) {
+      auto warp_wait = [&](uint64_t* bar, uint32_t parity) {
+        bool ok = true;
+        if ((tid & 31) == 0) ok = mbar_wait(bar, parity, kWaitNs);
+        return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      };
+      uint32_t ph_f = 0, ph_m = 0;
+      auto pf_issue = [&](int cp) {
+        if (tid == 0) {
+          const int st = cp & 3;
+          const int tc = (int)(t0 + (int64_t)cp * kC);
+          unsigned char* b = sm + L::pf(st);
+          mbar_expect_tx(pf_full + st, 32768);
+          tma_load_3d(b, &maps.k_sw, 0, h, tc, pf_full + st);
+          tma_load_3d(b + 16384, &maps.k_sw, 64, h, tc, pf_full + st);
+          tma_load_3d(b + 8192, &maps.v, 0, h, tc, pf_full + st);
+          tma_load_3d(b + 24576, &maps.v, 64, h, tc, pf_full + st);
+        }
+      };
+      for (int cp = 0; cp < 3 && cp < c_begin; ++cp) pf_issue(cp);
+#pragma unroll 1
+      for (int cp = 0; cp < c_begin; ++cp) {
+        const int st = cp & 3;
+        if (!warp_wait(pf_full + st, (ph_f >> st) & 1u)) { pf_ok = false; break; }
+        ph_f ^= 1u << st;
+        const Opnd opK{x.sb + L::pf(st), 16384, true};
+        const Opnd opV{x.sb + L::pf(st) + 8192, 16384, true};
+        mma_run<kC>(x.tm + kColS, opK, opV, id_s, true);
+        mma_commit_elect(pf_mma + st);
+        if (cp + 3 < c_begin) {  // stage (cp + 3) & 3 held chunk cp - 1: its MMA must be done
+          if (cp >= 1) {
+            const int sp = (cp - 1) & 3;
+            if (!warp_wait(pf_mma + sp, (ph_m >> sp) & 1u)) { pf_ok = false; break; }
+            ph_m ^= 1u << sp;
+          }
+          pf_issue(cp + 3);
+        }
+      }
+      mma_commit_elect(bar_s);  // every prefix MMA complete
+    }
+    if (__syncthreads_or(!pf_ok) || !wait_bar(bar_s, x.ph_mma)) {
+      failed = true;
+    } else {
+      s_epilogue<DH>(x, sm + L::SS);  // the bf16 operand copy of the run's entering state
+      cta_sync_tc();
+    }
+  }
+
+  const int64_t ts = t0 + (int64_t)c_begin * kC;
+  const int64_t te = t0 + (int64_t)c_end * kC < t1 ? t0 + (int64_t)c_end * kC : t1;
+  const int nloc = c_end - c_begin;
+  auto issue_ld = [&](int i) {  // chunk c_begin + i into buffer i & 1
+    if (tid == 0) {
+      const int b = i & 1;
+      const int tc = (int)(ts + (int64_t)i * kC);
+      unsigned char* kq = sm + L::KQ + b * 32768;
+      unsigned char* vv = sm + L::VIN + b * 16384;
+      mbar_expect_tx(bar_ld + b, 32768 + 16384);
+      tma_load_3d(kq, &maps.k_sw, 0, h, tc, bar_ld + b);
+      tma_load_3d(kq + 8192, &maps.q_sw, 0, h, tc, bar_ld + b);
+      tma_load_3d(kq + 16384, &maps.k_sw, 64, h, tc, bar_ld + b);
+      tma_load_3d(kq + 24576, &maps.q_sw, 64, h, tc, bar_ld + b);
+      tma_load_3d(vv, &maps.v, 0, h, tc, bar_ld + b);
+      tma_load_3d(vv + 8192, &maps.v, 64, h, tc, bar_ld + b);
+    }
+  };
+  const bool o_rows = (warp & 3) >= 2;  // TMEM lanes 64-127 (Q rows) of this warp
+  const int qrow = (warp & 3) * 32 + (tid & 31) - 64;
+  auto d_col = [](int i) { return (i & 1) ? kColD1 : kColD0; };
+  // O rows of local chunk i (lanes 64-127 of its D) -> out rows [tc, tc + n) of head h
+  auto o_store = [&](int i, int64_t tc, int n) {
+    float v[64];
+    tmem_ld64(x.tm + x.lane_base + d_col(i) + x.wh * 64, v);
+    if (qrow < n) {
+      __nv_bfloat16* dst = out + ((size_t)(tc + qrow) * H + h) * kD + x.wh * 64;
+#pragma unroll
+      for (int j = 0; j < 64; j += 8) {
+        __align__(16) __nv_bfloat162 hv[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) hv[k] = __floats2bfloat162_rn(v[j + 2 * k], v[j + 2 * k + 1]);
+        *reinterpret_cast<uint4*>(dst + j) = *reinterpret_cast<const uint4*>(hv);
+      }
+    }
+  };
+  uint32_t ph_ld[2] = {0, 0}, ph_q = 0, ph_m2 = 0;
+  if (!failed && nloc > 0) issue_ld(0);
+#pragma unroll 1
+  for (int i = 0; i < nloc && !failed; ++i) {
+    const int b = i & 1;
+    const int64_t tc = ts + (int64_t)i * kC;
+    const int n = (int)((te - tc) < (int64_t)kC ? (te - tc) : (int64_t)kC);
+    {
+      const bool ok = mbar_wait(bar_ld + b, ph_ld[b], kWaitNs);
+      ph_ld[b] ^= 1u;
+      if (ok && n < kC) zero_v_tail<kD>(x, sm + L::VIN + b * 16384, n);  // padded rows: no K^T V
+      if (__syncthreads_or(!ok)) { failed = true; break; }
+      fence_after_sync();
+    }
+    if (i + 1 < nloc) issue_ld(i + 1);  // buffer b ^ 1: chunk i - 1's MMAs are complete
+    const Opnd opKQ{x.sb + L::KQ + b * 32768, 16384, false};  // [K; Q], K-major A (M = 128)
+    const Opnd opKa{x.sb + L::KQ + b * 32768, 16384, true};   // K as MN-major A (M = d_k)
+    const Opnd opKb{x.sb + L::KQ + b * 32768, 16384, false};  // K rows as K-major B (N = 64)
+    const Opnd opV{x.sb + L::VIN + b * 16384, 8192, true};
+    const Opnd opS{x.sb + L::SS + b * 32768, 16384, true};    // this chunk's entering S
+    const Opnd opZM{x.sb + L::ZM, 16384, false};
+    if (warp == 0) {
+      mma_run<kC>(x.tm + kColS, opKa, opV, id_s, true);  // S += K^T V
+      mma_commit_elect(bar_s);
+      mma_run<kD>(x.tm + d_col(i), opKQ, opS, id_d, false);  // [K; Q] S
+      mma_run<kD>(x.tm + kColA, opKQ, opKb, id_a, false);    // [K; Q] K^T
+      mma_commit_elect(bar_q);
+    }
+    if (i > 0 && o_rows) o_store(i - 1, tc - kC, kC);
+    // the state's bf16 operand for the next chunk (the other buffer: this chunk's Q S reads this)
+    if (!wait_bar(bar_s, x.ph_mma)) { failed = true; break; }
+    s_epilogue<DH>(x, sm + L::SS + (b ^ 1) * 32768);
+    if (!wait_bar(bar_q, ph_q)) { failed = true; break; }
+    if (o_rows) {  // M = lower(Q K^T) -> bf16 K-major A rows 64-127 of [Z; M]
+      float v[32];
+      tmem_ld32(x.tm + x.lane_base + kColA + 32 * x.wh, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = (32 * x.wh + j <= qrow) ? v[j] : 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; j += 8) st_chunk8(sm + L::ZM + 8192, 8192, qrow, 32 * x.wh + j, v + j);
+      fence_async_smem();
+    }
+    cta_sync_tc();
+    if (warp == 0) {
+      mma_run<kC>(x.tm + d_col(i), opZM, opV, id_d, true);  // rows 64-127 += M V
+      mma_commit_elect(bar_m2);
+    }
+    // buffer b (q, k, v) and M are reused only after this MMA completes
+    if (!wait_bar(bar_m2, ph_m2)) { failed = true; break; }
+  }
+  if (!failed && nloc > 0 && o_rows) {
+    const int64_t tl = ts + (int64_t)(nloc - 1) * kC;
+    o_store(nloc - 1, tl, (int)(te - tl));
+  }
+  if (failed) {
+    if (tid == 0) report(a.status, GDR_DEVCHECK_TIMEOUT);
+    // let copies already in flight land before the shared memory is released
+    mbar_wait(bar_ld, ph_ld[0], kWaitNs);
+    mbar_wait(bar_ld + 1, ph_ld[1], kWaitNs);
+  } else if (a.S_final && c_end == nch) {  // the last run of the sequence hands the state on
+    s_final<DH>(x, a.S_final + sidx + (size_t)x.lrow * kD);
+  }
+  cta_sync_tc();
+  if (warp == 0) tmem_dealloc(x.tm, kTmemCols);
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return n;
+}
+
+}  // namespace
+
+cudaError_t launch_linear_tc(const gdr_shape& sh, const PrefillArgs& a, const TcMaps& maps,
+                             cudaStream_t s) {
+  // few (sequence, head) pairs: runs of at least 16 chunks per CTA, as many as fill the SMs once
+  const long pairs = (long)sh.n_seqs * sh.H;
+  const long avg_chunks = sh.total_tokens / ((long)sh.n_seqs * kC);
+  long nseg = pairs > 0 ? sm_count() / pairs : 1;
+  if (nseg > avg_chunks / 16) nseg = avg_chunks / 16;
+  if (nseg > 8) nseg = 8;
+  if (nseg < 1) nseg = 1;
+  cudaError_t e = cudaFuncSetAttribute(linear_tc_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)LinSmem::bytes);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = (unsigned)sh.n_seqs * (unsigned)sh.H * (unsigned)nseg;
+  linear_tc_kernel<<<grid, kThreads, LinSmem::bytes, s>>>(maps, a, (int)nseg);
+  return cudaGetLastError();
+}
+
+}  // namespace tc
+}  // namespace gdr

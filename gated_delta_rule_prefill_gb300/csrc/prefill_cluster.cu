@@ -366,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!wait_bar(bar_qk, ph_qk)) { failed = true; break; }
       if (kAlphaTile && !wait_bar(bar_a, ph_a)) { failed = true; break; }
 
-      const bool safe = gate_stage<L, CHANNEL, false>(x, n);
+      const bool safe = gate_stage<L, CHANNEL>(x, n);
       // ... and the second (-W, T', M), before the Gram epilogue rewrites M
       if (tid == 0) bulk_wait_read<0>();
       fence_async_smem();
@@ -375,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         issue_qk(tn);
         issue_a(tn);
       }
-      if (!gram_stage<L, CHANNEL, false>(x, n, safe)) { failed = true; break; }
+      if (!gram_stage<L, CHANNEL>(x, n, safe)) { failed = true; break; }
       if (!safe && cn < nch) {
         issue_qk(tn);
         issue_a(tn);

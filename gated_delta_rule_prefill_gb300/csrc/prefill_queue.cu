@@ -434,12 +434,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!wait_bar(bar_qk, ph_qk)) { failed = true; break; }
       if (kAlphaTile && !wait_bar(bar_a, ph_a)) { failed = true; break; }
 
-      const bool safe = gate_stage<L, CHANNEL, false>(x, cur.n);
+      const bool safe = gate_stage<L, CHANNEL>(x, cur.n);
       fence_async_smem();
       cta_sync_tc();
       Item nxt{-1, 0, 0, 0, 0};
       if (safe) nxt = take();  // q, k and alpha tiles are consumed: fetch the next item's
-      if (!gram_stage<L, CHANNEL, false>(x, cur.n, safe)) { failed = true; break; }
+      if (!gram_stage<L, CHANNEL>(x, cur.n, safe)) { failed = true; break; }
       if (!safe) nxt = take();
       load_scalars(nxt, nb_beta, nb_alpha);
       solve_stage<L>(x);

@@ -1,7 +1,9 @@
 // prefill_tc.cu -- chunked prefill of the gated delta rule on the 5th-generation tensor cores
 // (tcgen05.mma, bf16 operands in shared memory, fp32 accumulators in TMEM, inputs staged by
-// TMA), d_k = d_v = 128, chunks of C = 64 tokens.  Also the plain linear-attention pass
-// (alpha = 1, no erase).
+// TMA), d_k = d_v = 128, chunks of C = 64 tokens, one CTA per chain (the kernels with helper CTAs
+// for few chains are in prefill_cluster.cu and prefill_queue.cu; linear attention, which needs
+// none of the per-chunk preparation, in linear_tc.cu).  This file also holds the tensor-map
+// set-up and the dispatch between those kernels.
 //
 // Chunk algebra (derived from the recurrence; the alpha = 1 case is the per-chunk triangular
 // solve of engineermaxxing "From GPT-2 to Kimi K3: one memory, seven eviction policies" §04e-§04f
@@ -20,7 +22,7 @@
 // min_c Gam_n[c] above e^-40, so every factor and product stays far inside the bf16 / fp32
 // range.  Chunks with stronger decay (an alpha = 0 reset, say) take log-gate prefix sums
 // G = sum max(log alpha, -60) and form A' and M from direct pairwise exponentials (exact,
-// slower).  Linear attention: no gates (K~ = Kr = K^ = K, Q~ = Q), U = V, no solve.
+// slower).
 //
 // Mapping: one CTA (8 warps) per (sequence, head, block of DV value columns); columns of S are
 // independent, so the value dimension splits across CTAs.  Warp w reads TMEM lane quarter w & 3
@@ -62,8 +64,8 @@ struct TcSmem {
   static constexpr uint32_t GAM = ALPHA + 256;      // gamma [128]
   static constexpr uint32_t RED = GAM + 512;        // reductions [8]
   static constexpr uint32_t GS = RED + 64;          // scalar gates: log prefix sums [64]
-  static constexpr uint32_t BARS = GS + 256;        // 12 mbarriers + TMEM slot
-  static constexpr uint32_t END = BARS + 128;
+  static constexpr uint32_t BARS = GS + 256;        // 4 mbarriers + TMEM slot
+  static constexpr uint32_t END = BARS + 64;
   static constexpr size_t bytes = END + 1024;       // + alignment slack
   // fp32 scratch of the solve, in tiles that are dead while it runs
   static constexpr uint32_t SA = KR;                // A [64][64]  (Kr is consumed by then)
@@ -71,23 +73,17 @@ struct TcSmem {
   static constexpr uint32_t SX = UU;                // [32][32] (U is written later)
   static constexpr uint32_t TOT = WW;               // gate carries [17][128] (W later)
   static constexpr uint32_t DIAGP = UU;             // q_r . k_r partials [64][16] (U later)
-  // linear attention, segment prefix: 4 stages of [K tile 16 KB | V tile DV x 128 B] in tiles
-  // that are dead before the chunk loop starts (QIN+KIN, AIN, KQ, KR+KH)
-  __host__ __device__ static constexpr uint32_t pf(int st) {
-    return st == 0 ? QIN : st == 1 ? AIN : st == 2 ? KQ : KR;
-  }
   static_assert(bytes <= 232448, "shared memory per CTA");
   static_assert(DV * 128 >= 32 * 32 * 4, "block scratch fits in U");
-  static_assert(DV * 128 <= 16384 && KIN == QIN + 16384 && KH == KR + 16384, "prefix stages");
 };
 
-template <int DV, bool CHANNEL, bool LINEAR>
+template <int DV, bool CHANNEL>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_tc_kernel(const __grid_constant__ TcMaps maps, const PrefillArgs a, int nseg) {
+    prefill_tc_kernel(const __grid_constant__ TcMaps maps, const PrefillArgs a) {
   using L = TcSmem<DV>;
   constexpr int NB = kD / DV;
   constexpr int DH = DV / 2;  // accumulator columns per warp half
-  constexpr bool kAlphaTile = CHANNEL && !LINEAR;
+  constexpr bool kAlphaTile = CHANNEL;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -99,42 +95,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_qk = bars + 1;
   uint64_t* bar_a = bars + 2;
   uint64_t* bar_v = bars + 3;
-  uint64_t* pf_full = bars + 4;  // [4] segment prefix: stage loaded
-  uint64_t* pf_mma = bars + 8;   // [4] segment prefix: stage consumed
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 12);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5;
   const int H = a.H;
-  // block -> (sequence rank, head, segment g of nseg, value-column block vb)
-  const int per_seq = H * nseg * NB;
-  const int rank = blockIdx.x / per_seq;
-  const int rem = blockIdx.x % per_seq;
-  const int h = rem / (nseg * NB);
-  const int g = (rem % (nseg * NB)) / NB, vb = rem % NB;
+  const int rank = blockIdx.x / (H * NB);
+  const int rem = blockIdx.x % (H * NB);
+  const int h = rem / NB, vb = rem % NB;
   const int seq = a.order ? a.order[rank] : rank;
   int64_t t0, t1;
   if (!seq_range(a, seq, t0, t1)) return;
-  // Linear attention splits a sequence into nseg runs of whole chunks; run g starts from
-  // S0 + sum over the earlier chunks of K^T V (its prefix, recomputed here).  nseg = 1 otherwise.
-  const int nch = (int)((t1 - t0 + kC - 1) / kC);
-  const int lseg = (nch + nseg - 1) / nseg;
-  const int c_begin = g * lseg, c_end = min(nch, c_begin + lseg);
-  if (g > 0 && c_begin >= c_end) return;
-  const int64_t ts = t0 + (int64_t)c_begin * kC;
-  const int64_t te = t0 + (int64_t)c_end * kC < t1 ? t0 + (int64_t)c_end * kC : t1;
   __nv_bfloat16* __restrict__ out = static_cast<__nv_bfloat16*>(a.out);
   const int vc0 = vb * DV;
   const size_t sidx = ((size_t)seq * H + h) * kD * kD;
 
   if (warp == 0) tmem_alloc(tslot, kTmemCols);
   if (tid == 0) {
-    for (int i = 0; i < 12; ++i) mbar_init(bars + i, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(bars + i, 1);
     fence_mbar_init();
     prefetch_tmap(&maps.q);
     prefetch_tmap(&maps.k);
     prefetch_tmap(&maps.v);
     if (kAlphaTile) prefetch_tmap(&maps.alpha);
-    if (LINEAR && c_begin > 0) prefetch_tmap(&maps.k_sw);
   }
   cta_sync_tc();
   TcCtx x = make_ctx(sm, *tslot, bars + 0);
@@ -166,79 +148,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto load_scalars = [&](int64_t tc, float& b, float& al) {
     b = 0.f;
     al = 1.f;
-    if (tid < kC && tc + tid < te) {
+    if (tid < kC && tc + tid < t1) {
       const size_t o = (size_t)(tc + tid) * H + h;
-      if (!LINEAR) b = a.beta[o];
-      if (!CHANNEL && !LINEAR) al = a.alpha[o];
+      b = a.beta[o];
+      if (!CHANNEL) al = a.alpha[o];
     }
   };
 
+  if (t0 < t1) {
+    issue_qk(t0);
+    issue_a(t0);
+    issue_v(t0);
+  }
   s_init<DH>(x, a.S0 ? a.S0 + sidx + (size_t)x.lrow * kD + vc0 : nullptr, sm + L::SS);
-  if constexpr (LINEAR) {
-    if (c_begin > 0) {
-      // segment prefix: S += K_c^T V_c over chunks [0, c_begin) (all full), 4 TMA stages, one
-      // chunk's MMA per step; warp 0 drives it, the other warps wait at the barrier below
-      cta_sync_tc();  // S0 is in TMEM
-      bool pf_ok = true;
-      if (warp == 0) {
-        // lane 0 waits, the warp follows its verdict (the MMAs are issued warp-wide)
-        auto warp_wait = [&](uint64_t* bar, uint32_t parity) {
-          bool ok = true;
-          if ((tid & 31) == 0) ok = mbar_wait(bar, parity, kWaitNs);
-          return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        };
-        uint32_t ph_f = 0, ph_m = 0;  // per-stage phase bits
-        auto pf_issue = [&](int cp) {
-          if (tid == 0) {
-            const int st = cp & 3;
-            const int64_t tc = t0 + (int64_t)cp * kC;
-            mbar_expect_tx(pf_full + st, 16384 + DV * 128);
-            tma_load_3d(sm + L::pf(st), &maps.k_sw, 0, h, (int)tc, pf_full + st);
-            tma_load_3d(sm + L::pf(st) + 8192, &maps.k_sw, 64, h, (int)tc, pf_full + st);
-#pragma unroll
-            for (int s2 = 0; s2 < DV / 64; ++s2)
-              tma_load_3d(sm + L::pf(st) + 16384 + s2 * 8192, &maps.v, vc0 + 64 * s2, h, (int)tc,
-                          pf_full + st);
-          }
-        };
-        for (int cp = 0; cp < 3 && cp < c_begin; ++cp) pf_issue(cp);
-#pragma unroll 1
-        for (int cp = 0; cp < c_begin; ++cp) {
-          const int st = cp & 3;
-          if (!warp_wait(pf_full + st, (ph_f >> st) & 1u)) { pf_ok = false; break; }
-          ph_f ^= 1u << st;
-          const Opnd opKp{x.sb + L::pf(st), 8192, true};           // K as MN-major A
-          const Opnd opVp{x.sb + L::pf(st) + 16384, 8192, true};   // V as MN-major B
-          mma_run<kC>(x.tm + kColS, opKp, opVp, idesc_bf16(128, DV, false, true, true), true);
-          mma_commit_elect(pf_mma + st);
-          if (cp + 3 < c_begin) {  // stage (cp + 3) & 3 held chunk cp - 1: its MMA must be done
-            if (cp >= 1) {
-              const int sp = (cp - 1) & 3;
-              if (!warp_wait(pf_mma + sp, (ph_m >> sp) & 1u)) { pf_ok = false; break; }
-              ph_m ^= 1u << sp;
-            }
-            pf_issue(cp + 3);
-          }
-        }
-        mma_commit_elect(x.bar_mma);  // every prefix MMA complete
-      }
-      if (__syncthreads_or(!pf_ok)) {
-        failed = true;
-      } else if (!wait_bar(x.bar_mma, x.ph_mma)) {
-        failed = true;
-      } else {
-        s_epilogue<DH>(x, sm + L::SS);  // the bf16 operand copy of the segment's entering state
-        cta_sync_tc();
-      }
-    }
-  }
-  if (!failed && ts < te) {
-    issue_qk(ts);
-    issue_a(ts);
-    issue_v(ts);
-  }
   float nb_beta, nb_alpha;
-  load_scalars(ts, nb_beta, nb_alpha);
+  load_scalars(t0, nb_beta, nb_alpha);
 
   // operand views of the state pass
   const Opnd opQ{x.sb + L::KQ + 8192, 16384, false};  // Q~ rows as K-major A (M = 64)
@@ -253,29 +177,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t id_s = idesc_bf16(128, DV, false, true, true);
 
 #pragma unroll 1
-  for (int64_t tc = ts; tc < te && !failed; tc += kC) {
-    const int n = (int)((te - tc) < (int64_t)kC ? (te - tc) : (int64_t)kC);
+  for (int64_t tc = t0; tc < t1 && !failed; tc += kC) {
+    const int n = (int)((t1 - tc) < (int64_t)kC ? (t1 - tc) : (int64_t)kC);
     const int64_t tn = tc + kC;  // next chunk
 
     if (tid < kC) {
       sBeta[tid] = nb_beta;
       sAlpha[tid] = nb_alpha;
     }
-    if (tn < te) load_scalars(tn, nb_beta, nb_alpha);
+    if (tn < t1) load_scalars(tn, nb_beta, nb_alpha);
     if (!wait_bar(bar_qk, ph_qk)) { failed = true; break; }
     if (kAlphaTile && !wait_bar(bar_a, ph_a)) { failed = true; break; }
 
     // 1. gates and operand tiles
-    const bool safe = gate_stage<L, CHANNEL, LINEAR>(x, n);
+    const bool safe = gate_stage<L, CHANNEL>(x, n);
     fence_async_smem();
     cta_sync_tc();
-    if (safe && tn < te) {  // q, k and alpha tiles are consumed: fetch the next chunk's
+    if (safe && tn < t1) {  // q, k and alpha tiles are consumed: fetch the next chunk's
       issue_qk(tn);
       issue_a(tn);
     }
     // 2. decay-weighted Gram matrices [A'; M]
-    if (!gram_stage<L, CHANNEL, LINEAR>(x, n, safe)) { failed = true; break; }
-    if (!safe && tn < te) {
+    if (!gram_stage<L, CHANNEL>(x, n, safe)) { failed = true; break; }
+    if (!safe && tn < t1) {
       issue_qk(tn);
       issue_a(tn);
     }
@@ -283,35 +207,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!wait_bar(bar_v, ph_v)) { failed = true; break; }
     zero_v_tail<DV>(x, sm + L::VIN, n);
 
-    if (!LINEAR) {
-      // 3. T' = (I + A)^-1 diag(beta);  4. W = T' K~ and U~ = T' V
-      solve_stage<L>(x);
-      if (!w_stage<L>(x, true, opV, id_v)) { failed = true; break; }
-      if (tn < te) issue_v(tn);  // V is consumed
-      w_epilogue<L>(x);
-    }
+    // 3. T' = (I + A)^-1 diag(beta);  4. W = T' K~ and U~ = T' V
+    solve_stage<L>(x);
+    if (!w_stage<L>(x, true, opV, id_v)) { failed = true; break; }
+    if (tn < t1) issue_v(tn);  // V is consumed
+    w_epilogue<L>(x);
     cta_sync_tc();
 
     // 5. U = U~ - W S and O = Q~ S; the state master is faded meanwhile
     if (warp == 0) {
-      if (!LINEAR) mma_run<kD>(x.tm + kColU, opW, opS, id_negw, true);
+      mma_run<kD>(x.tm + kColU, opW, opS, id_negw, true);
       mma_run<kD>(x.tm + kColWO, opQ, opS, id_v, false);
       mma_commit_elect(x.bar_mma);
     }
-    if (!LINEAR) gamma_fade<DH>(x, sGam);
+    gamma_fade<DH>(x, sGam);
     if (!wait_bar(x.bar_mma, x.ph_mma)) { failed = true; break; }
-    if (!LINEAR) u_epilogue<DH>(x, sm + L::UU);
+    u_epilogue<DH>(x, sm + L::UU);
     cta_sync_tc();
 
     // 6. O += M U and S += K^^T U
     if (warp == 0) {
-      const Opnd opUse = LINEAR ? opV : opU;
-      mma_run<kC>(x.tm + kColWO, opM, opUse, id_v, true);
-      mma_run<kC>(x.tm + kColS, opKH, opUse, id_s, true);
+      mma_run<kC>(x.tm + kColWO, opM, opU, id_v, true);
+      mma_run<kC>(x.tm + kColS, opKH, opU, id_s, true);
       mma_commit_elect(x.bar_mma);
     }
     if (!wait_bar(x.bar_mma, x.ph_mma)) { failed = true; break; }
-    if (LINEAR && tn < te) issue_v(tn);
     o_epilogue<DH>(x, out, tc, n, H, h, vc0);
     s_epilogue<DH>(x, sm + L::SS);
     cta_sync_tc();
@@ -323,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait(bar_qk, ph_qk, kWaitNs);
     if (kAlphaTile) mbar_wait(bar_a, ph_a, kWaitNs);
     mbar_wait(bar_v, ph_v, kWaitNs);
-  } else if (a.S_final && c_end == nch) {  // the last run of the sequence hands the state on
+  } else if (a.S_final) {
     s_final<DH>(x, a.S_final + sidx + (size_t)x.lrow * kD + vc0);
   }
   cta_sync_tc();
@@ -375,6 +295,8 @@ bool make_tc_maps(const gdr_shape& sh, const PrefillArgs& a, bool linear, TcMaps
                      CU_TENSOR_MAP_SWIZZLE_128B);
   if (ok && linear)
     ok = make_map(&maps->k_sw, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, T, 64,
+                  CU_TENSOR_MAP_SWIZZLE_128B) &&
+         make_map(&maps->q_sw, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, T, 64,
                   CU_TENSOR_MAP_SWIZZLE_128B);
   if (ok && !linear && sh.gate == GDR_GATE_CHANNEL)
     ok = make_map(&maps->alpha, a.alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, T, kD,
@@ -385,34 +307,24 @@ bool make_tc_maps(const gdr_shape& sh, const PrefillArgs& a, bool linear, TcMaps
 
 namespace {
 
-template <int DV, bool CHANNEL, bool LINEAR>
-cudaError_t launch_one(const gdr_shape& sh, const PrefillArgs& a, const TcMaps& maps, int nseg,
+template <int DV, bool CHANNEL>
+cudaError_t launch_one(const gdr_shape& sh, const PrefillArgs& a, const TcMaps& maps,
                        cudaStream_t s) {
-  auto kern = prefill_tc_kernel<DV, CHANNEL, LINEAR>;
+  auto kern = prefill_tc_kernel<DV, CHANNEL>;
   const size_t smem = TcSmem<DV>::bytes;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const unsigned grid =
-      (unsigned)sh.n_seqs * (unsigned)sh.H * (unsigned)nseg * (unsigned)(kD / DV);
-  kern<<<grid, kThreads, smem, s>>>(maps, a, nseg);
+  const unsigned grid = (unsigned)sh.n_seqs * (unsigned)sh.H * (unsigned)(kD / DV);
+  kern<<<grid, kThreads, smem, s>>>(maps, a);
   return cudaGetLastError();
 }
 
 template <int DV>
-cudaError_t launch_dv(const gdr_shape& sh, const PrefillArgs& a, const TcMaps& maps, bool linear,
-                      int nseg, cudaStream_t s) {
-  if (linear) return launch_one<DV, true, true>(sh, a, maps, nseg, s);
-  if (sh.gate == GDR_GATE_CHANNEL) return launch_one<DV, true, false>(sh, a, maps, 1, s);
-  return launch_one<DV, false, false>(sh, a, maps, 1, s);
-}
-
-int sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return 0;
-  return n;
+cudaError_t launch_dv(const gdr_shape& sh, const PrefillArgs& a, const TcMaps& maps,
+                      cudaStream_t s) {
+  if (sh.gate == GDR_GATE_CHANNEL) return launch_one<DV, true>(sh, a, maps, s);
+  return launch_one<DV, false>(sh, a, maps, s);
 }
 
 }  // namespace
@@ -427,30 +339,21 @@ cudaError_t launch_prefill_tc(const gdr_shape& sh, const PrefillArgs& a, bool li
                               cudaStream_t s) {
   TcMaps maps;
   if (!tc::make_tc_maps(sh, a, linear, &maps)) return cudaErrorInvalidValue;
+  if (linear) return tc::launch_linear_tc(sh, a, maps, s);  // linear_tc.cu
   // few (sequence, head) chains: helper CTAs prepare the chunks of each chain, in clusters (the
   // operands cross over DSMEM) or, when clusters would give a chain a single helper, from a
   // work queue over every SM (the operands cross through L2 rings in the workspace)
-  if (!linear && !(sh.flags & GDR_FLAG_NO_CLUSTER)) {
+  if (!(sh.flags & GDR_FLAG_NO_CLUSTER)) {
     const int ncl = tc::cluster_size_for(sh);
     const int G = tc::queue_grid_for(sh, a);
     if (G > 0 && (ncl <= 2 || (sh.flags & GDR_FLAG_PREFER_QUEUE)))
       return tc::launch_prefill_queue(sh, a, maps, G, s);
     if (ncl > 1) return tc::launch_prefill_cluster(sh, a, maps, ncl, s);
   }
-  const long pairs = (long)sh.n_seqs * sh.H;
-  if (linear) {
-    // linear attention with few (sequence, head) pairs: runs of at least 16 chunks per CTA, as
-    // many as fill the SMs once (each run recomputes its entering state from the chunks before)
-    const long sms = sm_count();
-    const long avg_chunks = sh.total_tokens / ((long)sh.n_seqs * kC);
-    long nseg = pairs > 0 ? sms / pairs : 1;
-    if (nseg > avg_chunks / 16) nseg = avg_chunks / 16;
-    if (nseg > 8) nseg = 8;
-    if (nseg > 1) return launch_dv<128>(sh, a, maps, true, (int)nseg, s);
-  }
   // value-column split: enough CTAs to cover the SMs when there are few (sequence, head) pairs
-  if (pairs >= 120) return launch_dv<128>(sh, a, maps, linear, 1, s);
-  return launch_dv<64>(sh, a, maps, linear, 1, s);
+  const long pairs = (long)sh.n_seqs * sh.H;
+  if (pairs >= 120) return launch_dv<128>(sh, a, maps, s);
+  return launch_dv<64>(sh, a, maps, s);
 }
 
 }  // namespace gdr

@@ -245,7 +245,7 @@ __device__ __forceinline__ void ld_bf16x8(const __nv_bfloat16* p, float* x) {
 
 struct TcMaps {
   CUtensorMap q, k, v, alpha;
-  CUtensorMap k_sw;  // k in 64-channel SW128 boxes (linear attention's segment prefix)
+  CUtensorMap k_sw, q_sw;  // k, q in 64-channel SW128 boxes (linear attention)
 };
 
 
@@ -298,9 +298,9 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t& ph) {
 // or raw K and Q for scalar gates), KR (Kr) and KH (K^), gamma, the exact diagonal q_r . k_r and,
 // for scalar gates, the per-token log prefix sums.  Returns whether the chunk's decay allows the
 // factorised Gram products (otherwise the log prefix sums are left in the alpha tile).
-template <class L, bool CHANNEL, bool LINEAR>
+template <class L, bool CHANNEL>
 __device__ bool gate_stage(const TcCtx& x, int n) {
-  constexpr bool kScalar = !CHANNEL && !LINEAR;
+  constexpr bool kScalar = !CHANNEL;
   unsigned char* sm = x.sm;
   const int tid = x.tid, warp = x.warp, lane = x.lane;
   const __nv_bfloat16* sQin = reinterpret_cast<const __nv_bfloat16*>(sm + L::QIN);
@@ -373,7 +373,7 @@ __device__ bool gate_stage(const TcCtx& x, int n) {
         }
       }
     } else {
-      // Per-channel gates (and linear attention): running products of the gates down the
+      // Per-channel gates: running products of the gates down the
       // thread's rows, then the carry of the earlier row blocks through shared memory.
       float p[4][8];  // prefix products Gam[4 rb + rr][8 g8 + cc]
       float gn[8];    // Gam_n (= gamma) of the 8 channels
@@ -387,7 +387,7 @@ __device__ bool gate_stage(const TcCtx& x, int n) {
           float a8[8];
 #pragma unroll
           for (int cc = 0; cc < 8; ++cc) a8[cc] = 1.f;
-          if (!LINEAR && r < n) {
+          if (r < n) {
             const float4 u0 = *reinterpret_cast<const float4*>(sAin + r * kD + 8 * g8);
             const float4 u1 = *reinterpret_cast<const float4*>(sAin + r * kD + 8 * g8 + 4);
             a8[0] = u0.x, a8[1] = u0.y, a8[2] = u0.z, a8[3] = u0.w;
@@ -401,7 +401,7 @@ __device__ bool gate_stage(const TcCtx& x, int n) {
         }
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) gn[cc] = 1.f;
-        if (!LINEAR) {
+        {
           // row-block totals -> exclusive products down the 16 row blocks (one thread per
           // channel; row 16 receives Gam_n) -> each thread's carry
           float* sTot = reinterpret_cast<float*>(sm + L::TOT);  // [17][128 channels]
@@ -458,14 +458,14 @@ __device__ bool gate_stage(const TcCtx& x, int n) {
 #pragma unroll
           for (int cc = 0; cc < 8; ++cc) {
             const float G = p[rr][cc];
-            const float inv = LINEAR ? 1.f : __fdividef(1.f, G);
+            const float inv = __fdividef(1.f, G);
             ke[cc] = k8[cc] * G;
             qe[cc] = q8[cc] * G;
             ki[cc] = k8[cc] * inv;
             kh[cc] = ki[cc] * gn[cc];
             dq = fmaf(q8[cc], k8[cc], dq);
           }
-          if (!LINEAR) sDiagP[r * 16 + g8] = dq;  // M's diagonal carries no decay: q_r . k_r
+          sDiagP[r * 16 + g8] = dq;  // M's diagonal carries no decay: q_r . k_r
           st_chunk8(sm + L::KQ, 16384, r, 8 * g8, ke);       // K~
           st_chunk8(sm + L::KQ, 16384, 64 + r, 8 * g8, qe);  // Q~
           st_chunk8(sm + L::KR, 8192, r, 8 * g8, ki);        // Kr
@@ -511,9 +511,9 @@ __device__ bool gate_stage(const TcCtx& x, int n) {
 // TMEM, then the epilogue: A = diag(beta) strict_lower(A') as fp32 (swizzled) and M as the bf16
 // operand MM; strong-decay chunks form both from direct pairwise exponentials instead.
 // Returns false if the MMA wait gave up.
-template <class L, bool CHANNEL, bool LINEAR>
+template <class L, bool CHANNEL>
 __device__ bool gram_stage(TcCtx& x, int n, bool safe) {
-  constexpr bool kScalar = !CHANNEL && !LINEAR;
+  constexpr bool kScalar = !CHANNEL;
   unsigned char* sm = x.sm;
   const int tid = x.tid, lrow = x.lrow, wh = x.wh;
   const uint32_t tm = x.tm, lane_base = x.lane_base;
@@ -544,7 +544,7 @@ __device__ bool gram_stage(TcCtx& x, int n, bool safe) {
           xv[j] = (c0 + j <= r) ? xv[j] * __expf(sGs[r] - sGs[c0 + j]) : 0.f;
       }
       if (lrow < 64) {
-        if (!LINEAR) {
+        {
           const float b = sBeta[r];
 #pragma unroll
           for (int j = 0; j < 32; j += 4)
@@ -555,7 +555,7 @@ __device__ bool gram_stage(TcCtx& x, int n, bool safe) {
         }
       } else {
         float dg = 0.f;  // q_r . k_r, summed from the gate stage's 16 partials
-        if (!LINEAR && r >= c0 && r < c0 + 32) {
+        if (r >= c0 && r < c0 + 32) {
 #pragma unroll
           for (int i = 0; i < 16; i += 4) {
             const float4 p4 = *reinterpret_cast<const float4*>(sDiagP + r * 16 + i);
@@ -565,7 +565,7 @@ __device__ bool gram_stage(TcCtx& x, int n, bool safe) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           xv[j] = (c0 + j <= r) ? xv[j] : 0.f;
-          if (!LINEAR && c0 + j == r) xv[j] = dg;
+          if (c0 + j == r) xv[j] = dg;
         }
         unsigned char* mm = x.gslot ? x.gslot + kSlotM : sm + L::MM;  // M: hand-over only
 #pragma unroll
@@ -782,6 +782,9 @@ __device__ void zero_v_tail(const TcCtx& x, unsigned char* vin, int n) {
 
 // host side: tensor maps of q, k, v and (per-channel gates) alpha; false if encoding failed
 bool make_tc_maps(const gdr_shape& sh, const PrefillArgs& a, bool linear, TcMaps* maps);
+// host side: the linear-attention kernel (bf16, d = 128)
+cudaError_t launch_linear_tc(const gdr_shape& sh, const PrefillArgs& a, const TcMaps& maps,
+                             cudaStream_t s);
 // host side: CTAs of the work-queue prefill for this shape and workspace (0: use another kernel)
 int queue_grid_for(const gdr_shape& sh, const PrefillArgs& a);
 cudaError_t launch_prefill_queue(const gdr_shape& sh, const PrefillArgs& a, const TcMaps& maps,
