@@ -85,7 +85,8 @@ def source_digest(files):
     return h.hexdigest()[:16]
 
 
-KERNEL_SOURCES = {"prefill": ["prefill_queue.cu", "prefill_tc.cu", "tc_common.cuh", "umma.cuh"],
+KERNEL_SOURCES = {"prefill": ["prefill_cluster.cu", "prefill_queue.cu", "prefill_tc.cu", "tc_common.cuh",
+                              "umma.cuh"],
                   "linear_attn": ["linear_tc.cu", "tc_common.cuh", "umma.cuh"],
                   "decode": ["decode.cu"]}
 
