@@ -56,8 +56,8 @@ struct HelperSmem {
   static constexpr uint32_t GAM = ALPHA + 256;
   static constexpr uint32_t RED = GAM + 512;
   static constexpr uint32_t GS = RED + 64;
-  static constexpr uint32_t TOT = GS + 256;       // gate carries [17][128] fp32
-  static constexpr uint32_t CONS = TOT + 8704;    // chunks consumed by the chain CTA (u32)
+  static constexpr uint32_t TOT = GS + 256;       // gate carries [32][128] fp32
+  static constexpr uint32_t CONS = TOT + 16384;   // chunks consumed by the chain CTA (u32)
   static constexpr uint32_t BARS = CONS + 64;     // qk, alpha, mma, TMEM slot
   static constexpr uint32_t END = BARS + 64;
   static constexpr uint32_t SA = KR;              // A [64][64] fp32 (Kr is consumed by then)
@@ -232,13 +232,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Opnd opZM{x.sb + slot + kSlotZ, 16384, false};
       const Opnd opWQ{x.sb + slot + kSlotWQ, 16384, false};
       const Opnd opKH{x.sb + slot + kSlotKH, 8192, true};
-      {  // the chunk's operands and V tile
-        bool ok = mbar_wait(full + s, ph_full[s], kWaitNs);
-        ok = ok && mbar_wait(bar_v, ph_v, kWaitNs);
+      // Waits inside a chunk are per thread (no CTA barrier where the mbarrier already orders
+      // what a thread reads); a wait that gave up is remembered in `bad`, and the CTA agrees on
+      // it at the chunk's closing barrier and unwinds.
+      bool bad = false;
+      {  // the chunk's operands (every thread reads gamma) and V tile
+        bad |= !mbar_wait(full + s, ph_full[s], kWaitNs);
+        bad |= !mbar_wait(bar_v, ph_v, kWaitNs);
         ph_full[s] ^= 1u;
         ph_v ^= 1u;
-        if (ok && n < kC) zero_v_tail<DV>(x, sm + L::VIN, n);
-        if (__syncthreads_or(!ok)) { failed = true; break; }
+        if (n < kC) {  // the last chunk: every thread zeroes part of the V tail
+          zero_v_tail<DV>(x, sm + L::VIN, n);
+          __syncthreads();
+        }
         fence_after_sync();
       }
       // D = [T'; Z] V + [-W; Q~] S; meanwhile the state master is faded and the previous
@@ -250,7 +256,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       gamma_fade<DH>(x, reinterpret_cast<const float*>(sm + slot + kSlotGam));
       if (c > 0 && !u_rows) o_store(c - 1, tc - kC, kC);
-      if (!wait_bar(x.bar_mma, x.ph_mma)) { failed = true; break; }
+      bad |= !mbar_wait(x.bar_mma, x.ph_mma, kWaitNs);
+      x.ph_mma ^= 1u;
+      fence_after_sync();
       if (c + 1 < nch) issue_v(tc + kC);  // V is consumed
       if (u_rows) {  // U rows -> bf16 [tok][DV] tile (MN-major B operand)
         float v[64];
@@ -259,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 64; j += 8) st_chunk8(sm + L::UU, 8192, drow, x.wh * 64 + j, v + j);
         fence_async_smem();
       }
-      cta_sync_tc();
+      cta_sync_tc();  // U is written and every warp's fade of the state master is complete
       // S += K^^T U (on the chain's critical path), then O += M U
       if (warp == 0) {
         mma_run<kC>(x.tm + kColS, opKH, opU, id_s, true);
@@ -267,13 +275,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_run<kC>(x.tm + d_col(c), opZM, opU, id_d, true);
         mma_commit_elect(bar_o);
       }
-      if (!wait_bar(x.bar_mma, x.ph_mma)) { failed = true; break; }
+      bad |= !mbar_wait(x.bar_mma, x.ph_mma, kWaitNs);
+      x.ph_mma ^= 1u;
+      fence_after_sync();
       s_epilogue<DH>(x, sm + L::SS);
       // the slot is consumed once O's MMA is complete (gamma was read before a barrier): re-arm
       // it for chunk c + 2 and tell the helpers
-      bool ok_o = true;
       if (tid == 0) {
-        ok_o = mbar_wait(bar_o, ph_o, kWaitNs);
+        const bool ok_o = mbar_wait(bar_o, ph_o, kWaitNs);
+        bad |= !ok_o;
         if (ok_o) {
           if (c + 2 < nch) mbar_expect_tx(full + s, kSlotPayload);
           for (int r = 1; r < ncl; ++r) st_relaxed_remote(map_to(cons_local, r), (uint32_t)(c + 1));
@@ -281,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ph_o ^= 1u;
       fence_before_sync();
-      if (__syncthreads_or(!ok_o)) { failed = true; break; }
+      if (__syncthreads_or(bad)) { failed = true; break; }
       fence_after_sync();
     }
     if (!failed && nch > 0 && !u_rows) {

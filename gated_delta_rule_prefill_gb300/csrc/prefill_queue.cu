@@ -59,8 +59,8 @@ struct QHelperSmem {
   static constexpr uint32_t GAM = ALPHA + 256;
   static constexpr uint32_t RED = GAM + 512;
   static constexpr uint32_t GS = RED + 64;
-  static constexpr uint32_t TOT = GS + 256;       // gate carries [17][128] fp32
-  static constexpr uint32_t ITEM = TOT + 8704;    // the next work item (int32 x 2, x 2 buffers)
+  static constexpr uint32_t TOT = GS + 256;       // gate carries [32][128] fp32
+  static constexpr uint32_t ITEM = TOT + 16384;   // the next work item (int32 x 2, x 2 buffers)
   static constexpr uint32_t CHAINS = ITEM + 64;   // per chain: first token, tokens, head [76]
   static constexpr uint32_t BARS = CHAINS + 76 * 16;  // qk, alpha, mma, TMEM slot
   static constexpr uint32_t END = BARS + 64;

@@ -71,7 +71,7 @@ struct TcSmem {
   static constexpr uint32_t SA = KR;                // A [64][64]  (Kr is consumed by then)
   static constexpr uint32_t ST32 = WW;              // T [64][64]  (W is written later)
   static constexpr uint32_t SX = UU;                // [32][32] (U is written later)
-  static constexpr uint32_t TOT = WW;               // gate carries [17][128] (W later)
+  static constexpr uint32_t TOT = WW;               // gate carries [32][128] (W later)
   static constexpr uint32_t DIAGP = UU;             // q_r . k_r partials [64][16] (U later)
   static_assert(bytes <= 232448, "shared memory per CTA");
   static_assert(DV * 128 >= 32 * 32 * 4, "block scratch fits in U");

@@ -377,6 +377,7 @@ __device__ bool gate_stage(const TcCtx& x, int n) {
       // thread's rows, then the carry of the earlier row blocks through shared memory.
       float p[4][8];  // prefix products Gam[4 rb + rr][8 g8 + cc]
       float gn[8];    // Gam_n (= gamma) of the 8 channels
+      float sufc[8];  // product of the gates of the later row blocks, per channel
       {
         float run[8];
 #pragma unroll
@@ -399,12 +400,10 @@ __device__ bool gate_stage(const TcCtx& x, int n) {
             p[rr][cc] = run[cc];
           }
         }
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) gn[cc] = 1.f;
         {
-          // row-block totals -> exclusive products down the 16 row blocks (one thread per
-          // channel; row 16 receives Gam_n) -> each thread's carry
-          float* sTot = reinterpret_cast<float*>(sm + L::TOT);  // [17][128 channels]
+          // row-block totals -> exclusive prefix and suffix products over the 16 row blocks
+          // (one thread per channel) -> each thread's carries; gamma = the full product
+          float* sTot = reinterpret_cast<float*>(sm + L::TOT);  // [32][128 channels]
           *reinterpret_cast<float4*>(sTot + rb * kD + 8 * g8) = make_float4(run[0], run[1], run[2], run[3]);
           *reinterpret_cast<float4*>(sTot + rb * kD + 8 * g8 + 4) = make_float4(run[4], run[5], run[6], run[7]);
           __syncthreads();
@@ -418,7 +417,12 @@ __device__ bool gate_stage(const TcCtx& x, int n) {
               sTot[b2 * kD + tid] = acc;
               acc *= t16[b2];
             }
-            sTot[16 * kD + tid] = acc;
+            float suf = 1.f;
+#pragma unroll
+            for (int b2 = 15; b2 >= 0; --b2) {
+              sTot[(16 + b2) * kD + tid] = suf;
+              suf *= t16[b2];
+            }
             sGam[tid] = acc;
             if (x.gslot) reinterpret_cast<float*>(x.gslot + kSlotGam)[tid] = acc;
             float mn = acc;
@@ -429,9 +433,13 @@ __device__ bool gate_stage(const TcCtx& x, int n) {
           __syncthreads();
           const float4 c0 = *reinterpret_cast<const float4*>(sTot + rb * kD + 8 * g8);
           const float4 c1 = *reinterpret_cast<const float4*>(sTot + rb * kD + 8 * g8 + 4);
-          const float4 n0 = *reinterpret_cast<const float4*>(sTot + 16 * kD + 8 * g8);
-          const float4 n1 = *reinterpret_cast<const float4*>(sTot + 16 * kD + 8 * g8 + 4);
+          const float4 s0 = *reinterpret_cast<const float4*>(sTot + (16 + rb) * kD + 8 * g8);
+          const float4 s1 = *reinterpret_cast<const float4*>(sTot + (16 + rb) * kD + 8 * g8 + 4);
+          const float4 n0 = *reinterpret_cast<const float4*>(sGam + 8 * g8);
+          const float4 n1 = *reinterpret_cast<const float4*>(sGam + 8 * g8 + 4);
           const float carry[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          sufc[0] = s0.x, sufc[1] = s0.y, sufc[2] = s0.z, sufc[3] = s0.w;
+          sufc[4] = s1.x, sufc[5] = s1.y, sufc[6] = s1.z, sufc[7] = s1.w;
           gn[0] = n0.x, gn[1] = n0.y, gn[2] = n0.z, gn[3] = n0.w;
           gn[4] = n1.x, gn[5] = n1.y, gn[6] = n1.z, gn[7] = n1.w;
 #pragma unroll
@@ -443,8 +451,17 @@ __device__ bool gate_stage(const TcCtx& x, int n) {
       }
 
       if (safe) {
+        // K^ = K * Gam_n / Gam = K * (product of the later gates): a suffix product, no division;
+        // Kr = K / Gam = K^ / Gam_n with one reciprocal per channel.  Rows go last to first so
+        // the within-block suffix grows by one gate per row.
+        float rgn[8], suf[8];
 #pragma unroll
-        for (int rr = 0; rr < 4; ++rr) {
+        for (int cc = 0; cc < 8; ++cc) {
+          rgn[cc] = __fdividef(1.f, gn[cc]);
+          suf[cc] = sufc[cc];
+        }
+#pragma unroll
+        for (int rr = 3; rr >= 0; --rr) {
           const int r = 4 * rb + rr;
           float k8[8], q8[8];
           if (r < n) {
@@ -458,12 +475,17 @@ __device__ bool gate_stage(const TcCtx& x, int n) {
 #pragma unroll
           for (int cc = 0; cc < 8; ++cc) {
             const float G = p[rr][cc];
-            const float inv = __fdividef(1.f, G);
             ke[cc] = k8[cc] * G;
             qe[cc] = q8[cc] * G;
-            ki[cc] = k8[cc] * inv;
-            kh[cc] = ki[cc] * gn[cc];
+            kh[cc] = k8[cc] * suf[cc];
+            ki[cc] = kh[cc] * rgn[cc];
             dq = fmaf(q8[cc], k8[cc], dq);
+          }
+          if (rr > 0 && r < n) {  // the suffix of row r - 1 gains this row's gates
+            const float4 u0 = *reinterpret_cast<const float4*>(sAin + r * kD + 8 * g8);
+            const float4 u1 = *reinterpret_cast<const float4*>(sAin + r * kD + 8 * g8 + 4);
+            suf[0] *= u0.x, suf[1] *= u0.y, suf[2] *= u0.z, suf[3] *= u0.w;
+            suf[4] *= u1.x, suf[5] *= u1.y, suf[6] *= u1.z, suf[7] *= u1.w;
           }
           sDiagP[r * 16 + g8] = dq;  // M's diagonal carries no decay: q_r . k_r
           st_chunk8(sm + L::KQ, 16384, r, 8 * g8, ke);       // K~
