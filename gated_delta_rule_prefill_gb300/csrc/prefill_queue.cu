@@ -230,18 +230,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Opnd opZM{x.sb + slot + kSlotZ, 16384, false};
       const Opnd opWQ{x.sb + slot + kSlotWQ, 16384, false};
       const Opnd opKH{x.sb + slot + kSlotKH, 8192, true};
-      {  // the chunk's operands and V tile
-        bool ok = true;
+      // Waits inside a chunk are per thread (no CTA barrier where the mbarrier already orders
+      // what a thread reads); a wait that gave up is remembered in `bad`, and the CTA agrees on
+      // it at the chunk's closing barrier and unwinds.
+      bool bad = false;
+      {  // the chunk's operands (every thread reads gamma) and V tile
         if (loader && issued == c) {
-          ok = load_chunk(c) == 1;
+          bad |= load_chunk(c) != 1;
           issued = c + 1;
         }
-        ok = ok && mbar_wait(full + s, ph_full[s], kWaitNs);
-        ok = ok && mbar_wait(bar_v, ph_v, kWaitNs);
+        bad |= !mbar_wait(full + s, ph_full[s], kWaitNs);
+        bad |= !mbar_wait(bar_v, ph_v, kWaitNs);
         ph_full[s] ^= 1u;
         ph_v ^= 1u;
-        if (ok && n < kC) zero_v_tail<DV>(x, sm + L::VIN, n);
-        if (__syncthreads_or(!ok)) { failed = true; break; }
+        if (n < kC) {  // the last chunk: every thread zeroes part of the V tail
+          zero_v_tail<DV>(x, sm + L::VIN, n);
+          __syncthreads();
+        }
         fence_after_sync();
         landed = c + 1;
       }
@@ -264,7 +269,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         issue_load(c + 1);
         issued = c + 2;
       }
-      if (!wait_bar(x.bar_mma, x.ph_mma)) { failed = true; break; }
+      bad |= !mbar_wait(x.bar_mma, x.ph_mma, kWaitNs);
+      x.ph_mma ^= 1u;
+      fence_after_sync();
       if (c + 1 < nch) issue_v(tc + kC);  // V is consumed
       if (loader && issued == c + 1 && c + 1 < nch &&  // a second look (warp 2 is idle here)
           ld_acquire_gpu(q_ready + p * kR + ((c + 1) % kR)) >= (uint32_t)(c + 2)) {
@@ -278,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 64; j += 8) st_chunk8(sm + L::UU, 8192, drow, x.wh * 64 + j, v + j);
         fence_async_smem();
       }
-      cta_sync_tc();
+      cta_sync_tc();  // U is written and every warp's fade of the state master is complete
       // S += K^^T U (on the chain's critical path), then O += M U
       if (warp == 0) {
         mma_run<kC>(x.tm + kColS, opKH, opU, id_s, true);
@@ -286,15 +293,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_run<kC>(x.tm + d_col(c), opZM, opU, id_d, true);
         mma_commit_elect(bar_o);
       }
-      if (!wait_bar(x.bar_mma, x.ph_mma)) { failed = true; break; }
+      bad |= !mbar_wait(x.bar_mma, x.ph_mma, kWaitNs);
+      x.ph_mma ^= 1u;
+      fence_after_sync();
       s_epilogue<DH>(x, sm + L::SS);
       // the local slot is free for chunk c + 2 once O's MMA is complete (gamma was read before
       // a barrier)
-      bool ok_o = true;
-      if (tid == 0) ok_o = mbar_wait(bar_o, ph_o, kWaitNs);
+      if (tid == 0) bad |= !mbar_wait(bar_o, ph_o, kWaitNs);
       ph_o ^= 1u;
       fence_before_sync();
-      if (__syncthreads_or(!ok_o)) { failed = true; break; }
+      if (__syncthreads_or(bad)) { failed = true; break; }
       fence_after_sync();
     }
     if (!failed && nch > 0 && !u_rows) {

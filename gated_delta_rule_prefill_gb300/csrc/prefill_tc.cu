@@ -221,7 +221,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit_elect(x.bar_mma);
     }
     gamma_fade<DH>(x, sGam);
-    if (!wait_bar(x.bar_mma, x.ph_mma)) { failed = true; break; }
+    // the MMA waits of stages 5-6 are per thread; one that gave up is remembered and the CTA
+    // agrees on it at the chunk's closing barrier
+    bool bad = !mbar_wait(x.bar_mma, x.ph_mma, kWaitNs);
+    x.ph_mma ^= 1u;
+    fence_after_sync();
     u_epilogue<DH>(x, sm + L::UU);
     cta_sync_tc();
 
@@ -231,10 +235,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_run<kC>(x.tm + kColS, opKH, opU, id_s, true);
       mma_commit_elect(x.bar_mma);
     }
-    if (!wait_bar(x.bar_mma, x.ph_mma)) { failed = true; break; }
+    bad |= !mbar_wait(x.bar_mma, x.ph_mma, kWaitNs);
+    x.ph_mma ^= 1u;
+    fence_after_sync();
     o_epilogue<DH>(x, out, tc, n, H, h, vc0);
     s_epilogue<DH>(x, sm + L::SS);
-    cta_sync_tc();
+    fence_before_sync();
+    if (__syncthreads_or(bad)) { failed = true; break; }
+    fence_after_sync();
   }
 
   if (failed) {
