@@ -10,8 +10,8 @@
 //   S master -> bf16 operand for the next chunk (double-buffered, so this waits only for the
 //   state MMA), lower(Q K^T) -> bf16 M,  then  D += [Z; M] V  (rows 64-127: O)
 // and the O rows leave TMEM while the next chunk's MMAs run.  q, k, v of the next chunk are
-// fetched one chunk ahead.  Like the one-CTA kernel, a sequence of few (sequence, head) pairs is
-// split into runs of whole chunks, run g starting from S0 + sum of K^T V over the chunks before it.
+// fetched one chunk ahead.  With few (sequence, head) pairs each sequence is split into runs of
+// whole chunks, one CTA each, run g starting from S0 + sum of K^T V over the chunks before it.
 #include <cuda.h>
 
 #include "tc_common.cuh"
@@ -263,7 +263,9 @@ cudaError_t launch_linear_tc(const gdr_shape& sh, const PrefillArgs& a, const Tc
   long nseg = pairs > 0 ? sm_count() / pairs : 1;
   if (nseg > avg_chunks / 16) nseg = avg_chunks / 16;
   if (nseg > 8) nseg = 8;
-  if (nseg < 1) nseg = 1;
+  // an in-place hand-off (S_final = S0) keeps one run per sequence: a later run reads S0 while
+  // the last run of the same sequence writes S_final
+  if (nseg < 1 || (a.S0 && a.S0 == a.S_final)) nseg = 1;
   cudaError_t e = cudaFuncSetAttribute(linear_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)LinSmem::bytes);

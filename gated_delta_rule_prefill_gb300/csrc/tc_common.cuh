@@ -115,6 +115,12 @@ __device__ __forceinline__ void frag_a(const float* m, int r0, int k0, int g, in
   a[2] = tf32(m[f32x(r0 + g, k0 + t + 4)]);
   a[3] = tf32(m[f32x(r0 + g + 8, k0 + t + 4)]);
 }
+// two bf16 entries (r, c), (r, c + 1) of T' = T diag(beta) in the 64 x 64 K-major operand tile
+__device__ __forceinline__ void st_tp2(unsigned char* tt, const float* beta, int r, int c,
+                                       float t0, float t1) {
+  *reinterpret_cast<__nv_bfloat162*>(tt + sw128_offset(r, c, 8192)) =
+      __floats2bfloat162_rn(t0 * beta[c], t1 * beta[c + 1]);
+}
 // 32 x 32 fp32 scratch, columns XOR-swizzled by 8 * (row % 4) against bank conflicts
 __device__ __forceinline__ int x32(int r, int c) { return r * 32 + (c ^ ((r & 3) << 3)); }
 
@@ -124,8 +130,10 @@ __device__ __forceinline__ int x32(int r, int c) { return r * 32 + (c ^ ((r & 3)
 // T_ba = -T_bb (A_ba T_aa) over the pairs of diagonal blocks (a, b) of the level below (level 64:
 // T_[23][01] = -T_[23][23] (A_[23][01] T_[01][01])).  The two products of each doubling step run
 // on the tensor cores as warp-level tf32 MMAs with fp32 accumulation (T' is rounded to bf16
-// afterwards, 4x coarser than tf32).  sX holds the intermediates (up to 32 x 32 fp32).
-__device__ inline void unit_lower_inverse(const float* sA, float* sT, float* sX, int tid) {
+// afterwards, 4x coarser than tf32).  sX holds the intermediates (up to 32 x 32 fp32).  Every
+// entry of T is also written as the bf16 operand T' = T diag(beta) into tt where it is produced.
+__device__ inline void unit_lower_inverse(const float* sA, float* sT, float* sX, int tid,
+                                          unsigned char* tt, const float* beta) {
   const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
   if (tid < 64) {
     const int b = tid >> 3, c = tid & 7, o = 8 * b;
@@ -138,13 +146,20 @@ __device__ inline void unit_lower_inverse(const float* sA, float* sT, float* sX,
 #pragma unroll
       for (int i = j + 1; i < 8; ++i) acc[i] = fmaf(-sA[f32x(o + i, o + j)], xj, acc[i]);
     }
+    const float bc = beta[o + c];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) sT[f32x(o + i, o + c)] = acc[i];
+    for (int i = 0; i < 8; ++i) {
+      sT[f32x(o + i, o + c)] = acc[i];
+      st_bf16(tt, sw128_offset(o + i, o + c, 8192), acc[i] * bc);
+    }
   } else {
     // everything right of the 8 x 8 diagonal blocks is zero
     for (int e = tid - 64; e < kC * 16; e += kThreads - 64) {
       const int r = e >> 4, grp = e & 15;
-      if (grp >= 2 * ((r >> 3) + 1)) st4x(sT, r, grp, make_float4(0.f, 0.f, 0.f, 0.f));
+      if (grp >= 2 * ((r >> 3) + 1)) {
+        st4x(sT, r, grp, make_float4(0.f, 0.f, 0.f, 0.f));
+        *reinterpret_cast<uint2*>(tt + sw128_offset(r, 4 * grp, 8192)) = make_uint2(0u, 0u);
+      }
     }
   }
   __syncthreads();
@@ -166,6 +181,7 @@ __device__ inline void unit_lower_inverse(const float* sA, float* sT, float* sX,
     float y[4] = {0.f, 0.f, 0.f, 0.f};
     mma_tf32(y, a, tf32(sXw[t * 8 + g]), tf32(sXw[(t + 4) * 8 + g]));
     *reinterpret_cast<float2*>(sT + f32x(rb + g, ra + 2 * t)) = make_float2(-y[0], -y[1]);
+    st_tp2(tt, beta, rb + g, ra + 2 * t, -y[0], -y[1]);
   }
   __syncthreads();
   // ---- level 32: warp (p, j) of warps 0-3 computes the 8 columns 8j.. of pair p's blocks
@@ -197,6 +213,8 @@ __device__ inline void unit_lower_inverse(const float* sA, float* sT, float* sX,
     *reinterpret_cast<float2*>(sT + f32x(rb + g, ra + 8 * j + 2 * t)) = make_float2(-y[0], -y[1]);
     *reinterpret_cast<float2*>(sT + f32x(rb + g + 8, ra + 8 * j + 2 * t)) =
         make_float2(-y[2], -y[3]);
+    st_tp2(tt, beta, rb + g, ra + 8 * j + 2 * t, -y[0], -y[1]);
+    st_tp2(tt, beta, rb + g + 8, ra + 8 * j + 2 * t, -y[2], -y[3]);
   }
   __syncthreads();
   // ---- level 64: warp (mi, ni) computes the 16 x 8 tile (rows 16 mi.., columns 8 ni..)
@@ -227,6 +245,8 @@ __device__ inline void unit_lower_inverse(const float* sA, float* sT, float* sX,
         make_float2(-y[0], -y[1]);
     *reinterpret_cast<float2*>(sT + f32x(32 + 16 * mi + g + 8, 8 * ni + 2 * t)) =
         make_float2(-y[2], -y[3]);
+    st_tp2(tt, beta, 32 + 16 * mi + g, 8 * ni + 2 * t, -y[0], -y[1]);
+    st_tp2(tt, beta, 32 + 16 * mi + g + 8, 8 * ni + 2 * t, -y[2], -y[3]);
     __syncthreads();
   }
 }
@@ -653,16 +673,10 @@ __device__ void solve_stage(const TcCtx& x) {
   float* sT32 = reinterpret_cast<float*>(sm + L::ST32);
   float* sX = reinterpret_cast<float*>(sm + L::SX);
   const float* sBeta = reinterpret_cast<const float*>(sm + L::BETA);
-  unit_lower_inverse(sA, sT32, sX, x.tid);
-  for (int e = x.tid; e < kC * kC / 8; e += kThreads) {
-    const int r = e >> 3, j0 = (e & 7) * 8;
-    const float4 t0 = ld4x(sT32, r, j0 >> 2), t1 = ld4x(sT32, r, (j0 >> 2) + 1);
-    const float4 b0 = *reinterpret_cast<const float4*>(sBeta + j0);
-    const float4 b1 = *reinterpret_cast<const float4*>(sBeta + j0 + 4);
-    const float v[8] = {t0.x * b0.x, t0.y * b0.y, t0.z * b0.z, t0.w * b0.w,
-                        t1.x * b1.x, t1.y * b1.y, t1.z * b1.z, t1.w * b1.w};
-    st_chunk8(sm + L::TT, 8192, r, j0, v);
-    if (x.gslot) st_chunk8(x.gslot + kSlotT, 8192, r, j0, v);
+  unit_lower_inverse(sA, sT32, sX, x.tid, sm + L::TT, sBeta);
+  if (x.gslot) {  // T' of the hand-over (the tile image, 16 bytes at a time)
+    for (int e = x.tid; e < 8192 / 16; e += kThreads)
+      reinterpret_cast<uint4*>(x.gslot + kSlotT)[e] = reinterpret_cast<const uint4*>(sm + L::TT)[e];
   }
   fence_async_smem();
   cta_sync_tc();

@@ -93,6 +93,27 @@ def test_linear_attn_segmented(lens, H):
           "linear segmented %s H=%d" % (lens, H))
 
 
+@pytest.mark.parametrize("linear", [False, True])
+def test_in_place_state_hand_off(linear):
+    """S_final = S0 (the documented in-place hand-off) on a workload whose linear pass would
+    otherwise be split into runs, and whose gated pass runs with helper CTAs."""
+    import gated_delta_rule_prefill_gb300 as g
+    wl = gi.custom(seed=27, seqlens=[5000, 4000], H=2, d_k=128, d_v=128, dtype="bf16",
+                   s0="normal")
+    a = gi.gen_full(wl)
+    d = dev_inputs(a, "bf16")
+    S = d["S0"].clone()
+    if linear:
+        out, _ = g.gdr_linear_attn(d["q"], d["k"], d["v"], S0=S, S_final=S,
+                                   cu_seqlens=d["cu_seqlens"])
+    else:
+        out, _ = g.gdr_prefill(d["q"], d["k"], d["v"], d["alpha"], d["beta"], S0=S, S_final=S,
+                               cu_seqlens=d["cu_seqlens"])
+    torch.cuda.synchronize()
+    check((host(out), host(S)), ref_prefill(a, linear=linear), TOL["bf16"],
+          "in-place %s" % ("linear" if linear else "gated"))
+
+
 @pytest.mark.parametrize("case", ["alpha0", "alpha1_beta0", "beta1", "tiny_alpha"])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_prefill_special_gates(case, dtype):
