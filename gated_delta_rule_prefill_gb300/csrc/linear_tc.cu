@@ -86,6 +86,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   TcCtx x = make_ctx(sm, *tslot, bar_s);
   bool failed = false;
   s_init<DH>(x, a.S0 ? a.S0 + sidx + (size_t)x.lrow * kD : nullptr, sm + L::SS);
+  cta_sync_tc();  // every row of the bf16 state tile is written before the first MMA
   const uint32_t id_s = idesc_bf16(128, kD, false, true, true);   // K as MN-major A, V MN-major B
   const uint32_t id_d = idesc_bf16(128, kD, false, false, true);  // K-major A, MN-major B
   const uint32_t id_a = idesc_bf16(128, kC, false, false, false);  // [K; Q] K^T (K-major B)

@@ -194,6 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     if (nch > 0) issue_v(t0);
     s_init<DH>(x, a.S0 ? a.S0 + sidx + (size_t)x.lrow * kD : nullptr, sm + L::SS);
+    cta_sync_tc();  // every row of the bf16 state tile is written before the first MMA
     const Opnd opV{x.sb + L::VIN, 8192, true};
     const Opnd opU{x.sb + L::UU, 8192, true};
     const Opnd opS{x.sb + L::SS, 16384, true};
@@ -204,23 +205,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int drow = (warp & 3) * 32 + (tid & 31) - (u_rows ? 0 : 64);
     uint32_t ph_o = 0;
 
-    // D alternates between two accumulators, so a chunk's output rows are written out while
-    // the next chunk's first MMAs run.
-    auto d_col = [](int c) { return (c & 1) ? kColWO : kColU; };
-    // O rows (TMEM lanes 64-127 of D) -> out rows [tc, tc + n) of head h
+    // D alternates between two accumulators, so a chunk's output rows are written out during the
+    // next chunk.  The state update K^^T U goes to a third accumulator (kColU) and is folded into
+    // the fp32 master as S <- gamma S + K^^T U when the bf16 operand copy is made, so no TMEM
+    // load or store of the master runs while the chunk's first products are on the tensor pipe.
+    auto d_col = [](int c) { return (c & 1) ? kColAM : kColWO; };
+    // O rows (TMEM lanes 64-127 of D) -> out rows [tc, tc + n) of head h.  A warp's 32 rows x 64
+    // columns go through its own 4 KB of the bf16 state tile (the rows it rewrites itself in
+    // s_update, free between the chunk's first MMA and that update), so that each global store
+    // instruction writes four whole 128-byte row segments instead of 32 scattered pieces.
     auto o_store = [&](int c, int64_t tc, int n) {
       float v[64];
       tmem_ld64(x.tm + x.lane_base + d_col(c) + x.wh * 64, v);
-      if (drow < n) {
-        __nv_bfloat16* dst = out + ((size_t)(tc + drow) * H + h) * kD + x.wh * 64;
+      unsigned char* stage = sm + L::SS + x.wh * 16384 + (warp & 3) * 4096;
+      const int lane = tid & 31;
 #pragma unroll
-        for (int j = 0; j < 64; j += 8) {
-          __align__(16) __nv_bfloat162 hv[4];
+      for (int j = 0; j < 64; j += 8) {
+        __align__(16) __nv_bfloat162 hv[4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) hv[i] = __floats2bfloat162_rn(v[j + 2 * i], v[j + 2 * i + 1]);
-          *reinterpret_cast<uint4*>(dst + j) = *reinterpret_cast<const uint4*>(hv);
-        }
+        for (int i = 0; i < 4; ++i) hv[i] = __floats2bfloat162_rn(v[j + 2 * i], v[j + 2 * i + 1]);
+        *reinterpret_cast<uint4*>(stage + lane * 128 + (((j >> 3) ^ (lane & 7)) << 4)) =
+            *reinterpret_cast<const uint4*>(hv);
       }
+      __syncwarp();
+      const int row0 = (warp & 3) * 32 - 64;  // this warp's first O row
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int r = 4 * j + (lane >> 3), ch = lane & 7;
+        const uint4 w = *reinterpret_cast<const uint4*>(stage + r * 128 + ((ch ^ (r & 7)) << 4));
+        if (row0 + r < n)
+          *reinterpret_cast<uint4*>(out + ((size_t)(tc + row0 + r) * H + h) * kD + x.wh * 64 + ch * 8) = w;
+      }
+      __syncwarp();
+    };
+    // S <- gamma S + K^^T U on this thread's row (key channel) and column half; the bf16 copy of
+    // the new state is the next chunk's B operand
+    auto s_update = [&](float gm) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const uint32_t c0 = (uint32_t)(x.wh * 64 + hh * 32);
+        float v[64];
+        tmem_ld32x2(x.tm + x.lane_base + kColS + c0, x.tm + x.lane_base + kColU + c0, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = fmaf(gm, v[j], v[32 + j]);
+        tmem_st32(x.tm + x.lane_base + kColS + c0, *reinterpret_cast<const float(*)[32]>(v));
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) st_chunk8(sm + L::SS, 16384, x.lrow, (int)c0 + j, v + j);
+      }
+      tmem_wait_st();
+      fence_async_smem();
     };
 #pragma unroll 1
     for (int c = 0; c < nch && !failed; ++c) {
@@ -236,63 +269,64 @@ __global__ void __launch_bounds__(kThreads, 1)
       // what a thread reads); a wait that gave up is remembered in `bad`, and the CTA agrees on
       // it at the chunk's closing barrier and unwinds.
       bool bad = false;
-      {  // the chunk's operands (every thread reads gamma) and V tile
+      float gm;
+      {  // the chunk's operands (every thread reads gamma of its row now) and V tile
         bad |= !mbar_wait(full + s, ph_full[s], kWaitNs);
         bad |= !mbar_wait(bar_v, ph_v, kWaitNs);
         ph_full[s] ^= 1u;
         ph_v ^= 1u;
+        gm = reinterpret_cast<const float*>(sm + slot + kSlotGam)[x.lrow];
         if (n < kC) {  // the last chunk: every thread zeroes part of the V tail
           zero_v_tail<DV>(x, sm + L::VIN, n);
           __syncthreads();
         }
         fence_after_sync();
       }
-      // D = [T'; Z] V + [-W; Q~] S; meanwhile the state master is faded and the previous
-      // chunk's output rows are stored
+      // D = [T'; Z] V + [-W; Q~] S, alone on the tensor pipe
       if (warp == 0) {
         mma_run<kC>(x.tm + d_col(c), opTZ, opV, id_d, false);
         mma_run<kD>(x.tm + d_col(c), opWQ, opS, id_d, true);
         mma_commit_elect(x.bar_mma);
       }
-      gamma_fade<DH>(x, reinterpret_cast<const float*>(sm + slot + kSlotGam));
-      if (c > 0 && !u_rows) o_store(c - 1, tc - kC, kC);
       bad |= !mbar_wait(x.bar_mma, x.ph_mma, kWaitNs);
       x.ph_mma ^= 1u;
       fence_after_sync();
       if (c + 1 < nch) issue_v(tc + kC);  // V is consumed
-      if (u_rows) {  // U rows -> bf16 [tok][DV] tile (MN-major B operand)
+      if (u_rows) {
+        // U rows -> bf16 [tok][DV] tile (MN-major B operand); the four warps holding them meet
+        // at a named barrier, then K^^T U (on the chain's critical path) and O += M U are issued
         float v[64];
         tmem_ld64(x.tm + x.lane_base + d_col(c) + x.wh * 64, v);
 #pragma unroll
         for (int j = 0; j < 64; j += 8) st_chunk8(sm + L::UU, 8192, drow, x.wh * 64 + j, v + j);
         fence_async_smem();
-      }
-      cta_sync_tc();  // U is written and every warp's fade of the state master is complete
-      // S += K^^T U (on the chain's critical path), then O += M U
-      if (warp == 0) {
-        mma_run<kC>(x.tm + kColS, opKH, opU, id_s, true);
-        mma_commit_elect(x.bar_mma);
-        mma_run<kC>(x.tm + d_col(c), opZM, opU, id_d, true);
-        mma_commit_elect(bar_o);
+        fence_before_sync();
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        fence_after_sync();
+        if (warp == 0) {
+          mma_run<kC>(x.tm + kColU, opKH, opU, id_s, false);
+          mma_commit_elect(x.bar_mma);
+          mma_run<kC>(x.tm + d_col(c), opZM, opU, id_d, true);
+          mma_commit_elect(bar_o);
+        }
+      } else if (c > 0) {
+        o_store(c - 1, tc - kC, kC);  // the previous chunk's output rows, off the tensor pipe
       }
       bad |= !mbar_wait(x.bar_mma, x.ph_mma, kWaitNs);
       x.ph_mma ^= 1u;
       fence_after_sync();
-      s_epilogue<DH>(x, sm + L::SS);
-      // the slot is consumed once O's MMA is complete (gamma was read before a barrier): re-arm
-      // it for chunk c + 2 and tell the helpers
-      if (tid == 0) {
-        const bool ok_o = mbar_wait(bar_o, ph_o, kWaitNs);
-        bad |= !ok_o;
-        if (ok_o) {
-          if (c + 2 < nch) mbar_expect_tx(full + s, kSlotPayload);
-          for (int r = 1; r < ncl; ++r) st_relaxed_remote(map_to(cons_local, r), (uint32_t)(c + 1));
-        }
-      }
+      s_update(gm);
+      // the slot is consumed once O's MMA is complete (gamma was read before the barrier below):
+      // re-arm it for chunk c + 2 and tell the helpers
+      if (tid == 0) bad |= !mbar_wait(bar_o, ph_o, kWaitNs);
       ph_o ^= 1u;
       fence_before_sync();
       if (__syncthreads_or(bad)) { failed = true; break; }
       fence_after_sync();
+      if (tid == 0) {
+        if (c + 2 < nch) mbar_expect_tx(full + s, kSlotPayload);
+        for (int r = 1; r < ncl; ++r) st_relaxed_remote(map_to(cons_local, r), (uint32_t)(c + 1));
+      }
     }
     if (!failed && nch > 0 && !u_rows) {
       const int64_t tl = t0 + (int64_t)(nch - 1) * kC;
@@ -371,12 +405,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         sAlpha[tid] = nb_alpha;
       }
       if (cn < nch) load_scalars(tn, nb_beta, nb_alpha);
-      // the previous chunk's first copy group (Q~, K^, gamma) has read its tiles
-      if (tid == 0) bulk_wait_read<1>();
       if (!wait_bar(bar_qk, ph_qk)) { failed = true; break; }
       if (kAlphaTile && !wait_bar(bar_a, ph_a)) { failed = true; break; }
 
-      const bool safe = gate_stage<L, CHANNEL>(x, n);
+      // the previous chunk's first copy group (Q~, K^, gamma) reads its tiles while the gate
+      // prefix runs; the gate waits for it before it rewrites them
+      const bool safe = gate_stage<L, CHANNEL>(x, n, [&] {
+        if (tid == 0) bulk_wait_read<1>();
+      });
       // ... and the second (-W, T', M), before the Gram epilogue rewrites M
       if (tid == 0) bulk_wait_read<0>();
       fence_async_smem();

@@ -195,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     if (nch > 0) issue_v(t0);
     s_init<DH>(x, a.S0 ? a.S0 + sidx + (size_t)x.lrow * kD : nullptr, sm + L::SS);
+    cta_sync_tc();  // every row of the bf16 state tile is written before the first MMA
     const Opnd opV{x.sb + L::VIN, 8192, true};
     const Opnd opU{x.sb + L::UU, 8192, true};
     const Opnd opS{x.sb + L::SS, 16384, true};

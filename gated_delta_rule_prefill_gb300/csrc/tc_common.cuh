@@ -318,8 +318,14 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t& ph) {
 // or raw K and Q for scalar gates), KR (Kr) and KH (K^), gamma, the exact diagonal q_r . k_r and,
 // for scalar gates, the per-token log prefix sums.  Returns whether the chunk's decay allows the
 // factorised Gram products (otherwise the log prefix sums are left in the alpha tile).
-template <class L, bool CHANNEL>
-__device__ bool gate_stage(const TcCtx& x, int n) {
+// `before_writes` runs on every thread just before the stage's first CTA barrier, after which the
+// stage writes the operand tiles and gamma (until then it writes only its own scratch); a caller
+// that still reads those tiles asynchronously waits for the reads there.
+struct NoHook {
+  __device__ void operator()() const {}
+};
+template <class L, bool CHANNEL, class Hook = NoHook>
+__device__ bool gate_stage(const TcCtx& x, int n, Hook before_writes = Hook()) {
   constexpr bool kScalar = !CHANNEL;
   unsigned char* sm = x.sm;
   const int tid = x.tid, warp = x.warp, lane = x.lane;
@@ -352,6 +358,7 @@ __device__ bool gate_stage(const TcCtx& x, int n) {
         sGs[r0] = sc - g1;
         sGs[r0 + 1] = sc;
       }
+      before_writes();
       __syncthreads();
       const float Gn = sGs[kC - 1];
 #pragma unroll
@@ -426,6 +433,7 @@ __device__ bool gate_stage(const TcCtx& x, int n) {
           float* sTot = reinterpret_cast<float*>(sm + L::TOT);  // [32][128 channels]
           *reinterpret_cast<float4*>(sTot + rb * kD + 8 * g8) = make_float4(run[0], run[1], run[2], run[3]);
           *reinterpret_cast<float4*>(sTot + rb * kD + 8 * g8 + 4) = make_float4(run[4], run[5], run[6], run[7]);
+          before_writes();
           __syncthreads();
           if (tid < kD) {
             float t16[16];
@@ -793,6 +801,7 @@ __device__ void s_init(const TcCtx& x, const float* s0_row, unsigned char* ss) {
 #pragma unroll
   for (int j = 0; j < DH; j += 8) st_chunk8(ss, 16384, x.lrow, x.wh * DH + j, v + j);
   tmem_wait_st();
+  fence_async_smem();  // the caller's next CTA barrier then orders the tile before any MMA
 }
 // state master -> S_final row (fp32)
 template <int DH>

@@ -160,8 +160,9 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// 64 consecutive columns (two 32-column loads, one wait): twice the bytes per round trip.
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+// Two 32-column blocks from columns `ta` and `tb` of this thread's lane, one wait: v[0..31] from
+// ta, v[32..63] from tb.
+__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float (&v)[64]) {
   uint32_t r[64];
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
@@ -179,10 +180,15 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
         "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
         "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]),
         "=r"(r[63])
-      : "r"(taddr), "r"(taddr + 32u)
+      : "r"(ta), "r"(tb)
       : "memory");
 #pragma unroll
   for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 64 consecutive columns (two 32-column loads, one wait): twice the bytes per round trip.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  tmem_ld32x2(taddr, taddr + 32u, v);
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
