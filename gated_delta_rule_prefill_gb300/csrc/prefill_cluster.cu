@@ -363,6 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     cta_sync_tc();
     cluster_sync();
     TcCtx x = make_ctx(sm, *tslot, bars + 2);
+    zero_upper_tp(sm + L::TT, tid);
     uint32_t ph_qk = 0, ph_a = 0;
     const uint32_t chain_full = map_to(smem_u32(sm + ChainSmem::BARS), 0);
     const uint32_t chain_slots = map_to(smem_u32(sm + ChainSmem::SLOT), 0);
@@ -405,9 +406,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         sAlpha[tid] = nb_alpha;
       }
       if (cn < nch) load_scalars(tn, nb_beta, nb_alpha);
-      if (!wait_bar(bar_qk, ph_qk)) { failed = true; break; }
-      if (kAlphaTile && !wait_bar(bar_a, ph_a)) { failed = true; break; }
-
+      {  // the chunk's q, k (and alpha) tiles: per-thread waits, one barrier
+        bool ok = mbar_wait(bar_qk, ph_qk, kWaitNs);
+        ph_qk ^= 1u;
+        if (kAlphaTile) {
+          ok &= mbar_wait(bar_a, ph_a, kWaitNs);
+          ph_a ^= 1u;
+        }
+        if (__syncthreads_or(!ok)) { failed = true; break; }
+      }
       // the previous chunk's first copy group (Q~, K^, gamma) reads its tiles while the gate
       // prefix runs; the gate waits for it before it rewrites them
       const bool safe = gate_stage<L, CHANNEL>(x, n, [&] {

@@ -342,6 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     cta_sync_tc();
     TcCtx x = make_ctx(sm, *tslot, bars + 2);
+    zero_upper_tp(sm + L::TT, tid);
     uint32_t ph_qk = 0, ph_a = 0;
     bool failed = false;
     // the chains' (first token, tokens, head), once: a work item then needs no global reads

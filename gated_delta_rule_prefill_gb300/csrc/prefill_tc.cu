@@ -161,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     issue_v(t0);
   }
   s_init<DH>(x, a.S0 ? a.S0 + sidx + (size_t)x.lrow * kD + vc0 : nullptr, sm + L::SS);
+  zero_upper_tp(sm + L::TT, tid);
   float nb_beta, nb_alpha;
   load_scalars(t0, nb_beta, nb_alpha);
 

@@ -124,6 +124,13 @@ __device__ __forceinline__ void st_tp2(unsigned char* tt, const float* beta, int
 // 32 x 32 fp32 scratch, columns XOR-swizzled by 8 * (row % 4) against bank conflicts
 __device__ __forceinline__ int x32(int r, int c) { return r * 32 + (c ^ ((r & 3) << 3)); }
 
+// Zeroes the bf16 T' tile (64 x 64, 8 KB); the solve never writes its part right of the 8 x 8
+// diagonal blocks, so a CTA does this once before its first chunk.
+__device__ __forceinline__ void zero_upper_tp(unsigned char* tt, int tid) {
+  for (int i = tid; i < 8192 / 16; i += kThreads)
+    reinterpret_cast<uint4*>(tt)[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 // T = (I + A)^-1 for A strictly lower (64 x 64, fp32, swizzled layout above), by doubling the
 // inverted block size: the eight 8 x 8 diagonal blocks by right-looking forward substitution (one
 // column per thread, held in registers); then the 16, 32 and 64 levels, each
@@ -152,16 +159,10 @@ __device__ inline void unit_lower_inverse(const float* sA, float* sT, float* sX,
       sT[f32x(o + i, o + c)] = acc[i];
       st_bf16(tt, sw128_offset(o + i, o + c, 8192), acc[i] * bc);
     }
-  } else {
-    // everything right of the 8 x 8 diagonal blocks is zero
-    for (int e = tid - 64; e < kC * 16; e += kThreads - 64) {
-      const int r = e >> 4, grp = e & 15;
-      if (grp >= 2 * ((r >> 3) + 1)) {
-        st4x(sT, r, grp, make_float4(0.f, 0.f, 0.f, 0.f));
-        *reinterpret_cast<uint2*>(tt + sw128_offset(r, 4 * grp, 8192)) = make_uint2(0u, 0u);
-      }
-    }
   }
+  // Nothing right of the 8 x 8 diagonal blocks is stored: the fp32 products below take those
+  // zeros as constant fragments, and the bf16 tile's upper part is zeroed once per CTA
+  // (zero_upper_tp), before its first chunk.
   __syncthreads();
   // ---- level 16: warp p of warps 0-3 takes the 16 x 16 block p (8-blocks a = 2p, b = 2p + 1);
   // the MMAs are 16 rows high, the 8 rows of the block padded with zeros
@@ -207,6 +208,7 @@ __device__ inline void unit_lower_inverse(const float* sA, float* sT, float* sX,
     for (int ks = 0; ks < 2; ++ks) {
       uint32_t a[4];
       frag_a(sT, rb, rb + 8 * ks, g, t, a);
+      if (ks == 1) a[0] = a[2] = 0u;  // T_bb's upper-right 8 x 8 block is zero
       mma_tf32(y, a, tf32(sXp[x32(8 * ks + t, 8 * j + g)]),
                tf32(sXp[x32(8 * ks + t + 4, 8 * j + g)]));
     }
@@ -238,6 +240,7 @@ __device__ inline void unit_lower_inverse(const float* sA, float* sT, float* sX,
       if (ks > 2 * mi + 1) continue;  // T_[23][23] is zero right of the row tile's diagonal
       uint32_t a[4];
       frag_a(sT, 32 + 16 * mi, 32 + 8 * ks, g, t, a);
+      if (ks == 2 * mi + 1) a[0] = a[2] = 0u;  // upper-right 8 x 8 of the diagonal 16 x 16 block
       mma_tf32(y, a, tf32(sX[x32(8 * ks + t, 8 * ni + g)]),
                tf32(sX[x32(8 * ks + t + 4, 8 * ni + g)]));
     }
@@ -693,7 +696,7 @@ __device__ void solve_stage(const TcCtx& x) {
 // ---- Stage 4: W = T' K~ (and, with a V operand, U~ = T' V into the U accumulator), then W (or
 // -W) as the bf16 K-major A operand WW.  Returns false if the MMA wait gave up.
 template <class L>
-__device__ bool w_stage(TcCtx& x, bool with_v, Opnd opV, uint32_t id_v) {
+__device__ void w_issue(TcCtx& x, bool with_v, Opnd opV, uint32_t id_v) {
   const Opnd opT{x.sb + L::TT, 8192, false};
   const Opnd opKt{x.sb + L::KQ, 16384, true};  // K~ rows as MN-major B (K = tokens)
   if (x.warp == 0) {
@@ -701,8 +704,11 @@ __device__ bool w_stage(TcCtx& x, bool with_v, Opnd opV, uint32_t id_v) {
     if (with_v) mma_run<kC>(x.tm + kColU, opT, opV, id_v, false);
     mma_commit_elect(x.bar_mma);
   }
-  if (!wait_bar(x.bar_mma, x.ph_mma)) return false;
-  return true;
+}
+template <class L>
+__device__ bool w_stage(TcCtx& x, bool with_v, Opnd opV, uint32_t id_v) {
+  w_issue<L>(x, with_v, opV, id_v);
+  return wait_bar(x.bar_mma, x.ph_mma);
 }
 template <class L, bool NEG = false>
 __device__ void w_epilogue(const TcCtx& x) {
