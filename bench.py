@@ -348,19 +348,17 @@ def run_gpu(args):
 
     # ---- end to end through the public API with host buffers (prefill), rank-local
     host_in = {k: P[k].cpu().pin_memory() for k in ("q", "k", "v", "alpha", "beta", "S0")}
+    host_cu = P["cu_seqlens"].cpu().pin_memory()
     host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     host_sf = torch.empty(Sf.shape, dtype=Sf.dtype).pin_memory()
-    dev_in = {k: torch.empty_like(P[k]) for k in host_in}
+    hbuf = torch.empty(g.gdr_prefill_host_buffer_size(wp.n_seqs, H, T, d, d), dtype=torch.uint8,
+                       device=dev)
     e2e_steps = max(1, min(args.steps, 5))
 
-    def e2e_step():
-        for k in host_in:
-            dev_in[k].copy_(host_in[k], non_blocking=True)
-        g.gdr_prefill(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["alpha"], dev_in["beta"],
-                      S0=dev_in["S0"], cu_seqlens=P["cu_seqlens"], out=out, S_final=Sf,
-                      workspace=ws)
-        host_out.copy_(out, non_blocking=True)
-        host_sf.copy_(Sf, non_blocking=True)
+    def e2e_step():  # one call: host inputs in, out and S_final back, copies inside the call
+        g.gdr_prefill_host(host_in["q"], host_in["k"], host_in["v"], host_in["alpha"],
+                           host_in["beta"], S0=host_in["S0"], cu_seqlens=host_cu, out=host_out,
+                           S_final=host_sf, buffer=hbuf)
 
     e2e_step()
     torch.cuda.synchronize()
@@ -376,7 +374,7 @@ def run_gpu(args):
     e2e_ms = max_over_ranks([e0.elapsed_time(e1) / e2e_steps], dev, world)[0]
     if world > 1:
         dist.barrier()
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + host_cu.numel() * 4
     d2h = host_out.numel() * host_out.element_size() + host_sf.numel() * host_sf.element_size()
 
     if rank != 0:
@@ -431,8 +429,8 @@ def run_gpu(args):
         "roofline": main_roof,
         "kernels": kern,
         "e2e": {"value": job_tokens_per_s(n, T, e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "what": "gdr_prefill with pinned host inputs copied "
-                "in and out/S_final copied back, per step"},
+                "d2h_bytes_per_step": d2h, "what": "gdr_prefill_host: pinned host inputs in, "
+                "out and S_final back, copies pipelined with the kernels inside the call"},
         "gpu_launches": 5 * K,
         "clocks": clk,
     }

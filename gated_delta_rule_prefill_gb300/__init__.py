@@ -8,6 +8,8 @@ library's CUDA kernels; there is no Python or CPU fallback.
     gdr_decode_step(q, k, v, alpha, beta, S_inout, out=None)
     gdr_linear_attn(q, k, v, S0=None, cu_seqlens=None, out=None, S_final=None, ...)
     gdr_prefill_workspace_size(n_seqs, H, d_k, d_v, dtype)  /  gdr_workspace_status(workspace)
+    gdr_prefill_host(q, k, v, alpha, beta, ...)  -- host (CPU) tensors in and out, copies inside
+    gdr_prefill_host_buffer_size(n_seqs, H, total_tokens, d_k, d_v, dtype, gate, piece_tokens)
 """
 from __future__ import annotations
 
@@ -21,7 +23,8 @@ from ._abi import (GDR_BF16, GDR_F32, GDR_FLAG_FORCE_SIMT, GDR_FLAG_NO_CLUSTER, 
                    GdrError, GdrShape)
 
 __all__ = ["gdr_prefill", "gdr_decode_step", "gdr_linear_attn", "gdr_prefill_workspace_size",
-           "gdr_workspace_status", "make_shape", "GdrError"]
+           "gdr_workspace_status", "gdr_prefill_host", "gdr_prefill_host_buffer_size",
+           "make_shape", "GdrError"]
 
 _DT = {torch.float32: GDR_F32, torch.bfloat16: GDR_BF16}
 
@@ -116,6 +119,65 @@ def gdr_prefill(q, k, v, alpha, beta, S0=None, cu_seqlens=None, out=None, S_fina
     [N+1] or None.  Returns (out [T,H,d_v], S_final [N,H,d_k,d_v] or None)."""
     return _prefill_like(False, q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, workspace,
                          chunk_size, force_simt, stream, want_final, no_cluster, prefer_queue)
+
+
+def _check_host(t, name, dtype=None):
+    if t is None:
+        return
+    if t.is_cuda:
+        raise ValueError("%s must be a host (CPU) tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+
+
+def gdr_prefill_host_buffer_size(n_seqs, H, total_tokens, d_k=128, d_v=128, dtype="bf16",
+                                 gate=GDR_GATE_CHANNEL, piece_tokens=0) -> int:
+    """Bytes of the device buffer gdr_prefill_host needs."""
+    sh = make_shape(n_seqs, H, total_tokens, d_k, d_v, GDR_BF16 if dtype == "bf16" else GDR_F32,
+                    gate)
+    return int(_abi.load().gdr_prefill_host_buffer_size(ctypes.byref(sh), int(piece_tokens)))
+
+
+def gdr_prefill_host(q, k, v, alpha, beta, S0=None, cu_seqlens=None, out=None, S_final=None,
+                     piece_tokens=0, buffer=None, device=None, stream=None, want_final=True):
+    """gdr_prefill on host (CPU) tensors -- pinned memory lets the copies overlap the kernels.
+    q, k, v, alpha, beta, S0, out, S_final and cu_seqlens (int32) are CPU tensors; `buffer` is
+    a CUDA uint8 tensor of gdr_prefill_host_buffer_size bytes (allocated on `device` if None).
+    The call is asynchronous on `stream`: synchronise it before reading out / S_final."""
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    dtype = _DT.get(q.dtype)
+    if dtype is None:
+        raise ValueError("q/k/v must be float32 or bfloat16")
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check_host(t, n, q.dtype)
+    _check_host(alpha, "alpha", torch.float32)
+    _check_host(beta, "beta", torch.float32)
+    _check_host(S0, "S0", torch.float32)
+    _check_host(cu_seqlens, "cu_seqlens", torch.int32)
+    gate = GDR_GATE_CHANNEL if alpha.dim() == 3 else GDR_GATE_SCALAR
+    n_seqs = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=q.dtype).pin_memory()
+    _check_host(out, "out", q.dtype)
+    if S_final is None and want_final:
+        S_final = torch.empty((n_seqs, H, dk, dv), dtype=torch.float32).pin_memory()
+    _check_host(S_final, "S_final", torch.float32)
+    sh = make_shape(n_seqs, H, T, dk, dv, dtype, gate)
+    lib = _abi.load()
+    if buffer is None:
+        need = int(lib.gdr_prefill_host_buffer_size(ctypes.byref(sh), int(piece_tokens)))
+        dev = torch.device("cuda") if device is None else torch.device(device)
+        buffer = torch.empty(need, dtype=torch.uint8, device=dev)
+    _check(buffer, "buffer", torch.uint8)
+    rc = lib.gdr_prefill_host(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
+                              _ptr(beta), _ptr(S0), _ptr(cu_seqlens), _ptr(out), _ptr(S_final),
+                              int(piece_tokens), _ptr(buffer), buffer.numel(), _stream(stream))
+    if rc != 0:
+        raise GdrError(rc, "gdr_prefill_host")
+    return out, S_final
 
 
 def gdr_linear_attn(q, k, v, S0=None, cu_seqlens=None, out=None, S_final=None, workspace=None,

@@ -17,7 +17,8 @@ GDR_DEVCHECK_OK, GDR_DEVCHECK_SEQLENS, GDR_DEVCHECK_TIMEOUT = 0, 1, 2
 
 # every symbol include/gdr.h declares
 EXPORTS = ("gdr_prefill", "gdr_prefill_workspace_size", "gdr_decode_step", "gdr_linear_attn",
-           "gdr_workspace_status", "gdr_status_string", "gdr_prefill_noalloc")
+           "gdr_workspace_status", "gdr_status_string", "gdr_prefill_noalloc", "gdr_prefill_host",
+           "gdr_prefill_host_buffer_size")
 GDR_NOALLOC_MAX_SEQS = 4096
 
 
@@ -53,6 +54,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.gdr_workspace_status.restype = ctypes.c_int
     lib.gdr_prefill_noalloc.argtypes = [S, P, P, P, P, P, P, P, P, P, P]
     lib.gdr_prefill_noalloc.restype = ctypes.c_int
+    lib.gdr_prefill_host.argtypes = [S, P, P, P, P, P, P, P, P, P, ctypes.c_int64, P,
+                                     ctypes.c_size_t, P]
+    lib.gdr_prefill_host.restype = ctypes.c_int
+    lib.gdr_prefill_host_buffer_size.argtypes = [S, ctypes.c_int64]
+    lib.gdr_prefill_host_buffer_size.restype = ctypes.c_size_t
     lib.gdr_status_string.argtypes = [ctypes.c_int]
     lib.gdr_status_string.restype = ctypes.c_char_p
     _lib = lib

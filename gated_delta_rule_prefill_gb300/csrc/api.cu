@@ -106,6 +106,8 @@ gdr_status prefill_common(const gdr_shape* sh, const void* q, const void* k, con
 
 }  // namespace
 
+gdr_status validate_shape(const gdr_shape* sh, bool need_gate) { return check_shape(sh, need_gate); }
+
 gdr_status prefill_launch(const gdr_shape* sh, const void* q, const void* k, const void* v,
                           const float* alpha, const float* beta, const float* S0,
                           const int32_t* cu, void* out, float* S_final, void* ws,

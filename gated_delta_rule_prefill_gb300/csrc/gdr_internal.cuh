@@ -97,6 +97,9 @@ __device__ __forceinline__ bool seq_range(const PrefillArgs& a, int seq, int64_t
   return true;
 }
 
+// The shape checks every prefill-like call makes (GDR_OK or the error to return).
+gdr_status validate_shape(const gdr_shape* sh, bool need_gate);
+
 // gdr_prefill with an explicit workspace (validation, pre-pass and launch).
 gdr_status prefill_launch(const gdr_shape* sh, const void* q, const void* k, const void* v,
                           const float* alpha, const float* beta, const float* S0,

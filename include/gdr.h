@@ -22,7 +22,9 @@
  *
  * Conventions shared by every call
  *   - Pointers are DEVICE pointers unless stated otherwise; the caller owns every buffer.  The
- *     library allocates nothing, keeps no state between calls and never frees caller memory.
+ *     library allocates nothing, keeps no state between calls and never frees caller memory
+ *     (two stated exceptions: gdr_prefill_noalloc's fixed scratch array and gdr_prefill_host's
+ *     internal copy streams).
  *   - Layouts are packed and token-major, row-major, no padding:
  *       q, k            [T_total, H, d_k]   dtype = shape->dtype
  *       v, out          [T_total, H, d_v]   dtype = shape->dtype
@@ -171,6 +173,44 @@ gdr_status gdr_prefill_noalloc(const gdr_shape* shape, const void* q, const void
                                const void* v, const float* alpha, const float* beta,
                                const float* S0, const int32_t* cu_seqlens, void* out,
                                float* S_final, void* stream);
+
+/*
+ * gdr_prefill_host -- gdr_prefill on arrays in HOST memory, with the host<->device copies inside
+ * the call and overlapped with the kernels.  The result is that of gdr_prefill (same chunking,
+ * same kernels): the pages define the operation (see gdr_prefill); how its inputs reach the GPU
+ * is a property of this library, which the pages do not discuss.
+ *
+ * The packed token axis is cut into pieces of about piece_tokens tokens (0: max(4096, T / 8));
+ * a cut inside a sequence is moved forward to that sequence's next 64-token chunk boundary.
+ * Each piece's inputs are copied in on an internal stream while the previous piece runs on
+ * `stream`, and its outputs are copied out on a second internal stream while the next piece
+ * runs; the states of all sequences stay on the device between pieces (in place).  With a
+ * 1.35 GB KDA input the call is bound by the host link, not by the kernels.
+ *   q, k, v, alpha, beta, S0, out, S_final: HOST pointers, layouts as gdr_prefill.  Page-locked
+ *               (pinned) memory is needed for the copies to overlap; pageable memory works but the
+ *               copies then serialise with the host.  S0 NULL = zeros; S_final may be NULL.
+ *   cu_seqlens: HOST int32 offsets, or NULL for one sequence.  Checked on the host: cu[0] = 0,
+ *               non-decreasing, cu[n_seqs] = total_tokens (GDR_ERR_INVALID_ARG otherwise).
+ *   buffer:     DEVICE scratch of gdr_prefill_host_buffer_size(shape, piece_tokens) bytes,
+ *               256-byte aligned (states, offsets, the prefill workspace, two staging sets).
+ *   stream:     the prefill kernels run on it; the copies wait for the work already enqueued on
+ *               it, and it waits for the last copy, so the call is ordered on `stream` like any
+ *               other.  Host arrays must stay valid and unmodified until `stream` has passed the
+ *               call.
+ * Returns after enqueueing (asynchronous, like gdr_prefill).  The first call on a device creates
+ * two non-blocking streams and a few events on it, kept until the process exits; calls from
+ * several host threads on one device are serialised by a lock while they enqueue.  The
+ * device-check word is internal (cu_seqlens is checked on the host instead).
+ */
+gdr_status gdr_prefill_host(const gdr_shape* shape, const void* q, const void* k, const void* v,
+                            const float* alpha, const float* beta, const float* S0,
+                            const int32_t* cu_seqlens, void* out, float* S_final,
+                            int64_t piece_tokens, void* buffer, size_t buffer_bytes,
+                            void* stream);
+
+/* Device buffer bytes gdr_prefill_host needs for this shape and piece size (0 if the shape is
+ * malformed). */
+size_t gdr_prefill_host_buffer_size(const gdr_shape* shape, int64_t piece_tokens);
 
 /* Static, human-readable name of a status. */
 const char* gdr_status_string(gdr_status status);

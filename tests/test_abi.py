@@ -93,3 +93,39 @@ def test_workspace_size(lib):
     n = lib.gdr_prefill_workspace_size(ctypes.byref(sh))
     assert n >= 256 + 64 * 4 and n % 256 == 0
     assert lib.gdr_prefill_workspace_size(None) == 0
+
+
+def _host_call(lib, sh, cu, buf=FAKE * 4, buf_bytes=1 << 40, piece=0):
+    """gdr_prefill_host with fake host pointers: every case here fails validation first."""
+    P = ctypes.c_void_p
+    cu_arr = None if cu is None else (ctypes.c_int32 * len(cu))(*cu)
+    return lib.gdr_prefill_host(ctypes.byref(sh), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE),
+                                None, cu_arr, P(FAKE), None, piece, P(buf), buf_bytes, None)
+
+
+def test_host_pipeline_argument_errors(lib):
+    INV, UNS = 1, 2
+    sh = _shape(n_seqs=2, total_tokens=100)
+    assert _host_call(lib, sh, [0, 60, 50]) == INV     # offsets decrease
+    assert _host_call(lib, sh, [0, 60, 90]) == INV     # do not end at total_tokens
+    assert _host_call(lib, sh, [4, 60, 100]) == INV    # do not start at 0
+    assert _host_call(lib, sh, None) == INV            # two sequences need offsets
+    assert _host_call(lib, sh, [0, 60, 100], buf=FAKE * 4 + 16) == INV  # buffer misaligned
+    assert _host_call(lib, sh, [0, 60, 100], buf_bytes=4096) == INV     # buffer too small
+    assert _host_call(lib, _shape(d_k=96, d_v=96), [0, 60, 100]) == UNS
+    assert _host_call(lib, _shape(gate=5), [0, 60, 100]) == INV
+
+
+def test_host_pipeline_buffer_size(lib):
+    # states + offsets + workspace + two staging sets of (piece + 64) tokens
+    sh = _shape(n_seqs=1, H=32, total_tokens=32768)
+    small = lib.gdr_prefill_host_buffer_size(ctypes.byref(sh), 1024)
+    big = lib.gdr_prefill_host_buffer_size(ctypes.byref(sh), 8192)
+    per_tok = 32 * (2 * 128 * 2 + 128 * 2 + 128 * 4 + 4) + 32 * 128 * 2  # inputs + output
+    assert small % 256 == 0 and big % 256 == 0
+    assert big - small >= 2 * (8192 - 1024) * per_tok
+    assert small >= 32 * 128 * 128 * 4 + 2 * (1024 + 64) * per_tok
+    assert lib.gdr_prefill_host_buffer_size(None, 0) == 0
+    # scalar gates stage one gate per (token, head)
+    assert (lib.gdr_prefill_host_buffer_size(ctypes.byref(_shape(n_seqs=1, H=32, total_tokens=32768, gate=0)), 1024)
+            < small)
