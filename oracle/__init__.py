@@ -7,6 +7,8 @@ It shares no code with the GPU library and never imports it.
                     S <- Diag(alpha_t) S;  v_hat = S^T k_t;  S <- S + beta_t k_t (v_t - v_hat)^T;
                     o_t = S^T q_t.
   linear_attn(...)  S <- S + k_t v_t^T;  o_t = S^T q_t   (alpha = 1, no erase term, no beta).
+  gated_linear(...) S <- Diag(alpha_t) S + k_t v_t^T;  o_t = S^T q_t   (no erase term, no beta;
+                    engineermaxxing §05b, heqinghuang §11; per key channel as dev.to §5).
   chunked           (module) the chunk-parallel rewrite of the same recurrence in numpy fp64; a
                     derivation check for the chunk algebra, itself compared against gated_delta.
 
@@ -113,6 +115,12 @@ def gated_delta(q, k, v, alpha, beta, S0=None, cu_seqlens=None, pairs=None, thre
 def linear_attn(q, k, v, S0=None, cu_seqlens=None, pairs=None, threads=None):
     """Unnormalised linear attention (alpha = 1, no erase term); returns (out, S_final)."""
     return _run(1, q, k, v, None, None, S0, cu_seqlens, pairs, threads)
+
+
+def gated_linear(q, k, v, alpha, S0=None, cu_seqlens=None, pairs=None, threads=None):
+    """Gated linear attention: S <- Diag(alpha_t) S + k_t v_t^T (per-channel alpha [T,H,d_k] or
+    scalar alpha [T,H]), o_t = S^T q_t; returns (out, S_final) in fp64."""
+    return _run(2, q, k, v, alpha, None, S0, cu_seqlens, pairs, threads)
 
 
 def decode_step(q, k, v, alpha, beta, S):

@@ -24,6 +24,9 @@
  *   4. output:  o_t = S^T q_t              (read after the write, [HH] §09 and §10)
  * Plain (unnormalised) linear attention ([EM] §03b: the identity transition): S <- S + k_t v_t^T,
  * o_t = S^T q_t.  No feature map, no normaliser, no 1/sqrt(d) on q.
+ * Gated linear attention (the decayed additive update without the erase term, [EM] §05b and
+ * [HH] §11 for a scalar gate; one gate per key channel = row of S as in [DT] §5):
+ * S <- Diag(a_t) S + k_t v_t^T, o_t = S^T q_t.  No beta.
  * A decode step is this loop run for one token from a given state.
  *
  * Layouts (all row-major, fp64):
@@ -36,7 +39,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { ORACLE_GATED_DELTA = 0, ORACLE_LINEAR = 1 };
+enum { ORACLE_GATED_DELTA = 0, ORACLE_LINEAR = 1, ORACLE_GATED_LINEAR = 2 };
 
 typedef struct {
   int mode;
@@ -75,6 +78,14 @@ static void run_pair(const oracle_job* J, int n, int h, double* S, double* vhat)
       for (int i = 0; i < dk; ++i) {
         double* Si = S + (size_t)i * dv;
         for (int j = 0; j < dv; ++j) Si[j] += kt[i] * vt[j];
+      }
+    } else if (J->mode == ORACLE_GATED_LINEAR) {
+      /* S <- Diag(a) S + k v^T: each row i faded by its channel's gate, then the outer product */
+      for (int i = 0; i < dk; ++i) {
+        const double ai = J->alpha_per_channel ? J->alpha[((size_t)t * H + h) * dk + i]
+                                               : J->alpha[(size_t)t * H + h];
+        double* Si = S + (size_t)i * dv;
+        for (int j = 0; j < dv; ++j) Si[j] = ai * Si[j] + kt[i] * vt[j];
       }
     } else {
       const double bt = J->beta[(size_t)t * H + h];
@@ -141,7 +152,8 @@ static void* worker_main(void* arg) {
 
 /*
  * Run the recurrence.  mode 0: gated delta rule (alpha and beta required); mode 1: plain linear
- * attention (alpha and beta ignored).  S0 may be NULL (zeros), S_final may be NULL.  pairs (if
+ * attention (alpha and beta ignored); mode 2: gated linear attention (alpha required, beta
+ * ignored).  S0 may be NULL (zeros), S_final may be NULL.  pairs (if
  * not NULL) restricts the work to n_pairs (seq, head) pairs; outputs of other pairs are left
  * untouched.  Returns 0 on success, -1 on a bad argument, -2 if a thread could not be run.
  */
@@ -150,8 +162,9 @@ int gdr_oracle_run(int mode, int n_seqs, int H, int dk, int dv, const int64_t* c
                    int alpha_per_channel, const double* beta, const double* S0, double* out,
                    double* S_final, const int32_t* pairs, int n_pairs, int n_threads) {
   if (n_seqs < 0 || H <= 0 || dk <= 0 || dv <= 0 || !cu_seqlens || !out) return -1;
-  if (mode != ORACLE_GATED_DELTA && mode != ORACLE_LINEAR) return -1;
+  if (mode != ORACLE_GATED_DELTA && mode != ORACLE_LINEAR && mode != ORACLE_GATED_LINEAR) return -1;
   if (mode == ORACLE_GATED_DELTA && (!alpha || !beta)) return -1;
+  if (mode == ORACLE_GATED_LINEAR && !alpha) return -1;
   for (int n = 0; n < n_seqs; ++n)
     if (cu_seqlens[n + 1] < cu_seqlens[n]) return -1;
   if (n_threads < 1) n_threads = 1;

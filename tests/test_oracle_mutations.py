@@ -28,6 +28,10 @@ PIN_TESTS = [
     pins.test_beta_zero_is_pure_decay,
     pins.test_read_back_after_write,
     pins.test_orthonormal_keys_store_last_value,
+    pins.test_gated_linear_unit_gate_is_masked_qk_v,
+    lambda: pins.test_gated_linear_survival_sum(True),
+    lambda: pins.test_gated_linear_survival_sum(False),
+    pins.test_gated_linear_zero_gate_resets,
 ]
 
 
@@ -50,6 +54,12 @@ def _fade_after_write(src):
 
 
 MUTANTS = {
+    "gated linear: fade after the write": lambda s: s.replace(
+        "Si[j] = ai * Si[j] + kt[i] * vt[j]", "Si[j] = ai * (Si[j] + kt[i] * vt[j])"),
+    "gated linear: gate on the wrong channel": lambda s: s.replace(
+        "J->alpha[((size_t)t * H + h) * dk + i]", "J->alpha[((size_t)t * H + h) * dk + (dk - 1 - i)]"),
+    "gated linear: scalar gate ignored": lambda s: s.replace(
+        ": J->alpha[(size_t)t * H + h];\n        double* Si", ": 1.0;\n        double* Si"),
     "read the unfaded state": _swap_fade_and_read,
     "erase before fade": _fade_after_write,
     "dropped beta": lambda s: s.replace("vhat[j] = bt * (vt[j] - vhat[j])",

@@ -343,3 +343,57 @@ def test_chunked_equals_recurrence(C, channel):
     o, s = chunked.run_packed(q, k, v, None, None, S0, cu, C, linear=True)
     np.testing.assert_allclose(o, lo, atol=1e-10, rtol=1e-10)
     np.testing.assert_allclose(s, ls, atol=1e-10, rtol=1e-10)
+
+
+# ------------------------------------------------------------------------------------------
+# gated linear attention (S <- Diag(alpha) S + k v^T): closed forms and brute force
+# ------------------------------------------------------------------------------------------
+def test_gated_linear_unit_gate_is_masked_qk_v():
+    """alpha = 1: gated linear attention is plain linear attention, O = tril(Q K^T) V + Q S0."""
+    rng = np.random.default_rng(21)
+    lens = [13, 0, 30]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    T, H, dk, dv = cu[-1], 2, 6, 5
+    q, k, v, _, _ = rand_inputs(rng, T, H, dk, dv, unit_k=False)
+    S0 = rng.standard_normal((len(lens), H, dk, dv))
+    out, Sf = oracle.gated_linear(q, k, v, np.ones((T, H, dk)), S0=S0, cu_seqlens=cu)
+    for n in range(len(lens)):
+        t0, t1 = cu[n], cu[n + 1]
+        for h in range(H):
+            Q, K, V = q[t0:t1, h], k[t0:t1, h], v[t0:t1, h]
+            np.testing.assert_allclose(out[t0:t1, h], np.tril(Q @ K.T) @ V + Q @ S0[n, h], atol=1e-10)
+            np.testing.assert_allclose(Sf[n, h], S0[n, h] + K.T @ V, atol=1e-10)
+
+
+@pytest.mark.parametrize("channel", [True, False])
+def test_gated_linear_survival_sum(channel):
+    """Unrolled recurrence: S_t = sum_{s<=t} Diag(prod_{s<i<=t} alpha_i) k_s v_s^T
+    + Diag(prod_{i<=t} alpha_i) S0, so o_t = sum_s ((q_t * D_st) . k_s) v_s + (q_t * D_0t)^T S0
+    (engineermaxxing §05d's survival products, a write at step s not decayed by alpha_s)."""
+    rng = np.random.default_rng(22 + channel)
+    T, dk, dv = 11, 5, 3
+    q, k, v, alpha, _ = rand_inputs(rng, T, 1, dk, dv, channel=channel, unit_k=False)
+    S0 = rng.standard_normal((1, 1, dk, dv))
+    out, Sf = oracle.gated_linear(q, k, v, alpha, S0=S0)
+    a = alpha[:, 0] if channel else np.repeat(alpha[:, 0:1], dk, axis=1)  # [T, dk]
+    for t in range(T):
+        D0 = np.prod(a[:t + 1], axis=0)
+        ref = (q[t, 0] * D0) @ S0[0, 0]
+        for s in range(t + 1):
+            D = np.prod(a[s + 1:t + 1], axis=0)  # empty product = 1
+            ref = ref + np.dot(q[t, 0] * D, k[s, 0]) * v[s, 0]
+        np.testing.assert_allclose(out[t, 0], ref, atol=1e-12)
+    D0 = np.prod(a, axis=0)
+    Sref = D0[:, None] * S0[0, 0] + sum(np.prod(a[s + 1:], axis=0)[:, None] * np.outer(k[s, 0], v[s, 0])
+                                       for s in range(T))
+    np.testing.assert_allclose(Sf[0, 0], Sref, atol=1e-12)
+
+
+def test_gated_linear_zero_gate_resets():
+    """alpha_t = 0 forgets everything before t: S_t = k_t v_t^T, o_t = (q_t . k_t) v_t."""
+    rng = np.random.default_rng(24)
+    T, dk, dv = 6, 4, 3
+    q, k, v, alpha, _ = rand_inputs(rng, T, 1, dk, dv, unit_k=False)
+    alpha[3] = 0.0
+    out, _ = oracle.gated_linear(q, k, v, alpha, S0=rng.standard_normal((1, 1, dk, dv)))
+    np.testing.assert_allclose(out[3, 0], np.dot(q[3, 0], k[3, 0]) * v[3, 0], atol=1e-12)
