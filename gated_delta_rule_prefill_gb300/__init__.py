@@ -7,6 +7,7 @@ library's CUDA kernels; there is no Python or CPU fallback.
     gdr_prefill(q, k, v, alpha, beta, S0=None, cu_seqlens=None, out=None, S_final=None, ...)
     gdr_decode_step(q, k, v, alpha, beta, S_inout, out=None)
     gdr_linear_attn(q, k, v, S0=None, cu_seqlens=None, out=None, S_final=None, ...)
+    gdr_gated_linear_attn(q, k, v, alpha, S0=None, cu_seqlens=None, out=None, S_final=None, ...)
     gdr_prefill_workspace_size(n_seqs, H, d_k, d_v, dtype)  /  gdr_workspace_status(workspace)
     gdr_prefill_host(q, k, v, alpha, beta, ...)  -- host (CPU) tensors in and out, copies inside
     gdr_prefill_host_buffer_size(n_seqs, H, total_tokens, d_k, d_v, dtype, gate, piece_tokens)
@@ -22,7 +23,8 @@ from ._abi import (GDR_BF16, GDR_F32, GDR_FLAG_FORCE_SIMT, GDR_FLAG_NO_CLUSTER, 
                    GDR_GATE_CHANNEL, GDR_GATE_SCALAR,
                    GdrError, GdrShape)
 
-__all__ = ["gdr_prefill", "gdr_decode_step", "gdr_linear_attn", "gdr_prefill_workspace_size",
+__all__ = ["gdr_prefill", "gdr_decode_step", "gdr_linear_attn", "gdr_gated_linear_attn",
+           "gdr_prefill_workspace_size",
            "gdr_workspace_status", "gdr_prefill_host", "gdr_prefill_host_buffer_size",
            "make_shape", "GdrError"]
 
@@ -68,9 +70,12 @@ def _workspace(n_seqs, H, d_k, d_v, dtype, device, workspace):
     return workspace
 
 
-def _prefill_like(linear, q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, workspace,
+def _prefill_like(kind, q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, workspace,
                   chunk_size, force_simt, stream, want_final, no_cluster=False,
                   prefer_queue=False):
+    """kind: "delta" (gdr_prefill), "linear" (gdr_linear_attn) or "gla"
+    (gdr_gated_linear_attn)."""
+    linear = kind == "linear"
     T, H, dk = q.shape
     dv = v.shape[2]
     dtype = _DT.get(q.dtype)
@@ -82,7 +87,8 @@ def _prefill_like(linear, q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, wo
     gate = GDR_GATE_CHANNEL
     if not linear:
         _check(alpha, "alpha", torch.float32)
-        _check(beta, "beta", torch.float32)
+        if kind == "delta":
+            _check(beta, "beta", torch.float32)
         gate = GDR_GATE_CHANNEL if alpha.dim() == 3 else GDR_GATE_SCALAR
     _check(S0, "S0", torch.float32)
     _check(cu_seqlens, "cu_seqlens", torch.int32)
@@ -102,12 +108,17 @@ def _prefill_like(linear, q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, wo
         rc = lib.gdr_linear_attn(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(S0),
                                  _ptr(cu_seqlens), _ptr(out), _ptr(S_final), _ptr(ws),
                                  ws.numel(), _stream(stream))
+    elif kind == "gla":
+        rc = lib.gdr_gated_linear_attn(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
+                                       _ptr(S0), _ptr(cu_seqlens), _ptr(out), _ptr(S_final),
+                                       _ptr(ws), ws.numel(), _stream(stream))
     else:
         rc = lib.gdr_prefill(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
                              _ptr(beta), _ptr(S0), _ptr(cu_seqlens), _ptr(out), _ptr(S_final),
                              _ptr(ws), ws.numel(), _stream(stream))
     if rc != 0:
-        raise GdrError(rc, "gdr_linear_attn" if linear else "gdr_prefill")
+        raise GdrError(rc, {"linear": "gdr_linear_attn", "gla": "gdr_gated_linear_attn"}.get(
+            kind, "gdr_prefill"))
     return out, S_final
 
 
@@ -117,7 +128,7 @@ def gdr_prefill(q, k, v, alpha, beta, S0=None, cu_seqlens=None, out=None, S_fina
     """Chunked packed-varlen prefill.  q,k [T,H,d_k], v [T,H,d_v] (fp32 or bf16); alpha
     [T,H,d_k] or [T,H] fp32; beta [T,H] fp32; S0 [N,H,d_k,d_v] fp32 or None; cu_seqlens int32
     [N+1] or None.  Returns (out [T,H,d_v], S_final [N,H,d_k,d_v] or None)."""
-    return _prefill_like(False, q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, workspace,
+    return _prefill_like("delta", q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, workspace,
                          chunk_size, force_simt, stream, want_final, no_cluster, prefer_queue)
 
 
@@ -183,7 +194,16 @@ def gdr_prefill_host(q, k, v, alpha, beta, S0=None, cu_seqlens=None, out=None, S
 def gdr_linear_attn(q, k, v, S0=None, cu_seqlens=None, out=None, S_final=None, workspace=None,
                     chunk_size=0, force_simt=False, stream=None, want_final=True):
     """Plain linear attention (alpha = 1, no erase).  Returns (out, S_final)."""
-    return _prefill_like(True, q, k, v, None, None, S0, cu_seqlens, out, S_final, workspace,
+    return _prefill_like("linear", q, k, v, None, None, S0, cu_seqlens, out, S_final, workspace,
+                         chunk_size, force_simt, stream, want_final)
+
+
+def gdr_gated_linear_attn(q, k, v, alpha, S0=None, cu_seqlens=None, out=None, S_final=None,
+                          workspace=None, chunk_size=0, force_simt=False, stream=None,
+                          want_final=True):
+    """Gated linear attention: S <- Diag(alpha) S + k v^T (no erase, no beta); alpha [T,H,d_k]
+    or [T,H] fp32.  Returns (out, S_final)."""
+    return _prefill_like("gla", q, k, v, alpha, None, S0, cu_seqlens, out, S_final, workspace,
                          chunk_size, force_simt, stream, want_final)
 
 

@@ -68,13 +68,15 @@ gdr_status check_shape(const gdr_shape* sh, bool need_gate) {
 gdr_status prefill_common(const gdr_shape* sh, const void* q, const void* k, const void* v,
                           const float* alpha, const float* beta, const float* S0,
                           const int32_t* cu, void* out, float* S_final, void* ws,
-                          size_t ws_bytes, void* stream, bool linear) {
+                          size_t ws_bytes, void* stream, int kind) {
+  const bool linear = kind == kKindLinear;
   gdr_status st = check_shape(sh, !linear);
   if (st != GDR_OK) return st;
   if (!cu && sh->n_seqs != 1) return GDR_ERR_INVALID_ARG;
   if (sh->total_tokens > 0) {
     if (!q || !k || !v || !out) return GDR_ERR_INVALID_ARG;
-    if (!linear && (!alpha || !beta)) return GDR_ERR_INVALID_ARG;
+    if (!linear && !alpha) return GDR_ERR_INVALID_ARG;
+    if (kind == kKindDelta && !beta) return GDR_ERR_INVALID_ARG;
   }
   const void* ptrs[] = {q, k, v, alpha, beta, S0, cu, out, S_final};
   for (const void* p : ptrs)
@@ -99,8 +101,8 @@ gdr_status prefill_common(const gdr_shape* sh, const void* q, const void* k, con
   prep_kernel<<<1, kPrepThreads, 0, s>>>(cu, sh->n_seqs, sh->total_tokens, order, status);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess)
-    e = prefill_tc_supported(*sh) ? launch_prefill_tc(*sh, a, linear, s)
-                                  : launch_prefill_simt(*sh, a, linear, s);
+    e = prefill_tc_supported(*sh) ? launch_prefill_tc(*sh, a, kind, s)
+                                  : launch_prefill_simt(*sh, a, kind, s);
   return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }
 
@@ -113,7 +115,7 @@ gdr_status prefill_launch(const gdr_shape* sh, const void* q, const void* k, con
                           const int32_t* cu, void* out, float* S_final, void* ws,
                           size_t ws_bytes, void* stream) {
   return prefill_common(sh, q, k, v, alpha, beta, S0, cu, out, S_final, ws, ws_bytes, stream,
-                        false);
+                        kKindDelta);
 }
 
 }  // namespace gdr
@@ -130,14 +132,22 @@ gdr_status gdr_prefill(const gdr_shape* shape, const void* q, const void* k, con
                        const int32_t* cu_seqlens, void* out, float* S_final, void* workspace,
                        size_t workspace_bytes, void* stream) {
   return gdr::prefill_common(shape, q, k, v, alpha, beta, S0, cu_seqlens, out, S_final,
-                             workspace, workspace_bytes, stream, false);
+                             workspace, workspace_bytes, stream, gdr::kKindDelta);
 }
 
 gdr_status gdr_linear_attn(const gdr_shape* shape, const void* q, const void* k, const void* v,
                            const float* S0, const int32_t* cu_seqlens, void* out, float* S_final,
                            void* workspace, size_t workspace_bytes, void* stream) {
   return gdr::prefill_common(shape, q, k, v, nullptr, nullptr, S0, cu_seqlens, out, S_final,
-                             workspace, workspace_bytes, stream, true);
+                             workspace, workspace_bytes, stream, gdr::kKindLinear);
+}
+
+gdr_status gdr_gated_linear_attn(const gdr_shape* shape, const void* q, const void* k,
+                                 const void* v, const float* alpha, const float* S0,
+                                 const int32_t* cu_seqlens, void* out, float* S_final,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  return gdr::prefill_common(shape, q, k, v, alpha, nullptr, S0, cu_seqlens, out, S_final,
+                             workspace, workspace_bytes, stream, gdr::kKindGatedLinear);
 }
 
 gdr_status gdr_decode_step(const gdr_shape* shape, const void* q, const void* k, const void* v,

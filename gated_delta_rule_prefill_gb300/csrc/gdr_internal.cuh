@@ -97,6 +97,10 @@ __device__ __forceinline__ bool seq_range(const PrefillArgs& a, int seq, int64_t
   return true;
 }
 
+// What a prefill-like call computes: the gated delta rule, plain linear attention (alpha = 1,
+// no erase), or gated linear attention (S <- Diag(alpha) S + k v^T: no erase, no beta).
+enum PrefillKind : int { kKindDelta = 0, kKindLinear = 1, kKindGatedLinear = 2 };
+
 // The shape checks every prefill-like call makes (GDR_OK or the error to return).
 gdr_status validate_shape(const gdr_shape* sh, bool need_gate);
 
@@ -108,10 +112,10 @@ gdr_status prefill_launch(const gdr_shape* sh, const void* q, const void* k, con
 
 // Host-side launchers (each returns cudaSuccess or the launch error).
 cudaError_t launch_prep(const PrefillArgs& a, int32_t* order, cudaStream_t s);
-cudaError_t launch_prefill_simt(const gdr_shape& sh, const PrefillArgs& a, bool linear,
+cudaError_t launch_prefill_simt(const gdr_shape& sh, const PrefillArgs& a, int kind,
                                 cudaStream_t s);
 bool prefill_tc_supported(const gdr_shape& sh);
-cudaError_t launch_prefill_tc(const gdr_shape& sh, const PrefillArgs& a, bool linear,
+cudaError_t launch_prefill_tc(const gdr_shape& sh, const PrefillArgs& a, int kind,
                               cudaStream_t s);
 cudaError_t launch_decode(const gdr_shape& sh, const void* q, const void* k, const void* v,
                           const float* alpha, const float* beta, float* S, void* out,

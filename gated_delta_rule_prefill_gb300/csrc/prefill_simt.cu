@@ -14,6 +14,8 @@
 //   (I + A) [W | U~] = diag(beta) [K * e^G | V]                (forward substitution)
 //   U = U~ - W S;   O = (Q * e^G) S + M U;   S <- Diag(e^{G_n}) S + (K * e^{G_n - G})^T U
 // Plain linear attention: O = Q S + tril(Q K^T) V;  S <- S + K^T V.
+// Gated linear attention (no erase, no beta): U = V, the rest as the gated rule:
+//   O = (Q * e^G) S + M V;  S <- Diag(e^{G_n}) S + (K * e^{G_n - G})^T V.
 //
 // Mapping: one CTA (256 threads) per (sequence, head, block of DVB value columns); the columns
 // of S are independent (v and U enter column-wise), so the value dimension splits across CTAs
@@ -50,10 +52,12 @@ struct SimtSmem {
   static constexpr size_t bytes = (size_t)total_floats * 4;
 };
 
-template <int D, int C, typename T, bool CHANNEL, bool LINEAR>
+template <int D, int C, typename T, bool CHANNEL, int KIND>
 __global__ void __launch_bounds__(kSimtThreads) prefill_simt_kernel(PrefillArgs a) {
   using L = SimtSmem<D, C>;
   constexpr int NB = D / kDVB;
+  constexpr bool LINEAR = KIND == kKindLinear;  // no gates
+  constexpr bool ERASE = KIND == kKindDelta;    // the delta rule's correction (solve, beta)
   extern __shared__ float sm[];
   float* sQ = sm + L::off_Q;
   float* sK = sm + L::off_K;
@@ -110,7 +114,7 @@ __global__ void __launch_bounds__(kSimtThreads) prefill_simt_kernel(PrefillArgs 
       const int r = i / kDVB, c = i % kDVB;
       sV[r * L::LV + c] = r < n ? to_f32(v[((size_t)(tc + r) * H + h) * D + vc0 + c]) : 0.f;
     }
-    if (!LINEAR && tid < C) sB[tid] = tid < n ? a.beta[(size_t)(tc + tid) * H + h] : 0.f;
+    if (ERASE && tid < C) sB[tid] = tid < n ? a.beta[(size_t)(tc + tid) * H + h] : 0.f;
     __syncthreads();
 
     if (!LINEAR) {
@@ -145,7 +149,7 @@ __global__ void __launch_bounds__(kSimtThreads) prefill_simt_kernel(PrefillArgs 
           acc_a = fmaf(kr[c], w, acc_a);
           acc_m = fmaf(qr[c], w, acc_m);
         }
-        sA[r * L::LC + j] = (j < r) ? sB[r] * acc_a : 0.f;
+        if (ERASE) sA[r * L::LC + j] = (j < r) ? sB[r] * acc_a : 0.f;
       }
       sM[r * L::LC + j] = acc_m;
     }
@@ -158,17 +162,20 @@ __global__ void __launch_bounds__(kSimtThreads) prefill_simt_kernel(PrefillArgs 
         const float g = sG[r * L::LD + c];
         const float gam = __expf(g);
         const float kv = sK[r * L::LD + c];
-        sX[r * L::LX + c] = sB[r] * kv * gam;                               // beta K~
+        if (ERASE) sX[r * L::LX + c] = sB[r] * kv * gam;                    // beta K~
         sKh[r * L::LD + c] = kv * __expf(sG[(C - 1) * L::LD + c] - g);      // K^
         sQ[r * L::LD + c] *= gam;                                           // Q~
       }
-      for (int i = tid; i < C * kDVB; i += kSimtThreads) {
-        const int r = i / kDVB, c = i % kDVB;
-        sX[r * L::LX + D + c] = sB[r] * sV[r * L::LV + c];  // beta V
+      if (ERASE) {
+        for (int i = tid; i < C * kDVB; i += kSimtThreads) {
+          const int r = i / kDVB, c = i % kDVB;
+          sX[r * L::LX + D + c] = sB[r] * sV[r * L::LV + c];  // beta V
+        }
       }
       for (int c = tid; c < D; c += kSimtThreads) sGam[c] = __expf(sG[(C - 1) * L::LD + c]);
       __syncthreads();
-
+    }
+    if (ERASE) {
       // ---- 5. forward substitution (I + A) X = rhs; each thread owns whole columns of X
       for (int col = tid; col < D + kDVB; col += kSimtThreads) {
         for (int r = 1; r < n; ++r) {
@@ -198,7 +205,7 @@ __global__ void __launch_bounds__(kSimtThreads) prefill_simt_kernel(PrefillArgs 
       }
       __syncthreads();
     }
-    const float* sUse = LINEAR ? sV : sU;  // the values the chunk writes
+    const float* sUse = ERASE ? sU : sV;  // the values the chunk writes
 
     // ---- 7. O = Q~ S + M U
     for (int i = tid; i < C * kDVB; i += kSimtThreads) {
@@ -234,9 +241,9 @@ __global__ void __launch_bounds__(kSimtThreads) prefill_simt_kernel(PrefillArgs 
   }
 }
 
-template <int D, int C, typename T, bool CHANNEL, bool LINEAR>
+template <int D, int C, typename T, bool CHANNEL, int KIND>
 cudaError_t launch_one(const gdr_shape& sh, const PrefillArgs& a, cudaStream_t s) {
-  auto kern = prefill_simt_kernel<D, C, T, CHANNEL, LINEAR>;
+  auto kern = prefill_simt_kernel<D, C, T, CHANNEL, KIND>;
   const size_t smem = SimtSmem<D, C>::bytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
@@ -247,21 +254,25 @@ cudaError_t launch_one(const gdr_shape& sh, const PrefillArgs& a, cudaStream_t s
 }
 
 template <int D, int C, typename T>
-cudaError_t launch_t(const gdr_shape& sh, const PrefillArgs& a, bool linear, cudaStream_t s) {
-  if (linear) return launch_one<D, C, T, true, true>(sh, a, s);
-  if (sh.gate == GDR_GATE_CHANNEL) return launch_one<D, C, T, true, false>(sh, a, s);
-  return launch_one<D, C, T, false, false>(sh, a, s);
+cudaError_t launch_t(const gdr_shape& sh, const PrefillArgs& a, int kind, cudaStream_t s) {
+  if (kind == kKindLinear) return launch_one<D, C, T, true, kKindLinear>(sh, a, s);
+  const bool ch = sh.gate == GDR_GATE_CHANNEL;
+  if (kind == kKindGatedLinear)
+    return ch ? launch_one<D, C, T, true, kKindGatedLinear>(sh, a, s)
+              : launch_one<D, C, T, false, kKindGatedLinear>(sh, a, s);
+  return ch ? launch_one<D, C, T, true, kKindDelta>(sh, a, s)
+            : launch_one<D, C, T, false, kKindDelta>(sh, a, s);
 }
 
 }  // namespace
 
-cudaError_t launch_prefill_simt(const gdr_shape& sh, const PrefillArgs& a, bool linear,
+cudaError_t launch_prefill_simt(const gdr_shape& sh, const PrefillArgs& a, int kind,
                                 cudaStream_t s) {
   if (sh.d_k == 128)
-    return sh.dtype == GDR_BF16 ? launch_t<128, 32, __nv_bfloat16>(sh, a, linear, s)
-                                : launch_t<128, 32, float>(sh, a, linear, s);
-  return sh.dtype == GDR_BF16 ? launch_t<64, 64, __nv_bfloat16>(sh, a, linear, s)
-                              : launch_t<64, 64, float>(sh, a, linear, s);
+    return sh.dtype == GDR_BF16 ? launch_t<128, 32, __nv_bfloat16>(sh, a, kind, s)
+                                : launch_t<128, 32, float>(sh, a, kind, s);
+  return sh.dtype == GDR_BF16 ? launch_t<64, 64, __nv_bfloat16>(sh, a, kind, s)
+                              : launch_t<64, 64, float>(sh, a, kind, s);
 }
 
 }  // namespace gdr

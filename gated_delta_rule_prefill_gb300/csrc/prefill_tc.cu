@@ -77,7 +77,9 @@ struct TcSmem {
   static_assert(DV * 128 >= 32 * 32 * 4, "block scratch fits in U");
 };
 
-template <int DV, bool CHANNEL>
+// ERASE = false: gated linear attention (no correction, no beta): stages 3-4 are skipped and V
+// itself is the U of the state pass.
+template <int DV, bool CHANNEL, bool ERASE = true>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ TcMaps maps, const PrefillArgs a) {
   using L = TcSmem<DV>;
@@ -150,7 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     al = 1.f;
     if (tid < kC && tc + tid < t1) {
       const size_t o = (size_t)(tc + tid) * H + h;
-      b = a.beta[o];
+      if (ERASE) b = a.beta[o];
       if (!CHANNEL) al = a.alpha[o];
     }
   };
@@ -208,16 +210,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!wait_bar(bar_v, ph_v)) { failed = true; break; }
     zero_v_tail<DV>(x, sm + L::VIN, n);
 
-    // 3. T' = (I + A)^-1 diag(beta);  4. W = T' K~ and U~ = T' V
-    solve_stage<L>(x);
-    if (!w_stage<L>(x, true, opV, id_v)) { failed = true; break; }
-    if (tn < t1) issue_v(tn);  // V is consumed
-    w_epilogue<L>(x);
+    if constexpr (ERASE) {
+      // 3. T' = (I + A)^-1 diag(beta);  4. W = T' K~ and U~ = T' V
+      solve_stage<L>(x);
+      if (!w_stage<L>(x, true, opV, id_v)) { failed = true; break; }
+      if (tn < t1) issue_v(tn);  // V is consumed
+      w_epilogue<L>(x);
+    } else {
+      fence_async_smem();  // the zeroed V tail, before the MMAs read V
+    }
     cta_sync_tc();
 
     // 5. U = U~ - W S and O = Q~ S; the state master is faded meanwhile
     if (warp == 0) {
-      mma_run<kD>(x.tm + kColU, opW, opS, id_negw, true);
+      if (ERASE) mma_run<kD>(x.tm + kColU, opW, opS, id_negw, true);
       mma_run<kD>(x.tm + kColWO, opQ, opS, id_v, false);
       mma_commit_elect(x.bar_mma);
     }
@@ -227,18 +233,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool bad = !mbar_wait(x.bar_mma, x.ph_mma, kWaitNs);
     x.ph_mma ^= 1u;
     fence_after_sync();
-    u_epilogue<DH>(x, sm + L::UU);
+    if (ERASE) u_epilogue<DH>(x, sm + L::UU);
     cta_sync_tc();
 
-    // 6. O += M U and S += K^^T U
+    // 6. O += M U and S += K^^T U (U = V without the correction)
+    const Opnd& opUse = ERASE ? opU : opV;
     if (warp == 0) {
-      mma_run<kC>(x.tm + kColWO, opM, opU, id_v, true);
-      mma_run<kC>(x.tm + kColS, opKH, opU, id_s, true);
+      mma_run<kC>(x.tm + kColWO, opM, opUse, id_v, true);
+      mma_run<kC>(x.tm + kColS, opKH, opUse, id_s, true);
       mma_commit_elect(x.bar_mma);
     }
     bad |= !mbar_wait(x.bar_mma, x.ph_mma, kWaitNs);
     x.ph_mma ^= 1u;
     fence_after_sync();
+    if (!ERASE && tn < t1) issue_v(tn);  // V is consumed
     o_epilogue<DH>(x, out, tc, n, H, h, vc0);
     s_epilogue<DH>(x, sm + L::SS);
     fence_before_sync();
@@ -316,10 +324,10 @@ bool make_tc_maps(const gdr_shape& sh, const PrefillArgs& a, bool linear, TcMaps
 
 namespace {
 
-template <int DV, bool CHANNEL>
+template <int DV, bool CHANNEL, bool ERASE>
 cudaError_t launch_one(const gdr_shape& sh, const PrefillArgs& a, const TcMaps& maps,
                        cudaStream_t s) {
-  auto kern = prefill_tc_kernel<DV, CHANNEL>;
+  auto kern = prefill_tc_kernel<DV, CHANNEL, ERASE>;
   const size_t smem = TcSmem<DV>::bytes;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -330,10 +338,13 @@ cudaError_t launch_one(const gdr_shape& sh, const PrefillArgs& a, const TcMaps& 
 }
 
 template <int DV>
-cudaError_t launch_dv(const gdr_shape& sh, const PrefillArgs& a, const TcMaps& maps,
+cudaError_t launch_dv(const gdr_shape& sh, const PrefillArgs& a, const TcMaps& maps, bool erase,
                       cudaStream_t s) {
-  if (sh.gate == GDR_GATE_CHANNEL) return launch_one<DV, true>(sh, a, maps, s);
-  return launch_one<DV, false>(sh, a, maps, s);
+  const bool ch = sh.gate == GDR_GATE_CHANNEL;
+  if (!erase)
+    return ch ? launch_one<DV, true, false>(sh, a, maps, s)
+              : launch_one<DV, false, false>(sh, a, maps, s);
+  return ch ? launch_one<DV, true, true>(sh, a, maps, s) : launch_one<DV, false, true>(sh, a, maps, s);
 }
 
 }  // namespace
@@ -344,11 +355,16 @@ bool prefill_tc_supported(const gdr_shape& sh) {
          sh.total_tokens < ((int64_t)1 << 31) && encode_fn() != nullptr;
 }
 
-cudaError_t launch_prefill_tc(const gdr_shape& sh, const PrefillArgs& a, bool linear,
+cudaError_t launch_prefill_tc(const gdr_shape& sh, const PrefillArgs& a, int kind,
                               cudaStream_t s) {
+  const bool linear = kind == kKindLinear;
   TcMaps maps;
   if (!tc::make_tc_maps(sh, a, linear, &maps)) return cudaErrorInvalidValue;
   if (linear) return tc::launch_linear_tc(sh, a, maps, s);  // linear_tc.cu
+  const long pairs = (long)sh.n_seqs * sh.H;
+  // gated linear attention: the one-CTA kernel without stages 3-4 (no helper CTAs)
+  if (kind == kKindGatedLinear)
+    return pairs >= 120 ? launch_dv<128>(sh, a, maps, false, s) : launch_dv<64>(sh, a, maps, false, s);
   // few (sequence, head) chains: helper CTAs prepare the chunks of each chain, in clusters (the
   // operands cross over DSMEM) or, when clusters would give a chain a single helper, from a
   // work queue over every SM (the operands cross through L2 rings in the workspace)
@@ -360,9 +376,8 @@ cudaError_t launch_prefill_tc(const gdr_shape& sh, const PrefillArgs& a, bool li
     if (ncl > 1) return tc::launch_prefill_cluster(sh, a, maps, ncl, s);
   }
   // value-column split: enough CTAs to cover the SMs when there are few (sequence, head) pairs
-  const long pairs = (long)sh.n_seqs * sh.H;
-  if (pairs >= 120) return launch_dv<128>(sh, a, maps, s);
-  return launch_dv<64>(sh, a, maps, s);
+  if (pairs >= 120) return launch_dv<128>(sh, a, maps, true, s);
+  return launch_dv<64>(sh, a, maps, true, s);
 }
 
 }  // namespace gdr

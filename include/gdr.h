@@ -143,6 +143,21 @@ gdr_status gdr_linear_attn(const gdr_shape* shape, const void* q, const void* k,
                            void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * gdr_gated_linear_attn -- gated linear attention, the decayed additive update without the
+ * delta rule's erase term: S_t = Diag(alpha_t) S_{t-1} + k_t v_t^T, o_t = S_t^T q_t.
+ * engineermaxxing §05b (the scalar-gated additive update, RetNet / Mamba-2 / GLA lineage),
+ * heqinghuang §11 (decay applied to the state before the write); one gate per key channel
+ * (row of S) as in dev.to §5.  Chunked with the gated rule's decay products and no triangular
+ * solve: O = (Q * Gamma) S + M V, S <- Diag(Gamma_n) S + (K * Gamma_n / Gamma)^T V.
+ * Arguments as gdr_prefill without beta; alpha per channel [T, H, d_k] or scalar [T, H]
+ * (shape->gate).
+ */
+gdr_status gdr_gated_linear_attn(const gdr_shape* shape, const void* q, const void* k,
+                                 const void* v, const float* alpha, const float* S0,
+                                 const int32_t* cu_seqlens, void* out, float* S_final,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * gdr_workspace_status -- synchronise `stream`, read the device-check word of a workspace used
  * by gdr_prefill / gdr_linear_attn into *code (a GDR_DEVCHECK_* value) and clear it.
  * Returns GDR_OK, or GDR_ERR_CUDA if the copy or the synchronisation failed.

@@ -129,3 +129,17 @@ def test_host_pipeline_buffer_size(lib):
     # scalar gates stage one gate per (token, head)
     assert (lib.gdr_prefill_host_buffer_size(ctypes.byref(_shape(n_seqs=1, H=32, total_tokens=32768, gate=0)), 1024)
             < small)
+
+
+def test_gated_linear_argument_errors(lib):
+    """gdr_gated_linear_attn needs alpha but no beta."""
+    INV = 1
+    P = ctypes.c_void_p
+    sh = _shape()
+
+    def call(alpha=FAKE, ws=FAKE * 2):
+        return lib.gdr_gated_linear_attn(ctypes.byref(sh), P(FAKE), P(FAKE + 4096), P(FAKE + 8192),
+                                         P(alpha), None, P(FAKE), P(FAKE + 65536), None, P(ws),
+                                         8, None)
+    assert call(alpha=None) == INV
+    assert call() == INV  # workspace too small (8 bytes): alpha present, beta not needed

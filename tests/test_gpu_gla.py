@@ -1,0 +1,70 @@
+"""GPU parity of gdr_gated_linear_attn (S <- Diag(alpha) S + k v^T, no erase, no beta) against
+the oracle's gated-linear mode: the fp32 FFMA path (fp32 inputs, d = 64, or forced), the
+one-CTA tensor-core kernel with both value-column splits (64 and 128 columns per CTA), both gate
+kinds, ragged and empty sequences, entering states, resets and strong decay."""
+import numpy as np
+import pytest
+import torch
+
+import gdr_inputs as gi
+import oracle
+from tests.parity import TOL, dev_inputs, host, rel_rows, rel_states
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def check(a, dtype, force_simt=False, what=""):
+    import gated_delta_rule_prefill_gb300 as g
+    d = dev_inputs(a, dtype)
+    out, sf = g.gdr_gated_linear_attn(d["q"], d["k"], d["v"], d["alpha"], S0=d["S0"],
+                                      cu_seqlens=d["cu_seqlens"], force_simt=force_simt)
+    torch.cuda.synchronize()
+    ref = oracle.gated_linear(a["q"], a["k"], a["v"], a["alpha"], S0=a["S0"],
+                              cu_seqlens=a["cu_seqlens"])
+    eo, es = rel_rows(host(out), ref[0]), rel_states(host(sf), ref[1])
+    print("%s: output err %.3g, state err %.3g" % (what, eo, es))
+    assert eo <= TOL[dtype] and es <= TOL[dtype], (what, eo, es)
+    assert np.isfinite(host(out)).all()
+
+
+@pytest.mark.parametrize("gate", ["channel", "scalar"])
+def test_gla_fp32_d64(gate):
+    wl = gi.custom(seed=301, seqlens=[256, 37, 0, 130], H=2, d_k=64, d_v=64, dtype="f32",
+                   gate=gate, s0="normal")
+    check(gi.gen_full(wl), "f32", what="fp32 d64 " + gate)
+
+
+@pytest.mark.parametrize("gate", ["channel", "scalar"])
+@pytest.mark.parametrize("case", ["dv64", "dv128"])
+def test_gla_tensor_core(gate, case):
+    # fewer than 120 (sequence, head) pairs run 64 value columns per CTA, more run 128
+    lens, H = ([700, 1, 64, 65, 0, 300], 4) if case == "dv64" else ([200, 131, 64, 90], 32)
+    wl = gi.custom(seed=302, seqlens=lens, H=H, d_k=128, d_v=128, dtype="bf16", gate=gate,
+                   s0="normal")
+    check(gi.gen_full(wl), "bf16", what="bf16 %s %s" % (case, gate))
+
+
+def test_gla_forced_simt_bf16():
+    wl = gi.custom(seed=303, seqlens=[300, 100], H=2, d_k=128, d_v=128, dtype="bf16",
+                   gate="channel", s0="normal")
+    check(gi.gen_full(wl), "bf16", force_simt=True, what="bf16 forced fp32 path")
+
+
+@pytest.mark.parametrize("case", ["alpha0", "tiny_alpha", "mixed_decay"])
+def test_gla_special_gates(case):
+    wl = gi.custom(seed=304, seqlens=[450, 77], H=2, d_k=128, d_v=128, dtype="bf16", s0="normal")
+    a = gi.gen_full(wl)
+    if case == "alpha0":
+        a["alpha"][::17] = 0.0
+    elif case == "tiny_alpha":
+        a["alpha"][:] = np.float32(1e-3)
+    else:
+        a["alpha"][64:128] = np.float32(1e-3)
+        a["alpha"][300:340] = np.float32(0.05)
+    check(a, "bf16", what=case)
