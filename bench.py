@@ -46,10 +46,10 @@ CSRC = os.path.join(ROOT, "gated_delta_rule_prefill_gb300", "csrc")
 # ----------------------------------------------------------------------------------------------
 # algorithmic counts (per launch)
 # ----------------------------------------------------------------------------------------------
-def prefill_bytes(T, H, d, n_seqs, channel=True, linear=False, elt=2):
+def prefill_bytes(T, H, d, n_seqs, channel=True, linear=False, elt=2, beta=True):
     per_tok_head = (3 * d * elt + d * elt)  # q, k, v in; out
     if not linear:
-        per_tok_head += (d if channel else 1) * 4 + 4  # alpha, beta
+        per_tok_head += (d if channel else 1) * 4 + (4 if beta else 0)  # alpha, beta
     return T * H * per_tok_head + 2 * n_seqs * H * d * d * 4  # + S0 in, S_final out
 
 
@@ -85,8 +85,10 @@ def source_digest(files):
     return h.hexdigest()[:16]
 
 
-KERNEL_SOURCES = {"prefill": ["prefill_cluster.cu", "prefill_queue.cu", "prefill_tc.cu", "tc_common.cuh",
-                              "umma.cuh"],
+# the files that hold each measured kernel's device code (the bench's KDA prefill runs the
+# clustered kernel; its gated-linear pass, the one-CTA kernel)
+KERNEL_SOURCES = {"gated_linear_attn": ["prefill_tc.cu", "tc_common.cuh", "umma.cuh"],
+                  "prefill": ["prefill_cluster.cu", "tc_common.cuh", "umma.cuh"],
                   "linear_attn": ["linear_tc.cu", "tc_common.cuh", "umma.cuh"],
                   "decode": ["decode.cu"]}
 
@@ -346,6 +348,29 @@ def run_gpu(args):
     total_ms, pre_tot, lin_tot, dec_tot = max_over_ranks(
         [total_ms, sum(pre_ms), sum(lin_ms), sum(dec_ms)], dev, world)
 
+    # ---- gated linear attention (S <- Diag(alpha) S + k v^T) on the prefill inputs: reported
+    # beside the step, timed on its own after it (not part of the step or of gpu_launches)
+    out_g = torch.empty_like(out)
+    Sf_g = torch.empty_like(P["S0"])
+
+    def gla():
+        g.gdr_gated_linear_attn(P["q"], P["k"], P["v"], P["alpha"], S0=P["S0"],
+                                cu_seqlens=P["cu_seqlens"], out=out_g, S_final=Sf_g, workspace=ws)
+
+    gla_steps = max(1, min(args.steps, 10))
+    for _ in range(3):
+        gla()
+    torch.cuda.synchronize()
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(gla_steps):
+        gla()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    gla_ms = max_over_ranks([g0.elapsed_time(g1) / gla_steps], dev, world)[0]
+    del out_g, Sf_g
+
     # ---- end to end through the public API with host buffers (prefill), rank-local
     host_in = {k: P[k].cpu().pin_memory() for k in ("q", "k", "v", "alpha", "beta", "S0")}
     host_cu = P["cu_seqlens"].cpu().pin_memory()
@@ -408,6 +433,11 @@ def run_gpu(args):
         "decode": roof("decode", decode_bytes(wd.n_seqs, wd.H, wd.d_k),
                        decode_flops(wd.n_seqs, wd.H, wd.d_k), dec_s),
     }
+    kern_extra = {
+        "gated_linear_attn": roof("gated_linear_attn",
+                                  prefill_bytes(T, H, d, wp.n_seqs, beta=False),
+                                  prefill_flops(T, H, d, linear=True), gla_ms / 1e3),
+    }
     dominant = max(kern, key=lambda k: kern[k]["launch_us"])
     main_roof = {k: kern[dominant][k] for k in ("bound", "achieved", "peak", "unit", "frac",
                                                  "traffic")}
@@ -426,8 +456,10 @@ def run_gpu(args):
                    "parallelism": "replicas" if n > 1 else "1 GPU"},
         "decode_tokens_per_s": decode_tps,
         "linear_attn_tokens_per_s": linear_tps,
+        "gated_linear_attn_tokens_per_s": job_tokens_per_s(n, T, gla_ms / 1e3),
         "roofline": main_roof,
         "kernels": kern,
+        "kernels_outside_step": kern_extra,
         "e2e": {"value": job_tokens_per_s(n, T, e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "what": "gdr_prefill_host: pinned host inputs in, "
                 "out and S_final back, copies pipelined with the kernels inside the call"},
