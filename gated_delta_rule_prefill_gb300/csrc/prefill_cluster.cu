@@ -134,6 +134,7 @@ __device__ bool wait_consumed(const uint32_t* cons, uint32_t need) {
       __nanosleep(64);
     }
   }
+  __syncwarp();  // lane 0 rejoins its warp before the aligned CTA barrier
   return !__syncthreads_or(!ok);
 }
 
@@ -276,6 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ph_full[s] ^= 1u;
         ph_v ^= 1u;
         gm = reinterpret_cast<const float*>(sm + slot + kSlotGam)[x.lrow];
+        __syncwarp();  // lanes leave their polling loops at different times
         if (n < kC) {  // the last chunk: every thread zeroes part of the V tail
           zero_v_tail<DV>(x, sm + L::VIN, n);
           __syncthreads();
@@ -292,6 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       x.ph_mma ^= 1u;
       fence_after_sync();
       if (c + 1 < nch) issue_v(tc + kC);  // V is consumed
+      __syncwarp();
       if (u_rows) {
         // U rows -> bf16 [tok][DV] tile (MN-major B operand); the four warps holding them meet
         // at a named barrier, then K^^T U (on the chain's critical path) and O += M U are issued
@@ -314,11 +317,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       bad |= !mbar_wait(x.bar_mma, x.ph_mma, kWaitNs);
       x.ph_mma ^= 1u;
+      __syncwarp();
       fence_after_sync();
       s_update(gm);
       // the slot is consumed once O's MMA is complete (gamma was read before the barrier below):
       // re-arm it for chunk c + 2 and tell the helpers
       if (tid == 0) bad |= !mbar_wait(bar_o, ph_o, kWaitNs);
+      __syncwarp();  // warp 0 reconverges before the aligned CTA barrier below
       ph_o ^= 1u;
       fence_before_sync();
       if (__syncthreads_or(bad)) { failed = true; break; }
@@ -419,9 +424,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // prefix runs; the gate waits for it before it rewrites them
       const bool safe = gate_stage<L, CHANNEL>(x, n, [&] {
         if (tid == 0) bulk_wait_read<1>();
+        __syncwarp();
       });
       // ... and the second (-W, T', M), before the Gram epilogue rewrites M
       if (tid == 0) bulk_wait_read<0>();
+      __syncwarp();
       fence_async_smem();
       cta_sync_tc();
       if (safe && cn < nch) {

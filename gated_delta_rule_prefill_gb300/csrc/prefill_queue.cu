@@ -301,6 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the local slot is free for chunk c + 2 once O's MMA is complete (gamma was read before
       // a barrier)
       if (tid == 0) bad |= !mbar_wait(bar_o, ph_o, kWaitNs);
+      __syncwarp();  // warp 0 reconverges before the aligned CTA barrier below
       ph_o ^= 1u;
       fence_before_sync();
       if (__syncthreads_or(bad)) { failed = true; break; }
@@ -439,6 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ring slot c mod R must be free: the chain CTA has loaded chunk c - R from it
       bool ok = true;
       if (tid == 0 && cur.c >= kR) ok = poll_ge(q_loaded + cur.p, (uint32_t)(cur.c - kR + 1));
+      __syncwarp();  // lane 0 rejoins its warp before the aligned CTA barrier
       if (__syncthreads_or(!ok)) { failed = true; break; }
       x.gslot = a.ring + ((size_t)cur.p * kR + (size_t)(cur.c % kR)) * kSlotBytes;
       if (!wait_bar(bar_qk, ph_qk)) { failed = true; break; }

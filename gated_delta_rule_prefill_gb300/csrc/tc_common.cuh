@@ -311,6 +311,7 @@ __device__ __forceinline__ TcCtx make_ctx(unsigned char* sm, uint32_t tm, uint64
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t& ph) {
   const bool ok = mbar_wait(bar, ph, kWaitNs);
   ph ^= 1u;
+  __syncwarp();  // lanes leave the polling loop at different times; reconverge before the barrier
   const bool all_ok = !__syncthreads_or(!ok);
   fence_after_sync();
   return all_ok;
