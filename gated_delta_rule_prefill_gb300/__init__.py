@@ -200,11 +200,11 @@ def gdr_linear_attn(q, k, v, S0=None, cu_seqlens=None, out=None, S_final=None, w
 
 def gdr_gated_linear_attn(q, k, v, alpha, S0=None, cu_seqlens=None, out=None, S_final=None,
                           workspace=None, chunk_size=0, force_simt=False, stream=None,
-                          want_final=True):
+                          want_final=True, no_cluster=False):
     """Gated linear attention: S <- Diag(alpha) S + k v^T (no erase, no beta); alpha [T,H,d_k]
     or [T,H] fp32.  Returns (out, S_final)."""
     return _prefill_like("gla", q, k, v, alpha, None, S0, cu_seqlens, out, S_final, workspace,
-                         chunk_size, force_simt, stream, want_final)
+                         chunk_size, force_simt, stream, want_final, no_cluster)
 
 
 def gdr_decode_step(q, k, v, alpha, beta, S_inout, out=None, stream=None):

@@ -138,7 +138,9 @@ __device__ bool wait_consumed(const uint32_t* cons, uint32_t need) {
   return !__syncthreads_or(!ok);
 }
 
-template <bool CHANNEL>
+// ERASE = false: gated linear attention.  The helpers skip the triangular solve and W and hand
+// over T' = I and W = 0 (written once), so the chain's U is V itself and its code is unchanged.
+template <bool CHANNEL, bool ERASE = true>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_cluster_kernel(const __grid_constant__ TcMaps maps, const PrefillArgs a, int ncl) {
   constexpr bool kAlphaTile = CHANNEL;
@@ -369,6 +371,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     cluster_sync();
     TcCtx x = make_ctx(sm, *tslot, bars + 2);
     zero_upper_tp(sm + L::TT, tid);
+    if (!ERASE) {  // T' = I and W = 0 for every chunk
+      if (tid < kC) st_bf16(sm + L::TT, sw128_offset(tid, tid, 8192), 1.f);
+      for (int i = tid; i < 16384 / 16; i += kThreads)
+        reinterpret_cast<uint4*>(sm + L::WW)[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
     uint32_t ph_qk = 0, ph_a = 0;
     const uint32_t chain_full = map_to(smem_u32(sm + ChainSmem::BARS), 0);
     const uint32_t chain_slots = map_to(smem_u32(sm + ChainSmem::SLOT), 0);
@@ -390,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       al = 1.f;
       if (tid < kC && tc + tid < t1) {
         const size_t o = (size_t)(tc + tid) * H + h;
-        b = a.beta[o];
+        if (ERASE) b = a.beta[o];
         if (!CHANNEL) al = a.alpha[o];
       }
     };
@@ -440,9 +447,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         issue_qk(tn);
         issue_a(tn);
       }
-      solve_stage<L>(x);
-      if (!w_stage<L>(x, false, Opnd{0, 0, false}, 0)) { failed = true; break; }
-      w_epilogue<L, true>(x);  // -W
+      if (ERASE) {
+        solve_stage<L>(x);
+        if (!w_stage<L>(x, false, Opnd{0, 0, false}, 0)) { failed = true; break; }
+        w_epilogue<L, true>(x);  // -W
+      }
       fence_async_smem();
       cta_sync_tc();
       // hand the operands over: slot c & 1 is free once chunk c - 2 has been consumed
@@ -475,10 +484,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync();  // no CTA leaves while the cluster may still address its shared memory
 }
 
-template <bool CHANNEL>
+template <bool CHANNEL, bool ERASE>
 cudaError_t launch_typed(const gdr_shape& sh, const PrefillArgs& a, const TcMaps& maps, int ncl,
                          cudaStream_t s) {
-  auto kern = prefill_cluster_kernel<CHANNEL>;
+  auto kern = prefill_cluster_kernel<CHANNEL, ERASE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kClusterSmem);
   if (e != cudaSuccess) return e;
@@ -545,9 +554,13 @@ int cluster_size_for(const gdr_shape& sh) {
 }
 
 cudaError_t launch_prefill_cluster(const gdr_shape& sh, const PrefillArgs& a, const TcMaps& maps,
-                                   int ncl, cudaStream_t s) {
-  if (sh.gate == GDR_GATE_CHANNEL) return launch_typed<true>(sh, a, maps, ncl, s);
-  return launch_typed<false>(sh, a, maps, ncl, s);
+                                   int ncl, bool erase, cudaStream_t s) {
+  const bool ch = sh.gate == GDR_GATE_CHANNEL;
+  if (!erase)
+    return ch ? launch_typed<true, false>(sh, a, maps, ncl, s)
+              : launch_typed<false, false>(sh, a, maps, ncl, s);
+  return ch ? launch_typed<true, true>(sh, a, maps, ncl, s)
+            : launch_typed<false, true>(sh, a, maps, ncl, s);
 }
 
 }  // namespace tc

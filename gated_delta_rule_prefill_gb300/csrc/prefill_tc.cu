@@ -362,9 +362,13 @@ cudaError_t launch_prefill_tc(const gdr_shape& sh, const PrefillArgs& a, int kin
   if (!tc::make_tc_maps(sh, a, linear, &maps)) return cudaErrorInvalidValue;
   if (linear) return tc::launch_linear_tc(sh, a, maps, s);  // linear_tc.cu
   const long pairs = (long)sh.n_seqs * sh.H;
-  // gated linear attention: the one-CTA kernel without stages 3-4 (no helper CTAs)
-  if (kind == kKindGatedLinear)
+  // gated linear attention: without stages 3-4; helper CTAs in clusters where they fit, else
+  // the one-CTA kernel
+  if (kind == kKindGatedLinear) {
+    const int ncl = (sh.flags & GDR_FLAG_NO_CLUSTER) ? 1 : tc::cluster_size_for(sh);
+    if (ncl > 1) return tc::launch_prefill_cluster(sh, a, maps, ncl, false, s);
     return pairs >= 120 ? launch_dv<128>(sh, a, maps, false, s) : launch_dv<64>(sh, a, maps, false, s);
+  }
   // few (sequence, head) chains: helper CTAs prepare the chunks of each chain, in clusters (the
   // operands cross over DSMEM) or, when clusters would give a chain a single helper, from a
   // work queue over every SM (the operands cross through L2 rings in the workspace)
@@ -373,7 +377,7 @@ cudaError_t launch_prefill_tc(const gdr_shape& sh, const PrefillArgs& a, int kin
     const int G = tc::queue_grid_for(sh, a);
     if (G > 0 && (ncl <= 2 || (sh.flags & GDR_FLAG_PREFER_QUEUE)))
       return tc::launch_prefill_queue(sh, a, maps, G, s);
-    if (ncl > 1) return tc::launch_prefill_cluster(sh, a, maps, ncl, s);
+    if (ncl > 1) return tc::launch_prefill_cluster(sh, a, maps, ncl, true, s);
   }
   // value-column split: enough CTAs to cover the SMs when there are few (sequence, head) pairs
   if (pairs >= 120) return launch_dv<128>(sh, a, maps, true, s);

@@ -844,7 +844,7 @@ cudaError_t launch_prefill_queue(const gdr_shape& sh, const PrefillArgs& a, cons
 // host side: CTAs per cluster of the clustered prefill for this shape (1: use the one-CTA kernel)
 int cluster_size_for(const gdr_shape& sh);
 cudaError_t launch_prefill_cluster(const gdr_shape& sh, const PrefillArgs& a, const TcMaps& maps,
-                                   int ncl, cudaStream_t s);
+                                   int ncl, bool erase, cudaStream_t s);
 
 }  // namespace tc
 }  // namespace gdr

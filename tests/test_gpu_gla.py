@@ -1,7 +1,8 @@
 """GPU parity of gdr_gated_linear_attn (S <- Diag(alpha) S + k v^T, no erase, no beta) against
 the oracle's gated-linear mode: the fp32 FFMA path (fp32 inputs, d = 64, or forced), the
-one-CTA tensor-core kernel with both value-column splits (64 and 128 columns per CTA), both gate
-kinds, ragged and empty sequences, entering states, resets and strong decay."""
+clustered tensor-core kernel (helpers without the solve), the one-CTA tensor-core kernel with
+both value-column splits (64 and 128 columns per CTA), both gate kinds, ragged and empty
+sequences, entering states, resets and strong decay."""
 import numpy as np
 import pytest
 import torch
@@ -19,11 +20,12 @@ def _gpu():
         pytest.skip("no CUDA device")
 
 
-def check(a, dtype, force_simt=False, what=""):
+def check(a, dtype, force_simt=False, what="", no_cluster=False):
     import gated_delta_rule_prefill_gb300 as g
     d = dev_inputs(a, dtype)
     out, sf = g.gdr_gated_linear_attn(d["q"], d["k"], d["v"], d["alpha"], S0=d["S0"],
-                                      cu_seqlens=d["cu_seqlens"], force_simt=force_simt)
+                                      cu_seqlens=d["cu_seqlens"], force_simt=force_simt,
+                                      no_cluster=no_cluster)
     torch.cuda.synchronize()
     ref = oracle.gated_linear(a["q"], a["k"], a["v"], a["alpha"], S0=a["S0"],
                               cu_seqlens=a["cu_seqlens"])
@@ -41,13 +43,14 @@ def test_gla_fp32_d64(gate):
 
 
 @pytest.mark.parametrize("gate", ["channel", "scalar"])
-@pytest.mark.parametrize("case", ["dv64", "dv128"])
+@pytest.mark.parametrize("case", ["cluster", "dv64", "dv128"])
 def test_gla_tensor_core(gate, case):
-    # fewer than 120 (sequence, head) pairs run 64 value columns per CTA, more run 128
-    lens, H = ([700, 1, 64, 65, 0, 300], 4) if case == "dv64" else ([200, 131, 64, 90], 32)
+    # few chains run in clusters with helper CTAs; without clusters, fewer than 120 (sequence,
+    # head) pairs run 64 value columns per CTA and more run 128 (too many for clusters anyway)
+    lens, H = ([700, 1, 64, 65, 0, 300], 4) if case != "dv128" else ([200, 131, 64, 90], 32)
     wl = gi.custom(seed=302, seqlens=lens, H=H, d_k=128, d_v=128, dtype="bf16", gate=gate,
                    s0="normal")
-    check(gi.gen_full(wl), "bf16", what="bf16 %s %s" % (case, gate))
+    check(gi.gen_full(wl), "bf16", what="bf16 %s %s" % (case, gate), no_cluster=(case == "dv64"))
 
 
 def test_gla_forced_simt_bf16():
