@@ -138,8 +138,9 @@ __device__ bool wait_consumed(const uint32_t* cons, uint32_t need) {
   return !__syncthreads_or(!ok);
 }
 
-// ERASE = false: gated linear attention.  The helpers skip the triangular solve and W and hand
-// over T' = I and W = 0 (written once), so the chain's U is V itself and its code is unchanged.
+// ERASE = false: gated linear attention.  The helpers skip the triangular solve and W; the chain
+// CTA's slots hold T' = I and W = 0 from the start, so its U is V itself and its code is
+// unchanged, and a chunk's hand-over shrinks from 66 KB to 41 KB.
 template <bool CHANNEL, bool ERASE = true>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_cluster_kernel(const __grid_constant__ TcMaps maps, const PrefillArgs a, int ncl) {
@@ -163,6 +164,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const size_t sidx = ((size_t)seq * H + h) * kD * kD;
   bool failed = false;
 
+  // bytes a helper copies into a slot per chunk (gated linear attention: T' = I and W = 0 stay
+  // in the slots from the start instead)
+  constexpr uint32_t kPayload = ERASE ? kSlotPayload : kSlotPayload - 16384 - 8192;
   if (crank == 0) {
     // ===================================================================== chain CTA
     using L = ChainSmem;
@@ -176,12 +180,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       *reinterpret_cast<uint4*>(sm + L::SLOT + (i >> 9) * kSlotBytes + kSlotZ + (i & 511) * 16) =
           make_uint4(0, 0, 0, 0);
     }
+    if (!ERASE) {  // T' = I and -W = 0 in both slots, for every chunk
+      for (int i = tid; i < 2 * 3 * 8192 / 16; i += kThreads) {
+        const int sl = i / (3 * 512), part = (i / 512) % 3, e = i % 512;
+        const uint32_t off = part == 0 ? kSlotWQ : (part == 1 ? kSlotWQ + 16384 : kSlotT);
+        *reinterpret_cast<uint4*>(sm + L::SLOT + sl * kSlotBytes + off + e * 16) =
+            make_uint4(0, 0, 0, 0);
+      }
+      __syncthreads();
+      if (tid < 2 * kC) {
+        const int sl = tid / kC, r = tid % kC;
+        st_bf16(sm + L::SLOT + sl * kSlotBytes + kSlotT, sw128_offset(r, r, 8192), 1.f);
+      }
+    }
     fence_async_smem();
     if (tid == 0) {
       for (int i = 0; i < 5; ++i) mbar_init(bars + i, 1);
       fence_mbar_init();
       prefetch_tmap(&maps.v);
-      for (int s = 0; s < 2 && s < nch; ++s) mbar_expect_tx(full + s, kSlotPayload);
+      for (int s = 0; s < 2 && s < nch; ++s) mbar_expect_tx(full + s, kPayload);
     }
     cta_sync_tc();
     cluster_sync();  // every CTA's barriers and counters are initialised
@@ -331,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (__syncthreads_or(bad)) { failed = true; break; }
       fence_after_sync();
       if (tid == 0) {
-        if (c + 2 < nch) mbar_expect_tx(full + s, kSlotPayload);
+        if (c + 2 < nch) mbar_expect_tx(full + s, kPayload);
         for (int r = 1; r < ncl; ++r) st_relaxed_remote(map_to(cons_local, r), (uint32_t)(c + 1));
       }
     }
@@ -371,11 +388,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     cluster_sync();
     TcCtx x = make_ctx(sm, *tslot, bars + 2);
     zero_upper_tp(sm + L::TT, tid);
-    if (!ERASE) {  // T' = I and W = 0 for every chunk
-      if (tid < kC) st_bf16(sm + L::TT, sw128_offset(tid, tid, 8192), 1.f);
-      for (int i = tid; i < 16384 / 16; i += kThreads)
-        reinterpret_cast<uint4*>(sm + L::WW)[i] = make_uint4(0u, 0u, 0u, 0u);
-    }
     uint32_t ph_qk = 0, ph_a = 0;
     const uint32_t chain_full = map_to(smem_u32(sm + ChainSmem::BARS), 0);
     const uint32_t chain_slots = map_to(smem_u32(sm + ChainSmem::SLOT), 0);
@@ -465,9 +477,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         bulk_copy_to(dst + kSlotKH, src + L::KH, 16384, mbar);
         bulk_copy_to(dst + kSlotGam, src + L::GAM, 512, mbar);
         bulk_commit();
-        bulk_copy_to(dst + kSlotWQ, src + L::WW, 8192, mbar);           // -W, channels 0-63
-        bulk_copy_to(dst + kSlotWQ + 16384, src + L::WW + 8192, 8192, mbar);  // -W, 64-127
-        bulk_copy_to(dst + kSlotT, src + L::TT, 8192, mbar);
+        if (ERASE) {
+          bulk_copy_to(dst + kSlotWQ, src + L::WW, 8192, mbar);           // -W, channels 0-63
+          bulk_copy_to(dst + kSlotWQ + 16384, src + L::WW + 8192, 8192, mbar);  // -W, 64-127
+          bulk_copy_to(dst + kSlotT, src + L::TT, 8192, mbar);
+        }
         bulk_copy_to(dst + kSlotM, src + L::MM, 8192, mbar);
         bulk_commit();
       }
