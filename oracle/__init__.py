@@ -9,6 +9,10 @@ It shares no code with the GPU library and never imports it.
   linear_attn(...)  S <- S + k_t v_t^T;  o_t = S^T q_t   (alpha = 1, no erase term, no beta).
   gated_linear(...) S <- Diag(alpha_t) S + k_t v_t^T;  o_t = S^T q_t   (no erase term, no beta;
                     engineermaxxing §05b, heqinghuang §11; per key channel as dev.to §5).
+  output_gate(o, g) o * sigmoid(g), element by element (numpy fp64): the KDA layer's output
+                    gate (dev.to §5: full rank and input dependent in K3; a sigmoid multiplied
+                    into the output feature by feature, as heqinghuang §15 describes the gate of
+                    the attention layers).
   chunked           (module) the chunk-parallel rewrite of the same recurrence in numpy fp64; a
                     derivation check for the chunk algebra, itself compared against gated_delta.
 
@@ -121,6 +125,13 @@ def gated_linear(q, k, v, alpha, S0=None, cu_seqlens=None, pairs=None, threads=N
     """Gated linear attention: S <- Diag(alpha_t) S + k_t v_t^T (per-channel alpha [T,H,d_k] or
     scalar alpha [T,H]), o_t = S^T q_t; returns (out, S_final) in fp64."""
     return _run(2, q, k, v, alpha, None, S0, cu_seqlens, pairs, threads)
+
+
+def output_gate(o, g):
+    """o * sigmoid(g) in fp64 (o and g of one shape, e.g. [T, H, d_v])."""
+    o = np.asarray(o, dtype=np.float64)
+    g = np.asarray(g, dtype=np.float64)
+    return o / (1.0 + np.exp(-g))
 
 
 def decode_step(q, k, v, alpha, beta, S):

@@ -397,3 +397,20 @@ def test_gated_linear_zero_gate_resets():
     alpha[3] = 0.0
     out, _ = oracle.gated_linear(q, k, v, alpha, S0=rng.standard_normal((1, 1, dk, dv)))
     np.testing.assert_allclose(out[3, 0], np.dot(q[3, 0], k[3, 0]) * v[3, 0], atol=1e-12)
+
+
+# ------------------------------------------------------------------------------------------
+# the output gate o * sigmoid(g): closed forms
+# ------------------------------------------------------------------------------------------
+def test_output_gate_closed_forms():
+    """sigmoid(0) = 1/2; sigmoid(ln 3) = 3/4; sigmoid(x) + sigmoid(-x) = 1; the gate opens fully
+    for large g and shuts for very negative g."""
+    o = np.array([2.0, -4.0, 8.0, 1.0])
+    np.testing.assert_allclose(oracle.output_gate(o, np.zeros(4)), o / 2, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(oracle.output_gate(o, np.full(4, np.log(3.0))), 0.75 * o, atol=1e-14)
+    x = np.linspace(-6, 6, 13)
+    one = np.ones_like(x)
+    np.testing.assert_allclose(oracle.output_gate(one, x) + oracle.output_gate(one, -x), one,
+                               atol=1e-15)
+    np.testing.assert_allclose(oracle.output_gate(o, np.full(4, 50.0)), o, rtol=1e-15)
+    np.testing.assert_allclose(oracle.output_gate(o, np.full(4, -50.0)), 0 * o, atol=1e-20)
