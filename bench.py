@@ -85,9 +85,10 @@ def source_digest(files):
     return h.hexdigest()[:16]
 
 
-# the files that hold each measured kernel's device code (the bench's KDA prefill runs the
-# clustered kernel; its gated-linear pass, the one-CTA kernel)
-KERNEL_SOURCES = {"gated_linear_attn": ["prefill_tc.cu", "tc_common.cuh", "umma.cuh"],
+# the files that hold each measured kernel's device code (the bench's KDA prefill, its gated
+# variant and its gated-linear pass run the clustered kernel)
+KERNEL_SOURCES = {"gated_linear_attn": ["prefill_cluster.cu", "tc_common.cuh", "umma.cuh"],
+                  "prefill_output_gate": ["prefill_cluster.cu", "tc_common.cuh", "umma.cuh"],
                   "prefill": ["prefill_cluster.cu", "tc_common.cuh", "umma.cuh"],
                   "linear_attn": ["linear_tc.cu", "tc_common.cuh", "umma.cuh"],
                   "decode": ["decode.cu"]}
@@ -369,7 +370,27 @@ def run_gpu(args):
     g1.record(stream)
     torch.cuda.synchronize()
     gla_ms = max_over_ranks([g0.elapsed_time(g1) / gla_steps], dev, world)[0]
-    del out_g, Sf_g
+
+    # ---- the same prefill with the KDA output gate (out = o * sigmoid(g)), also outside the step
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4242 + rank)
+    gate_in = torch.randn(out.shape, generator=gen, device=dev).mul_(2.0).to(torch.bfloat16)
+
+    def pre_gated():
+        g.gdr_prefill_output_gate(P["q"], P["k"], P["v"], P["alpha"], P["beta"], gate_in,
+                                  S0=P["S0"], cu_seqlens=P["cu_seqlens"], out=out_g,
+                                  S_final=Sf_g, workspace=ws)
+
+    for _ in range(3):
+        pre_gated()
+    torch.cuda.synchronize()
+    g0.record(stream)
+    for _ in range(gla_steps):
+        pre_gated()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    og_ms = max_over_ranks([g0.elapsed_time(g1) / gla_steps], dev, world)[0]
+    del out_g, Sf_g, gate_in
 
     # ---- end to end through the public API with host buffers (prefill), rank-local
     host_in = {k: P[k].cpu().pin_memory() for k in ("q", "k", "v", "alpha", "beta", "S0")}
@@ -437,6 +458,9 @@ def run_gpu(args):
         "gated_linear_attn": roof("gated_linear_attn",
                                   prefill_bytes(T, H, d, wp.n_seqs, beta=False),
                                   prefill_flops(T, H, d, linear=True), gla_ms / 1e3),
+        "prefill_output_gate": roof("prefill_output_gate",
+                                    prefill_bytes(T, H, d, wp.n_seqs) + T * H * d * 2,
+                                    prefill_flops(T, H, d), og_ms / 1e3),
     }
     dominant = max(kern, key=lambda k: kern[k]["launch_us"])
     main_roof = {k: kern[dominant][k] for k in ("bound", "achieved", "peak", "unit", "frac",
@@ -457,6 +481,7 @@ def run_gpu(args):
         "decode_tokens_per_s": decode_tps,
         "linear_attn_tokens_per_s": linear_tps,
         "gated_linear_attn_tokens_per_s": job_tokens_per_s(n, T, gla_ms / 1e3),
+        "prefill_output_gate_tokens_per_s": job_tokens_per_s(n, T, og_ms / 1e3),
         "roofline": main_roof,
         "kernels": kern,
         "kernels_outside_step": kern_extra,

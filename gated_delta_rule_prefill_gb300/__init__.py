@@ -23,7 +23,8 @@ from ._abi import (GDR_BF16, GDR_F32, GDR_FLAG_FORCE_SIMT, GDR_FLAG_NO_CLUSTER, 
                    GDR_GATE_CHANNEL, GDR_GATE_SCALAR,
                    GdrError, GdrShape)
 
-__all__ = ["gdr_prefill", "gdr_decode_step", "gdr_linear_attn", "gdr_gated_linear_attn",
+__all__ = ["gdr_prefill", "gdr_prefill_output_gate", "gdr_decode_step", "gdr_linear_attn",
+           "gdr_gated_linear_attn",
            "gdr_prefill_workspace_size",
            "gdr_workspace_status", "gdr_prefill_host", "gdr_prefill_host_buffer_size",
            "make_shape", "GdrError"]
@@ -72,7 +73,7 @@ def _workspace(n_seqs, H, d_k, d_v, dtype, device, workspace):
 
 def _prefill_like(kind, q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, workspace,
                   chunk_size, force_simt, stream, want_final, no_cluster=False,
-                  prefer_queue=False):
+                  prefer_queue=False, g=None):
     """kind: "delta" (gdr_prefill), "linear" (gdr_linear_attn) or "gla"
     (gdr_gated_linear_attn)."""
     linear = kind == "linear"
@@ -108,6 +109,12 @@ def _prefill_like(kind, q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, work
         rc = lib.gdr_linear_attn(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(S0),
                                  _ptr(cu_seqlens), _ptr(out), _ptr(S_final), _ptr(ws),
                                  ws.numel(), _stream(stream))
+    elif g is not None:
+        _check(g, "g", q.dtype)
+        rc = lib.gdr_prefill_output_gate(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
+                                         _ptr(beta), _ptr(g), _ptr(S0), _ptr(cu_seqlens),
+                                         _ptr(out), _ptr(S_final), _ptr(ws), ws.numel(),
+                                         _stream(stream))
     elif kind == "gla":
         rc = lib.gdr_gated_linear_attn(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
                                        _ptr(S0), _ptr(cu_seqlens), _ptr(out), _ptr(S_final),
@@ -130,6 +137,15 @@ def gdr_prefill(q, k, v, alpha, beta, S0=None, cu_seqlens=None, out=None, S_fina
     [N+1] or None.  Returns (out [T,H,d_v], S_final [N,H,d_k,d_v] or None)."""
     return _prefill_like("delta", q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, workspace,
                          chunk_size, force_simt, stream, want_final, no_cluster, prefer_queue)
+
+
+def gdr_prefill_output_gate(q, k, v, alpha, beta, g, S0=None, cu_seqlens=None, out=None,
+                            S_final=None, workspace=None, chunk_size=0, force_simt=False,
+                            stream=None, want_final=True, no_cluster=False, prefer_queue=False):
+    """gdr_prefill with the output gate: out = o * sigmoid(g), g [T,H,d_v] in q's dtype."""
+    return _prefill_like("delta", q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, workspace,
+                         chunk_size, force_simt, stream, want_final, no_cluster, prefer_queue,
+                         g=g)
 
 
 def _check_host(t, name, dtype=None):

@@ -68,7 +68,7 @@ gdr_status check_shape(const gdr_shape* sh, bool need_gate) {
 gdr_status prefill_common(const gdr_shape* sh, const void* q, const void* k, const void* v,
                           const float* alpha, const float* beta, const float* S0,
                           const int32_t* cu, void* out, float* S_final, void* ws,
-                          size_t ws_bytes, void* stream, int kind) {
+                          size_t ws_bytes, void* stream, int kind, const void* og = nullptr) {
   const bool linear = kind == kKindLinear;
   gdr_status st = check_shape(sh, !linear);
   if (st != GDR_OK) return st;
@@ -78,9 +78,10 @@ gdr_status prefill_common(const gdr_shape* sh, const void* q, const void* k, con
     if (!linear && !alpha) return GDR_ERR_INVALID_ARG;
     if (kind == kKindDelta && !beta) return GDR_ERR_INVALID_ARG;
   }
-  const void* ptrs[] = {q, k, v, alpha, beta, S0, cu, out, S_final};
+  const void* ptrs[] = {q, k, v, alpha, beta, S0, cu, out, S_final, og};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return GDR_ERR_INVALID_ARG;
+  if (og && og == out) return GDR_ERR_INVALID_ARG;
   if (!ws || ((uintptr_t)ws & 255u) || ws_bytes < WorkspaceLayout::total(sh->n_seqs))
     return GDR_ERR_INVALID_ARG;
   if (out && (out == q || out == k || out == v)) return GDR_ERR_INVALID_ARG;
@@ -97,7 +98,7 @@ gdr_status prefill_common(const gdr_shape* sh, const void* q, const void* k, con
            WorkspaceLayout::flag_bytes(WorkspaceLayout::ring_pairs(*sh));
   }
   PrefillArgs a{sh->n_seqs, sh->H, sh->total_tokens, q, k, v, alpha, beta, S0, cu,
-                out, S_final, order, status, ring_flags, ring};
+                out, S_final, order, status, ring_flags, ring, og};
   prep_kernel<<<1, kPrepThreads, 0, s>>>(cu, sh->n_seqs, sh->total_tokens, order, status);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess)
@@ -140,6 +141,16 @@ gdr_status gdr_linear_attn(const gdr_shape* shape, const void* q, const void* k,
                            void* workspace, size_t workspace_bytes, void* stream) {
   return gdr::prefill_common(shape, q, k, v, nullptr, nullptr, S0, cu_seqlens, out, S_final,
                              workspace, workspace_bytes, stream, gdr::kKindLinear);
+}
+
+gdr_status gdr_prefill_output_gate(const gdr_shape* shape, const void* q, const void* k,
+                                   const void* v, const float* alpha, const float* beta,
+                                   const void* g, const float* S0, const int32_t* cu_seqlens,
+                                   void* out, float* S_final, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  if (!g && shape && shape->total_tokens > 0) return GDR_ERR_INVALID_ARG;
+  return gdr::prefill_common(shape, q, k, v, alpha, beta, S0, cu_seqlens, out, S_final,
+                             workspace, workspace_bytes, stream, gdr::kKindDelta, g);
 }
 
 gdr_status gdr_gated_linear_attn(const gdr_shape* shape, const void* q, const void* k,

@@ -72,7 +72,11 @@ struct PrefillArgs {
   int32_t* status;       // device-check word
   uint32_t* ring_flags;  // work-queue prefill: counter, ready, loaded (null: not available)
   unsigned char* ring;   // work-queue prefill: operand slots
+  const void* og = nullptr;  // output gate g [T, H, d_v] (dtype of out): out = o * sigmoid(g)
 };
+
+// The output gate of one element: o * sigmoid(g).
+__device__ __forceinline__ float gate_out(float o, float g) { return o / (1.f + __expf(-g)); }
 
 // Records the first device-check failure (0 -> code).
 __device__ __forceinline__ void report(int32_t* status, int32_t code) {

@@ -141,7 +141,8 @@ __device__ bool wait_consumed(const uint32_t* cons, uint32_t need) {
 // ERASE = false: gated linear attention.  The helpers skip the triangular solve and W; the chain
 // CTA's slots hold T' = I and W = 0 from the start, so its U is V itself and its code is
 // unchanged, and a chunk's hand-over shrinks from 66 KB to 41 KB.
-template <bool CHANNEL, bool ERASE = true>
+// OGATE: the output gate out = o * sigmoid(g) on the stored output rows (a.og).
+template <bool CHANNEL, bool ERASE = true, bool OGATE = false>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_cluster_kernel(const __grid_constant__ TcMaps maps, const PrefillArgs a, int ncl) {
   constexpr bool kAlphaTile = CHANNEL;
@@ -234,6 +235,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // columns go through its own 4 KB of the bf16 state tile (the rows it rewrites itself in
     // s_update, free between the chunk's first MMA and that update), so that each global store
     // instruction writes four whole 128-byte row segments instead of 32 scattered pieces.
+    // the output gate's values for the O rows this thread stores next (lane -> 8 row segments of
+    // 16 bytes, the coalesced store pattern below), loaded ahead so their latency is hidden
+    uint4 gv[8];
+    auto load_gates = [&](int64_t tc, int n) {
+      if constexpr (OGATE) {
+        const __nv_bfloat16* og = static_cast<const __nv_bfloat16*>(a.og);
+        const int lane = tid & 31, row0 = (warp & 3) * 32 - 64;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int r = 4 * j + (lane >> 3), ch = lane & 7;
+          gv[j] = make_uint4(0u, 0u, 0u, 0u);
+          if (row0 + r < n)
+            gv[j] = *reinterpret_cast<const uint4*>(og + ((size_t)(tc + row0 + r) * H + h) * kD +
+                                                    x.wh * 64 + ch * 8);
+        }
+      }
+    };
     auto o_store = [&](int c, int64_t tc, int n) {
       float v[64];
       tmem_ld64(x.tm + x.lane_base + d_col(c) + x.wh * 64, v);
@@ -249,12 +267,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       const int row0 = (warp & 3) * 32 - 64;  // this warp's first O row
+      if constexpr (OGATE) {
+        // the output gate (values in gv, loaded ahead), on the rounded output: one more rounding
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int r = 4 * j + (lane >> 3), ch = lane & 7;
-        const uint4 w = *reinterpret_cast<const uint4*>(stage + r * 128 + ((ch ^ (r & 7)) << 4));
-        if (row0 + r < n)
-          *reinterpret_cast<uint4*>(out + ((size_t)(tc + row0 + r) * H + h) * kD + x.wh * 64 + ch * 8) = w;
+        for (int j = 0; j < 8; ++j) {
+          const int r = 4 * j + (lane >> 3), ch = lane & 7;
+          uint4 w = *reinterpret_cast<const uint4*>(stage + r * 128 + ((ch ^ (r & 7)) << 4));
+          if (row0 + r < n) {
+            __nv_bfloat162* hw = reinterpret_cast<__nv_bfloat162*>(&w);
+            const __nv_bfloat162* hg = reinterpret_cast<const __nv_bfloat162*>(&gv[j]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 o2 = __bfloat1622float2(hw[i]), g2 = __bfloat1622float2(hg[i]);
+              hw[i] = __floats2bfloat162_rn(gate_out_bf16(o2.x, g2.x), gate_out_bf16(o2.y, g2.y));
+            }
+            *reinterpret_cast<uint4*>(out + ((size_t)(tc + row0 + r) * H + h) * kD + x.wh * 64 +
+                                      ch * 8) = w;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int r = 4 * j + (lane >> 3), ch = lane & 7;
+          const uint4 w = *reinterpret_cast<const uint4*>(stage + r * 128 + ((ch ^ (r & 7)) << 4));
+          if (row0 + r < n)
+            *reinterpret_cast<uint4*>(out + ((size_t)(tc + row0 + r) * H + h) * kD + x.wh * 64 +
+                                      ch * 8) = w;
+        }
       }
       __syncwarp();
     };
@@ -290,6 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // it at the chunk's closing barrier and unwinds.
       bool bad = false;
       float gm;
+      if (OGATE && tid == 96)  // this chunk's gate rows into L2, read back in the next chunk
+        tma_prefetch_l2_3d(&maps.og, 0, h, (int)tc);
       {  // the chunk's operands (every thread reads gamma of its row now) and V tile
         bad |= !mbar_wait(full + s, ph_full[s], kWaitNs);
         bad |= !mbar_wait(bar_v, ph_v, kWaitNs);
@@ -309,6 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_run<kD>(x.tm + d_col(c), opWQ, opS, id_d, true);
         mma_commit_elect(x.bar_mma);
       }
+      if (OGATE && !u_rows && c > 0) load_gates(tc - kC, kC);  // for o_store(c - 1) below
       bad |= !mbar_wait(x.bar_mma, x.ph_mma, kWaitNs);
       x.ph_mma ^= 1u;
       fence_after_sync();
@@ -354,6 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!failed && nch > 0 && !u_rows) {
       const int64_t tl = t0 + (int64_t)(nch - 1) * kC;
+      load_gates(tl, (int)(t1 - tl));
       o_store(nch - 1, tl, (int)(t1 - tl));
     }
     if (failed) {
@@ -498,10 +541,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync();  // no CTA leaves while the cluster may still address its shared memory
 }
 
-template <bool CHANNEL, bool ERASE>
+template <bool CHANNEL, bool ERASE, bool OGATE = false>
 cudaError_t launch_typed(const gdr_shape& sh, const PrefillArgs& a, const TcMaps& maps, int ncl,
                          cudaStream_t s) {
-  auto kern = prefill_cluster_kernel<CHANNEL, ERASE>;
+  auto kern = prefill_cluster_kernel<CHANNEL, ERASE, OGATE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kClusterSmem);
   if (e != cudaSuccess) return e;
@@ -573,6 +616,9 @@ cudaError_t launch_prefill_cluster(const gdr_shape& sh, const PrefillArgs& a, co
   if (!erase)
     return ch ? launch_typed<true, false>(sh, a, maps, ncl, s)
               : launch_typed<false, false>(sh, a, maps, ncl, s);
+  if (a.og)
+    return ch ? launch_typed<true, true, true>(sh, a, maps, ncl, s)
+              : launch_typed<false, true, true>(sh, a, maps, ncl, s);
   return ch ? launch_typed<true, true>(sh, a, maps, ncl, s)
             : launch_typed<false, true>(sh, a, maps, ncl, s);
 }

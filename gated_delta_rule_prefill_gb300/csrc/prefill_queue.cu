@@ -211,9 +211,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       float v[64];
       tmem_ld64(x.tm + x.lane_base + d_col(c) + x.wh * 64, v);
       if (drow < n) {
-        __nv_bfloat16* dst = out + ((size_t)(tc + drow) * H + h) * kD + x.wh * 64;
+        const size_t o0 = ((size_t)(tc + drow) * H + h) * kD + x.wh * 64;
+        __nv_bfloat16* dst = out + o0;
+        const __nv_bfloat16* og = static_cast<const __nv_bfloat16*>(a.og);
 #pragma unroll
         for (int j = 0; j < 64; j += 8) {
+          if (og) gate8(v + j, og + o0 + j);
           __align__(16) __nv_bfloat162 hv[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) hv[i] = __floats2bfloat162_rn(v[j + 2 * i], v[j + 2 * i + 1]);

@@ -219,7 +219,10 @@ __global__ void __launch_bounds__(kSimtThreads) prefill_simt_kernel(PrefillArgs 
       }
       const float* mr = sM + r * L::LC;
       for (int j = 0; j <= r; ++j) acc0 = fmaf(mr[j], sUse[j * L::LV + c], acc0);
-      out[((size_t)(tc + r) * H + h) * D + vc0 + c] = from_f32<T>(acc0 + acc1);
+      const size_t oi = ((size_t)(tc + r) * H + h) * D + vc0 + c;
+      float o = acc0 + acc1;
+      if (a.og) o = gate_out(o, to_f32(static_cast<const T*>(a.og)[oi]));
+      out[oi] = from_f32<T>(o);
     }
     __syncthreads();
 

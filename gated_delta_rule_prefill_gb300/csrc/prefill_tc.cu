@@ -247,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     x.ph_mma ^= 1u;
     fence_after_sync();
     if (!ERASE && tn < t1) issue_v(tn);  // V is consumed
-    o_epilogue<DH>(x, out, tc, n, H, h, vc0);
+    o_epilogue<DH>(x, out, tc, n, H, h, vc0, kColWO, static_cast<const __nv_bfloat16*>(a.og));
     s_epilogue<DH>(x, sm + L::SS);
     fence_before_sync();
     if (__syncthreads_or(bad)) { failed = true; break; }
@@ -315,6 +315,9 @@ bool make_tc_maps(const gdr_shape& sh, const PrefillArgs& a, bool linear, TcMaps
                   CU_TENSOR_MAP_SWIZZLE_128B) &&
          make_map(&maps->q_sw, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, T, 64,
                   CU_TENSOR_MAP_SWIZZLE_128B);
+  if (ok && a.og)
+    ok = make_map(&maps->og, a.og, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, T, kD,
+                  CU_TENSOR_MAP_SWIZZLE_NONE);
   if (ok && !linear && sh.gate == GDR_GATE_CHANNEL)
     ok = make_map(&maps->alpha, a.alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, T, kD,
                   CU_TENSOR_MAP_SWIZZLE_NONE);

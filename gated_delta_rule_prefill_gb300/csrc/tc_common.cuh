@@ -254,6 +254,27 @@ __device__ inline void unit_lower_inverse(const float* sA, float* sT, float* sX,
   }
 }
 
+// The output gate for bf16 outputs: o * sigmoid(g) with sigmoid(g) = (1 + tanh(g / 2)) / 2 on
+// the hardware tanh approximation (absolute error ~2^-11, below bf16's 2^-8 relative rounding),
+// without the IEEE division of gate_out.
+__device__ __forceinline__ float gate_out_bf16(float o, float g) {
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * g));
+  return o * fmaf(0.5f, t, 0.5f);
+}
+
+// The output gate on 8 consecutive outputs: v[i] <- v[i] * sigmoid(g[i]) (g: 16-byte aligned bf16).
+__device__ __forceinline__ void gate8(float* v, const __nv_bfloat16* g) {
+  const uint4 u = *reinterpret_cast<const uint4*>(g);
+  const __nv_bfloat162* hg = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(hg[i]);
+    v[2 * i] = gate_out_bf16(v[2 * i], f.x);
+    v[2 * i + 1] = gate_out_bf16(v[2 * i + 1], f.y);
+  }
+}
+
 // 8 bf16 values (one 16-byte chunk) -> fp32
 __device__ __forceinline__ void ld_bf16x8(const __nv_bfloat16* p, float* x) {
   const uint4 u = *reinterpret_cast<const uint4*>(p);
@@ -269,6 +290,7 @@ __device__ __forceinline__ void ld_bf16x8(const __nv_bfloat16* p, float* x) {
 struct TcMaps {
   CUtensorMap q, k, v, alpha;
   CUtensorMap k_sw, q_sw;  // k, q in 64-channel SW128 boxes (linear attention)
+  CUtensorMap og;          // output gate g, 128-channel boxes (prefetched into L2)
 };
 
 
@@ -775,13 +797,15 @@ __device__ void u_epilogue(const TcCtx& x, unsigned char* uu) {
 // columns [vc0, vc0 + DV)
 template <int DH>
 __device__ void o_epilogue(const TcCtx& x, __nv_bfloat16* out, int64_t tc, int n, int H, int h,
-                           int vc0, uint32_t col = kColWO) {
+                           int vc0, uint32_t col = kColWO, const __nv_bfloat16* og = nullptr) {
   float v[DH];
   tmem_ld_half<DH>(x.tm + x.lane_base + col + x.wh * DH, v);
   if (x.m64ok && x.m64row < n) {
-    __nv_bfloat16* dst = out + ((size_t)(tc + x.m64row) * H + h) * kD + vc0 + x.wh * DH;
+    const size_t o0 = ((size_t)(tc + x.m64row) * H + h) * kD + vc0 + x.wh * DH;
+    __nv_bfloat16* dst = out + o0;
 #pragma unroll
     for (int j = 0; j < DH; j += 8) {
+      if (og) gate8(v + j, og + o0 + j);
       __align__(16) __nv_bfloat162 hv[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) hv[i] = __floats2bfloat162_rn(v[j + 2 * i], v[j + 2 * i + 1]);

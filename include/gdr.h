@@ -143,6 +143,21 @@ gdr_status gdr_linear_attn(const gdr_shape* shape, const void* q, const void* k,
                            void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * gdr_prefill_output_gate -- gdr_prefill with the KDA layer's output gate applied as the outputs
+ * are written: out = o * sigmoid(g), element by element.  dev.to §5 (Kimi K3 replaces the
+ * low-rank output gate by a full-rank, input-dependent one); the sigmoid multiplied into the
+ * output feature by feature follows heqinghuang §15's description of the attention layers' gate.
+ *   g: gate pre-activations [T_total, H, d_v], dtype = shape->dtype, 16-byte aligned, not `out`.
+ * Every other argument as gdr_prefill (bf16 outputs are gated after their rounding to bf16 on
+ * the tensor-core path: one more bf16 rounding).
+ */
+gdr_status gdr_prefill_output_gate(const gdr_shape* shape, const void* q, const void* k,
+                                   const void* v, const float* alpha, const float* beta,
+                                   const void* g, const float* S0, const int32_t* cu_seqlens,
+                                   void* out, float* S_final, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+
+/*
  * gdr_gated_linear_attn -- gated linear attention, the decayed additive update without the
  * delta rule's erase term: S_t = Diag(alpha_t) S_{t-1} + k_t v_t^T, o_t = S_t^T q_t.
  * engineermaxxing §05b (the scalar-gated additive update, RetNet / Mamba-2 / GLA lineage),

@@ -143,3 +143,9 @@ def test_gated_linear_argument_errors(lib):
                                          8, None)
     assert call(alpha=None) == INV
     assert call() == INV  # workspace too small (8 bytes): alpha present, beta not needed
+
+
+def test_output_gate_needs_g(lib):
+    """gdr_prefill_output_gate without its gate tensor is an argument error (no launch)."""
+    sh = _shape(n_seqs=1, total_tokens=64)
+    assert lib.gdr_prefill_output_gate(ctypes.byref(sh), *([None] * 11), 0, None) == 1
