@@ -9,6 +9,10 @@ It shares no code with the GPU library and never imports it.
   linear_attn(...)  S <- S + k_t v_t^T;  o_t = S^T q_t   (alpha = 1, no erase term, no beta).
   gated_linear(...) S <- Diag(alpha_t) S + k_t v_t^T;  o_t = S^T q_t   (no erase term, no beta;
                     engineermaxxing §05b, heqinghuang §11; per key channel as dev.to §5).
+  layer_prologue(xq, xk, a, b)  the layer's input maps (numpy fp64): q = normalize(silu(xq)),
+                    k = normalize(silu(xk)) over d_k (x / max(||x||, 1e-12)) and beta = sigmoid(b)
+                    as heqinghuang §09 writes them; alpha = sigmoid(a), scalar per head as
+                    engineermaxxing §05c, per channel as its §06b.
   output_gate(o, g) o * sigmoid(g), element by element (numpy fp64): the KDA layer's output
                     gate (dev.to §5: full rank and input dependent in K3; a sigmoid multiplied
                     into the output feature by feature, as heqinghuang §15 describes the gate of
@@ -125,6 +129,25 @@ def gated_linear(q, k, v, alpha, S0=None, cu_seqlens=None, pairs=None, threads=N
     """Gated linear attention: S <- Diag(alpha_t) S + k_t v_t^T (per-channel alpha [T,H,d_k] or
     scalar alpha [T,H]), o_t = S^T q_t; returns (out, S_final) in fp64."""
     return _run(2, q, k, v, alpha, None, S0, cu_seqlens, pairs, threads)
+
+
+def _sigmoid(x):
+    return 1.0 / (1.0 + np.exp(-x))
+
+
+def layer_prologue(xq, xk, a, b):
+    """The layer's maps from raw projections to the rule's inputs, in fp64: returns
+    (q, k, alpha, beta) with q = xq*sigmoid(xq) / max(||.||, 1e-12) over the last axis (likewise
+    k), alpha = sigmoid(a) (per channel or scalar, as a's shape), beta = sigmoid(b)."""
+    out = []
+    for x in (xq, xk):
+        x = np.asarray(x, dtype=np.float64)
+        s = x * _sigmoid(x)
+        n = np.sqrt(np.sum(s * s, axis=-1, keepdims=True))
+        out.append(s / np.maximum(n, 1e-12))
+    out.append(_sigmoid(np.asarray(a, dtype=np.float64)))
+    out.append(_sigmoid(np.asarray(b, dtype=np.float64)))
+    return tuple(out)
 
 
 def output_gate(o, g):

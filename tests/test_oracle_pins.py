@@ -414,3 +414,26 @@ def test_output_gate_closed_forms():
                                atol=1e-15)
     np.testing.assert_allclose(oracle.output_gate(o, np.full(4, 50.0)), o, rtol=1e-15)
     np.testing.assert_allclose(oracle.output_gate(o, np.full(4, -50.0)), 0 * o, atol=1e-20)
+
+
+# ------------------------------------------------------------------------------------------
+# the layer prologue (raw projections -> q, k, alpha, beta): closed forms
+# ------------------------------------------------------------------------------------------
+def test_layer_prologue_closed_forms():
+    """Unit-length q and k along silu(x) = x / (1 + e^-x); alpha = sigmoid(a) =
+    exp(-softplus(-a)); beta = sigmoid(b) with sigmoid(0) = 1/2; silu(0) = 0 rows stay zero."""
+    rng = np.random.default_rng(31)
+    xq = rng.normal(0, 1.5, (5, 3, 8))
+    xk = rng.normal(0, 1.5, (5, 3, 8))
+    a = rng.normal(4, 1, (5, 3, 8))
+    b = rng.normal(0, 1, (5, 3))
+    q, k, al, be = oracle.layer_prologue(xq, xk, a, b)
+    for x, y in ((xq, q), (xk, k)):
+        np.testing.assert_allclose(np.linalg.norm(y, axis=-1), 1.0, atol=1e-14)
+        silu = x / (1.0 + np.exp(-x))
+        cos = np.sum(y * silu, axis=-1) / np.linalg.norm(silu, axis=-1)
+        np.testing.assert_allclose(cos, 1.0, atol=1e-14)
+    np.testing.assert_allclose(al, np.exp(-np.log1p(np.exp(-a))), atol=1e-15)
+    np.testing.assert_allclose(oracle.layer_prologue(xq, xk, np.zeros(1), np.zeros(1))[3], 0.5)
+    z = oracle.layer_prologue(np.zeros((1, 1, 4)), xk[:1, :1, :4], a[:1], b[:1])[0]
+    assert np.all(z == 0.0)
