@@ -89,6 +89,8 @@ def source_digest(files):
 # variant and its gated-linear pass run the clustered kernel)
 KERNEL_SOURCES = {"gated_linear_attn": ["prefill_cluster.cu", "tc_common.cuh", "umma.cuh"],
                   "prefill_output_gate": ["prefill_cluster.cu", "tc_common.cuh", "umma.cuh"],
+                  "prefill_prologue": ["prefill_cluster.cu", "tc_common.cuh", "umma.cuh"],
+                  "layer_prologue": ["prologue.cu", "gdr_internal.cuh"],
                   "prefill": ["prefill_cluster.cu", "tc_common.cuh", "umma.cuh"],
                   "linear_attn": ["linear_tc.cu", "tc_common.cuh", "umma.cuh"],
                   "decode": ["decode.cu"]}
@@ -390,7 +392,56 @@ def run_gpu(args):
     g1.record(stream)
     torch.cuda.synchronize()
     og_ms = max_over_ranks([g0.elapsed_time(g1) / gla_steps], dev, world)[0]
-    del out_g, Sf_g, gate_in
+    del gate_in
+
+    # ---- the prefill with the layer prologue on load (raw projections in: q, k =
+    # normalize(silu(.)), alpha, beta = sigmoid(.) inside the kernels), also outside the step
+    R = gi.device_full(wp, dev, seed_offset=7 + rank, raw=True)
+
+    def pre_prologue():
+        g.gdr_prefill(R["q"], R["k"], P["v"], R["alpha"], R["beta"], S0=P["S0"],
+                      cu_seqlens=P["cu_seqlens"], out=out_g, S_final=Sf_g, workspace=ws,
+                      prologue=True)
+
+    for _ in range(3):
+        pre_prologue()
+    torch.cuda.synchronize()
+    g0.record(stream)
+    for _ in range(gla_steps):
+        pre_prologue()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    pro_ms = max_over_ranks([g0.elapsed_time(g1) / gla_steps], dev, world)[0]
+
+    # ... and unfused: the prologue as its own pass (raw -> mapped tensors in HBM), then the
+    # prefill on the mapped tensors; both kernels timed per step, the pass also on its own
+    M = {kk: torch.empty_like(R[kk]) for kk in ("q", "k", "alpha", "beta")}
+
+    def pass_only():
+        g.gdr_layer_prologue(R["q"], R["k"], R["alpha"], R["beta"], q=M["q"], k=M["k"],
+                             alpha=M["alpha"], beta=M["beta"])
+
+    def pre_unfused():
+        pass_only()
+        g.gdr_prefill(M["q"], M["k"], P["v"], M["alpha"], M["beta"], S0=P["S0"],
+                      cu_seqlens=P["cu_seqlens"], out=out_g, S_final=Sf_g, workspace=ws)
+
+    for _ in range(3):
+        pre_unfused()
+    torch.cuda.synchronize()
+    g0.record(stream)
+    for _ in range(gla_steps):
+        pre_unfused()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    unf_ms = max_over_ranks([g0.elapsed_time(g1) / gla_steps], dev, world)[0]
+    g0.record(stream)
+    for _ in range(gla_steps):
+        pass_only()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    lp_ms = max_over_ranks([g0.elapsed_time(g1) / gla_steps], dev, world)[0]
+    del out_g, Sf_g, R, M
 
     # ---- end to end through the public API with host buffers (prefill), rank-local
     host_in = {k: P[k].cpu().pin_memory() for k in ("q", "k", "v", "alpha", "beta", "S0")}
@@ -461,6 +512,11 @@ def run_gpu(args):
         "prefill_output_gate": roof("prefill_output_gate",
                                     prefill_bytes(T, H, d, wp.n_seqs) + T * H * d * 2,
                                     prefill_flops(T, H, d), og_ms / 1e3),
+        "prefill_prologue": roof("prefill_prologue", prefill_bytes(T, H, d, wp.n_seqs),
+                                 prefill_flops(T, H, d), pro_ms / 1e3),
+        # read xq, xk (bf16), a (fp32 per channel), b; write q, k, alpha, beta
+        "layer_prologue": roof("layer_prologue", 2 * T * H * (2 * d * 2 + d * 4 + 4), 0.0,
+                               lp_ms / 1e3),
     }
     dominant = max(kern, key=lambda k: kern[k]["launch_us"])
     main_roof = {k: kern[dominant][k] for k in ("bound", "achieved", "peak", "unit", "frac",
@@ -482,6 +538,8 @@ def run_gpu(args):
         "linear_attn_tokens_per_s": linear_tps,
         "gated_linear_attn_tokens_per_s": job_tokens_per_s(n, T, gla_ms / 1e3),
         "prefill_output_gate_tokens_per_s": job_tokens_per_s(n, T, og_ms / 1e3),
+        "prefill_prologue_tokens_per_s": job_tokens_per_s(n, T, pro_ms / 1e3),
+        "prefill_unfused_prologue_tokens_per_s": job_tokens_per_s(n, T, unf_ms / 1e3),
         "roofline": main_roof,
         "kernels": kern,
         "kernels_outside_step": kern_extra,

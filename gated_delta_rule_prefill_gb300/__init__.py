@@ -11,6 +11,10 @@ library's CUDA kernels; there is no Python or CPU fallback.
     gdr_prefill_workspace_size(n_seqs, H, d_k, d_v, dtype)  /  gdr_workspace_status(workspace)
     gdr_prefill_host(q, k, v, alpha, beta, ...)  -- host (CPU) tensors in and out, copies inside
     gdr_prefill_host_buffer_size(n_seqs, H, total_tokens, d_k, d_v, dtype, gate, piece_tokens)
+    gdr_layer_prologue(xq, xk, a=None, b=None, q=None, k=None, alpha=None, beta=None)
+
+prologue=True (GDR_FLAG_LAYER_PROLOGUE) makes q, k, alpha, beta the layer's raw projections: the
+kernels form q, k = normalize(silu(.)) and alpha, beta = sigmoid(.) as they load them.
 """
 from __future__ import annotations
 
@@ -20,11 +24,11 @@ import torch
 
 from . import _abi
 from ._abi import (GDR_BF16, GDR_F32, GDR_FLAG_FORCE_SIMT, GDR_FLAG_NO_CLUSTER, GDR_FLAG_PREFER_QUEUE,
-                   GDR_GATE_CHANNEL, GDR_GATE_SCALAR,
+                   GDR_FLAG_LAYER_PROLOGUE, GDR_GATE_CHANNEL, GDR_GATE_SCALAR,
                    GdrError, GdrShape)
 
 __all__ = ["gdr_prefill", "gdr_prefill_output_gate", "gdr_decode_step", "gdr_linear_attn",
-           "gdr_gated_linear_attn",
+           "gdr_gated_linear_attn", "gdr_layer_prologue",
            "gdr_prefill_workspace_size",
            "gdr_workspace_status", "gdr_prefill_host", "gdr_prefill_host_buffer_size",
            "make_shape", "GdrError"]
@@ -73,7 +77,7 @@ def _workspace(n_seqs, H, d_k, d_v, dtype, device, workspace):
 
 def _prefill_like(kind, q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, workspace,
                   chunk_size, force_simt, stream, want_final, no_cluster=False,
-                  prefer_queue=False, g=None):
+                  prefer_queue=False, g=None, prologue=False):
     """kind: "delta" (gdr_prefill), "linear" (gdr_linear_attn) or "gla"
     (gdr_gated_linear_attn)."""
     linear = kind == "linear"
@@ -102,7 +106,8 @@ def _prefill_like(kind, q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, work
     ws = _workspace(n_seqs, H, dk, dv, "bf16" if dtype == GDR_BF16 else "f32", q.device,
                     workspace)
     flags = ((GDR_FLAG_FORCE_SIMT if force_simt else 0) | (GDR_FLAG_NO_CLUSTER if no_cluster else 0)
-             | (GDR_FLAG_PREFER_QUEUE if prefer_queue else 0))
+             | (GDR_FLAG_PREFER_QUEUE if prefer_queue else 0)
+             | (GDR_FLAG_LAYER_PROLOGUE if prologue else 0))
     sh = make_shape(n_seqs, H, T, dk, dv, dtype, gate, chunk_size, flags)
     lib = _abi.load()
     if linear:
@@ -131,21 +136,23 @@ def _prefill_like(kind, q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, work
 
 def gdr_prefill(q, k, v, alpha, beta, S0=None, cu_seqlens=None, out=None, S_final=None,
                 workspace=None, chunk_size=0, force_simt=False, stream=None, want_final=True,
-                no_cluster=False, prefer_queue=False):
+                no_cluster=False, prefer_queue=False, prologue=False):
     """Chunked packed-varlen prefill.  q,k [T,H,d_k], v [T,H,d_v] (fp32 or bf16); alpha
     [T,H,d_k] or [T,H] fp32; beta [T,H] fp32; S0 [N,H,d_k,d_v] fp32 or None; cu_seqlens int32
     [N+1] or None.  Returns (out [T,H,d_v], S_final [N,H,d_k,d_v] or None)."""
     return _prefill_like("delta", q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, workspace,
-                         chunk_size, force_simt, stream, want_final, no_cluster, prefer_queue)
+                         chunk_size, force_simt, stream, want_final, no_cluster, prefer_queue,
+                         prologue=prologue)
 
 
 def gdr_prefill_output_gate(q, k, v, alpha, beta, g, S0=None, cu_seqlens=None, out=None,
                             S_final=None, workspace=None, chunk_size=0, force_simt=False,
-                            stream=None, want_final=True, no_cluster=False, prefer_queue=False):
+                            stream=None, want_final=True, no_cluster=False, prefer_queue=False,
+                            prologue=False):
     """gdr_prefill with the output gate: out = o * sigmoid(g), g [T,H,d_v] in q's dtype."""
     return _prefill_like("delta", q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, workspace,
                          chunk_size, force_simt, stream, want_final, no_cluster, prefer_queue,
-                         g=g)
+                         g=g, prologue=prologue)
 
 
 def _check_host(t, name, dtype=None):
@@ -168,7 +175,8 @@ def gdr_prefill_host_buffer_size(n_seqs, H, total_tokens, d_k=128, d_v=128, dtyp
 
 
 def gdr_prefill_host(q, k, v, alpha, beta, S0=None, cu_seqlens=None, out=None, S_final=None,
-                     piece_tokens=0, buffer=None, device=None, stream=None, want_final=True):
+                     piece_tokens=0, buffer=None, device=None, stream=None, want_final=True,
+                     prologue=False):
     """gdr_prefill on host (CPU) tensors -- pinned memory lets the copies overlap the kernels.
     q, k, v, alpha, beta, S0, out, S_final and cu_seqlens (int32) are CPU tensors; `buffer` is
     a CUDA uint8 tensor of gdr_prefill_host_buffer_size bytes (allocated on `device` if None).
@@ -192,7 +200,8 @@ def gdr_prefill_host(q, k, v, alpha, beta, S0=None, cu_seqlens=None, out=None, S
     if S_final is None and want_final:
         S_final = torch.empty((n_seqs, H, dk, dv), dtype=torch.float32).pin_memory()
     _check_host(S_final, "S_final", torch.float32)
-    sh = make_shape(n_seqs, H, T, dk, dv, dtype, gate)
+    sh = make_shape(n_seqs, H, T, dk, dv, dtype, gate, 0,
+                    GDR_FLAG_LAYER_PROLOGUE if prologue else 0)
     lib = _abi.load()
     if buffer is None:
         need = int(lib.gdr_prefill_host_buffer_size(ctypes.byref(sh), int(piece_tokens)))
@@ -216,14 +225,48 @@ def gdr_linear_attn(q, k, v, S0=None, cu_seqlens=None, out=None, S_final=None, w
 
 def gdr_gated_linear_attn(q, k, v, alpha, S0=None, cu_seqlens=None, out=None, S_final=None,
                           workspace=None, chunk_size=0, force_simt=False, stream=None,
-                          want_final=True, no_cluster=False):
+                          want_final=True, no_cluster=False, prologue=False):
     """Gated linear attention: S <- Diag(alpha) S + k v^T (no erase, no beta); alpha [T,H,d_k]
     or [T,H] fp32.  Returns (out, S_final)."""
     return _prefill_like("gla", q, k, v, alpha, None, S0, cu_seqlens, out, S_final, workspace,
-                         chunk_size, force_simt, stream, want_final, no_cluster)
+                         chunk_size, force_simt, stream, want_final, no_cluster,
+                         prologue=prologue)
 
 
-def gdr_decode_step(q, k, v, alpha, beta, S_inout, out=None, stream=None):
+def gdr_layer_prologue(xq, xk, a=None, b=None, q=None, k=None, alpha=None, beta=None,
+                       stream=None):
+    """The layer prologue as its own pass: q, k = normalize(silu(xq, xk)) over d_k, alpha =
+    sigmoid(a) ([T,H,d_k] or [T,H]), beta = sigmoid(b) ([T,H]).  Outputs are allocated when None
+    and may be the inputs themselves (in place).  Returns (q, k, alpha, beta)."""
+    T, H, dk = xq.shape
+    dtype = _DT.get(xq.dtype)
+    if dtype is None:
+        raise ValueError("xq/xk must be float32 or bfloat16")
+    _check(xq, "xq", xq.dtype)
+    _check(xk, "xk", xq.dtype)
+    _check(a, "a", torch.float32)
+    _check(b, "b", torch.float32)
+    q = torch.empty_like(xq) if q is None else q
+    k = torch.empty_like(xk) if k is None else k
+    if a is not None and alpha is None:
+        alpha = torch.empty_like(a)
+    if b is not None and beta is None:
+        beta = torch.empty_like(b)
+    for t, n in ((q, "q"), (k, "k")):
+        _check(t, n, xq.dtype)
+    _check(alpha, "alpha", torch.float32)
+    _check(beta, "beta", torch.float32)
+    gate = GDR_GATE_CHANNEL if (a is None or a.dim() == 3) else GDR_GATE_SCALAR
+    sh = make_shape(1, H, T, dk, dk, dtype, gate)
+    rc = _abi.load().gdr_layer_prologue(ctypes.byref(sh), _ptr(xq), _ptr(xk), _ptr(a), _ptr(b),
+                                        _ptr(q), _ptr(k), _ptr(alpha), _ptr(beta),
+                                        _stream(stream))
+    if rc != 0:
+        raise GdrError(rc, "gdr_layer_prologue")
+    return q, k, alpha, beta
+
+
+def gdr_decode_step(q, k, v, alpha, beta, S_inout, out=None, stream=None, prologue=False):
     """One token per sequence; S_inout [N,H,d_k,d_v] fp32 is updated in place.  Returns out."""
     N, H, dk = q.shape
     dv = v.shape[2]
@@ -239,7 +282,7 @@ def gdr_decode_step(q, k, v, alpha, beta, S_inout, out=None, stream=None):
         out = torch.empty((N, H, dv), dtype=q.dtype, device=q.device)
     _check(out, "out", q.dtype)
     gate = GDR_GATE_CHANNEL if alpha.dim() == 3 else GDR_GATE_SCALAR
-    sh = make_shape(N, H, N, dk, dv, dtype, gate)
+    sh = make_shape(N, H, N, dk, dv, dtype, gate, 0, GDR_FLAG_LAYER_PROLOGUE if prologue else 0)
     rc = _abi.load().gdr_decode_step(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
                                      _ptr(beta), _ptr(S_inout), _ptr(out), _stream(stream))
     if rc != 0:

@@ -58,7 +58,8 @@ gdr_status check_shape(const gdr_shape* sh, bool need_gate) {
   if (sh->dtype != GDR_F32 && sh->dtype != GDR_BF16) return GDR_ERR_INVALID_ARG;
   if (need_gate && sh->gate != GDR_GATE_SCALAR && sh->gate != GDR_GATE_CHANNEL)
     return GDR_ERR_INVALID_ARG;
-  if (sh->chunk_size < 0 || (sh->flags & ~(GDR_FLAG_FORCE_SIMT | GDR_FLAG_NO_CLUSTER | GDR_FLAG_PREFER_QUEUE))) return GDR_ERR_INVALID_ARG;
+  if (sh->chunk_size < 0 || (sh->flags & ~(GDR_FLAG_FORCE_SIMT | GDR_FLAG_NO_CLUSTER | GDR_FLAG_PREFER_QUEUE |
+                                                GDR_FLAG_LAYER_PROLOGUE))) return GDR_ERR_INVALID_ARG;
   if (sh->d_k != sh->d_v || (sh->d_k != 64 && sh->d_k != 128)) return GDR_ERR_UNSUPPORTED;
   // grid sizes stay within 32-bit block counts
   if ((int64_t)sh->n_seqs * sh->H * 4 > (int64_t)INT32_MAX) return GDR_ERR_UNSUPPORTED;
@@ -72,6 +73,8 @@ gdr_status prefill_common(const gdr_shape* sh, const void* q, const void* k, con
   const bool linear = kind == kKindLinear;
   gdr_status st = check_shape(sh, !linear);
   if (st != GDR_OK) return st;
+  const bool prologue = (sh->flags & GDR_FLAG_LAYER_PROLOGUE) != 0;
+  if (linear && prologue) return GDR_ERR_UNSUPPORTED;
   if (!cu && sh->n_seqs != 1) return GDR_ERR_INVALID_ARG;
   if (sh->total_tokens > 0) {
     if (!q || !k || !v || !out) return GDR_ERR_INVALID_ARG;
@@ -98,7 +101,7 @@ gdr_status prefill_common(const gdr_shape* sh, const void* q, const void* k, con
            WorkspaceLayout::flag_bytes(WorkspaceLayout::ring_pairs(*sh));
   }
   PrefillArgs a{sh->n_seqs, sh->H, sh->total_tokens, q, k, v, alpha, beta, S0, cu,
-                out, S_final, order, status, ring_flags, ring, og};
+                out, S_final, order, status, ring_flags, ring, og, prologue};
   prep_kernel<<<1, kPrepThreads, 0, s>>>(cu, sh->n_seqs, sh->total_tokens, order, status);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess)
@@ -174,6 +177,24 @@ gdr_status gdr_decode_step(const gdr_shape* shape, const void* q, const void* k,
   if (out == q || out == k || out == v || (const void*)S_inout == out) return GDR_ERR_INVALID_ARG;
   cudaError_t e = gdr::launch_decode(*shape, q, k, v, alpha, beta, S_inout, out,
                                      (cudaStream_t)stream);
+  return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+}
+
+gdr_status gdr_layer_prologue(const gdr_shape* shape, const void* xq, const void* xk,
+                              const float* a, const float* b, void* q, void* k, float* alpha,
+                              float* beta, void* stream) {
+  gdr_status st = gdr::check_shape(shape, a != nullptr);
+  if (st != GDR_OK) return st;
+  if (shape->total_tokens == 0) return GDR_OK;
+  if (!xq || !xk || !q || !k) return GDR_ERR_INVALID_ARG;
+  if (!a != !alpha || !b != !beta) return GDR_ERR_INVALID_ARG;
+  const void* ptrs[] = {xq, xk, a, b, q, k, alpha, beta};
+  for (const void* p : ptrs)
+    if (p && !gdr::aligned16(p)) return GDR_ERR_INVALID_ARG;
+  // outputs either are their own input (in place) or do not meet another operand's start
+  if ((q != xq && (q == xk || q == k)) || (k != xk && k == xq)) return GDR_ERR_INVALID_ARG;
+  cudaError_t e = gdr::launch_layer_prologue(*shape, xq, xk, a, b, q, k, alpha, beta,
+                                             (cudaStream_t)stream);
   return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }
 

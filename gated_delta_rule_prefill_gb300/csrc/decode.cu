@@ -43,11 +43,12 @@ template <int D, typename T, bool CHANNEL>
 __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
     decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                   const float* __restrict__ alpha, const float* __restrict__ beta,
-                  float* __restrict__ S, T* __restrict__ out) {
+                  float* __restrict__ S, T* __restrict__ out, bool prologue) {
   constexpr int CPL = D / 32;           // columns per lane
   constexpr int RPW = D / kDecodeWarps;  // rows per warp
   __shared__ float s_q[D], s_k[D], s_a[D], s_v[D], s_delta[D];
   __shared__ float s_red_k[kDecodeWarps][D], s_red_q[kDecodeWarps][D];
+  __shared__ float s_ss[2][D / 32];
 
   const int pair = blockIdx.x;  // n * H + h
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -59,15 +60,35 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
 #pragma unroll
   for (int r = 0; r < RPW; ++r) vload(x[r], Sp + (size_t)(warp * RPW + r) * D + col0);
 
-  // 2. the token's vectors
+  // 2. the token's vectors; with the layer prologue (heqinghuang "gpt2-to-kimi" §09,
+  // engineermaxxing §05c/§06b) q, k are the silu of their projections, to be scaled to unit
+  // length by iq, ik below, and alpha the sigmoid of its projection
   if (tid < D) {
     const size_t o = (size_t)pair * D + tid;
-    s_q[tid] = to_f32(q[o]);
-    s_k[tid] = to_f32(k[o]);
+    float qv = to_f32(q[o]), kv = to_f32(k[o]), av = CHANNEL ? alpha[o] : alpha[pair];
+    if (prologue) {
+      qv = silu_f(qv), kv = silu_f(kv), av = sigmoid_f(av);
+      float sq = qv * qv, sk = kv * kv;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        sq += __shfl_xor_sync(0xffffffffu, sq, off);
+        sk += __shfl_xor_sync(0xffffffffu, sk, off);
+      }
+      if (lane == 0) s_ss[0][warp] = sq, s_ss[1][warp] = sk;
+    }
+    s_q[tid] = qv;
+    s_k[tid] = kv;
     s_v[tid] = to_f32(v[o]);
-    s_a[tid] = CHANNEL ? alpha[o] : alpha[pair];
+    s_a[tid] = av;
   }
   __syncthreads();
+  float iq = 1.f, ik = 1.f;
+  if (prologue) {
+    float sq = 0.f, sk = 0.f;
+#pragma unroll
+    for (int w = 0; w < D / 32; ++w) sq += s_ss[0][w], sk += s_ss[1][w];
+    iq = inv_norm(sq), ik = inv_norm(sk);
+  }
 
   // 3. fade the rows and accumulate the two column reads
   float yk[CPL], yq[CPL];
@@ -76,7 +97,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
 #pragma unroll
   for (int r = 0; r < RPW; ++r) {
     const int row = warp * RPW + r;
-    const float a = s_a[row], kr = s_k[row], qr = s_q[row];
+    const float a = s_a[row], kr = s_k[row] * ik, qr = s_q[row] * iq;
 #pragma unroll
     for (int c = 0; c < CPL; ++c) {
       x[r][c] *= a;
@@ -95,6 +116,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
   for (int c = lane; c < D; c += 32) qk = fmaf(s_q[c], s_k[c], qk);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) qk += __shfl_xor_sync(0xffffffffu, qk, off);
+  qk *= iq * ik;
   __syncthreads();
 
   // 4. finish the columns: delta and the read-out
@@ -105,7 +127,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
       tk += s_red_k[w][tid];
       tq += s_red_q[w][tid];
     }
-    const float d = beta[pair] * (s_v[tid] - tk);
+    const float bt = prologue ? sigmoid_f(beta[pair]) : beta[pair];
+    const float d = bt * (s_v[tid] - tk);
     s_delta[tid] = d;
     out[(size_t)pair * D + tid] = from_f32<T>(fmaf(qk, d, tq));
   }
@@ -117,7 +140,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
   for (int c = 0; c < CPL; ++c) dl[c] = s_delta[col0 + c];
 #pragma unroll
   for (int r = 0; r < RPW; ++r) {
-    const float kr = s_k[warp * RPW + r];
+    const float kr = s_k[warp * RPW + r] * ik;
 #pragma unroll
     for (int c = 0; c < CPL; ++c) x[r][c] = fmaf(kr, dl[c], x[r][c]);
     vstore(Sp + (size_t)(warp * RPW + r) * D + col0, x[r]);
@@ -129,12 +152,13 @@ cudaError_t launch_typed(const gdr_shape& sh, const void* q, const void* k, cons
                          const float* alpha, const float* beta, float* S, void* out,
                          cudaStream_t s) {
   const unsigned grid = (unsigned)sh.n_seqs * (unsigned)sh.H;
+  const bool prologue = (sh.flags & GDR_FLAG_LAYER_PROLOGUE) != 0;
   if (sh.gate == GDR_GATE_CHANNEL)
     decode_kernel<D, T, true><<<grid, kDecodeWarps * 32, 0, s>>>(
-        (const T*)q, (const T*)k, (const T*)v, alpha, beta, S, (T*)out);
+        (const T*)q, (const T*)k, (const T*)v, alpha, beta, S, (T*)out, prologue);
   else
     decode_kernel<D, T, false><<<grid, kDecodeWarps * 32, 0, s>>>(
-        (const T*)q, (const T*)k, (const T*)v, alpha, beta, S, (T*)out);
+        (const T*)q, (const T*)k, (const T*)v, alpha, beta, S, (T*)out, prologue);
   return cudaGetLastError();
 }
 

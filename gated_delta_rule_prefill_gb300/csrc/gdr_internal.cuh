@@ -73,7 +73,19 @@ struct PrefillArgs {
   uint32_t* ring_flags;  // work-queue prefill: counter, ready, loaded (null: not available)
   unsigned char* ring;   // work-queue prefill: operand slots
   const void* og = nullptr;  // output gate g [T, H, d_v] (dtype of out): out = o * sigmoid(g)
+  // q, k, alpha, beta hold the layer's raw projections: the kernels apply the layer prologue
+  // (q, k = normalize(silu(.)), alpha, beta = sigmoid(.)) as they load them.
+  bool prologue = false;
 };
+
+// The layer prologue's maps in fp32: sigmoid(x) = 1 / (1 + e^-x) (the exponent capped at 80 so
+// the fast division never meets an infinite divisor), silu(x) = x sigmoid(x), and the scale
+// 1 / max(||x||, 1e-12) of the L2 normalisation from the squared norm ss.
+__device__ __forceinline__ float sigmoid_f(float x) {
+  return __fdividef(1.f, 1.f + __expf(fminf(-x, 80.f)));
+}
+__device__ __forceinline__ float silu_f(float x) { return x * sigmoid_f(x); }
+__device__ __forceinline__ float inv_norm(float ss) { return ss >= 1e-24f ? rsqrtf(ss) : 1e12f; }
 
 // The output gate of one element: o * sigmoid(g).
 __device__ __forceinline__ float gate_out(float o, float g) { return o / (1.f + __expf(-g)); }
@@ -121,6 +133,9 @@ cudaError_t launch_prefill_simt(const gdr_shape& sh, const PrefillArgs& a, int k
 bool prefill_tc_supported(const gdr_shape& sh);
 cudaError_t launch_prefill_tc(const gdr_shape& sh, const PrefillArgs& a, int kind,
                               cudaStream_t s);
+cudaError_t launch_layer_prologue(const gdr_shape& sh, const void* xq, const void* xk,
+                                  const float* a, const float* b, void* q, void* k, float* alpha,
+                                  float* beta, cudaStream_t s);
 cudaError_t launch_decode(const gdr_shape& sh, const void* q, const void* k, const void* v,
                           const float* alpha, const float* beta, float* S, void* out,
                           cudaStream_t s);

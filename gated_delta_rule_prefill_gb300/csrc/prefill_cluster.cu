@@ -142,7 +142,9 @@ __device__ bool wait_consumed(const uint32_t* cons, uint32_t need) {
 // CTA's slots hold T' = I and W = 0 from the start, so its U is V itself and its code is
 // unchanged, and a chunk's hand-over shrinks from 66 KB to 41 KB.
 // OGATE: the output gate out = o * sigmoid(g) on the stored output rows (a.og).
-template <bool CHANNEL, bool ERASE = true, bool OGATE = false>
+// PRO: the layer prologue on load (a.prologue): the helpers map the staged raw q, k, alpha tiles
+// and the scalar gates before the gate stage.
+template <bool CHANNEL, bool ERASE = true, bool OGATE = false, bool PRO = false>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_cluster_kernel(const __grid_constant__ TcMaps maps, const PrefillArgs a, int ncl) {
   constexpr bool kAlphaTile = CHANNEL;
@@ -204,6 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     cta_sync_tc();
     cluster_sync();  // every CTA's barriers and counters are initialised
     TcCtx x = make_ctx(sm, *tslot, bars + 3);
+    x.prologue = PRO;
     uint32_t ph_v = 0, ph_full[2] = {0, 0};
     __nv_bfloat16* __restrict__ out = static_cast<__nv_bfloat16*>(a.out);
     auto issue_v = [&](int64_t tc) {
@@ -430,6 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     cta_sync_tc();
     cluster_sync();
     TcCtx x = make_ctx(sm, *tslot, bars + 2);
+    x.prologue = PRO;
     zero_upper_tp(sm + L::TT, tid);
     uint32_t ph_qk = 0, ph_a = 0;
     const uint32_t chain_full = map_to(smem_u32(sm + ChainSmem::BARS), 0);
@@ -468,9 +472,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n = (int)((t1 - tc) < (int64_t)kC ? (t1 - tc) : (int64_t)kC);
       const int cn = c + nh;  // this helper's next chunk
       const int64_t tn = t0 + (int64_t)cn * kC;
-      if (tid < kC) {
-        sBeta[tid] = nb_beta;
-        sAlpha[tid] = nb_alpha;
+      if (tid < kC) {  // (the layer prologue maps the live tokens' raw gates here, not at the load)
+        const bool pro = PRO && tid < n;
+        sBeta[tid] = pro && ERASE ? sigmoid_ftz(nb_beta) : nb_beta;
+        sAlpha[tid] = pro && !CHANNEL ? sigmoid_ftz(nb_alpha) : nb_alpha;
       }
       if (cn < nch) load_scalars(tn, nb_beta, nb_alpha);
       {  // the chunk's q, k (and alpha) tiles: per-thread waits, one barrier
@@ -544,7 +549,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <bool CHANNEL, bool ERASE, bool OGATE = false>
 cudaError_t launch_typed(const gdr_shape& sh, const PrefillArgs& a, const TcMaps& maps, int ncl,
                          cudaStream_t s) {
-  auto kern = prefill_cluster_kernel<CHANNEL, ERASE, OGATE>;
+  auto kern = a.prologue ? prefill_cluster_kernel<CHANNEL, ERASE, OGATE, true>
+                         : prefill_cluster_kernel<CHANNEL, ERASE, OGATE, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kClusterSmem);
   if (e != cudaSuccess) return e;

@@ -162,6 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     cta_sync_tc();
     TcCtx x = make_ctx(sm, *tslot, bars + 3);
+    x.prologue = a.prologue;
     // The loader thread (warp 2, lane 0) loads chunk cc's ring slot into local slot cc & 1 once a
     // helper has marked it ready.  Warp 0 issues the MMAs and warp 2 stores O rows while they run,
     // so a look at a ring flag (a global-memory round trip) is started at the top of a chunk and
@@ -346,6 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     cta_sync_tc();
     TcCtx x = make_ctx(sm, *tslot, bars + 2);
+    x.prologue = a.prologue;
     zero_upper_tp(sm + L::TT, tid);
     uint32_t ph_qk = 0, ph_a = 0;
     bool failed = false;
@@ -431,9 +433,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 #pragma unroll 1
     while (cur.p >= 0) {
-      if (tid < kC) {
-        sBeta[tid] = nb_beta;
-        sAlpha[tid] = nb_alpha;
+      if (tid < kC) {  // (the layer prologue maps the live tokens' raw gates here, not at the load)
+        const bool pro = a.prologue && tid < cur.n;
+        sBeta[tid] = pro ? sigmoid_ftz(nb_beta) : nb_beta;
+        sAlpha[tid] = pro && !CHANNEL ? sigmoid_ftz(nb_alpha) : nb_alpha;
       }
       // hand the previous chunk over before waiting on any chain (a chain may need exactly that
       // chunk to move on): its ring stores are visible before its flag is set

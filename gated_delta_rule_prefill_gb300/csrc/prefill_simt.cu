@@ -102,11 +102,16 @@ __global__ void __launch_bounds__(kSimtThreads) prefill_simt_kernel(PrefillArgs 
       const int r = i / D, c = i % D;
       const bool ok = r < n;
       const size_t o = ((size_t)(tc + r) * H + h) * D + c;
-      sQ[r * L::LD + c] = ok ? to_f32(q[o]) : 0.f;
-      sK[r * L::LD + c] = ok ? to_f32(k[o]) : 0.f;
+      float qv = ok ? to_f32(q[o]) : 0.f, kv = ok ? to_f32(k[o]) : 0.f;
+      if (a.prologue) qv = silu_f(qv), kv = silu_f(kv);  // normalised below
+      sQ[r * L::LD + c] = qv;
+      sK[r * L::LD + c] = kv;
       if (!LINEAR) {
         float g = 0.f;
-        if (ok) g = log_gate(CHANNEL ? a.alpha[o] : a.alpha[(size_t)(tc + r) * H + h]);
+        if (ok) {
+          const float al = CHANNEL ? a.alpha[o] : a.alpha[(size_t)(tc + r) * H + h];
+          g = log_gate(a.prologue ? sigmoid_f(al) : al);
+        }
         sG[r * L::LD + c] = g;
       }
     }
@@ -114,8 +119,26 @@ __global__ void __launch_bounds__(kSimtThreads) prefill_simt_kernel(PrefillArgs 
       const int r = i / kDVB, c = i % kDVB;
       sV[r * L::LV + c] = r < n ? to_f32(v[((size_t)(tc + r) * H + h) * D + vc0 + c]) : 0.f;
     }
-    if (ERASE && tid < C) sB[tid] = tid < n ? a.beta[(size_t)(tc + tid) * H + h] : 0.f;
+    if (ERASE && tid < C) {
+      const float b = tid < n ? a.beta[(size_t)(tc + tid) * H + h] : 0.f;
+      sB[tid] = a.prologue && tid < n ? sigmoid_f(b) : b;
+    }
     __syncthreads();
+    if (a.prologue) {
+      // the layer prologue's L2 normalisation of the silu rows of q and k: one warp per row
+      // (heqinghuang "gpt2-to-kimi" §09); zero rows stay zero
+      const int warp = tid >> 5, lane = tid & 31;
+      for (int rw = warp; rw < 2 * C; rw += kSimtThreads / 32) {
+        float* row = (rw < C ? sQ : sK) + (rw % C) * L::LD;
+        float ss = 0.f;
+        for (int c = lane; c < D; c += 32) ss = fmaf(row[c], row[c], ss);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        const float inv = inv_norm(ss);
+        for (int c = lane; c < D; c += 32) row[c] *= inv;
+      }
+      __syncthreads();
+    }
 
     if (!LINEAR) {
       // ---- 2. in-chunk inclusive prefix sums of the log-gates, per key channel

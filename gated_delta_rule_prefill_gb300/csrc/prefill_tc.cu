@@ -122,6 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   cta_sync_tc();
   TcCtx x = make_ctx(sm, *tslot, bars + 0);
+  x.prologue = a.prologue;
   uint32_t ph_qk = 0, ph_a = 0, ph_v = 0;
   bool failed = false;
 
@@ -184,9 +185,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n = (int)((t1 - tc) < (int64_t)kC ? (t1 - tc) : (int64_t)kC);
     const int64_t tn = tc + kC;  // next chunk
 
-    if (tid < kC) {
-      sBeta[tid] = nb_beta;
-      sAlpha[tid] = nb_alpha;
+    if (tid < kC) {  // (the layer prologue maps the live tokens' raw gates here, not at the load)
+      const bool pro = a.prologue && tid < n;
+      sBeta[tid] = pro && ERASE ? sigmoid_ftz(nb_beta) : nb_beta;
+      sAlpha[tid] = pro && !CHANNEL ? sigmoid_ftz(nb_alpha) : nb_alpha;
     }
     if (tn < t1) load_scalars(tn, nb_beta, nb_alpha);
     if (!wait_bar(bar_qk, ph_qk)) { failed = true; break; }

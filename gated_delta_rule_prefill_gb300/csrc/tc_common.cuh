@@ -5,6 +5,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 
 #include "gdr_internal.cuh"
 #include "umma.cuh"
@@ -308,6 +309,7 @@ struct TcCtx {
   // this operand slot image in global memory, and skip the shared-memory copies only a chain
   // CTA would read (K^, M, W).
   unsigned char* gslot;
+  bool prologue;  // the staged q, k, alpha are raw projections (the layer prologue runs first)
 };
 
 __device__ __forceinline__ TcCtx make_ctx(unsigned char* sm, uint32_t tm, uint64_t* bar_mma) {
@@ -326,6 +328,7 @@ __device__ __forceinline__ TcCtx make_ctx(unsigned char* sm, uint32_t tm, uint64
   x.bar_mma = bar_mma;
   x.ph_mma = 0;
   x.gslot = nullptr;
+  x.prologue = false;
   return x;
 }
 
@@ -337,6 +340,142 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t& ph) {
   const bool all_ok = !__syncthreads_or(!ok);
   fence_after_sync();
   return all_ok;
+}
+
+// 8 fp32 values -> one 16-byte chunk of bf16 (row-major tiles)
+__device__ __forceinline__ void st_bf16x8(__nv_bfloat16* p, const float* x) {
+  uint4 u;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+  *reinterpret_cast<uint4*>(p) = u;
+}
+
+// The layer prologue's maps on the tensor-core paths.  sigmoid(x) = 1 / (1 + 2^(-x log2 e)) on
+// the hardware ex2 and rcp approximations (flush-to-zero forms; the exponent capped at 80 so the
+// divisor stays finite): relative error a few fp32 ulps, the precision the decay products need.
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_ftz(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float sigmoid_ftz(float x) {
+  return rcp_ftz(1.f + ex2_ftz(fminf(-x, 80.f) * 1.44269504f));
+}
+// silu of two bf16 values: silu(x) = x sigmoid(x) = h + h tanh(h) with h = x / 2, tanh on the
+// packed-half unit (one instruction for both; error ~2^-11 of h, below the bf16 rounding of the
+// normalised result).  |h| beyond the half range becomes +-inf, where tanh = +-1 gives the exact
+// limits silu = x and 0.
+__device__ __forceinline__ float2 silu2(__nv_bfloat162 v) {
+  const float2 f = __bfloat1622float2(v);
+  const float hx = 0.5f * f.x, hy = 0.5f * f.y;
+  const __half2 hh = __floats2half2_rn(hx, hy);
+  uint32_t t;
+  asm("tanh.approx.f16x2 %0, %1;" : "=r"(t) : "r"(*reinterpret_cast<const uint32_t*>(&hh)));
+  const float2 tf = __half22float2(*reinterpret_cast<const __half2*>(&t));
+  return make_float2(fmaf(hx, tf.x, hx), fmaf(hy, tf.y, hy));
+}
+
+// ---- Stage 0: the layer prologue on the staged tiles, in place (heqinghuang "gpt2-to-kimi"
+// §09: unit-length silu queries and keys; engineermaxxing "From GPT-2 to Kimi K3" §05c/§06b:
+// the decay is a sigmoid of its projection).  q, k <- normalize(silu(.)) over the 128 channels
+// of each token row, rounded to bf16 (the operand type of the tensor-core products); per-channel
+// alpha <- sigmoid(alpha).  Rows >= n are left alone.  The thread map is gate_stage's (8 channels
+// x 4 rows, a row's 16 threads one half-warp): each thread rewrites what it reads back itself
+// before the gate stage's first barrier, and the norms are half-warp shuffles.  The eight rows
+// of a thread (4 of q, 4 of k) go through each step together, so their latencies overlap.
+template <class L, bool CHANNEL>
+__device__ void prologue_stage(const TcCtx& x, int n) {
+  const int g8 = x.tid & 15, rb = x.tid >> 4;
+  __nv_bfloat16* sQin = reinterpret_cast<__nv_bfloat16*>(x.sm + L::QIN);
+  __nv_bfloat16* sKin = reinterpret_cast<__nv_bfloat16*>(x.sm + L::KIN);
+  float* sAin = reinterpret_cast<float*>(x.sm + L::AIN);
+  float v[8][8], ss[8];  // row j = 2 rr + (0: q, 1: k)
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int r = 4 * rb + (j >> 1);
+    uint4 u = make_uint4(0u, 0u, 0u, 0u);
+    if (r < n) u = *reinterpret_cast<const uint4*>(((j & 1) ? sKin : sQin) + r * kD + 8 * g8);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+    ss[j] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 sl = silu2(h[i]);
+      v[j][2 * i] = sl.x;
+      v[j][2 * i + 1] = sl.y;
+      ss[j] = fmaf(sl.x, sl.x, fmaf(sl.y, sl.y, ss[j]));
+    }
+  }
+  if (CHANNEL) {
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      const int r = 4 * rb + rr;
+      if (r < n) {
+        float4* pa = reinterpret_cast<float4*>(sAin + r * kD + 8 * g8);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          float4 u = pa[i];
+          u.x = sigmoid_ftz(u.x), u.y = sigmoid_ftz(u.y);
+          u.z = sigmoid_ftz(u.z), u.w = sigmoid_ftz(u.w);
+          pa[i] = u;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 8; off > 0; off >>= 1)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ss[j] += __shfl_xor_sync(0xffffffffu, ss[j], off);
+  // Rows whose silu norm is below 2 (squared 4), e.g. rows of only strongly negative values, take
+  // silu again in fp32 (ex2 and rcp): there the packed-half tanh's absolute error (~2e-3 per
+  // value at most) is no longer small against the norm that the row is divided by.  The test is
+  // per row (half-warp uniform); the redo runs on the whole warp when either half needs it.
+  unsigned redo = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) redo |= (ss[j] < 4.f ? 1u : 0u) << j;
+  redo = __reduce_or_sync(0xffffffffu, redo);
+  if (redo) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (!((redo >> j) & 1u)) continue;
+      const int r = 4 * rb + (j >> 1);
+      float e8[8];
+      if (r < n) {
+        ld_bf16x8(((j & 1) ? sKin : sQin) + r * kD + 8 * g8, e8);
+      } else {
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) e8[cc] = 0.f;
+      }
+      float s2 = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        e8[cc] *= sigmoid_ftz(e8[cc]);
+        s2 = fmaf(e8[cc], e8[cc], s2);
+      }
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, off);
+      if (ss[j] < 4.f) {
+        ss[j] = s2;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) v[j][cc] = e8[cc];
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int r = 4 * rb + (j >> 1);
+    if (r < n) {
+      const float inv = inv_norm(ss[j]);
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) v[j][cc] *= inv;
+      st_bf16x8(((j & 1) ? sKin : sQin) + r * kD + 8 * g8, v[j]);
+    }
+  }
 }
 
 // ---- Stage 1: gate prologue.  Reads the staged q, k (row-major bf16) and alpha (row-major
@@ -363,6 +502,7 @@ __device__ bool gate_stage(const TcCtx& x, int n, Hook before_writes = Hook()) {
   float* sRed = reinterpret_cast<float*>(sm + L::RED);
   float* sDiagP = reinterpret_cast<float*>(sm + L::DIAGP);  // [64 rows][16] partial q_r . k_r
   float* sGs = reinterpret_cast<float*>(sm + L::GS);
+  if (x.prologue) prologue_stage<L, CHANNEL>(x, n);
     // ================= 1. gates and operand tiles
     // thread = 8 key channels (group g8) x 4 tokens (row block rb)
     const int g8 = tid & 15, rb = tid >> 4;

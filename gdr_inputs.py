@@ -159,12 +159,28 @@ def draw_qkv_gates(rngs, L: int, d_k: int, d_v: int, dtype: str, gate: str):
     return q, k, v, alpha, beta
 
 
-def gen_block(wl: Workload, seq: int, head: int) -> dict:
+def draw_raw(rngs, L: int, d_k: int, d_v: int, dtype: str, gate: str):
+    """Raw layer projections of the same workload: xq, xk ~ N(0, 1) (in the input dtype),
+    v as draw_qkv_gates, a = 4 - N(0, 1) (sigmoid(a) has draw_qkv_gates' alpha distribution),
+    b ~ N(0, 1) (fp32)."""
+    rq, rk, rv, ra, rb = rngs
+    xq = _cast(rq.standard_normal((L, d_k), dtype=np.float32), dtype)
+    xk = _cast(rk.standard_normal((L, d_k), dtype=np.float32), dtype)
+    v = _cast(rv.standard_normal((L, d_v), dtype=np.float32), dtype)
+    ashape = (L, d_k) if gate == "channel" else (L,)
+    a = (4.0 - ra.standard_normal(ashape, dtype=np.float32)).astype(np.float32)
+    b = rb.standard_normal((L,), dtype=np.float32).astype(np.float32)
+    return xq, xk, v, a, b
+
+
+def gen_block(wl: Workload, seq: int, head: int, raw: bool = False) -> dict:
     """Inputs of one (sequence, head): q [L,d_k], k [L,d_k], v [L,d_v], alpha [L,d_k] or [L],
-    beta [L], S0 [d_k,d_v] (all float32 holding exactly-representable values)."""
+    beta [L], S0 [d_k,d_v] (all float32 holding exactly-representable values).  raw=True: q, k,
+    alpha, beta hold the raw projections of draw_raw instead."""
     L = int(wl.seqlens[seq])
     rngs = [_rng(wl.seed, t, seq, head) for t in (_Q, _K, _V, _ALPHA, _BETA)]
-    q, k, v, alpha, beta = draw_qkv_gates(rngs, L, wl.d_k, wl.d_v, wl.dtype, wl.gate)
+    draw = draw_raw if raw else draw_qkv_gates
+    q, k, v, alpha, beta = draw(rngs, L, wl.d_k, wl.d_v, wl.dtype, wl.gate)
     if wl.s0 == "normal":
         S0 = (0.1 * _rng(wl.seed, _S0, seq, head).standard_normal((wl.d_k, wl.d_v),
                                                                      dtype=np.float32))
@@ -193,16 +209,17 @@ def alloc_full(wl: Workload, heads=None, seqs=None):
     return a, seqs, heads
 
 
-def gen_full(wl: Workload, heads=None, seqs=None, threads: int = 8) -> dict:
+def gen_full(wl: Workload, heads=None, seqs=None, threads: int = 8, raw: bool = False) -> dict:
     """Token-major inputs for the chosen sequences and heads:
     q, k [T,H',d_k]; v [T,H',d_v]; alpha [T,H',d_k] or [T,H']; beta [T,H']; S0 [N',H',d_k,d_v];
-    cu_seqlens [N'+1] (int64).  Blocks are drawn in parallel threads (numpy releases the GIL)."""
+    cu_seqlens [N'+1] (int64).  Blocks are drawn in parallel threads (numpy releases the GIL).
+    raw=True: q, k, alpha, beta hold raw projections (draw_raw)."""
     a, seqs, heads = alloc_full(wl, heads, seqs)
     cu = a["cu_seqlens"]
 
     def fill(job):
         si, hi = job
-        blk = gen_block(wl, seqs[si], heads[hi])
+        blk = gen_block(wl, seqs[si], heads[hi], raw)
         t0, t1 = cu[si], cu[si + 1]
         for name in ("q", "k", "v", "alpha", "beta"):
             a[name][t0:t1, hi] = blk[name]
@@ -218,12 +235,13 @@ def gen_full(wl: Workload, heads=None, seqs=None, threads: int = 8) -> dict:
     return a
 
 
-def gen_decode_step(wl: Workload, step: int) -> dict:
+def gen_decode_step(wl: Workload, step: int, raw: bool = False) -> dict:
     """Inputs of one decode step for all N sequences: q,k [N,H,d_k], v [N,H,d_v],
-    alpha [N,H,d_k] (or [N,H]), beta [N,H]."""
+    alpha [N,H,d_k] (or [N,H]), beta [N,H] (raw=True: raw projections, draw_raw)."""
     N, H = wl.n_seqs, wl.H
     rngs = [_rng(wl.seed, _STEP_BASE + t, step) for t in (_Q, _K, _V, _ALPHA, _BETA)]
-    q, k, v, alpha, beta = draw_qkv_gates(rngs, N * H, wl.d_k, wl.d_v, wl.dtype, wl.gate)
+    draw = draw_raw if raw else draw_qkv_gates
+    q, k, v, alpha, beta = draw(rngs, N * H, wl.d_k, wl.d_v, wl.dtype, wl.gate)
     shp = (N, H)
     return dict(q=q.reshape(shp + (wl.d_k,)), k=k.reshape(shp + (wl.d_k,)),
                 v=v.reshape(shp + (wl.d_v,)),
@@ -240,10 +258,11 @@ def random_state(seed: int, N: int, H: int, d_k: int, d_v: int, std: float = 0.1
 # ----------------------------------------------------------------------------------------------
 # device-side drawing (timing only)
 # ----------------------------------------------------------------------------------------------
-def device_full(wl: Workload, device, seed_offset: int = 0):
+def device_full(wl: Workload, device, seed_offset: int = 0, raw: bool = False):
     """The same distributions drawn on the device with torch's seeded generator (different
     numbers from the host streams above).  Used where only the shape and distribution of the
-    inputs matter (throughput runs); parity always uses the host streams."""
+    inputs matter (throughput runs); parity always uses the host streams.  raw=True: q, k,
+    alpha, beta are raw projections with draw_raw's distributions."""
     import torch
 
     g = torch.Generator(device=device)
@@ -255,13 +274,22 @@ def device_full(wl: Workload, device, seed_offset: int = 0):
         x = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
         return (x / x.norm(dim=-1, keepdim=True).clamp_min(1e-30)).to(tdt)
 
-    q = unit((T, H, dk))
-    k = unit((T, H, dk))
-    v = torch.randn((T, H, dv), generator=g, device=device, dtype=torch.float32).to(tdt)
+    def normal(shape):
+        return torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+
     ashape = (T, H, dk) if wl.gate == "channel" else (T, H)
-    alpha = torch.exp(-torch.nn.functional.softplus(
-        torch.randn(ashape, generator=g, device=device) - 4.0))
-    beta = torch.sigmoid(torch.randn((T, H), generator=g, device=device))
+    if raw:
+        q = normal((T, H, dk)).to(tdt)
+        k = normal((T, H, dk)).to(tdt)
+        v = normal((T, H, dv)).to(tdt)
+        alpha = 4.0 - normal(ashape)
+        beta = normal((T, H))
+    else:
+        q = unit((T, H, dk))
+        k = unit((T, H, dk))
+        v = normal((T, H, dv)).to(tdt)
+        alpha = torch.exp(-torch.nn.functional.softplus(normal(ashape) - 4.0))
+        beta = torch.sigmoid(normal((T, H)))
     if wl.s0 == "normal":
         S0 = 0.1 * torch.randn((wl.n_seqs, H, dk, dv), generator=g, device=device)
     else:

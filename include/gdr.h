@@ -92,6 +92,17 @@ typedef struct {
 /* Run the work-queue kernel wherever the workspace holds its operand rings, also where the
  * clustered kernel would be chosen (for cross-checks). */
 #define GDR_FLAG_PREFER_QUEUE 4
+/* The layer prologue on load (heqinghuang "gpt2-to-kimi" §09: unit-length silu queries and keys,
+ * beta a sigmoid of its projection; engineermaxxing "From GPT-2 to Kimi K3" §05c and §06b: the
+ * decay a sigmoid of its projection, per head or per channel).  q, k, alpha and beta then hold
+ * the layer's raw projections xq, xk, a, b (same dtypes and layouts as the rule's inputs), and
+ * every kernel forms q = xq * sigmoid(xq) / max(||.||_2, 1e-12) over the d_k channels of each
+ * (token, head) (likewise k), alpha = sigmoid(a) and beta = sigmoid(b) as it loads them; the
+ * inputs are not written.  Accepted by gdr_prefill, gdr_prefill_output_gate,
+ * gdr_gated_linear_attn (no beta), gdr_decode_step and gdr_prefill_host; gdr_linear_attn returns
+ * GDR_ERR_UNSUPPORTED.  On the tensor-core paths the normalised q and k are rounded to bf16 (the
+ * operand type) before use; the fp32 paths keep them in fp32. */
+#define GDR_FLAG_LAYER_PROLOGUE 8
 
 /*
  * gdr_prefill -- chunked, packed variable-length prefill of the gated delta rule.
@@ -118,6 +129,23 @@ gdr_status gdr_prefill(const gdr_shape* shape, const void* q, const void* k, con
  * status word, the visiting order and, for bf16 d = 128 shapes of at most 76 (sequence, head)
  * chains, the work-queue prefill's flags and 6 operand slots of 74752 bytes per chain. */
 size_t gdr_prefill_workspace_size(const gdr_shape* shape);
+
+/*
+ * gdr_layer_prologue -- the layer prologue as a pass of its own (the maps that
+ * GDR_FLAG_LAYER_PROLOGUE applies inside the kernels; heqinghuang "gpt2-to-kimi" §09,
+ * engineermaxxing "From GPT-2 to Kimi K3" §05c and §06b):
+ *   q = silu(xq) / max(||silu(xq)||_2, 1e-12) over the d_k channels of each (token, head),
+ *   k likewise, alpha = sigmoid(a), beta = sigmoid(b);   silu(x) = x sigmoid(x).
+ *   xq, xk -> q, k: [T, H, d_k] in shape->dtype (fp32 math, one rounding to the dtype).
+ *   a -> alpha: [T, H, d_k] (shape->gate = GDR_GATE_CHANNEL) or [T, H] fp32; both NULL to skip.
+ *   b -> beta:  [T, H] fp32; both NULL to skip.
+ * Uses shape->H, total_tokens, d_k (= d_v, 64 or 128), dtype and gate.  Outputs may be their
+ * own inputs (in place); otherwise they must not overlap an input.  All pointers device, 16-byte
+ * aligned, caller-owned.  One kernel, bound by HBM bandwidth; asynchronous on `stream`.
+ */
+gdr_status gdr_layer_prologue(const gdr_shape* shape, const void* xq, const void* xk,
+                              const float* a, const float* b, void* q, void* k, float* alpha,
+                              float* beta, void* stream);
 
 /*
  * gdr_decode_step -- one token per sequence, state updated in place.

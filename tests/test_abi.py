@@ -79,7 +79,7 @@ def test_argument_errors(lib):
     assert _prefill(lib, _shape(), cu=None) == INV              # n_seqs > 1 needs cu_seqlens
     assert _prefill(lib, _shape(), out=FAKE) == INV             # out aliases q
     assert _prefill(lib, _shape(chunk_size=48)) == UNS
-    assert _prefill(lib, _shape(flags=8)) == INV
+    assert _prefill(lib, _shape(flags=16)) == INV
     # decode: total_tokens must equal n_seqs
     P = ctypes.c_void_p
     sh = _shape(total_tokens=3)
@@ -149,3 +149,42 @@ def test_output_gate_needs_g(lib):
     """gdr_prefill_output_gate without its gate tensor is an argument error (no launch)."""
     sh = _shape(n_seqs=1, total_tokens=64)
     assert lib.gdr_prefill_output_gate(ctypes.byref(sh), *([None] * 11), 0, None) == 1
+
+
+def test_layer_prologue_flag(lib):
+    """GDR_FLAG_LAYER_PROLOGUE passes the shape checks of the rule's entry points (their other
+    argument errors still come first) and is unsupported for plain linear attention; unknown
+    flag bits stay argument errors."""
+    from gated_delta_rule_prefill_gb300._abi import GDR_FLAG_LAYER_PROLOGUE
+    P = ctypes.c_void_p
+    sh = _shape(n_seqs=1, total_tokens=64)
+    sh.flags = GDR_FLAG_LAYER_PROLOGUE
+    assert lib.gdr_linear_attn(ctypes.byref(sh), P(FAKE), P(FAKE + 4096), P(FAKE + 8192), None,
+                               None, P(FAKE + 65536), None, P(FAKE * 2), 1 << 20, None) == 2
+    # the prologue flag alone is no error: a missing beta still is
+    assert lib.gdr_prefill(ctypes.byref(sh), P(FAKE), P(FAKE + 4096), P(FAKE + 8192),
+                           P(FAKE + 16384), None, None, None, P(FAKE + 65536), None,
+                           P(FAKE * 2), 1 << 20, None) == 1
+    sh.flags = 16
+    assert lib.gdr_decode_step(ctypes.byref(sh), *([None] * 7), None) == 1
+
+
+def test_layer_prologue_argument_errors(lib):
+    """gdr_layer_prologue: shape checks, required q/k tensors, gate inputs and outputs in pairs,
+    alignment and output aliasing -- all rejected before any launch; T = 0 is a no-op."""
+    P = ctypes.c_void_p
+    sh = _shape(n_seqs=1, total_tokens=64)
+
+    def call(xq=FAKE, xk=FAKE + 65536, a=None, b=None, q=FAKE + 131072, k=FAKE + 196608,
+             alpha=None, beta=None, shape=sh):
+        return lib.gdr_layer_prologue(ctypes.byref(shape), P(xq), P(xk), P(a), P(b), P(q), P(k),
+                                      P(alpha), P(beta), None)
+    assert call(xq=None) == 1
+    assert call(k=None) == 1
+    assert call(a=FAKE * 4) == 1              # a without alpha
+    assert call(beta=FAKE * 4) == 1           # beta without b
+    assert call(q=FAKE + 8) == 1              # misaligned
+    assert call(q=FAKE + 65536) == 1          # q onto xk
+    assert call(k=FAKE) == 1                  # k onto xq
+    assert call(shape=_shape(n_seqs=1, total_tokens=64, d_k=96, d_v=96)) == 2
+    assert call(xq=None, shape=_shape(n_seqs=1, total_tokens=0)) == 0
