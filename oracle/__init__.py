@@ -13,6 +13,12 @@ It shares no code with the GPU library and never imports it.
                     k = normalize(silu(xk)) over d_k (x / max(||x||, 1e-12)) and beta = sigmoid(b)
                     as heqinghuang §09 writes them; alpha = sigmoid(a), scalar per head as
                     engineermaxxing §05c, per channel as its §06b.
+  phi(x)            elu(x) + 1 (x + 1 for x > 0, e^x otherwise): the feature map of normalised
+                    linear attention (heqinghuang §07, engineermaxxing §02g).
+  normalized_linear(q, k, v, S0, z0, cu_seqlens, eps)  normalised phi-linear attention, token by
+                    token in numpy fp64: S <- S + phi(k_t) v_t^T, z <- z + phi(k_t),
+                    o_t = S^T phi(q_t) / (phi(q_t) . z + eps) (both after the write, as the pages'
+                    listings order them).
   output_gate(o, g) o * sigmoid(g), element by element (numpy fp64): the KDA layer's output
                     gate (dev.to §5: full rank and input dependent in K3; a sigmoid multiplied
                     into the output feature by feature, as heqinghuang §15 describes the gate of
@@ -148,6 +154,37 @@ def layer_prologue(xq, xk, a, b):
     out.append(_sigmoid(np.asarray(a, dtype=np.float64)))
     out.append(_sigmoid(np.asarray(b, dtype=np.float64)))
     return tuple(out)
+
+
+def phi(x):
+    """elu(x) + 1 in fp64: x + 1 where x > 0, e^x elsewhere (always > 0)."""
+    x = np.asarray(x, dtype=np.float64)
+    return np.where(x > 0, x + 1.0, np.exp(np.minimum(x, 0.0)))
+
+
+def normalized_linear(q, k, v, S0=None, z0=None, cu_seqlens=None, eps=0.0):
+    """Normalised phi-linear attention, per (sequence, head), one token at a time in fp64.
+    q, k [T,H,d_k], v [T,H,d_v]; S0 [N,H,d_k,d_v] and z0 [N,H,d_k] or None (zeros).
+    Returns (out [T,H,d_v], S_final [N,H,d_k,d_v], z_final [N,H,d_k])."""
+    q, k, v = phi(q), phi(k), np.asarray(v, dtype=np.float64)
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    cu = np.array([0, T]) if cu_seqlens is None else np.asarray(cu_seqlens, dtype=np.int64)
+    N = len(cu) - 1
+    out = np.zeros((T, H, dv))
+    S_fin = np.zeros((N, H, dk, dv))
+    z_fin = np.zeros((N, H, dk))
+    for n in range(N):
+        for h in range(H):
+            S = np.zeros((dk, dv)) if S0 is None else np.array(S0[n, h], dtype=np.float64)
+            z = np.zeros(dk) if z0 is None else np.array(z0[n, h], dtype=np.float64)
+            for t in range(cu[n], cu[n + 1]):
+                S += np.outer(k[t, h], v[t, h])
+                z += k[t, h]
+                out[t, h] = (q[t, h] @ S) / (q[t, h] @ z + eps)
+            S_fin[n, h] = S
+            z_fin[n, h] = z
+    return out, S_fin, z_fin
 
 
 def output_gate(o, g):

@@ -116,3 +116,42 @@ def test_pins_catch_mutant(name, original_source, tmp_path):
     finally:
         oracle._lib = real
     assert caught, "no pin caught the mutant '%s'" % name
+
+
+# ---- the numpy statement of normalised phi-linear attention: mutants of its source text
+import inspect  # noqa: E402
+
+import numpy as np  # noqa: E402
+
+NL_PINS = [pins.test_phi_closed_forms, pins.test_normalized_linear_is_a_weighted_average,
+           pins.test_normalized_linear_state_handoff_and_eps]
+NL_MUTANTS = {
+    "phi_without_plus_one": ("phi", "x + 1.0, np.exp", "x, np.exp"),
+    "phi_threshold_sign": ("phi", "np.where(x > 0", "np.where(x < 0"),
+    "read_before_key_sum": ("normalized_linear",
+                            "                z += k[t, h]\n                out[t, h] = (q[t, h] @ S) / (q[t, h] @ z + eps)",
+                            "                out[t, h] = (q[t, h] @ S) / (q[t, h] @ z + eps)\n                z += k[t, h]"),
+    "eps_in_numerator": ("normalized_linear", "(q[t, h] @ S) / (q[t, h] @ z + eps)",
+                         "(q[t, h] @ S + eps) / (q[t, h] @ z + eps)"),
+    "outer_product_transposed": ("normalized_linear", "np.outer(k[t, h], v[t, h])",
+                                 "np.outer(k[t, h], v[t, h][::-1])"),
+    "query_without_phi": ("normalized_linear", "q, k, v = phi(q), phi(k)", "q, k, v = q, phi(k)"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(NL_MUTANTS))
+def test_pins_catch_normalized_linear_mutant(name, monkeypatch):
+    fn, old, new = NL_MUTANTS[name]
+    src = inspect.getsource(getattr(oracle, fn))
+    assert old in src, name
+    ns = {"np": np, "phi": oracle.phi}
+    exec(src.replace(old, new), ns)
+    monkeypatch.setattr(oracle, fn, ns[fn])
+    caught = 0
+    for pin in NL_PINS:
+        try:
+            with np.errstate(all="ignore"):  # a mutant may divide by a zero normaliser
+                pin()
+        except AssertionError:
+            caught += 1
+    assert caught > 0, "no pin catches mutant %s" % name

@@ -437,3 +437,60 @@ def test_layer_prologue_closed_forms():
     np.testing.assert_allclose(oracle.layer_prologue(xq, xk, np.zeros(1), np.zeros(1))[3], 0.5)
     z = oracle.layer_prologue(np.zeros((1, 1, 4)), xk[:1, :1, :4], a[:1], b[:1])[0]
     assert np.all(z == 0.0)
+
+
+# ------------------------------------------------------------------------------------------
+# normalised phi-linear attention: the feature map, and the read as a weighted average
+# ------------------------------------------------------------------------------------------
+def test_phi_closed_forms():
+    """phi = elu + 1: x + 1 above zero, e^x at and below zero; continuous with slope 1 at 0."""
+    x = np.array([-50.0, -2.0, -1e-9, 0.0, 1e-9, 0.5, 3.0])
+    np.testing.assert_allclose(oracle.phi(x), [np.exp(-50), np.exp(-2), np.exp(-1e-9), 1.0,
+                                               1.0 + 1e-9, 1.5, 4.0], rtol=1e-15)
+    h = 1e-7
+    assert abs((oracle.phi(h) - oracle.phi(-h)) / (2 * h) - 1.0) < 1e-6
+    assert np.all(oracle.phi(np.linspace(-700, 50, 1001)) > 0)
+
+
+def test_normalized_linear_is_a_weighted_average():
+    """From zero state with eps = 0 the read is sum_j w_j v_j with w_j = phi(q_t).phi(k_j) /
+    sum_i<=t phi(q_t).phi(k_i): computed here pair by pair, not through the running state.  The
+    first output is v_1 exactly; every output lies in the convex hull of the values so far."""
+    rng = np.random.default_rng(41)
+    T, H, dk, dv = 9, 2, 5, 3
+    q, k, v = rng.normal(size=(T, H, dk)), rng.normal(size=(T, H, dk)), rng.normal(size=(T, H, dv))
+    out, S, z = oracle.normalized_linear(q, k, v)
+    pq, pk = oracle.phi(q), oracle.phi(k)
+    for h in range(H):
+        for t in range(T):
+            w = np.array([pq[t, h] @ pk[j, h] for j in range(t + 1)])
+            ref = (w / w.sum()) @ v[: t + 1, h]
+            np.testing.assert_allclose(out[t, h], ref, rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(out[0, h], v[0, h], rtol=1e-14)
+        np.testing.assert_allclose(z[0, h], pk[:, h].sum(0), rtol=1e-14)
+        np.testing.assert_allclose(S[0, h], pk[:, h].T @ v[:, h], rtol=1e-13)
+
+
+def test_normalized_linear_state_handoff_and_eps():
+    """Two halves with (S, z) handed over equal one run; eps adds to the denominator only;
+    packed sequences are independent."""
+    rng = np.random.default_rng(42)
+    T, H, dk, dv = 12, 1, 4, 4
+    q, k, v = rng.normal(size=(T, H, dk)), rng.normal(size=(T, H, dk)), rng.normal(size=(T, H, dv))
+    S0 = rng.normal(size=(1, H, dk, dv))
+    z0 = np.abs(rng.normal(size=(1, H, dk)))
+    full = oracle.normalized_linear(q, k, v, S0, z0)
+    a = oracle.normalized_linear(q[:5], k[:5], v[:5], S0, z0)
+    b = oracle.normalized_linear(q[5:], k[5:], v[5:], a[1], a[2])
+    np.testing.assert_allclose(np.concatenate([a[0], b[0]]), full[0], rtol=1e-12)
+    np.testing.assert_allclose(b[1], full[1], rtol=1e-12)
+    np.testing.assert_allclose(b[2], full[2], rtol=1e-12)
+    e = oracle.normalized_linear(q, k, v, S0, z0, eps=0.25)[0]
+    pq = oracle.phi(q)
+    num = full[0] * (np.einsum("thd,thd->th", pq, np.cumsum(oracle.phi(k), 0) + z0[0]))[..., None]
+    den = np.einsum("thd,thd->th", pq, np.cumsum(oracle.phi(k), 0) + z0[0]) + 0.25
+    np.testing.assert_allclose(e, num / den[..., None], rtol=1e-12)
+    cu = np.array([0, 5, 12])
+    pk = oracle.normalized_linear(q, k, v, cu_seqlens=cu)
+    np.testing.assert_allclose(pk[0][5:], oracle.normalized_linear(q[5:], k[5:], v[5:])[0],
+                               rtol=1e-12)
