@@ -12,6 +12,7 @@ library's CUDA kernels; there is no Python or CPU fallback.
     gdr_prefill_host(q, k, v, alpha, beta, ...)  -- host (CPU) tensors in and out, copies inside
     gdr_prefill_host_buffer_size(n_seqs, H, total_tokens, d_k, d_v, dtype, gate, piece_tokens)
     gdr_layer_prologue(xq, xk, a=None, b=None, q=None, k=None, alpha=None, beta=None)
+    gdr_normalized_linear_attn(q, k, v, eps=0.0, S0=None, z0=None, cu_seqlens=None, ...)
 
 prologue=True (GDR_FLAG_LAYER_PROLOGUE) makes q, k, alpha, beta the layer's raw projections: the
 kernels form q, k = normalize(silu(.)) and alpha, beta = sigmoid(.) as they load them.
@@ -28,7 +29,7 @@ from ._abi import (GDR_BF16, GDR_F32, GDR_FLAG_FORCE_SIMT, GDR_FLAG_NO_CLUSTER, 
                    GdrError, GdrShape)
 
 __all__ = ["gdr_prefill", "gdr_prefill_output_gate", "gdr_decode_step", "gdr_linear_attn",
-           "gdr_gated_linear_attn", "gdr_layer_prologue",
+           "gdr_gated_linear_attn", "gdr_layer_prologue", "gdr_normalized_linear_attn",
            "gdr_prefill_workspace_size",
            "gdr_workspace_status", "gdr_prefill_host", "gdr_prefill_host_buffer_size",
            "make_shape", "GdrError"]
@@ -231,6 +232,46 @@ def gdr_gated_linear_attn(q, k, v, alpha, S0=None, cu_seqlens=None, out=None, S_
     return _prefill_like("gla", q, k, v, alpha, None, S0, cu_seqlens, out, S_final, workspace,
                          chunk_size, force_simt, stream, want_final, no_cluster,
                          prologue=prologue)
+
+
+def gdr_normalized_linear_attn(q, k, v, eps=0.0, S0=None, z0=None, cu_seqlens=None, out=None,
+                               S_final=None, z_final=None, workspace=None, chunk_size=0,
+                               force_simt=False, stream=None, want_final=True):
+    """Normalised phi-linear attention (phi = elu + 1): S <- S + phi(k) v^T, z <- z + phi(k),
+    o = S^T phi(q) / (phi(q) . z + eps).  q, k [T,H,d_k], v [T,H,d_v]; S0 [N,H,d_k,d_v] and z0
+    [N,H,d_k] fp32 or None.  Returns (out, S_final, z_final)."""
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    dtype = _DT.get(q.dtype)
+    if dtype is None:
+        raise ValueError("q/k/v must be float32 or bfloat16")
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, q.dtype)
+    n_seqs = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    _check(S0, "S0", torch.float32)
+    _check(z0, "z0", torch.float32)
+    _check(cu_seqlens, "cu_seqlens", torch.int32)
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=q.dtype, device=q.device)
+    _check(out, "out", q.dtype)
+    if want_final:
+        if S_final is None:
+            S_final = torch.empty((n_seqs, H, dk, dv), dtype=torch.float32, device=q.device)
+        if z_final is None:
+            z_final = torch.empty((n_seqs, H, dk), dtype=torch.float32, device=q.device)
+    _check(S_final, "S_final", torch.float32)
+    _check(z_final, "z_final", torch.float32)
+    ws = _workspace(n_seqs, H, dk, dv, "bf16" if dtype == GDR_BF16 else "f32", q.device,
+                    workspace)
+    sh = make_shape(n_seqs, H, T, dk, dv, dtype, GDR_GATE_CHANNEL, chunk_size,
+                    GDR_FLAG_FORCE_SIMT if force_simt else 0)
+    rc = _abi.load().gdr_normalized_linear_attn(
+        ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), float(eps), _ptr(S0), _ptr(z0),
+        _ptr(cu_seqlens), _ptr(out), _ptr(S_final), _ptr(z_final), _ptr(ws), ws.numel(),
+        _stream(stream))
+    if rc != 0:
+        raise GdrError(rc, "gdr_normalized_linear_attn")
+    return out, S_final, z_final
 
 
 def gdr_layer_prologue(xq, xk, a=None, b=None, q=None, k=None, alpha=None, beta=None,

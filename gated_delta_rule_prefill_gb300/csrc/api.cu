@@ -69,8 +69,9 @@ gdr_status check_shape(const gdr_shape* sh, bool need_gate) {
 gdr_status prefill_common(const gdr_shape* sh, const void* q, const void* k, const void* v,
                           const float* alpha, const float* beta, const float* S0,
                           const int32_t* cu, void* out, float* S_final, void* ws,
-                          size_t ws_bytes, void* stream, int kind, const void* og = nullptr) {
-  const bool linear = kind == kKindLinear;
+                          size_t ws_bytes, void* stream, int kind, const void* og = nullptr,
+                          const float* z0 = nullptr, float* z_final = nullptr, float eps = 0.f) {
+  const bool linear = kind == kKindLinear || kind == kKindNormLinear;
   gdr_status st = check_shape(sh, !linear);
   if (st != GDR_OK) return st;
   const bool prologue = (sh->flags & GDR_FLAG_LAYER_PROLOGUE) != 0;
@@ -81,7 +82,7 @@ gdr_status prefill_common(const gdr_shape* sh, const void* q, const void* k, con
     if (!linear && !alpha) return GDR_ERR_INVALID_ARG;
     if (kind == kKindDelta && !beta) return GDR_ERR_INVALID_ARG;
   }
-  const void* ptrs[] = {q, k, v, alpha, beta, S0, cu, out, S_final, og};
+  const void* ptrs[] = {q, k, v, alpha, beta, S0, cu, out, S_final, og, z0, z_final};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return GDR_ERR_INVALID_ARG;
   if (og && og == out) return GDR_ERR_INVALID_ARG;
@@ -101,12 +102,12 @@ gdr_status prefill_common(const gdr_shape* sh, const void* q, const void* k, con
            WorkspaceLayout::flag_bytes(WorkspaceLayout::ring_pairs(*sh));
   }
   PrefillArgs a{sh->n_seqs, sh->H, sh->total_tokens, q, k, v, alpha, beta, S0, cu,
-                out, S_final, order, status, ring_flags, ring, og, prologue};
+                out, S_final, order, status, ring_flags, ring, og, prologue, z0, z_final, eps};
   prep_kernel<<<1, kPrepThreads, 0, s>>>(cu, sh->n_seqs, sh->total_tokens, order, status);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess)
-    e = prefill_tc_supported(*sh) ? launch_prefill_tc(*sh, a, kind, s)
-                                  : launch_prefill_simt(*sh, a, kind, s);
+    e = prefill_tc_supported(*sh) && kind != kKindNormLinear ? launch_prefill_tc(*sh, a, kind, s)
+                                                             : launch_prefill_simt(*sh, a, kind, s);
   return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }
 
@@ -162,6 +163,19 @@ gdr_status gdr_gated_linear_attn(const gdr_shape* shape, const void* q, const vo
                                  void* workspace, size_t workspace_bytes, void* stream) {
   return gdr::prefill_common(shape, q, k, v, alpha, nullptr, S0, cu_seqlens, out, S_final,
                              workspace, workspace_bytes, stream, gdr::kKindGatedLinear);
+}
+
+gdr_status gdr_normalized_linear_attn(const gdr_shape* shape, const void* q, const void* k,
+                                      const void* v, float eps, const float* S0, const float* z0,
+                                      const int32_t* cu_seqlens, void* out, float* S_final,
+                                      float* z_final, void* workspace, size_t workspace_bytes,
+                                      void* stream) {
+  if (!(eps >= 0.f) || eps > 3.0e38f) return GDR_ERR_INVALID_ARG;  // also rejects NaN
+  // every value block of a (sequence, head) reads z0 at its start; one of them writes z_final
+  if (z0 && z0 == z_final) return GDR_ERR_INVALID_ARG;
+  return gdr::prefill_common(shape, q, k, v, nullptr, nullptr, S0, cu_seqlens, out, S_final,
+                             workspace, workspace_bytes, stream, gdr::kKindNormLinear, nullptr,
+                             z0, z_final, eps);
 }
 
 gdr_status gdr_decode_step(const gdr_shape* shape, const void* q, const void* k, const void* v,

@@ -76,7 +76,15 @@ struct PrefillArgs {
   // q, k, alpha, beta hold the layer's raw projections: the kernels apply the layer prologue
   // (q, k = normalize(silu(.)), alpha, beta = sigmoid(.)) as they load them.
   bool prologue = false;
+  // normalised phi-linear attention: entering / final normaliser z [N, H, d_k] (null: zeros /
+  // not written) and the eps added to phi(q) . z
+  const float* z0 = nullptr;
+  float* z_final = nullptr;
+  float eps = 0.f;
 };
+
+// phi(x) = elu(x) + 1: x + 1 above zero, e^x at and below it.
+__device__ __forceinline__ float phi_f(float x) { return x > 0.f ? x + 1.f : __expf(x); }
 
 // The layer prologue's maps in fp32: sigmoid(x) = 1 / (1 + e^-x) (the exponent capped at 80 so
 // the fast division never meets an infinite divisor), silu(x) = x sigmoid(x), and the scale
@@ -115,7 +123,12 @@ __device__ __forceinline__ bool seq_range(const PrefillArgs& a, int seq, int64_t
 
 // What a prefill-like call computes: the gated delta rule, plain linear attention (alpha = 1,
 // no erase), or gated linear attention (S <- Diag(alpha) S + k v^T: no erase, no beta).
-enum PrefillKind : int { kKindDelta = 0, kKindLinear = 1, kKindGatedLinear = 2 };
+enum PrefillKind : int {
+  kKindDelta = 0,        // the gated delta rule
+  kKindLinear = 1,       // plain linear attention
+  kKindGatedLinear = 2,  // gated linear attention (no erase)
+  kKindNormLinear = 3    // normalised phi-linear attention (phi = elu + 1, normaliser z)
+};
 
 // The shape checks every prefill-like call makes (GDR_OK or the error to return).
 gdr_status validate_shape(const gdr_shape* sh, bool need_gate);

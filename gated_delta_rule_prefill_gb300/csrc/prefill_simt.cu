@@ -48,7 +48,8 @@ struct SimtSmem {
   static constexpr int off_U = off_V + C * LV;
   static constexpr int off_B = off_U + C * LV;
   static constexpr int off_Gam = off_B + C;
-  static constexpr int total_floats = off_Gam + D;
+  static constexpr int off_Z = off_Gam + D;    // the normaliser z (normalised linear attention)
+  static constexpr int total_floats = off_Z + D;
   static constexpr size_t bytes = (size_t)total_floats * 4;
 };
 
@@ -56,7 +57,8 @@ template <int D, int C, typename T, bool CHANNEL, int KIND>
 __global__ void __launch_bounds__(kSimtThreads) prefill_simt_kernel(PrefillArgs a) {
   using L = SimtSmem<D, C>;
   constexpr int NB = D / kDVB;
-  constexpr bool LINEAR = KIND == kKindLinear;  // no gates
+  constexpr bool NORM = KIND == kKindNormLinear;        // phi features, normaliser z
+  constexpr bool LINEAR = KIND == kKindLinear || NORM;  // no gates
   constexpr bool ERASE = KIND == kKindDelta;    // the delta rule's correction (solve, beta)
   extern __shared__ float sm[];
   float* sQ = sm + L::off_Q;
@@ -71,6 +73,8 @@ __global__ void __launch_bounds__(kSimtThreads) prefill_simt_kernel(PrefillArgs 
   float* sU = sm + L::off_U;
   float* sB = sm + L::off_B;
   float* sGam = sm + L::off_Gam;
+  float* sZ = sm + L::off_Z;
+  float* sDen = sB;  // normalised linear attention: the chunk's denominators (no beta there)
 
   const int tid = threadIdx.x;
   const int H = a.H;
@@ -88,7 +92,10 @@ __global__ void __launch_bounds__(kSimtThreads) prefill_simt_kernel(PrefillArgs 
   const int vc0 = vb * kDVB;
   const size_t sidx = ((size_t)seq * H + h) * D * D;
 
-  // entering state block [D][DVB]
+  // entering state block [D][DVB] (and the whole normaliser z: every value block keeps a copy)
+  if (NORM)
+    for (int c = tid; c < D; c += kSimtThreads)
+      sZ[c] = a.z0 ? a.z0[((size_t)seq * H + h) * D + c] : 0.f;
   for (int i = tid; i < D * kDVB; i += kSimtThreads) {
     const int r = i / kDVB, c = i % kDVB;
     sS[r * L::LV + c] = a.S0 ? a.S0[sidx + (size_t)r * D + vc0 + c] : 0.f;
@@ -104,6 +111,7 @@ __global__ void __launch_bounds__(kSimtThreads) prefill_simt_kernel(PrefillArgs 
       const size_t o = ((size_t)(tc + r) * H + h) * D + c;
       float qv = ok ? to_f32(q[o]) : 0.f, kv = ok ? to_f32(k[o]) : 0.f;
       if (a.prologue) qv = silu_f(qv), kv = silu_f(kv);  // normalised below
+      if (NORM && ok) qv = phi_f(qv), kv = phi_f(kv);    // rows >= n stay 0: no write, no z
       sQ[r * L::LD + c] = qv;
       sK[r * L::LD + c] = kv;
       if (!LINEAR) {
@@ -177,6 +185,21 @@ __global__ void __launch_bounds__(kSimtThreads) prefill_simt_kernel(PrefillArgs 
       sM[r * L::LC + j] = acc_m;
     }
     __syncthreads();
+    if (NORM) {
+      // ---- 3b. denominators phi(q_r) . z_r = phi(q_r) . z_entry + sum_{j <= r} M[r][j]
+      for (int r = tid; r < C; r += kSimtThreads) {
+        const float* qr = sQ + r * L::LD;
+        float acc0 = 0.f, acc1 = 0.f;
+        for (int c = 0; c < D; c += 2) {
+          acc0 = fmaf(qr[c], sZ[c], acc0);
+          acc1 = fmaf(qr[c + 1], sZ[c + 1], acc1);
+        }
+        const float* mr = sM + r * L::LC;
+        for (int j = 0; j <= r; ++j) acc0 += mr[j];
+        sDen[r] = acc0 + acc1 + a.eps;
+      }
+      __syncthreads();
+    }
 
     if (!LINEAR) {
       // ---- 4. gate-scaled operands and the right-hand sides of the solve
@@ -244,6 +267,7 @@ __global__ void __launch_bounds__(kSimtThreads) prefill_simt_kernel(PrefillArgs 
       for (int j = 0; j <= r; ++j) acc0 = fmaf(mr[j], sUse[j * L::LV + c], acc0);
       const size_t oi = ((size_t)(tc + r) * H + h) * D + vc0 + c;
       float o = acc0 + acc1;
+      if (NORM) o /= sDen[r];
       if (a.og) o = gate_out(o, to_f32(static_cast<const T*>(a.og)[oi]));
       out[oi] = from_f32<T>(o);
     }
@@ -257,8 +281,17 @@ __global__ void __launch_bounds__(kSimtThreads) prefill_simt_kernel(PrefillArgs 
       for (int j = 0; j < n; ++j) acc = fmaf(kh[j * L::LD + m], sUse[j * L::LV + c], acc);
       sS[m * L::LV + c] = acc;
     }
+    if (NORM) {  // z <- z + sum of the chunk's phi(k) rows (rows >= n are 0)
+      for (int c = tid; c < D; c += kSimtThreads) {
+        float acc = sZ[c];
+        for (int j = 0; j < n; ++j) acc += sK[j * L::LD + c];
+        sZ[c] = acc;
+      }
+    }
   }
   __syncthreads();
+  if (NORM && a.z_final && vb == 0)
+    for (int c = tid; c < D; c += kSimtThreads) a.z_final[((size_t)seq * H + h) * D + c] = sZ[c];
   if (a.S_final) {
     for (int i = tid; i < D * kDVB; i += kSimtThreads) {
       const int r = i / kDVB, c = i % kDVB;
@@ -282,6 +315,7 @@ cudaError_t launch_one(const gdr_shape& sh, const PrefillArgs& a, cudaStream_t s
 template <int D, int C, typename T>
 cudaError_t launch_t(const gdr_shape& sh, const PrefillArgs& a, int kind, cudaStream_t s) {
   if (kind == kKindLinear) return launch_one<D, C, T, true, kKindLinear>(sh, a, s);
+  if (kind == kKindNormLinear) return launch_one<D, C, T, true, kKindNormLinear>(sh, a, s);
   const bool ch = sh.gate == GDR_GATE_CHANNEL;
   if (kind == kKindGatedLinear)
     return ch ? launch_one<D, C, T, true, kKindGatedLinear>(sh, a, s)

@@ -131,6 +131,23 @@ gdr_status gdr_prefill(const gdr_shape* shape, const void* q, const void* k, con
 size_t gdr_prefill_workspace_size(const gdr_shape* shape);
 
 /*
+ * gdr_normalized_linear_attn -- normalised phi-linear attention, chunked, packed varlen
+ * (heqinghuang "gpt2-to-kimi" §07; engineermaxxing "From GPT-2 to Kimi K3" §02g):
+ *   phi(x) = elu(x) + 1   (x + 1 for x > 0, e^x otherwise; applied to q and k by the kernel)
+ *   S <- S + phi(k_t) v_t^T,   z <- z + phi(k_t),   o_t = S^T phi(q_t) / (phi(q_t) . z + eps)
+ * per (sequence, head), the read after the write.  q, k, v, out, S0, S_final, cu_seqlens,
+ * workspace: as gdr_prefill (no alpha, no beta; shape->gate ignored).  z0: entering
+ * normalisers [n_seqs, H, d_k] fp32 or NULL for zeros; z_final: final normalisers or NULL; z_final
+ * must not be z0.  eps: a finite value >= 0 (0 divides by phi(q) . z, which is > 0 from the
+ * first token on unless phi underflows).  GDR_FLAG_LAYER_PROLOGUE is unsupported here.
+ */
+gdr_status gdr_normalized_linear_attn(const gdr_shape* shape, const void* q, const void* k,
+                                      const void* v, float eps, const float* S0, const float* z0,
+                                      const int32_t* cu_seqlens, void* out, float* S_final,
+                                      float* z_final, void* workspace, size_t workspace_bytes,
+                                      void* stream);
+
+/*
  * gdr_layer_prologue -- the layer prologue as a pass of its own (the maps that
  * GDR_FLAG_LAYER_PROLOGUE applies inside the kernels; heqinghuang "gpt2-to-kimi" §09,
  * engineermaxxing "From GPT-2 to Kimi K3" §05c and §06b):

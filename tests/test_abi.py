@@ -188,3 +188,24 @@ def test_layer_prologue_argument_errors(lib):
     assert call(k=FAKE) == 1                  # k onto xq
     assert call(shape=_shape(n_seqs=1, total_tokens=64, d_k=96, d_v=96)) == 2
     assert call(xq=None, shape=_shape(n_seqs=1, total_tokens=0)) == 0
+
+
+def test_normalized_linear_argument_errors(lib):
+    """gdr_normalized_linear_attn: eps must be finite and >= 0, z_final must not be z0, the
+    layer-prologue flag is unsupported -- rejected before any launch."""
+    P = ctypes.c_void_p
+    sh = _shape(n_seqs=1, total_tokens=64)
+
+    def call(eps=0.0, z0=None, zf=None, shape=sh):
+        return lib.gdr_normalized_linear_attn(ctypes.byref(shape), P(FAKE), P(FAKE + 4096),
+                                              P(FAKE + 8192), eps, None, P(z0), None,
+                                              P(FAKE + 65536), None, P(zf), P(FAKE * 2), 8, None)
+    assert call(eps=-1.0) == 1
+    assert call(eps=float("nan")) == 1
+    assert call(eps=float("inf")) == 1
+    assert call(z0=FAKE * 4, zf=FAKE * 4) == 1
+    assert call() == 1  # workspace too small (8 bytes)
+    from gated_delta_rule_prefill_gb300._abi import GDR_FLAG_LAYER_PROLOGUE
+    sh2 = _shape(n_seqs=1, total_tokens=64)
+    sh2.flags = GDR_FLAG_LAYER_PROLOGUE
+    assert call(shape=sh2) == 2
