@@ -91,6 +91,7 @@ KERNEL_SOURCES = {"gated_linear_attn": ["prefill_cluster.cu", "tc_common.cuh", "
                   "prefill_output_gate": ["prefill_cluster.cu", "tc_common.cuh", "umma.cuh"],
                   "prefill_prologue": ["prefill_cluster.cu", "tc_common.cuh", "umma.cuh"],
                   "layer_prologue": ["prologue.cu", "gdr_internal.cuh"],
+                  "normalized_linear_attn": ["linear_tc.cu", "tc_common.cuh", "umma.cuh"],
                   "prefill": ["prefill_cluster.cu", "tc_common.cuh", "umma.cuh"],
                   "linear_attn": ["linear_tc.cu", "tc_common.cuh", "umma.cuh"],
                   "decode": ["decode.cu"]}
@@ -441,7 +442,26 @@ def run_gpu(args):
     g1.record(stream)
     torch.cuda.synchronize()
     lp_ms = max_over_ranks([g0.elapsed_time(g1) / gla_steps], dev, world)[0]
-    del out_g, Sf_g, R, M
+    del R, M
+
+    # ---- normalised phi-linear attention (phi = elu + 1, normaliser z) on the same q, k, v
+    Zf = torch.empty((wp.n_seqs, H, d), dtype=torch.float32, device=dev)
+
+    def nla():
+        g.gdr_normalized_linear_attn(P["q"], P["k"], P["v"], eps=1e-6, S0=P["S0"],
+                                     cu_seqlens=P["cu_seqlens"], out=out_g, S_final=Sf_g,
+                                     z_final=Zf, workspace=ws)
+
+    for _ in range(3):
+        nla()
+    torch.cuda.synchronize()
+    g0.record(stream)
+    for _ in range(gla_steps):
+        nla()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    nla_ms = max_over_ranks([g0.elapsed_time(g1) / gla_steps], dev, world)[0]
+    del out_g, Sf_g, Zf
 
     # ---- end to end through the public API with host buffers (prefill), rank-local
     host_in = {k: P[k].cpu().pin_memory() for k in ("q", "k", "v", "alpha", "beta", "S0")}
@@ -514,6 +534,9 @@ def run_gpu(args):
                                     prefill_flops(T, H, d), og_ms / 1e3),
         "prefill_prologue": roof("prefill_prologue", prefill_bytes(T, H, d, wp.n_seqs),
                                  prefill_flops(T, H, d), pro_ms / 1e3),
+        "normalized_linear_attn": roof("normalized_linear_attn",
+                                       prefill_bytes(T, H, d, wp.n_seqs, linear=True),
+                                       prefill_flops(T, H, d, linear=True), nla_ms / 1e3),
         # read xq, xk (bf16), a (fp32 per channel), b; write q, k, alpha, beta
         "layer_prologue": roof("layer_prologue", 2 * T * H * (2 * d * 2 + d * 4 + 4), 0.0,
                                lp_ms / 1e3),
@@ -540,6 +563,7 @@ def run_gpu(args):
         "prefill_output_gate_tokens_per_s": job_tokens_per_s(n, T, og_ms / 1e3),
         "prefill_prologue_tokens_per_s": job_tokens_per_s(n, T, pro_ms / 1e3),
         "prefill_unfused_prologue_tokens_per_s": job_tokens_per_s(n, T, unf_ms / 1e3),
+        "normalized_linear_attn_tokens_per_s": job_tokens_per_s(n, T, nla_ms / 1e3),
         "roofline": main_roof,
         "kernels": kern,
         "kernels_outside_step": kern_extra,

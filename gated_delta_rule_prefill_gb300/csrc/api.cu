@@ -106,8 +106,8 @@ gdr_status prefill_common(const gdr_shape* sh, const void* q, const void* k, con
   prep_kernel<<<1, kPrepThreads, 0, s>>>(cu, sh->n_seqs, sh->total_tokens, order, status);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess)
-    e = prefill_tc_supported(*sh) && kind != kKindNormLinear ? launch_prefill_tc(*sh, a, kind, s)
-                                                             : launch_prefill_simt(*sh, a, kind, s);
+    e = prefill_tc_supported(*sh) ? launch_prefill_tc(*sh, a, kind, s)
+                                  : launch_prefill_simt(*sh, a, kind, s);
   return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }
 

@@ -12,6 +12,17 @@
 // and the O rows leave TMEM while the next chunk's MMAs run.  q, k, v of the next chunk are
 // fetched one chunk ahead.  With few (sequence, head) pairs each sequence is split into runs of
 // whole chunks, one CTA each, run g starting from S0 + sum of K^T V over the chunks before it.
+//
+// NORM: normalised phi-linear attention (heqinghuang "gpt2-to-kimi" §07, engineermaxxing §02g):
+// phi = elu + 1 is applied in place to the staged [K; Q] tile (elementwise, so the swizzle does
+// not matter; the result is rounded to bf16, the operand type; key rows past the chunk's end
+// are zeroed), and each output row is divided by
+//   phi(q_r) . z_r + eps = phi(q_r) . z_entry + sum_{j <= r} (Q K^T)[r][j] + eps,
+// the second term being the row sums of the masked score tile the kernel forms anyway (fp32,
+// before its bf16 rounding) and the first a 128-term dot product per row.  The normaliser is
+// the state's extra column: z - z0 = phi(K)^T 1 accumulates in TMEM by one more M = 128, N = 16
+// MMA per chunk against a tile of ones (the same A operand as the state update), including over
+// a run's prefix chunks.
 #include <cuda.h>
 
 #include "tc_common.cuh"
@@ -27,8 +38,11 @@ struct LinSmem {
   static constexpr uint32_t VIN = 65536;       // V [64 tok][128] SW128 x 2 buffers, 16 KB each
   static constexpr uint32_t ZM = VIN + 32768;  // [Z; M]: zeros 8 KB, then M [64][64] K-major
   static constexpr uint32_t SS = ZM + 16384;   // S [d_k][128] (MN-major B) x 2 buffers, 32 KB each
-  static constexpr uint32_t BARS = SS + 65536;  // ld[2], s, q, m2, pf_full[4], pf_mma[4], TMEM
-  static constexpr uint32_t END = BARS + 128;
+  static constexpr uint32_t ONES = SS + 65536;  // NORM: 16 x 64 bf16 ones (K-major B, N = 16)
+  static constexpr uint32_t BARS = ONES + 2048;  // ld[2], s, q, m2, pf_full[4], pf_mma[4], TMEM
+  static constexpr uint32_t ZB = BARS + 128;    // NORM: z entering chunk i at [i & 1] (2 x 128 fp32)
+  static constexpr uint32_t DP = ZB + 1024;     // NORM: denominator halves [i & 1][half][64 rows]
+  static constexpr uint32_t END = DP + 1024;
   static constexpr size_t bytes = END + 1024;
   // prefix stages (32 KB each, K at +0 / +16K, V at +8K / +24K): dead before the chunk loop
   __host__ __device__ static constexpr uint32_t pf(int st) {
@@ -38,7 +52,41 @@ struct LinSmem {
 };
 
 constexpr uint32_t kColD0 = 128, kColD1 = 256, kColA = 384;  // TMEM columns (S at 0)
+constexpr uint32_t kColZ = 448;  // NORM: phi(K)^T 1, 16 equal columns
 
+// phi = elu + 1 on `chunks` 16-byte chunks of bf16 at p, in place (thread-strided)
+__device__ __forceinline__ void phi_tile(unsigned char* p, int chunks, int tid) {
+  for (int i = tid; i < chunks; i += kThreads) {
+    uint4 u = reinterpret_cast<uint4*>(p)[i];
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(h[e]);
+      h[e] = __floats2bfloat162_rn(phi_f(f.x), phi_f(f.y));
+    }
+    reinterpret_cast<uint4*>(p)[i] = u;
+  }
+}
+
+// phi on a [K; Q] tile pair (2 slabs of 128 rows x 128 B), key rows >= n set to 0 instead
+__device__ __forceinline__ void phi_kq(unsigned char* p, int n, int tid) {
+  for (int i = tid; i < 2048; i += kThreads) {
+    const int row = (i & 1023) >> 3;
+    uint4 u = make_uint4(0u, 0u, 0u, 0u);
+    if (row >= 64 || row < n) {
+      u = reinterpret_cast<uint4*>(p)[i];
+      __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(h[e]);
+        h[e] = __floats2bfloat162_rn(phi_f(f.x), phi_f(f.y));
+      }
+    }
+    reinterpret_cast<uint4*>(p)[i] = u;
+  }
+}
+
+template <bool NORM>
 __global__ void __launch_bounds__(kThreads, 1)
     linear_tc_kernel(const __grid_constant__ TcMaps maps, const PrefillArgs a, int nseg) {
   using L = LinSmem;
@@ -74,6 +122,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) tmem_alloc(tslot, kTmemCols);
   for (int i = tid; i < 8192 / 16; i += kThreads)  // the zero half of [Z; M]
     reinterpret_cast<uint4*>(sm + L::ZM)[i] = make_uint4(0, 0, 0, 0);
+  if (NORM)
+    for (int i = tid; i < 2048 / 16; i += kThreads)  // bf16 ones
+      reinterpret_cast<uint4*>(sm + L::ONES)[i] =
+          make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
   fence_async_smem();
   if (tid == 0) {
     for (int i = 0; i < 13; ++i) mbar_init(bars + i, 1);
@@ -86,12 +138,73 @@ __global__ void __launch_bounds__(kThreads, 1)
   TcCtx x = make_ctx(sm, *tslot, bar_s);
   bool failed = false;
   s_init<DH>(x, a.S0 ? a.S0 + sidx + (size_t)x.lrow * kD : nullptr, sm + L::SS);
+  float* sZ = reinterpret_cast<float*>(sm + L::ZB);   // NORM: [2][128] z entering a chunk
+  float* sDp = reinterpret_cast<float*>(sm + L::DP);  // NORM: [2][2 halves][64 rows]
+  const size_t zidx = ((size_t)seq * H + h) * kD;
+  const float z0v = (NORM && tid < kD && a.z0) ? a.z0[zidx + tid] : 0.f;  // z0 of channel tid
+  bool zinit = false;  // kColZ holds a sum (an MMA has written it)
+  const Opnd opOnes{x.sb + L::ONES, 2048, false};
+  const uint32_t id_z = idesc_bf16(128, 16, false, true, false);  // phi(K)^T (MN-major A) x ones
   cta_sync_tc();  // every row of the bf16 state tile is written before the first MMA
   const uint32_t id_s = idesc_bf16(128, kD, false, true, true);   // K as MN-major A, V MN-major B
   const uint32_t id_d = idesc_bf16(128, kD, false, false, true);  // K-major A, MN-major B
   const uint32_t id_a = idesc_bf16(128, kC, false, false, false);  // [K; Q] K^T (K-major B)
 
-  if (c_begin > 0) {
+  if (NORM && c_begin > 0) {
+    // run prefix with the feature map: every thread waits for each stage, applies phi to its K
+    // tile and adds its column sums to z; warp 0 then issues S += phi(K)^T V
+    cta_sync_tc();  // S0 is in TMEM
+    bool pf_ok = true, mma_ok = true;
+    uint32_t ph_f = 0, ph_m = 0;
+    auto pf_issue = [&](int cp) {
+      const int st = cp & 3;
+      const int tc = (int)(t0 + (int64_t)cp * kC);
+      unsigned char* b = sm + L::pf(st);
+      mbar_expect_tx(pf_full + st, 32768);
+      tma_load_3d(b, &maps.k_sw, 0, h, tc, pf_full + st);
+      tma_load_3d(b + 16384, &maps.k_sw, 64, h, tc, pf_full + st);
+      tma_load_3d(b + 8192, &maps.v, 0, h, tc, pf_full + st);
+      tma_load_3d(b + 24576, &maps.v, 64, h, tc, pf_full + st);
+    };
+    if (tid == 0)
+      for (int cp = 0; cp < 3 && cp < c_begin; ++cp) pf_issue(cp);
+#pragma unroll 1
+    for (int cp = 0; cp < c_begin; ++cp) {
+      const int st = cp & 3;
+      const bool ok = mbar_wait(pf_full + st, (ph_f >> st) & 1u, kWaitNs);
+      ph_f ^= 1u << st;
+      __syncwarp();
+      // (this barrier also orders every read of chunk cp - 1's stage before its refill below)
+      if (__syncthreads_or(!ok || !mma_ok)) { pf_ok = false; break; }
+      phi_tile(sm + L::pf(st), 512, tid);          // K, channels 0-63
+      phi_tile(sm + L::pf(st) + 16384, 512, tid);  // K, channels 64-127
+      fence_async_smem();
+      __syncthreads();
+      if (warp == 0) {
+        const Opnd opK{x.sb + L::pf(st), 16384, true};
+        const Opnd opV{x.sb + L::pf(st) + 8192, 16384, true};
+        mma_run<kC>(x.tm + kColS, opK, opV, id_s, true);
+        mma_run<kC>(x.tm + kColZ, opK, opOnes, id_z, cp > 0);  // z += phi(K)^T 1
+        mma_commit_elect(pf_mma + st);
+      }
+      if (cp + 3 < c_begin && tid == 0) {  // stage (cp + 3) & 3 held chunk cp - 1
+        if (cp >= 1) {
+          const int sp = (cp - 1) & 3;
+          mma_ok = mbar_wait(pf_mma + sp, (ph_m >> sp) & 1u, kWaitNs);
+          ph_m ^= 1u << sp;
+        }
+        if (mma_ok) pf_issue(cp + 3);
+      }
+    }
+    if (warp == 0) mma_commit_elect(bar_s);  // every prefix MMA complete
+    zinit = true;
+    if (__syncthreads_or(!pf_ok) || !wait_bar(bar_s, x.ph_mma)) {
+      failed = true;
+    } else {
+      s_epilogue<DH>(x, sm + L::SS);
+      cta_sync_tc();
+    }
+  } else if (c_begin > 0) {
     // run prefix: S += K_c^T V_c over chunks [0, c_begin) (all full), 4 TMA stages, one chunk's
     // MMA per step; warp 0 drives it, the other warps wait at the barrier below
     cta_sync_tc();  // S0 is in TMEM
@@ -169,6 +282,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto o_store = [&](int i, int64_t tc, int n) {
     float v[64];
     tmem_ld64(x.tm + x.lane_base + d_col(i) + x.wh * 64, v);
+    if (NORM && qrow < n) {  // divide by phi(q_r) . z_r + eps
+      const float* dp = sDp + (i & 1) * 128;
+      const float inv = 1.f / (dp[qrow] + dp[64 + qrow] + a.eps);
+#pragma unroll
+      for (int j = 0; j < 64; ++j) v[j] *= inv;
+    }
     if (qrow < n) {
       __nv_bfloat16* dst = out + ((size_t)(tc + qrow) * H + h) * kD + x.wh * 64;
 #pragma unroll
@@ -194,6 +313,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (__syncthreads_or(!ok)) { failed = true; break; }
       fence_after_sync();
     }
+    if (NORM) {
+      // z entering the chunk (z0 + the ones-column sum, final since the last bar_s wait), then
+      // the feature map on the whole [K; Q] tile before any MMA reads it
+      if (warp < 4)
+        sZ[(i & 1) * kD + tid] = z0v + (zinit ? tmem_ld1(x.tm + x.lane_base + kColZ) : 0.f);
+      phi_kq(sm + L::KQ + b * 32768, n, tid);
+      fence_async_smem();
+      cta_sync_tc();
+    }
     if (i + 1 < nloc) issue_ld(i + 1);  // buffer b ^ 1: chunk i - 1's MMAs are complete
     const Opnd opKQ{x.sb + L::KQ + b * 32768, 16384, false};  // [K; Q], K-major A (M = 128)
     const Opnd opKa{x.sb + L::KQ + b * 32768, 16384, true};   // K as MN-major A (M = d_k)
@@ -203,11 +331,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const Opnd opZM{x.sb + L::ZM, 16384, false};
     if (warp == 0) {
       mma_run<kC>(x.tm + kColS, opKa, opV, id_s, true);  // S += K^T V
+      if (NORM) mma_run<kC>(x.tm + kColZ, opKa, opOnes, id_z, zinit);  // z += phi(K)^T 1
       mma_commit_elect(bar_s);
       mma_run<kD>(x.tm + d_col(i), opKQ, opS, id_d, false);  // [K; Q] S
       mma_run<kD>(x.tm + kColA, opKQ, opKb, id_a, false);    // [K; Q] K^T
       mma_commit_elect(bar_q);
     }
+    zinit = true;
     if (i > 0 && o_rows) o_store(i - 1, tc - kC, kC);
     // the state's bf16 operand for the next chunk (the other buffer: this chunk's Q S reads this)
     if (!wait_bar(bar_s, x.ph_mma)) { failed = true; break; }
@@ -218,6 +348,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(x.tm + x.lane_base + kColA + 32 * x.wh, v);
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = (32 * x.wh + j <= qrow) ? v[j] : 0.f;
+      if (NORM) {  // this half's share of phi(q_r) . z_r: masked score sum + phi(q_r) . z_entry
+        float rs = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) rs += v[j];
+        const unsigned char* qp = sm + L::KQ + b * 32768 + x.wh * 16384 + (64 + qrow) * 128;
+        const float* z = sZ + (i & 1) * kD + 64 * x.wh;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          float q8[8];
+          ld_bf16x8(reinterpret_cast<const __nv_bfloat16*>(qp + ((ch ^ (qrow & 7)) << 4)), q8);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) rs = fmaf(q8[e], z[8 * ch + e], rs);
+        }
+        sDp[(i & 1) * 128 + x.wh * 64 + qrow] = rs;
+      }
 #pragma unroll
       for (int j = 0; j < 32; j += 8) st_chunk8(sm + L::ZM + 8192, 8192, qrow, 32 * x.wh + j, v + j);
       fence_async_smem();
@@ -239,8 +384,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // let copies already in flight land before the shared memory is released
     mbar_wait(bar_ld, ph_ld[0], kWaitNs);
     mbar_wait(bar_ld + 1, ph_ld[1], kWaitNs);
-  } else if (a.S_final && c_end == nch) {  // the last run of the sequence hands the state on
-    s_final<DH>(x, a.S_final + sidx + (size_t)x.lrow * kD);
+  } else {
+    if (a.S_final && c_end == nch)  // the last run of the sequence hands the state on
+      s_final<DH>(x, a.S_final + sidx + (size_t)x.lrow * kD);
+    if (NORM && a.z_final && c_end == nch && warp < 4) {
+      const float zt = zinit ? tmem_ld1(x.tm + x.lane_base + kColZ) : 0.f;
+      a.z_final[zidx + tid] = z0v + zt;
+    }
   }
   cta_sync_tc();
   if (warp == 0) tmem_dealloc(x.tm, kTmemCols);
@@ -257,7 +407,7 @@ int sm_count() {
 }  // namespace
 
 cudaError_t launch_linear_tc(const gdr_shape& sh, const PrefillArgs& a, const TcMaps& maps,
-                             cudaStream_t s) {
+                             bool norm, cudaStream_t s) {
   // few (sequence, head) pairs: runs of at least 16 chunks per CTA, as many as fill the SMs once
   const long pairs = (long)sh.n_seqs * sh.H;
   const long avg_chunks = sh.total_tokens / ((long)sh.n_seqs * kC);
@@ -267,12 +417,12 @@ cudaError_t launch_linear_tc(const gdr_shape& sh, const PrefillArgs& a, const Tc
   // an in-place hand-off (S_final = S0) keeps one run per sequence: a later run reads S0 while
   // the last run of the same sequence writes S_final
   if (nseg < 1 || (a.S0 && a.S0 == a.S_final)) nseg = 1;
-  cudaError_t e = cudaFuncSetAttribute(linear_tc_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto kern = norm ? linear_tc_kernel<true> : linear_tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)LinSmem::bytes);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)sh.n_seqs * (unsigned)sh.H * (unsigned)nseg;
-  linear_tc_kernel<<<grid, kThreads, LinSmem::bytes, s>>>(maps, a, (int)nseg);
+  kern<<<grid, kThreads, LinSmem::bytes, s>>>(maps, a, (int)nseg);
   return cudaGetLastError();
 }
 

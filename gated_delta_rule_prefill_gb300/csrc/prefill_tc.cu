@@ -362,10 +362,10 @@ bool prefill_tc_supported(const gdr_shape& sh) {
 
 cudaError_t launch_prefill_tc(const gdr_shape& sh, const PrefillArgs& a, int kind,
                               cudaStream_t s) {
-  const bool linear = kind == kKindLinear;
+  const bool linear = kind == kKindLinear || kind == kKindNormLinear;
   TcMaps maps;
   if (!tc::make_tc_maps(sh, a, linear, &maps)) return cudaErrorInvalidValue;
-  if (linear) return tc::launch_linear_tc(sh, a, maps, s);  // linear_tc.cu
+  if (linear) return tc::launch_linear_tc(sh, a, maps, kind == kKindNormLinear, s);  // linear_tc.cu
   const long pairs = (long)sh.n_seqs * sh.H;
   // gated linear attention: without stages 3-4; helper CTAs in clusters where they fit, else
   // the one-CTA kernel

@@ -1000,7 +1000,7 @@ __device__ void zero_v_tail(const TcCtx& x, unsigned char* vin, int n) {
 bool make_tc_maps(const gdr_shape& sh, const PrefillArgs& a, bool linear, TcMaps* maps);
 // host side: the linear-attention kernel (bf16, d = 128)
 cudaError_t launch_linear_tc(const gdr_shape& sh, const PrefillArgs& a, const TcMaps& maps,
-                             cudaStream_t s);
+                             bool norm, cudaStream_t s);
 // host side: CTAs of the work-queue prefill for this shape and workspace (0: use another kernel)
 int queue_grid_for(const gdr_shape& sh, const PrefillArgs& a);
 cudaError_t launch_prefill_queue(const gdr_shape& sh, const PrefillArgs& a, const TcMaps& maps,

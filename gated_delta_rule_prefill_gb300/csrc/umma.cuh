@@ -187,6 +187,17 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float (&v)
 }
 
 // 64 consecutive columns (two 32-column loads, one wait): twice the bytes per round trip.
+// one TMEM column of the warp's 32 lanes (one value per lane)
+__device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
+  uint32_t r;
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r)
+      : "r"(taddr));
+  return __uint_as_float(r);
+}
+
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
   tmem_ld32x2(taddr, taddr + 32u, v);
 }
