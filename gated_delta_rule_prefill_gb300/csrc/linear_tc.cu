@@ -12,6 +12,10 @@
 // and the O rows leave TMEM while the next chunk's MMAs run.  q, k, v of the next chunk are
 // fetched one chunk ahead.  With few (sequence, head) pairs each sequence is split into runs of
 // whole chunks, one CTA each, run g starting from S0 + sum of K^T V over the chunks before it.
+// Where the workspace has room (it holds the work-queue rings for such shapes), that sum comes
+// from a first launch (MODE 1: every run but the last computes its own sum_c K_c^T V_c, once)
+// and the second launch (MODE 2) adds the sums of the runs before it to S0; without the room,
+// each run rebuilds it from the chunks before it (MODE 0).
 //
 // NORM: normalised phi-linear attention (heqinghuang "gpt2-to-kimi" §07, engineermaxxing §02g):
 // phi = elu + 1 is applied in place to the staged [K; Q] tile (elementwise, so the swizzle does
@@ -86,9 +90,14 @@ __device__ __forceinline__ void phi_kq(unsigned char* p, int n, int tid) {
   }
 }
 
-template <bool NORM>
+// run sums in the workspace: per (sequence, head, run < nseg - 1) the d_k x d_v fp32 sum of
+// phi(K)^T V (or K^T V) over the run's chunks, then its d_k key sums (NORM)
+constexpr int kDeltaFloats = kD * kD + kD;
+
+template <bool NORM, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
-    linear_tc_kernel(const __grid_constant__ TcMaps maps, const PrefillArgs a, int nseg) {
+    linear_tc_kernel(const __grid_constant__ TcMaps maps, const PrefillArgs a, int nseg,
+                     float* delta) {
   using L = LinSmem;
   constexpr int DH = kD / 2;
   extern __shared__ unsigned char smem_raw[];
@@ -106,9 +115,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5;
   const int H = a.H;
-  const int per_seq = H * nseg;
+  const int nrun = MODE == 1 ? nseg - 1 : nseg;  // CTAs per (sequence, head)
+  const int per_seq = H * nrun;
   const int rank = blockIdx.x / per_seq;
-  const int h = (blockIdx.x % per_seq) / nseg, g = blockIdx.x % nseg;
+  const int h = (blockIdx.x % per_seq) / nrun, g = blockIdx.x % nrun;
   const int seq = a.order ? a.order[rank] : rank;
   int64_t t0, t1;
   if (!seq_range(a, seq, t0, t1)) return;
@@ -116,6 +126,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lseg = (nch + nseg - 1) / nseg;
   const int c_begin = g * lseg, c_end = min(nch, c_begin + lseg);
   if (g > 0 && c_begin >= c_end) return;
+  // MODE 1: only a run followed by a non-empty run has a sum to hand on (all its chunks full)
+  if (MODE == 1 && (c_begin >= c_end || c_end >= nch)) return;
+  // the chunks summed into the state before the chunk loop: the run's own (MODE 1), the ones
+  // before the run (MODE 0), none (MODE 2: the sums come from the workspace)
+  const int p_lo = MODE == 1 ? c_begin : 0;
+  const int p_hi = MODE == 1 ? c_end : MODE == 0 ? c_begin : 0;
+  float* drun = MODE == 1 ? delta + (((size_t)seq * H + h) * (nseg - 1) + g) * kDeltaFloats
+                          : nullptr;
   const size_t sidx = ((size_t)seq * H + h) * kD * kD;
   __nv_bfloat16* __restrict__ out = static_cast<__nv_bfloat16*>(a.out);
 
@@ -137,11 +155,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   cta_sync_tc();
   TcCtx x = make_ctx(sm, *tslot, bar_s);
   bool failed = false;
-  s_init<DH>(x, a.S0 ? a.S0 + sidx + (size_t)x.lrow * kD : nullptr, sm + L::SS);
+  if (MODE == 2 && g > 0) {  // S0 + the sums of the runs before this one
+    float v[DH];
+    const float* s0r = a.S0 ? a.S0 + sidx + (size_t)x.lrow * kD + x.wh * DH : nullptr;
+#pragma unroll
+    for (int j = 0; j < DH; ++j) v[j] = s0r ? s0r[j] : 0.f;
+    for (int gp = 0; gp < g; ++gp) {
+      const float* dr = delta + (((size_t)seq * H + h) * (nseg - 1) + gp) * kDeltaFloats +
+                        (size_t)x.lrow * kD + x.wh * DH;
+#pragma unroll
+      for (int j = 0; j < DH; j += 4) {
+        const float4 u = *reinterpret_cast<const float4*>(dr + j);
+        v[j] += u.x, v[j + 1] += u.y, v[j + 2] += u.z, v[j + 3] += u.w;
+      }
+    }
+    tmem_st_half<DH>(x.tm + x.lane_base + kColS + x.wh * DH, v);
+#pragma unroll
+    for (int j = 0; j < DH; j += 8) st_chunk8(sm + L::SS, 16384, x.lrow, x.wh * DH + j, v + j);
+    tmem_wait_st();
+    fence_async_smem();
+  } else {
+    s_init<DH>(x, MODE != 1 && a.S0 ? a.S0 + sidx + (size_t)x.lrow * kD : nullptr, sm + L::SS);
+  }
   float* sZ = reinterpret_cast<float*>(sm + L::ZB);   // NORM: [2][128] z entering a chunk
   float* sDp = reinterpret_cast<float*>(sm + L::DP);  // NORM: [2][2 halves][64 rows]
   const size_t zidx = ((size_t)seq * H + h) * kD;
-  const float z0v = (NORM && tid < kD && a.z0) ? a.z0[zidx + tid] : 0.f;  // z0 of channel tid
+  float z0v = (NORM && MODE != 1 && tid < kD && a.z0) ? a.z0[zidx + tid] : 0.f;  // channel tid
+  if (NORM && MODE == 2 && tid < kD)
+    for (int gp = 0; gp < g; ++gp)
+      z0v += delta[(((size_t)seq * H + h) * (nseg - 1) + gp) * kDeltaFloats + kD * kD + tid];
   bool zinit = false;  // kColZ holds a sum (an MMA has written it)
   const Opnd opOnes{x.sb + L::ONES, 2048, false};
   const uint32_t id_z = idesc_bf16(128, 16, false, true, false);  // phi(K)^T (MN-major A) x ones
@@ -150,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t id_d = idesc_bf16(128, kD, false, false, true);  // K-major A, MN-major B
   const uint32_t id_a = idesc_bf16(128, kC, false, false, false);  // [K; Q] K^T (K-major B)
 
-  if (NORM && c_begin > 0) {
+  if (NORM && p_hi > p_lo) {
     // run prefix with the feature map: every thread waits for each stage, applies phi to its K
     // tile and adds its column sums to z; warp 0 then issues S += phi(K)^T V
     cta_sync_tc();  // S0 is in TMEM
@@ -158,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t ph_f = 0, ph_m = 0;
     auto pf_issue = [&](int cp) {
       const int st = cp & 3;
-      const int tc = (int)(t0 + (int64_t)cp * kC);
+      const int tc = (int)(t0 + (int64_t)(p_lo + cp) * kC);
       unsigned char* b = sm + L::pf(st);
       mbar_expect_tx(pf_full + st, 32768);
       tma_load_3d(b, &maps.k_sw, 0, h, tc, pf_full + st);
@@ -167,9 +209,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_3d(b + 24576, &maps.v, 64, h, tc, pf_full + st);
     };
     if (tid == 0)
-      for (int cp = 0; cp < 3 && cp < c_begin; ++cp) pf_issue(cp);
+      for (int cp = 0; cp < 3 && cp < p_hi - p_lo; ++cp) pf_issue(cp);
 #pragma unroll 1
-    for (int cp = 0; cp < c_begin; ++cp) {
+    for (int cp = 0; cp < p_hi - p_lo; ++cp) {
       const int st = cp & 3;
       const bool ok = mbar_wait(pf_full + st, (ph_f >> st) & 1u, kWaitNs);
       ph_f ^= 1u << st;
@@ -187,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_run<kC>(x.tm + kColZ, opK, opOnes, id_z, cp > 0);  // z += phi(K)^T 1
         mma_commit_elect(pf_mma + st);
       }
-      if (cp + 3 < c_begin && tid == 0) {  // stage (cp + 3) & 3 held chunk cp - 1
+      if (cp + 3 < p_hi - p_lo && tid == 0) {  // stage (cp + 3) & 3 held chunk cp - 1
         if (cp >= 1) {
           const int sp = (cp - 1) & 3;
           mma_ok = mbar_wait(pf_mma + sp, (ph_m >> sp) & 1u, kWaitNs);
@@ -204,8 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       s_epilogue<DH>(x, sm + L::SS);
       cta_sync_tc();
     }
-  } else if (c_begin > 0) {
-    // run prefix: S += K_c^T V_c over chunks [0, c_begin) (all full), 4 TMA stages, one chunk's
+  } else if (p_hi > p_lo) {
+    // run prefix: S += K_c^T V_c over chunks [p_lo, p_hi) (all full), 4 TMA stages, one chunk's
     // MMA per step; warp 0 drives it, the other warps wait at the barrier below
     cta_sync_tc();  // S0 is in TMEM
     bool pf_ok = true;
@@ -219,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto pf_issue = [&](int cp) {
         if (tid == 0) {
           const int st = cp & 3;
-          const int tc = (int)(t0 + (int64_t)cp * kC);
+          const int tc = (int)(t0 + (int64_t)(p_lo + cp) * kC);
           unsigned char* b = sm + L::pf(st);
           mbar_expect_tx(pf_full + st, 32768);
           tma_load_3d(b, &maps.k_sw, 0, h, tc, pf_full + st);
@@ -228,9 +270,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(b + 24576, &maps.v, 64, h, tc, pf_full + st);
         }
       };
-      for (int cp = 0; cp < 3 && cp < c_begin; ++cp) pf_issue(cp);
+      for (int cp = 0; cp < 3 && cp < p_hi - p_lo; ++cp) pf_issue(cp);
 #pragma unroll 1
-      for (int cp = 0; cp < c_begin; ++cp) {
+      for (int cp = 0; cp < p_hi - p_lo; ++cp) {
         const int st = cp & 3;
         if (!warp_wait(pf_full + st, (ph_f >> st) & 1u)) { pf_ok = false; break; }
         ph_f ^= 1u << st;
@@ -238,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Opnd opV{x.sb + L::pf(st) + 8192, 16384, true};
         mma_run<kC>(x.tm + kColS, opK, opV, id_s, true);
         mma_commit_elect(pf_mma + st);
-        if (cp + 3 < c_begin) {  // stage (cp + 3) & 3 held chunk cp - 1: its MMA must be done
+        if (cp + 3 < p_hi - p_lo) {  // stage (cp + 3) & 3 held chunk cp - 1: its MMA must be done
           if (cp >= 1) {
             const int sp = (cp - 1) & 3;
             if (!warp_wait(pf_mma + sp, (ph_m >> sp) & 1u)) { pf_ok = false; break; }
@@ -257,6 +299,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  if (MODE == 1) {  // hand the run's sums on through the workspace
+    if (failed) {
+      if (tid == 0) report(a.status, GDR_DEVCHECK_TIMEOUT);
+    } else {
+      s_final<DH>(x, drun + (size_t)x.lrow * kD);
+      if (NORM && warp < 4) drun[kD * kD + tid] = tmem_ld1(x.tm + x.lane_base + kColZ);
+    }
+    cta_sync_tc();
+    if (warp == 0) tmem_dealloc(x.tm, kTmemCols);
+    return;
+  }
   const int64_t ts = t0 + (int64_t)c_begin * kC;
   const int64_t te = t0 + (int64_t)c_end * kC < t1 ? t0 + (int64_t)c_end * kC : t1;
   const int nloc = c_end - c_begin;
@@ -417,12 +470,31 @@ cudaError_t launch_linear_tc(const gdr_shape& sh, const PrefillArgs& a, const Tc
   // an in-place hand-off (S_final = S0) keeps one run per sequence: a later run reads S0 while
   // the last run of the same sequence writes S_final
   if (nseg < 1 || (a.S0 && a.S0 == a.S_final)) nseg = 1;
-  auto kern = norm ? linear_tc_kernel<true> : linear_tc_kernel<false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)LinSmem::bytes);
-  if (e != cudaSuccess) return e;
+  // the runs' sums through the workspace where its work-queue area holds them
+  const size_t need = (size_t)pairs * (size_t)(nseg - 1) * kDeltaFloats * sizeof(float);
+  const size_t room = a.ring ? (size_t)WorkspaceLayout::ring_pairs(sh) *
+                                   WorkspaceLayout::kRingSlots * WorkspaceLayout::kRingSlotBytes
+                             : 0;
+  const bool two = nseg > 1 && need <= room;
+  float* delta = two ? reinterpret_cast<float*>(a.ring) : nullptr;
+  auto k0 = norm ? linear_tc_kernel<true, 0> : linear_tc_kernel<false, 0>;
+  auto k1 = norm ? linear_tc_kernel<true, 1> : linear_tc_kernel<false, 1>;
+  auto k2 = norm ? linear_tc_kernel<true, 2> : linear_tc_kernel<false, 2>;
+  for (auto kern : {k0, k1, k2}) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)LinSmem::bytes);
+    if (e != cudaSuccess) return e;
+  }
   const unsigned grid = (unsigned)sh.n_seqs * (unsigned)sh.H * (unsigned)nseg;
-  kern<<<grid, kThreads, LinSmem::bytes, s>>>(maps, a, (int)nseg);
+  if (two) {
+    const unsigned grid1 = (unsigned)sh.n_seqs * (unsigned)sh.H * (unsigned)(nseg - 1);
+    k1<<<grid1, kThreads, LinSmem::bytes, s>>>(maps, a, (int)nseg, delta);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    k2<<<grid, kThreads, LinSmem::bytes, s>>>(maps, a, (int)nseg, delta);
+  } else {
+    k0<<<grid, kThreads, LinSmem::bytes, s>>>(maps, a, (int)nseg, nullptr);
+  }
   return cudaGetLastError();
 }
 

@@ -93,6 +93,32 @@ def test_linear_attn_segmented(lens, H):
           "linear segmented %s H=%d" % (lens, H))
 
 
+@pytest.mark.parametrize("lens,H", [([9000], 1), ([5000, 4000, 64], 2)])
+def test_linear_attn_segmented_min_workspace(lens, H):
+    """The same runs with a workspace too small to hold the runs' sums (header and visiting
+    order only): each run rebuilds its entering state from the chunks before it instead of
+    reading the sums a first launch wrote.  Also the normalised phi-linear form, whose runs
+    rebuild z the same way."""
+    g = _lib()
+    wl = gi.custom(seed=33 + H, seqlens=lens, H=H, d_k=128, d_v=128, dtype="bf16", s0="normal")
+    a = gi.gen_full(wl)
+    d = dev_inputs(a, "bf16")
+    n = len(lens)
+    ws = torch.empty(256 + (4 * n + 255) // 256 * 256, dtype=torch.uint8, device="cuda")
+    out, sf = g.gdr_linear_attn(d["q"], d["k"], d["v"], S0=d["S0"], cu_seqlens=d["cu_seqlens"],
+                                workspace=ws)
+    torch.cuda.synchronize()
+    check((host(out), host(sf)), ref_prefill(a, linear=True), TOL["bf16"],
+          "linear min-workspace %s H=%d" % (lens, H))
+    o2, s2, z2 = g.gdr_normalized_linear_attn(d["q"], d["k"], d["v"], eps=1e-6, S0=d["S0"],
+                                              cu_seqlens=d["cu_seqlens"], workspace=ws)
+    torch.cuda.synchronize()
+    ro, rs, rz = oracle.normalized_linear(a["q"], a["k"], a["v"], S0=a["S0"],
+                                          cu_seqlens=a["cu_seqlens"], eps=1e-6)
+    check((host(o2), host(s2)), (ro, rs), TOL["bf16"], "normalised min-workspace")
+    assert rel_rows(host(z2), rz) <= TOL["bf16"]
+
+
 @pytest.mark.parametrize("linear", [False, True])
 def test_in_place_state_hand_off(linear):
     """S_final = S0 (the documented in-place hand-off) on a workload whose linear pass would
