@@ -193,8 +193,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t id_a = idesc_bf16(128, kC, false, false, false);  // [K; Q] K^T (K-major B)
 
   if (NORM && p_hi > p_lo) {
-    // run prefix with the feature map: every thread waits for each stage, applies phi to its K
-    // tile and adds its column sums to z; warp 0 then issues S += phi(K)^T V
+    // run prefix with the feature map: every thread waits for each stage and applies phi to its
+    // K tile; warp 0 then issues S += phi(K)^T V and z += phi(K)^T 1
     cta_sync_tc();  // S0 is in TMEM
     bool pf_ok = true, mma_ok = true;
     uint32_t ph_f = 0, ph_m = 0;
@@ -208,20 +208,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_3d(b + 8192, &maps.v, 0, h, tc, pf_full + st);
       tma_load_3d(b + 24576, &maps.v, 64, h, tc, pf_full + st);
     };
-    if (tid == 0)
-      for (int cp = 0; cp < 3 && cp < p_hi - p_lo; ++cp) pf_issue(cp);
-#pragma unroll 1
-    for (int cp = 0; cp < p_hi - p_lo; ++cp) {
+    // a stage is made ready (loaded, phi on its K) while the previous stage's MMAs run
+    auto stage_ready = [&](int cp) {
       const int st = cp & 3;
       const bool ok = mbar_wait(pf_full + st, (ph_f >> st) & 1u, kWaitNs);
       ph_f ^= 1u << st;
+      if (ok) {
+        phi_tile(sm + L::pf(st), 512, tid);          // K, channels 0-63
+        phi_tile(sm + L::pf(st) + 16384, 512, tid);  // K, channels 64-127
+        fence_async_smem();
+      }
+      return ok;
+    };
+    if (tid == 0)
+      for (int cp = 0; cp < 3 && cp < p_hi - p_lo; ++cp) pf_issue(cp);
+    bool ok = stage_ready(0);
+#pragma unroll 1
+    for (int cp = 0; cp < p_hi - p_lo; ++cp) {
+      const int st = cp & 3;
       __syncwarp();
-      // (this barrier also orders every read of chunk cp - 1's stage before its refill below)
+      // stage cp is ready on every thread; this barrier also orders every read of chunk
+      // cp - 1's stage before its refill below
       if (__syncthreads_or(!ok || !mma_ok)) { pf_ok = false; break; }
-      phi_tile(sm + L::pf(st), 512, tid);          // K, channels 0-63
-      phi_tile(sm + L::pf(st) + 16384, 512, tid);  // K, channels 64-127
-      fence_async_smem();
-      __syncthreads();
       if (warp == 0) {
         const Opnd opK{x.sb + L::pf(st), 16384, true};
         const Opnd opV{x.sb + L::pf(st) + 8192, 16384, true};
@@ -237,6 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (mma_ok) pf_issue(cp + 3);
       }
+      if (cp + 1 < p_hi - p_lo) ok = stage_ready(cp + 1);
     }
     if (warp == 0) mma_commit_elect(bar_s);  // every prefix MMA complete
     zinit = true;
@@ -353,27 +362,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
   uint32_t ph_ld[2] = {0, 0}, ph_q = 0, ph_m2 = 0;
+  // NORM: wait for chunk j's tiles, zero its V tail, apply phi to its [K; Q] tile (all threads)
+  bool next_ok = true;
+  auto make_ready = [&](int j) {
+    const int bj = j & 1;
+    const int64_t tcj = ts + (int64_t)j * kC;
+    const int nj = (int)((te - tcj) < (int64_t)kC ? (te - tcj) : (int64_t)kC);
+    const bool ok = mbar_wait(bar_ld + bj, ph_ld[bj], kWaitNs);
+    ph_ld[bj] ^= 1u;
+    if (ok) {
+      if (nj < kC) zero_v_tail<kD>(x, sm + L::VIN + bj * 16384, nj);
+      phi_kq(sm + L::KQ + bj * 32768, nj, tid);
+      fence_async_smem();
+    }
+    return ok;
+  };
   if (!failed && nloc > 0) issue_ld(0);
 #pragma unroll 1
   for (int i = 0; i < nloc && !failed; ++i) {
     const int b = i & 1;
     const int64_t tc = ts + (int64_t)i * kC;
     const int n = (int)((te - tc) < (int64_t)kC ? (te - tc) : (int64_t)kC);
-    {
+    if (NORM) {
+      // the chunk's tiles were made ready (loaded, tail zeroed, phi applied) while the previous
+      // chunk's last MMA ran; z entering the chunk = z0 + the ones-column sum (final since the
+      // last bar_s wait)
+      if (i == 0) next_ok = make_ready(0);
+      if (warp < 4)
+        sZ[(i & 1) * kD + tid] = z0v + (zinit ? tmem_ld1(x.tm + x.lane_base + kColZ) : 0.f);
+      fence_before_sync();
+      if (__syncthreads_or(!next_ok)) { failed = true; break; }
+      fence_after_sync();
+    } else {
       const bool ok = mbar_wait(bar_ld + b, ph_ld[b], kWaitNs);
       ph_ld[b] ^= 1u;
       if (ok && n < kC) zero_v_tail<kD>(x, sm + L::VIN + b * 16384, n);  // padded rows: no K^T V
       if (__syncthreads_or(!ok)) { failed = true; break; }
       fence_after_sync();
-    }
-    if (NORM) {
-      // z entering the chunk (z0 + the ones-column sum, final since the last bar_s wait), then
-      // the feature map on the whole [K; Q] tile before any MMA reads it
-      if (warp < 4)
-        sZ[(i & 1) * kD + tid] = z0v + (zinit ? tmem_ld1(x.tm + x.lane_base + kColZ) : 0.f);
-      phi_kq(sm + L::KQ + b * 32768, n, tid);
-      fence_async_smem();
-      cta_sync_tc();
     }
     if (i + 1 < nloc) issue_ld(i + 1);  // buffer b ^ 1: chunk i - 1's MMAs are complete
     const Opnd opKQ{x.sb + L::KQ + b * 32768, 16384, false};  // [K; Q], K-major A (M = 128)
@@ -425,6 +450,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_run<kC>(x.tm + d_col(i), opZM, opV, id_d, true);  // rows 64-127 += M V
       mma_commit_elect(bar_m2);
     }
+    // NORM: the next chunk's tiles (buffer b ^ 1, loaded since this chunk began) made ready
+    // while that MMA runs
+    if (NORM && i + 1 < nloc) next_ok = make_ready(i + 1);
     // buffer b (q, k, v) and M are reused only after this MMA completes
     if (!wait_bar(bar_m2, ph_m2)) { failed = true; break; }
   }

@@ -99,7 +99,7 @@ def test_linear_attn_segmented_min_workspace(lens, H):
     order only): each run rebuilds its entering state from the chunks before it instead of
     reading the sums a first launch wrote.  Also the normalised phi-linear form, whose runs
     rebuild z the same way."""
-    g = _lib()
+    import gated_delta_rule_prefill_gb300 as g
     wl = gi.custom(seed=33 + H, seqlens=lens, H=H, d_k=128, d_v=128, dtype="bf16", s0="normal")
     a = gi.gen_full(wl)
     d = dev_inputs(a, "bf16")
