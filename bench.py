@@ -570,7 +570,7 @@ def run_gpu(args):
         "e2e": {"value": job_tokens_per_s(n, T, e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "what": "gdr_prefill_host: pinned host inputs in, "
                 "out and S_final back, copies pipelined with the kernels inside the call"},
-        "gpu_launches": 5 * K,
+        "gpu_launches": 6 * K,  # per step: prep + prefill, prep + linear run sums + linear runs, decode
         "clocks": clk,
     }
     if cpu:
