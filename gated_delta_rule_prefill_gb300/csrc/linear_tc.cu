@@ -386,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (NORM) {
       // the chunk's tiles were made ready (loaded, tail zeroed, phi applied) while the previous
       // chunk's last MMA ran; z entering the chunk = z0 + the ones-column sum (final since the
-      // last bar_s wait)
+      // previous chunk's m2 wait, or the prefix's bar_s wait)
       if (i == 0) next_ok = make_ready(0);
       if (warp < 4)
         sZ[(i & 1) * kD + tid] = z0v + (zinit ? tmem_ld1(x.tm + x.lane_base + kColZ) : 0.f);
@@ -409,14 +409,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const Opnd opZM{x.sb + L::ZM, 16384, false};
     if (warp == 0) {
       mma_run<kC>(x.tm + kColS, opKa, opV, id_s, true);  // S += K^T V
-      if (NORM) mma_run<kC>(x.tm + kColZ, opKa, opOnes, id_z, zinit);  // z += phi(K)^T 1
       mma_commit_elect(bar_s);
       mma_run<kD>(x.tm + d_col(i), opKQ, opS, id_d, false);  // [K; Q] S
       mma_run<kD>(x.tm + kColA, opKQ, opKb, id_a, false);    // [K; Q] K^T
       mma_commit_elect(bar_q);
     }
-    zinit = true;
     if (i > 0 && o_rows) o_store(i - 1, tc - kC, kC);
+    float qz = 0.f;  // NORM: this thread's half of phi(q_r) . z_entry, off the M-step path
+    if (NORM && o_rows) {
+      const unsigned char* qp = sm + L::KQ + b * 32768 + x.wh * 16384 + (64 + qrow) * 128;
+      const float* z = sZ + (i & 1) * kD + 64 * x.wh;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        float q8[8];
+        ld_bf16x8(reinterpret_cast<const __nv_bfloat16*>(qp + ((ch ^ (qrow & 7)) << 4)), q8);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e & 3] = fmaf(q8[e], z[8 * ch + e], acc[e & 3]);
+      }
+      qz = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    }
     // the state's bf16 operand for the next chunk (the other buffer: this chunk's Q S reads this)
     if (!wait_bar(bar_s, x.ph_mma)) { failed = true; break; }
     s_epilogue<DH>(x, sm + L::SS + (b ^ 1) * 32768);
@@ -427,19 +439,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = (32 * x.wh + j <= qrow) ? v[j] : 0.f;
       if (NORM) {  // this half's share of phi(q_r) . z_r: masked score sum + phi(q_r) . z_entry
-        float rs = 0.f;
+        float rs[4] = {qz, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int j = 0; j < 32; ++j) rs += v[j];
-        const unsigned char* qp = sm + L::KQ + b * 32768 + x.wh * 16384 + (64 + qrow) * 128;
-        const float* z = sZ + (i & 1) * kD + 64 * x.wh;
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          float q8[8];
-          ld_bf16x8(reinterpret_cast<const __nv_bfloat16*>(qp + ((ch ^ (qrow & 7)) << 4)), q8);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) rs = fmaf(q8[e], z[8 * ch + e], rs);
-        }
-        sDp[(i & 1) * 128 + x.wh * 64 + qrow] = rs;
+        for (int j = 0; j < 32; ++j) rs[j & 3] += v[j];
+        sDp[(i & 1) * 128 + x.wh * 64 + qrow] = (rs[0] + rs[1]) + (rs[2] + rs[3]);
       }
 #pragma unroll
       for (int j = 0; j < 32; j += 8) st_chunk8(sm + L::ZM + 8192, 8192, qrow, 32 * x.wh + j, v + j);
@@ -448,8 +451,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     cta_sync_tc();
     if (warp == 0) {
       mma_run<kC>(x.tm + d_col(i), opZM, opV, id_d, true);  // rows 64-127 += M V
+      // NORM: z += phi(K)^T 1 here, off the chain of the chunk's other MMAs (read at the next
+      // chunk's top, after the m2 wait)
+      if (NORM) mma_run<kC>(x.tm + kColZ, opKa, opOnes, id_z, zinit);
       mma_commit_elect(bar_m2);
     }
+    zinit = true;
     // NORM: the next chunk's tiles (buffer b ^ 1, loaded since this chunk began) made ready
     // while that MMA runs
     if (NORM && i + 1 < nloc) next_ok = make_ready(i + 1);
