@@ -58,35 +58,49 @@ struct LinSmem {
 constexpr uint32_t kColD0 = 128, kColD1 = 256, kColA = 384;  // TMEM columns (S at 0)
 constexpr uint32_t kColZ = 448;  // NORM: phi(K)^T 1, 16 equal columns
 
-// phi = elu + 1 on `chunks` 16-byte chunks of bf16 at p, in place (thread-strided)
-__device__ __forceinline__ void phi_tile(unsigned char* p, int chunks, int tid) {
-  for (int i = tid; i < chunks; i += kThreads) {
-    uint4 u = reinterpret_cast<uint4*>(p)[i];
-    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+// phi = elu + 1 for the bf16 operand tiles: x + 1 above zero, else e^x = 2^(x log2 e) on the
+// hardware ex2 (flush-to-zero form), its argument held at -126 or above so phi stays a normal
+// positive number (>= 2^-126; e^x itself for x >= -87.3)
+__device__ __forceinline__ float phi_tc(float x) {
+  float e;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(fmaxf(x * 1.44269504f, -126.f)));
+  return x > 0.f ? x + 1.f : e;
+}
+__device__ __forceinline__ uint4 phi8(uint4 u) {
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 f = __bfloat1622float2(h[e]);
-      h[e] = __floats2bfloat162_rn(phi_f(f.x), phi_f(f.y));
-    }
-    reinterpret_cast<uint4*>(p)[i] = u;
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = __bfloat1622float2(h[e]);
+    h[e] = __floats2bfloat162_rn(phi_tc(f.x), phi_tc(f.y));
+  }
+  return u;
+}
+
+// phi on `chunks` 16-byte chunks of bf16 at p, in place (thread-strided, all loads first)
+__device__ __forceinline__ void phi_tile(unsigned char* p, int chunks, int tid) {
+  for (int i = tid; i < chunks; i += 4 * kThreads) {
+    uint4 u[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (i + k * kThreads < chunks) u[k] = reinterpret_cast<uint4*>(p)[i + k * kThreads];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (i + k * kThreads < chunks) reinterpret_cast<uint4*>(p)[i + k * kThreads] = phi8(u[k]);
   }
 }
 
-// phi on a [K; Q] tile pair (2 slabs of 128 rows x 128 B), key rows >= n set to 0 instead
+// phi on a [K; Q] tile pair (2 slabs of 128 rows x 128 B), key rows >= n set to 0 instead;
+// a thread's 8 chunks are loaded before any is converted
 __device__ __forceinline__ void phi_kq(unsigned char* p, int n, int tid) {
-  for (int i = tid; i < 2048; i += kThreads) {
-    const int row = (i & 1023) >> 3;
-    uint4 u = make_uint4(0u, 0u, 0u, 0u);
-    if (row >= 64 || row < n) {
-      u = reinterpret_cast<uint4*>(p)[i];
-      __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+  uint4 u[8];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = __bfloat1622float2(h[e]);
-        h[e] = __floats2bfloat162_rn(phi_f(f.x), phi_f(f.y));
-      }
-    }
-    reinterpret_cast<uint4*>(p)[i] = u;
+  for (int k = 0; k < 8; ++k) u[k] = reinterpret_cast<uint4*>(p)[tid + k * kThreads];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int i = tid + k * kThreads;
+    const int row = (i & 1023) >> 3;
+    reinterpret_cast<uint4*>(p)[i] =
+        (row >= 64 || row < n) ? phi8(u[k]) : make_uint4(0u, 0u, 0u, 0u);
   }
 }
 
