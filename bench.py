@@ -92,6 +92,8 @@ KERNEL_SOURCES = {"gated_linear_attn": ["prefill_cluster.cu", "tc_common.cuh", "
                   "prefill_prologue": ["prefill_cluster.cu", "tc_common.cuh", "umma.cuh"],
                   "layer_prologue": ["prologue.cu", "gdr_internal.cuh"],
                   "normalized_linear_attn": ["linear_tc.cu", "tc_common.cuh", "umma.cuh"],
+                  "gated_linear_decode": ["decode.cu"],
+                  "normalized_linear_decode": ["decode.cu"],
                   "prefill": ["prefill_cluster.cu", "tc_common.cuh", "umma.cuh"],
                   "linear_attn": ["linear_tc.cu", "tc_common.cuh", "umma.cuh"],
                   "decode": ["decode.cu"]}
@@ -463,6 +465,28 @@ def run_gpu(args):
     nla_ms = max_over_ranks([g0.elapsed_time(g1) / gla_steps], dev, world)[0]
     del out_g, Sf_g, Zf
 
+    # ---- the decode steps of gated linear and normalised linear attention on the decode
+    # workload's states (z: the first states' channel sums, only its magnitude matters)
+    Zd = S_dec.sum(dim=3).abs_().add_(1.0)
+    dec_steps = max(10, min(args.steps, 100))
+
+    def time_dec(fn):
+        for i in range(3):
+            fn(steps_in[i % len(steps_in)])
+        torch.cuda.synchronize()
+        g0.record(stream)
+        for i in range(dec_steps):
+            fn(steps_in[i % len(steps_in)])
+        g1.record(stream)
+        torch.cuda.synchronize()
+        return max_over_ranks([g0.elapsed_time(g1) / dec_steps], dev, world)[0]
+
+    gld_ms = time_dec(lambda x: g.gdr_gated_linear_decode_step(x["q"], x["k"], x["v"], x["alpha"],
+                                                                 S_dec, out=out_d))
+    nld_ms = time_dec(lambda x: g.gdr_normalized_linear_decode_step(x["q"], x["k"], x["v"], S_dec,
+                                                                      Zd, eps=1e-6, out=out_d))
+    del Zd
+
     # ---- end to end through the public API with host buffers (prefill), rank-local
     host_in = {k: P[k].cpu().pin_memory() for k in ("q", "k", "v", "alpha", "beta", "S0")}
     host_cu = P["cu_seqlens"].cpu().pin_memory()
@@ -537,6 +561,15 @@ def run_gpu(args):
         "normalized_linear_attn": roof("normalized_linear_attn",
                                        prefill_bytes(T, H, d, wp.n_seqs, linear=True),
                                        prefill_flops(T, H, d, linear=True), nla_ms / 1e3),
+        # the delta decode's bytes without beta (gated linear); without alpha and beta, with
+        # z read and written (normalised linear)
+        "gated_linear_decode": roof("gated_linear_decode",
+                                    decode_bytes(wd.n_seqs, wd.H, wd.d_k) - wd.n_seqs * wd.H * 4,
+                                    decode_flops(wd.n_seqs, wd.H, wd.d_k), gld_ms / 1e3),
+        "normalized_linear_decode": roof("normalized_linear_decode",
+                                         decode_bytes(wd.n_seqs, wd.H, wd.d_k) +
+                                         wd.n_seqs * wd.H * (wd.d_k * 4 - 4),
+                                         decode_flops(wd.n_seqs, wd.H, wd.d_k), nld_ms / 1e3),
         # read xq, xk (bf16), a (fp32 per channel), b; write q, k, alpha, beta
         "layer_prologue": roof("layer_prologue", 2 * T * H * (2 * d * 2 + d * 4 + 4), 0.0,
                                lp_ms / 1e3),
@@ -564,6 +597,8 @@ def run_gpu(args):
         "prefill_prologue_tokens_per_s": job_tokens_per_s(n, T, pro_ms / 1e3),
         "prefill_unfused_prologue_tokens_per_s": job_tokens_per_s(n, T, unf_ms / 1e3),
         "normalized_linear_attn_tokens_per_s": job_tokens_per_s(n, T, nla_ms / 1e3),
+        "gated_linear_decode_tokens_per_s": job_tokens_per_s(n, wd.n_seqs, gld_ms / 1e3),
+        "normalized_linear_decode_tokens_per_s": job_tokens_per_s(n, wd.n_seqs, nld_ms / 1e3),
         "roofline": main_roof,
         "kernels": kern,
         "kernels_outside_step": kern_extra,

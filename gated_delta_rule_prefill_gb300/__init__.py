@@ -13,6 +13,8 @@ library's CUDA kernels; there is no Python or CPU fallback.
     gdr_prefill_host_buffer_size(n_seqs, H, total_tokens, d_k, d_v, dtype, gate, piece_tokens)
     gdr_layer_prologue(xq, xk, a=None, b=None, q=None, k=None, alpha=None, beta=None)
     gdr_normalized_linear_attn(q, k, v, eps=0.0, S0=None, z0=None, cu_seqlens=None, ...)
+    gdr_gated_linear_decode_step(q, k, v, alpha, S_inout)  /  gdr_normalized_linear_decode_step(
+        q, k, v, S_inout, z_inout, eps=0.0)
 
 prologue=True (GDR_FLAG_LAYER_PROLOGUE) makes q, k, alpha, beta the layer's raw projections: the
 kernels form q, k = normalize(silu(.)) and alpha, beta = sigmoid(.) as they load them.
@@ -30,6 +32,7 @@ from ._abi import (GDR_BF16, GDR_F32, GDR_FLAG_FORCE_SIMT, GDR_FLAG_NO_CLUSTER, 
 
 __all__ = ["gdr_prefill", "gdr_prefill_output_gate", "gdr_decode_step", "gdr_linear_attn",
            "gdr_gated_linear_attn", "gdr_layer_prologue", "gdr_normalized_linear_attn",
+           "gdr_gated_linear_decode_step", "gdr_normalized_linear_decode_step",
            "gdr_prefill_workspace_size",
            "gdr_workspace_status", "gdr_prefill_host", "gdr_prefill_host_buffer_size",
            "make_shape", "GdrError"]
@@ -328,6 +331,51 @@ def gdr_decode_step(q, k, v, alpha, beta, S_inout, out=None, stream=None, prolog
                                      _ptr(beta), _ptr(S_inout), _ptr(out), _stream(stream))
     if rc != 0:
         raise GdrError(rc, "gdr_decode_step")
+    return out
+
+
+def _decode_inputs(q, k, v, S_inout, out):
+    N, H, dk = q.shape
+    dv = v.shape[2]
+    dtype = _DT.get(q.dtype)
+    if dtype is None:
+        raise ValueError("q/k/v must be float32 or bfloat16")
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, q.dtype)
+    _check(S_inout, "S_inout", torch.float32)
+    if out is None:
+        out = torch.empty((N, H, dv), dtype=q.dtype, device=q.device)
+    _check(out, "out", q.dtype)
+    return N, H, dk, dv, dtype, out
+
+
+def gdr_gated_linear_decode_step(q, k, v, alpha, S_inout, out=None, stream=None, prologue=False):
+    """One token per sequence of gated linear attention: S <- Diag(alpha) S + k v^T, o = S^T q;
+    S_inout [N,H,d_k,d_v] fp32 updated in place; alpha [N,H,d_k] or [N,H].  Returns out."""
+    N, H, dk, dv, dtype, out = _decode_inputs(q, k, v, S_inout, out)
+    _check(alpha, "alpha", torch.float32)
+    gate = GDR_GATE_CHANNEL if alpha.dim() == 3 else GDR_GATE_SCALAR
+    sh = make_shape(N, H, N, dk, dv, dtype, gate, 0, GDR_FLAG_LAYER_PROLOGUE if prologue else 0)
+    rc = _abi.load().gdr_gated_linear_decode_step(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v),
+                                                  _ptr(alpha), _ptr(S_inout), _ptr(out),
+                                                  _stream(stream))
+    if rc != 0:
+        raise GdrError(rc, "gdr_gated_linear_decode_step")
+    return out
+
+
+def gdr_normalized_linear_decode_step(q, k, v, S_inout, z_inout, eps=0.0, out=None, stream=None):
+    """One token per sequence of normalised phi-linear attention: S <- S + phi(k) v^T,
+    z <- z + phi(k), o = S^T phi(q) / (phi(q) . z + eps); S_inout [N,H,d_k,d_v] and z_inout
+    [N,H,d_k] fp32 updated in place.  Returns out."""
+    N, H, dk, dv, dtype, out = _decode_inputs(q, k, v, S_inout, out)
+    _check(z_inout, "z_inout", torch.float32)
+    sh = make_shape(N, H, N, dk, dv, dtype, GDR_GATE_CHANNEL)
+    rc = _abi.load().gdr_normalized_linear_decode_step(ctypes.byref(sh), _ptr(q), _ptr(k),
+                                                       _ptr(v), float(eps), _ptr(S_inout),
+                                                       _ptr(z_inout), _ptr(out), _stream(stream))
+    if rc != 0:
+        raise GdrError(rc, "gdr_normalized_linear_decode_step")
     return out
 
 

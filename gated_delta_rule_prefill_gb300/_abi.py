@@ -20,7 +20,8 @@ GDR_DEVCHECK_OK, GDR_DEVCHECK_SEQLENS, GDR_DEVCHECK_TIMEOUT = 0, 1, 2
 EXPORTS = ("gdr_prefill", "gdr_prefill_workspace_size", "gdr_decode_step", "gdr_linear_attn",
            "gdr_workspace_status", "gdr_status_string", "gdr_prefill_noalloc", "gdr_prefill_host",
            "gdr_prefill_host_buffer_size", "gdr_gated_linear_attn",
-           "gdr_prefill_output_gate", "gdr_layer_prologue", "gdr_normalized_linear_attn")
+           "gdr_prefill_output_gate", "gdr_layer_prologue", "gdr_normalized_linear_attn",
+           "gdr_gated_linear_decode_step", "gdr_normalized_linear_decode_step")
 GDR_NOALLOC_MAX_SEQS = 4096
 
 
@@ -55,6 +56,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.gdr_normalized_linear_attn.argtypes = [S, P, P, P, ctypes.c_float, P, P, P, P, P, P, P,
                                                ctypes.c_size_t, P]
     lib.gdr_normalized_linear_attn.restype = ctypes.c_int
+    lib.gdr_gated_linear_decode_step.argtypes = [S, P, P, P, P, P, P, P]
+    lib.gdr_gated_linear_decode_step.restype = ctypes.c_int
+    lib.gdr_normalized_linear_decode_step.argtypes = [S, P, P, P, ctypes.c_float, P, P, P, P]
+    lib.gdr_normalized_linear_decode_step.restype = ctypes.c_int
     lib.gdr_layer_prologue.argtypes = [S, P, P, P, P, P, P, P, P, P]
     lib.gdr_layer_prologue.restype = ctypes.c_int
     lib.gdr_decode_step.argtypes = [S, P, P, P, P, P, P, P, P]

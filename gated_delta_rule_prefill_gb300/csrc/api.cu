@@ -115,6 +115,29 @@ gdr_status prefill_common(const gdr_shape* sh, const void* q, const void* k, con
 
 gdr_status validate_shape(const gdr_shape* sh, bool need_gate) { return check_shape(sh, need_gate); }
 
+// One decode step of the delta rule, gated linear or normalised linear attention.
+gdr_status decode_common(const gdr_shape* shape, int kind, const void* q, const void* k,
+                         const void* v, const float* alpha, const float* beta, float* S_inout,
+                         float* z_inout, float eps, void* out, void* stream) {
+  const bool norm = kind == kKindNormLinear;
+  gdr_status st = check_shape(shape, !norm);
+  if (st != GDR_OK) return st;
+  if (norm && (shape->flags & GDR_FLAG_LAYER_PROLOGUE)) return GDR_ERR_UNSUPPORTED;
+  if (shape->total_tokens != shape->n_seqs) return GDR_ERR_INVALID_ARG;
+  if (!q || !k || !v || !S_inout || !out) return GDR_ERR_INVALID_ARG;
+  if ((!norm && !alpha) || (kind == kKindDelta && !beta) || (norm && !z_inout))
+    return GDR_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, alpha, beta, S_inout, z_inout, out};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return GDR_ERR_INVALID_ARG;
+  if (out == q || out == k || out == v || (const void*)S_inout == out ||
+      (z_inout && ((const void*)z_inout == out || z_inout == S_inout)))
+    return GDR_ERR_INVALID_ARG;
+  cudaError_t e = launch_decode(*shape, kind, q, k, v, alpha, beta, S_inout, z_inout, eps, out,
+                                (cudaStream_t)stream);
+  return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+}
+
 gdr_status prefill_launch(const gdr_shape* sh, const void* q, const void* k, const void* v,
                           const float* alpha, const float* beta, const float* S0,
                           const int32_t* cu, void* out, float* S_final, void* ws,
@@ -181,17 +204,23 @@ gdr_status gdr_normalized_linear_attn(const gdr_shape* shape, const void* q, con
 gdr_status gdr_decode_step(const gdr_shape* shape, const void* q, const void* k, const void* v,
                            const float* alpha, const float* beta, float* S_inout, void* out,
                            void* stream) {
-  gdr_status st = gdr::check_shape(shape, true);
-  if (st != GDR_OK) return st;
-  if (shape->total_tokens != shape->n_seqs) return GDR_ERR_INVALID_ARG;
-  if (!q || !k || !v || !alpha || !beta || !S_inout || !out) return GDR_ERR_INVALID_ARG;
-  const void* ptrs[] = {q, k, v, alpha, beta, S_inout, out};
-  for (const void* p : ptrs)
-    if (!gdr::aligned16(p)) return GDR_ERR_INVALID_ARG;
-  if (out == q || out == k || out == v || (const void*)S_inout == out) return GDR_ERR_INVALID_ARG;
-  cudaError_t e = gdr::launch_decode(*shape, q, k, v, alpha, beta, S_inout, out,
-                                     (cudaStream_t)stream);
-  return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+  return gdr::decode_common(shape, gdr::kKindDelta, q, k, v, alpha, beta, S_inout, nullptr, 0.f,
+                            out, stream);
+}
+
+gdr_status gdr_gated_linear_decode_step(const gdr_shape* shape, const void* q, const void* k,
+                                        const void* v, const float* alpha, float* S_inout,
+                                        void* out, void* stream) {
+  return gdr::decode_common(shape, gdr::kKindGatedLinear, q, k, v, alpha, nullptr, S_inout,
+                            nullptr, 0.f, out, stream);
+}
+
+gdr_status gdr_normalized_linear_decode_step(const gdr_shape* shape, const void* q, const void* k,
+                                             const void* v, float eps, float* S_inout,
+                                             float* z_inout, void* out, void* stream) {
+  if (!(eps >= 0.f) || eps > 3.0e38f) return GDR_ERR_INVALID_ARG;
+  return gdr::decode_common(shape, gdr::kKindNormLinear, q, k, v, nullptr, nullptr, S_inout,
+                            z_inout, eps, out, stream);
 }
 
 gdr_status gdr_layer_prologue(const gdr_shape* shape, const void* xq, const void* xk,

@@ -12,6 +12,11 @@
 // Each element of S is read once and written once: the kernel is bound by HBM bandwidth
 // (2 * d_k * d_v * 4 bytes per head per step).
 //
+// The same pass serves two more rules (KIND): gated linear attention (engineermaxxing §05b:
+// S' = S_a + k v^T, no erase, no beta: delta = v) and normalised phi-linear attention
+// (heqinghuang §07, engineermaxxing §02g: phi = elu + 1 on q and k, no decay, delta = v, the
+// normaliser z <- z + phi(k) kept beside the state and o divided by phi(q) . z + eps).
+//
 // Mapping: one CTA (8 warps) per (sequence, head).  Lane l owns d_v columns [l*CPL, l*CPL+CPL)
 // (CPL = d_v / 32, one 16-byte load for d = 128); warp w owns d_k rows [w*RPW, w*RPW+RPW).  The
 // whole d_k x d_v slab is held in registers between the read and the write, so the state is
@@ -39,16 +44,20 @@ __device__ __forceinline__ void vstore(float* p, const float (&x)[2]) {
 
 constexpr int kDecodeWarps = 8;
 
-template <int D, typename T, bool CHANNEL>
+template <int D, typename T, bool CHANNEL, int KIND>
 __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
     decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                   const float* __restrict__ alpha, const float* __restrict__ beta,
-                  float* __restrict__ S, T* __restrict__ out, bool prologue) {
+                  float* __restrict__ S, T* __restrict__ out, bool prologue,
+                  float* __restrict__ z, float eps) {
+  constexpr bool ERASE = KIND == kKindDelta;      // the delta rule's correction
+  constexpr bool NORM = KIND == kKindNormLinear;  // phi features, normaliser, no decay
   constexpr int CPL = D / 32;           // columns per lane
   constexpr int RPW = D / kDecodeWarps;  // rows per warp
   __shared__ float s_q[D], s_k[D], s_a[D], s_v[D], s_delta[D];
   __shared__ float s_red_k[kDecodeWarps][D], s_red_q[kDecodeWarps][D];
   __shared__ float s_ss[2][D / 32];
+  __shared__ float s_qz[D / 32];
 
   const int pair = blockIdx.x;  // n * H + h
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -65,7 +74,17 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
   // length by iq, ik below, and alpha the sigmoid of its projection
   if (tid < D) {
     const size_t o = (size_t)pair * D + tid;
-    float qv = to_f32(q[o]), kv = to_f32(k[o]), av = CHANNEL ? alpha[o] : alpha[pair];
+    float qv = to_f32(q[o]), kv = to_f32(k[o]);
+    float av = NORM ? 1.f : CHANNEL ? alpha[o] : alpha[pair];
+    if (NORM) {  // z <- z + phi(k); this warp's share of phi(q) . z
+      qv = phi_f(qv), kv = phi_f(kv);
+      const float zn = z[o] + kv;
+      z[o] = zn;
+      float qz = qv * zn;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) qz += __shfl_xor_sync(0xffffffffu, qz, off);
+      if (lane == 0) s_qz[warp] = qz;
+    }
     if (prologue) {
       qv = silu_f(qv), kv = silu_f(kv), av = sigmoid_f(av);
       float sq = qv * qv, sk = kv * kv;
@@ -101,7 +120,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
 #pragma unroll
     for (int c = 0; c < CPL; ++c) {
       x[r][c] *= a;
-      yk[c] = fmaf(kr, x[r][c], yk[c]);
+      if (ERASE) yk[c] = fmaf(kr, x[r][c], yk[c]);
       yq[c] = fmaf(qr, x[r][c], yq[c]);
     }
   }
@@ -127,10 +146,17 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
       tk += s_red_k[w][tid];
       tq += s_red_q[w][tid];
     }
-    const float bt = prologue ? sigmoid_f(beta[pair]) : beta[pair];
-    const float d = bt * (s_v[tid] - tk);
+    float d = s_v[tid];  // gated linear and normalised linear attention write v itself
+    if (ERASE) d = (prologue ? sigmoid_f(beta[pair]) : beta[pair]) * (d - tk);
     s_delta[tid] = d;
-    out[(size_t)pair * D + tid] = from_f32<T>(fmaf(qk, d, tq));
+    float o = fmaf(qk, d, tq);
+    if (NORM) {
+      float den = eps;
+#pragma unroll
+      for (int w = 0; w < D / 32; ++w) den += s_qz[w];
+      o /= den;
+    }
+    out[(size_t)pair * D + tid] = from_f32<T>(o);
   }
   __syncthreads();
 
@@ -147,33 +173,45 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
   }
 }
 
-template <int D, typename T>
-cudaError_t launch_typed(const gdr_shape& sh, const void* q, const void* k, const void* v,
-                         const float* alpha, const float* beta, float* S, void* out,
-                         cudaStream_t s) {
+template <int D, typename T, int KIND>
+void launch_kind(const gdr_shape& sh, const void* q, const void* k, const void* v,
+                 const float* alpha, const float* beta, float* S, float* z, float eps,
+                 void* out, cudaStream_t s) {
   const unsigned grid = (unsigned)sh.n_seqs * (unsigned)sh.H;
   const bool prologue = (sh.flags & GDR_FLAG_LAYER_PROLOGUE) != 0;
-  if (sh.gate == GDR_GATE_CHANNEL)
-    decode_kernel<D, T, true><<<grid, kDecodeWarps * 32, 0, s>>>(
-        (const T*)q, (const T*)k, (const T*)v, alpha, beta, S, (T*)out, prologue);
+  if (KIND == kKindNormLinear || sh.gate == GDR_GATE_CHANNEL)
+    decode_kernel<D, T, true, KIND><<<grid, kDecodeWarps * 32, 0, s>>>(
+        (const T*)q, (const T*)k, (const T*)v, alpha, beta, S, (T*)out, prologue, z, eps);
   else
-    decode_kernel<D, T, false><<<grid, kDecodeWarps * 32, 0, s>>>(
-        (const T*)q, (const T*)k, (const T*)v, alpha, beta, S, (T*)out, prologue);
+    decode_kernel<D, T, false, KIND><<<grid, kDecodeWarps * 32, 0, s>>>(
+        (const T*)q, (const T*)k, (const T*)v, alpha, beta, S, (T*)out, prologue, z, eps);
+}
+
+template <int D, typename T>
+cudaError_t launch_typed(const gdr_shape& sh, int kind, const void* q, const void* k,
+                         const void* v, const float* alpha, const float* beta, float* S,
+                         float* z, float eps, void* out, cudaStream_t s) {
+  if (kind == kKindNormLinear)
+    launch_kind<D, T, kKindNormLinear>(sh, q, k, v, alpha, beta, S, z, eps, out, s);
+  else if (kind == kKindGatedLinear)
+    launch_kind<D, T, kKindGatedLinear>(sh, q, k, v, alpha, beta, S, z, eps, out, s);
+  else
+    launch_kind<D, T, kKindDelta>(sh, q, k, v, alpha, beta, S, z, eps, out, s);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_decode(const gdr_shape& sh, const void* q, const void* k, const void* v,
-                          const float* alpha, const float* beta, float* S, void* out,
-                          cudaStream_t s) {
+cudaError_t launch_decode(const gdr_shape& sh, int kind, const void* q, const void* k,
+                          const void* v, const float* alpha, const float* beta, float* S,
+                          float* z, float eps, void* out, cudaStream_t s) {
   if (sh.d_k == 128)
     return sh.dtype == GDR_BF16
-               ? launch_typed<128, __nv_bfloat16>(sh, q, k, v, alpha, beta, S, out, s)
-               : launch_typed<128, float>(sh, q, k, v, alpha, beta, S, out, s);
+               ? launch_typed<128, __nv_bfloat16>(sh, kind, q, k, v, alpha, beta, S, z, eps, out, s)
+               : launch_typed<128, float>(sh, kind, q, k, v, alpha, beta, S, z, eps, out, s);
   return sh.dtype == GDR_BF16
-             ? launch_typed<64, __nv_bfloat16>(sh, q, k, v, alpha, beta, S, out, s)
-             : launch_typed<64, float>(sh, q, k, v, alpha, beta, S, out, s);
+             ? launch_typed<64, __nv_bfloat16>(sh, kind, q, k, v, alpha, beta, S, z, eps, out, s)
+             : launch_typed<64, float>(sh, kind, q, k, v, alpha, beta, S, z, eps, out, s);
 }
 
 }  // namespace gdr

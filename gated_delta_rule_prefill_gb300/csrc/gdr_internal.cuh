@@ -149,8 +149,8 @@ cudaError_t launch_prefill_tc(const gdr_shape& sh, const PrefillArgs& a, int kin
 cudaError_t launch_layer_prologue(const gdr_shape& sh, const void* xq, const void* xk,
                                   const float* a, const float* b, void* q, void* k, float* alpha,
                                   float* beta, cudaStream_t s);
-cudaError_t launch_decode(const gdr_shape& sh, const void* q, const void* k, const void* v,
-                          const float* alpha, const float* beta, float* S, void* out,
-                          cudaStream_t s);
+cudaError_t launch_decode(const gdr_shape& sh, int kind, const void* q, const void* k,
+                          const void* v, const float* alpha, const float* beta, float* S,
+                          float* z, float eps, void* out, cudaStream_t s);
 
 }  // namespace gdr

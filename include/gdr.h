@@ -148,6 +148,30 @@ gdr_status gdr_normalized_linear_attn(const gdr_shape* shape, const void* q, con
                                       void* stream);
 
 /*
+ * gdr_gated_linear_decode_step -- one token per sequence of gated linear attention, state
+ * updated in place (engineermaxxing "From GPT-2 to Kimi K3" §05b; per key channel as dev.to §5):
+ *   S <- Diag(alpha) S + k v^T,   o = S^T q.
+ * Arguments as gdr_decode_step without beta.  GDR_FLAG_LAYER_PROLOGUE is accepted (q, k, alpha
+ * raw projections).
+ */
+gdr_status gdr_gated_linear_decode_step(const gdr_shape* shape, const void* q, const void* k,
+                                        const void* v, const float* alpha, float* S_inout,
+                                        void* out, void* stream);
+
+/*
+ * gdr_normalized_linear_decode_step -- one token per sequence of normalised phi-linear attention
+ * (heqinghuang "gpt2-to-kimi" §07; engineermaxxing §02g's decode step), state and normaliser
+ * updated in place:
+ *   S <- S + phi(k) v^T,   z <- z + phi(k),   o = S^T phi(q) / (phi(q) . z + eps).
+ * q, k, v, out: [n_seqs, H, d] in shape->dtype; S_inout [n_seqs, H, d_k, d_v] fp32; z_inout
+ * [n_seqs, H, d_k] fp32 (device, 16-byte aligned, caller-owned, not aliasing each other or out);
+ * shape->total_tokens must equal shape->n_seqs; eps finite and >= 0.  One HBM-bound kernel.
+ */
+gdr_status gdr_normalized_linear_decode_step(const gdr_shape* shape, const void* q, const void* k,
+                                             const void* v, float eps, float* S_inout,
+                                             float* z_inout, void* out, void* stream);
+
+/*
  * gdr_layer_prologue -- the layer prologue as a pass of its own (the maps that
  * GDR_FLAG_LAYER_PROLOGUE applies inside the kernels; heqinghuang "gpt2-to-kimi" §09,
  * engineermaxxing "From GPT-2 to Kimi K3" §05c and §06b):

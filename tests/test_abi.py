@@ -209,3 +209,28 @@ def test_normalized_linear_argument_errors(lib):
     sh2 = _shape(n_seqs=1, total_tokens=64)
     sh2.flags = GDR_FLAG_LAYER_PROLOGUE
     assert call(shape=sh2) == 2
+
+
+def test_decode_variants_argument_errors(lib):
+    """gdr_gated_linear_decode_step needs alpha; gdr_normalized_linear_decode_step needs z_inout
+    (not aliasing S_inout), a finite eps >= 0 and no layer-prologue flag."""
+    P = ctypes.c_void_p
+    sh = _shape(n_seqs=4, H=2, total_tokens=4)
+    a = [P(FAKE), P(FAKE + 4096), P(FAKE + 8192)]
+    assert lib.gdr_gated_linear_decode_step(ctypes.byref(sh), *a, None, P(FAKE * 2),
+                                            P(FAKE * 3), None) == 1
+    sh_bad = _shape(n_seqs=4, H=2, total_tokens=5)
+    assert lib.gdr_gated_linear_decode_step(ctypes.byref(sh_bad), *a, P(FAKE * 4), P(FAKE * 2),
+                                            P(FAKE * 3), None) == 1
+
+    def norm(eps=0.0, S=FAKE * 2, z=FAKE * 5, shape=sh):
+        return lib.gdr_normalized_linear_decode_step(ctypes.byref(shape), *a, eps, P(S), P(z),
+                                                     P(FAKE * 3), None)
+    assert norm(z=None) == 1
+    assert norm(z=FAKE * 2) == 1
+    assert norm(eps=-1.0) == 1
+    assert norm(eps=float("nan")) == 1
+    from gated_delta_rule_prefill_gb300._abi import GDR_FLAG_LAYER_PROLOGUE
+    sh2 = _shape(n_seqs=4, H=2, total_tokens=4)
+    sh2.flags = GDR_FLAG_LAYER_PROLOGUE
+    assert norm(shape=sh2) == 2

@@ -9,7 +9,7 @@ import torch
 
 import gdr_inputs as gi
 import oracle
-from tests.parity import TOL, dev_inputs, host, rel_rows, rel_states
+from tests.parity import TOL, dev_inputs, host, rel_rows, rel_states, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -71,3 +71,48 @@ def test_gla_special_gates(case):
         a["alpha"][64:128] = np.float32(1e-3)
         a["alpha"][300:340] = np.float32(0.05)
     check(a, "bf16", what=case)
+
+
+@pytest.mark.parametrize("dtype,d,gate", [("bf16", 128, "channel"), ("bf16", 128, "scalar"),
+                                          ("f32", 64, "channel")])
+def test_gla_decode_step(dtype, d, gate):
+    """gdr_gated_linear_decode_step from a given state, two steps (the second with alpha = 0 on
+    some sequences: a reset, then the write), against the oracle's gated-linear mode on one-token
+    sequences."""
+    import gated_delta_rule_prefill_gb300 as g
+    N, H = 40, 3
+    wl = gi.Workload("dec", 702, H, d, d, dtype, gate, np.array([1] * N), "zeros")
+    S = gi.random_state(703, N, H, d, d)
+    Sd = torch.from_numpy(S).cuda()
+    cu = np.arange(N + 1)
+    for step in range(2):
+        a = gi.gen_decode_step(wl, step)
+        if step == 1:
+            a["alpha"][:5] = 0.0
+        d_ = {kk: to_dev(a[kk], dtype) for kk in ("q", "k", "v")}
+        out = g.gdr_gated_linear_decode_step(d_["q"], d_["k"], d_["v"], to_dev(a["alpha"], "f32"),
+                                             Sd)
+        torch.cuda.synchronize()
+        ro, rs = oracle.gated_linear(a["q"], a["k"], a["v"], a["alpha"], S0=S, cu_seqlens=cu)
+        eo, es = rel_rows(host(out), ro), rel_states(host(Sd), rs)
+        print("gla decode %s %s step %d: out %.3g state %.3g" % (dtype, gate, step, eo, es))
+        assert eo <= TOL[dtype] and es <= TOL[dtype], (eo, es)
+        S = rs
+
+
+def test_gla_decode_step_prologue():
+    """The gated-linear decode step on raw projections (layer prologue on load)."""
+    import gated_delta_rule_prefill_gb300 as g
+    N, H, d = 32, 2, 128
+    wl = gi.Workload("dec", 704, H, d, d, "bf16", "channel", np.array([1] * N), "zeros")
+    S = gi.random_state(705, N, H, d, d)
+    Sd = torch.from_numpy(S).cuda()
+    a = gi.gen_decode_step(wl, 0, raw=True)
+    d_ = {kk: to_dev(a[kk], "bf16") for kk in ("q", "k", "v")}
+    out = g.gdr_gated_linear_decode_step(d_["q"], d_["k"], d_["v"], to_dev(a["alpha"], "f32"), Sd,
+                                         prologue=True)
+    torch.cuda.synchronize()
+    q, k, al, _ = oracle.layer_prologue(a["q"], a["k"], a["alpha"], a["beta"])
+    ro, rs = oracle.gated_linear(q, k, a["v"], al, S0=S, cu_seqlens=np.arange(N + 1))
+    eo, es = rel_rows(host(out), ro), rel_states(host(Sd), rs)
+    assert eo <= TOL["bf16"] and es <= TOL["bf16"], (eo, es)

@@ -9,7 +9,7 @@ import torch
 
 import gdr_inputs as gi
 import oracle
-from tests.parity import TOL, dev_inputs, host, rel_rows, rel_states
+from tests.parity import TOL, dev_inputs, host, rel_rows, rel_states, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -77,3 +77,26 @@ def test_normlinear_edge_rows():
     a["k"][12, :, :8] = 30.0
     for simt in (False, True):
         run(a, "bf16", 0.0, True, simt)
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f32", 64)])
+def test_normlinear_decode_step(dtype, d):
+    """gdr_normalized_linear_decode_step from a given (S, z), twice in a row, against the oracle
+    stepping the same tokens (one-token sequences)."""
+    import gated_delta_rule_prefill_gb300 as g
+    N, H = 48, 3
+    wl = gi.Workload("dec", 606, H, d, d, dtype, "channel", np.array([1] * N), "zeros")
+    S = gi.random_state(607, N, H, d, d)
+    z = np.abs(np.random.default_rng(608).normal(size=(N, H, d))).astype(np.float32) * 5
+    Sd, zd = torch.from_numpy(S).cuda(), torch.from_numpy(z).cuda()
+    cu = np.arange(N + 1)
+    for step in range(2):
+        a = gi.gen_decode_step(wl, step, raw=True)
+        d_ = {kk: to_dev(a[kk], dtype) for kk in ("q", "k", "v")}
+        out = g.gdr_normalized_linear_decode_step(d_["q"], d_["k"], d_["v"], Sd, zd, eps=1e-6)
+        torch.cuda.synchronize()
+        ro, rs, rz = oracle.normalized_linear(a["q"], a["k"], a["v"], S, z, cu, 1e-6)
+        eo, es, ez = rel_rows(host(out), ro), rel_states(host(Sd), rs), rel_rows(host(zd), rz)
+        print("norm decode %s step %d: out %.3g state %.3g z %.3g" % (dtype, step, eo, es, ez))
+        assert eo <= TOL[dtype] and es <= TOL[dtype] and ez <= TOL[dtype], (eo, es, ez)
+        S, z = rs, rz
