@@ -494,3 +494,22 @@ def test_normalized_linear_state_handoff_and_eps():
     pk = oracle.normalized_linear(q, k, v, cu_seqlens=cu)
     np.testing.assert_allclose(pk[0][5:], oracle.normalized_linear(q[5:], k[5:], v[5:])[0],
                                rtol=1e-12)
+
+
+def test_prologue_and_phi_match_the_pages_expressions():
+    """The pages print the maps as framework expressions (heqinghuang §09: normalize(silu(.)) and
+    sigmoid(.); heqinghuang §07 / engineermaxxing §02g: elu(.) + 1).  Evaluated with those
+    framework routines (torch, CPU, fp64) they agree with the oracle's own statement."""
+    import torch
+    import torch.nn.functional as F
+    rng = np.random.default_rng(77)
+    x = rng.normal(0, 3, (6, 2, 16))
+    a = rng.normal(3, 2, (6, 2, 16))
+    b = rng.normal(0, 2, (6, 2))
+    q, k, al, be = oracle.layer_prologue(x, -x, a, b)
+    tx = torch.from_numpy(x)
+    np.testing.assert_allclose(q, F.normalize(F.silu(tx), dim=-1).numpy(), rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(k, F.normalize(F.silu(-tx), dim=-1).numpy(), rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(al, torch.sigmoid(torch.from_numpy(a)).numpy(), rtol=1e-12)
+    np.testing.assert_allclose(be, torch.sigmoid(torch.from_numpy(b)).numpy(), rtol=1e-12)
+    np.testing.assert_allclose(oracle.phi(x), (F.elu(tx) + 1).numpy(), rtol=1e-12)
