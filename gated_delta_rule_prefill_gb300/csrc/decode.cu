@@ -44,12 +44,12 @@ __device__ __forceinline__ void vstore(float* p, const float (&x)[2]) {
 
 constexpr int kDecodeWarps = 8;
 
-template <int D, typename T, bool CHANNEL, int KIND>
+template <int D, typename T, bool CHANNEL, int KIND, bool PRO>
 __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
     decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                   const float* __restrict__ alpha, const float* __restrict__ beta,
-                  float* __restrict__ S, T* __restrict__ out, bool prologue,
-                  float* __restrict__ z, float eps) {
+                  float* __restrict__ S, T* __restrict__ out, float* __restrict__ z, float eps) {
+  constexpr bool prologue = PRO;  // the layer prologue on load (raw projections)
   constexpr bool ERASE = KIND == kKindDelta;      // the delta rule's correction
   constexpr bool NORM = KIND == kKindNormLinear;  // phi features, normaliser, no decay
   constexpr int CPL = D / 32;           // columns per lane
@@ -178,13 +178,14 @@ void launch_kind(const gdr_shape& sh, const void* q, const void* k, const void* 
                  const float* alpha, const float* beta, float* S, float* z, float eps,
                  void* out, cudaStream_t s) {
   const unsigned grid = (unsigned)sh.n_seqs * (unsigned)sh.H;
-  const bool prologue = (sh.flags & GDR_FLAG_LAYER_PROLOGUE) != 0;
-  if (KIND == kKindNormLinear || sh.gate == GDR_GATE_CHANNEL)
-    decode_kernel<D, T, true, KIND><<<grid, kDecodeWarps * 32, 0, s>>>(
-        (const T*)q, (const T*)k, (const T*)v, alpha, beta, S, (T*)out, prologue, z, eps);
-  else
-    decode_kernel<D, T, false, KIND><<<grid, kDecodeWarps * 32, 0, s>>>(
-        (const T*)q, (const T*)k, (const T*)v, alpha, beta, S, (T*)out, prologue, z, eps);
+  const bool pro = KIND != kKindNormLinear && (sh.flags & GDR_FLAG_LAYER_PROLOGUE) != 0;
+  const bool ch = KIND == kKindNormLinear || sh.gate == GDR_GATE_CHANNEL;
+  auto kern = ch ? (pro ? decode_kernel<D, T, true, KIND, true>
+                         : decode_kernel<D, T, true, KIND, false>)
+                 : (pro ? decode_kernel<D, T, false, KIND, true>
+                         : decode_kernel<D, T, false, KIND, false>);
+  kern<<<grid, kDecodeWarps * 32, 0, s>>>((const T*)q, (const T*)k, (const T*)v, alpha, beta, S,
+                                          (T*)out, z, eps);
 }
 
 template <int D, typename T>
