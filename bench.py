@@ -37,6 +37,8 @@ import gdr_inputs as gi  # noqa: E402
 
 PREFILL = "kda_b1_h32_t32768"
 DECODE = "decode_n256_h32"
+SMALL, GDN, VARLEN = "kda_t256_d64_f32", "gdn_b4_h16_t4096", "varlen_n64_h16"
+CONFIG_WORKLOADS = (SMALL, GDN, VARLEN)
 DECODE_PREFILL_LEN = 2048
 SAMPLE_TOKENS = 32768  # oracle sample: tokens of each sampled head
 METRIC = "gated-delta prefill tokens/s + decode tokens/s; % of TC/HBM roofline"
@@ -54,10 +56,22 @@ def prefill_bytes(T, H, d, n_seqs, channel=True, linear=False, elt=2, beta=True)
 
 
 def prefill_flops(T, H, d, C=64, linear=False):
+    """Algorithmic flops (2 per multiply-add), counting only the triangle entries a chunk needs.
+    Gated delta rule: W S, Q~ S, K^^T U (3 d^2), A (strict lower, (C-1)/2 d), M (lower incl. the
+    diagonal, (C+1)/2 d), the solve applied to [beta K~ | beta V] ((C-1)/2 2d) and M U
+    ((C+1)/2 d).  Linear attention, and gated linear attention (whose decay-weighted M has the
+    same triangle as Q K^T): Q S and K^T V (2 d^2), the score triangle and its product with V
+    ((C+1) d)."""
     if linear:
         return T * H * 2 * (2 * d * d + (C + 1) * d)
-    f = 3 * d * d + (C - 1) // 2 * d + (C + 1) // 2 * d + (C - 1) // 2 * 2 * d + (C + 1) // 2 * d
+    f = 3 * d * d + (C - 1) / 2 * d + (C + 1) / 2 * d + (C - 1) / 2 * 2 * d + (C + 1) / 2 * d
     return T * H * 2 * f
+
+
+def gated_linear_flops(T, H, d, C=64):
+    """Gated linear attention: Q~ S and K^^T V (2 d^2), the decay-weighted M (lower triangle
+    with the diagonal, (C+1)/2 d) and M V ((C+1)/2 d)."""
+    return T * H * 2 * (2 * d * d + (C + 1) / 2 * d + (C + 1) / 2 * d)
 
 
 def decode_bytes(N, H, d, elt=2):
@@ -103,6 +117,8 @@ def ncu_traffic(kernel):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on this source."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
+        return None
+    if kernel not in KERNEL_SOURCES:
         return None
     with open(p) as f:
         t = json.load(f).get(kernel)
@@ -518,6 +534,43 @@ def run_gpu(args):
     h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + host_cu.numel() * 4
     d2h = host_out.numel() * host_out.element_size() + host_sf.numel() * host_sf.element_size()
 
+    # ---- the other named workloads, each timed on its own (parity cases of the same path): the
+    # 256-token fp32 KDA prefill (latency only), the scalar-gate prefill of 4 x 4096 tokens and
+    # the packed variable-length prefill of 64 sequences with its linear-attention pass
+    cfg_ms = {}
+    cfg_iters = max(1, min(args.steps, 10))
+
+    def time_fn(fn, iters=cfg_iters):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        g0.record(stream)
+        for _ in range(iters):
+            fn()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        return max_over_ranks([g0.elapsed_time(g1) / iters], dev, world)[0]
+
+    cfg_wl = {}
+    for name in CONFIG_WORKLOADS:
+        wl = gi.workload(name)
+        cfg_wl[name] = wl
+        X = gi.device_full(wl, dev, seed_offset=rank)
+        o = torch.empty((wl.total_tokens, wl.H, wl.d_v),
+                        dtype=torch.bfloat16 if wl.dtype == "bf16" else torch.float32, device=dev)
+        sf = torch.empty_like(X["S0"])
+        w = torch.empty(g.gdr_prefill_workspace_size(wl.n_seqs, wl.H, wl.d_k, wl.d_v,
+                                                     wl.dtype), dtype=torch.uint8, device=dev)
+        cfg_ms[name] = time_fn(lambda: g.gdr_prefill(
+            X["q"], X["k"], X["v"], X["alpha"], X["beta"], S0=X["S0"],
+            cu_seqlens=X["cu_seqlens"], out=o, S_final=sf, workspace=w))
+        if name == VARLEN:
+            cfg_ms[name + " linear"] = time_fn(lambda: g.gdr_linear_attn(
+                X["q"], X["k"], X["v"], S0=X["S0"], cu_seqlens=X["cu_seqlens"], out=o,
+                S_final=sf, workspace=w))
+        del X, o, sf, w
+    torch.cuda.empty_cache()
+
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -552,7 +605,7 @@ def run_gpu(args):
     kern_extra = {
         "gated_linear_attn": roof("gated_linear_attn",
                                   prefill_bytes(T, H, d, wp.n_seqs, beta=False),
-                                  prefill_flops(T, H, d, linear=True), gla_ms / 1e3),
+                                  gated_linear_flops(T, H, d), gla_ms / 1e3),
         "prefill_output_gate": roof("prefill_output_gate",
                                     prefill_bytes(T, H, d, wp.n_seqs) + T * H * d * 2,
                                     prefill_flops(T, H, d), og_ms / 1e3),
@@ -574,6 +627,31 @@ def run_gpu(args):
         "layer_prologue": roof("layer_prologue", 2 * T * H * (2 * d * 2 + d * 4 + 4), 0.0,
                                lp_ms / 1e3),
     }
+    cfg = {}
+    for name, wl in cfg_wl.items():
+        ms = cfg_ms[name]
+        ch = wl.gate == "channel"
+        elt = 2 if wl.dtype == "bf16" else 4
+        e = {"tokens_per_s": job_tokens_per_s(n, wl.total_tokens, ms / 1e3), "ms": ms,
+             "total_tokens": int(wl.total_tokens), "n_seqs": int(wl.n_seqs), "H": wl.H,
+             "d": wl.d_k, "gate": wl.gate, "dtype": wl.dtype,
+             "compute_dtype": g.compute_dtype(wl.dtype, wl.d_k)}
+        if name == SMALL:
+            e["note"] = "latency-bound (256 tokens, one head): time only"
+        else:
+            e["roofline"] = roof("cfg:" + name, prefill_bytes(wl.total_tokens, wl.H, wl.d_k,
+                                                               wl.n_seqs, channel=ch, elt=elt),
+                                 prefill_flops(wl.total_tokens, wl.H, wl.d_k), ms / 1e3)
+        cfg[name] = e
+        if name == VARLEN:
+            lms = cfg_ms[name + " linear"]
+            cfg[name + " linear"] = {
+                "tokens_per_s": job_tokens_per_s(n, wl.total_tokens, lms / 1e3), "ms": lms,
+                "roofline": roof("cfg:" + name + " linear",
+                                 prefill_bytes(wl.total_tokens, wl.H, wl.d_k, wl.n_seqs,
+                                               linear=True, elt=elt),
+                                 prefill_flops(wl.total_tokens, wl.H, wl.d_k, linear=True),
+                                 lms / 1e3)}
     dominant = max(kern, key=lambda k: kern[k]["launch_us"])
     main_roof = {k: kern[dominant][k] for k in ("bound", "achieved", "peak", "unit", "frac",
                                                  "traffic")}
@@ -602,6 +680,7 @@ def run_gpu(args):
         "roofline": main_roof,
         "kernels": kern,
         "kernels_outside_step": kern_extra,
+        "configs": cfg,
         "e2e": {"value": job_tokens_per_s(n, T, e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "what": "gdr_prefill_host: pinned host inputs in, "
                 "out and S_final back, copies pipelined with the kernels inside the call"},

@@ -9,6 +9,7 @@ library's CUDA kernels; there is no Python or CPU fallback.
     gdr_linear_attn(q, k, v, S0=None, cu_seqlens=None, out=None, S_final=None, ...)
     gdr_gated_linear_attn(q, k, v, alpha, S0=None, cu_seqlens=None, out=None, S_final=None, ...)
     gdr_prefill_workspace_size(n_seqs, H, d_k, d_v, dtype)  /  gdr_workspace_status(workspace)
+    gdr_query_device_status()  -- takes the library's error word on the current device
     gdr_prefill_host(q, k, v, alpha, beta, ...)  -- host (CPU) tensors in and out, copies inside
     gdr_prefill_host_buffer_size(n_seqs, H, total_tokens, d_k, d_v, dtype, gate, piece_tokens)
     gdr_layer_prologue(xq, xk, a=None, b=None, q=None, k=None, alpha=None, beta=None)
@@ -26,15 +27,16 @@ import ctypes
 import torch
 
 from . import _abi
-from ._abi import (GDR_BF16, GDR_F32, GDR_FLAG_FORCE_SIMT, GDR_FLAG_NO_CLUSTER, GDR_FLAG_PREFER_QUEUE,
-                   GDR_FLAG_LAYER_PROLOGUE, GDR_GATE_CHANNEL, GDR_GATE_SCALAR,
-                   GdrError, GdrShape)
+from ._abi import (GDR_BF16, GDR_ERR_DEVICE_CHECK, GDR_F32, GDR_FLAG_FORCE_SIMT,
+                   GDR_FLAG_LAYER_PROLOGUE, GDR_FLAG_NO_CLUSTER, GDR_FLAG_PREFER_QUEUE,
+                   GDR_GATE_CHANNEL, GDR_GATE_SCALAR, GDR_OK, GdrError, GdrShape)
 
 __all__ = ["gdr_prefill", "gdr_prefill_output_gate", "gdr_decode_step", "gdr_linear_attn",
            "gdr_gated_linear_attn", "gdr_layer_prologue", "gdr_normalized_linear_attn",
            "gdr_gated_linear_decode_step", "gdr_normalized_linear_decode_step",
            "gdr_prefill_workspace_size",
-           "gdr_workspace_status", "gdr_prefill_host", "gdr_prefill_host_buffer_size",
+           "gdr_workspace_status", "gdr_query_device_status", "gdr_prefill_host",
+           "gdr_prefill_host_buffer_size",
            "make_shape", "GdrError"]
 
 _DT = {torch.float32: GDR_F32, torch.bfloat16: GDR_BF16}
@@ -386,6 +388,16 @@ def gdr_workspace_status(workspace, stream=None) -> int:
     if rc != 0:
         raise GdrError(rc, "gdr_workspace_status")
     return int(code.value)
+
+
+def gdr_query_device_status(stream=None) -> int:
+    """Synchronise, then take (read and clear) the library's error word on the current device.
+    Returns the C status: GDR_OK (0) if no device-side check failed since the last query,
+    GDR_ERR_DEVICE_CHECK (4) if one did; raises on a CUDA failure."""
+    rc = _abi.load().gdr_query_device_status(_stream(stream))
+    if rc not in (GDR_OK, GDR_ERR_DEVICE_CHECK):
+        raise GdrError(rc, "gdr_query_device_status")
+    return int(rc)
 
 
 def compute_dtype(dtype: str, d: int, force_simt: bool = False) -> str:

@@ -10,11 +10,21 @@ namespace {
 constexpr int kPrepThreads = 1024;
 constexpr int kSortMax = 8192;  // longest-first ordering up to this many sequences
 
+// The library's error word on each device: every device-check failure of a prefill-like call
+// is also recorded here (the first code since the last gdr_query_device_status, which takes it
+// with an atomic exchange into g_device_status_taken and reads that back).
+__device__ int32_t g_device_status;
+__device__ int32_t g_device_status_taken;
+
+__global__ void take_device_status_kernel() {
+  g_device_status_taken = atomicExch(&g_device_status, 0);
+}
+
 // One CTA: clears the status word, checks cu_seqlens, and writes the visiting order of the
 // sequences (longest first, ties by index) so that long sequences start first.
 __global__ void __launch_bounds__(kPrepThreads)
     prep_kernel(const int32_t* __restrict__ cu, int n_seqs, int64_t total, int32_t* order,
-                int32_t* status) {
+                int32_t* status, int32_t* dev_status) {
   __shared__ int32_t s_len[kSortMax];
   __shared__ int s_bad;
   if (threadIdx.x == 0) {
@@ -33,7 +43,10 @@ __global__ void __launch_bounds__(kPrepThreads)
     if (sort) s_len[i] = len;
   }
   __syncthreads();
-  if (s_bad && threadIdx.x == 0) atomicCAS(status, 0, GDR_DEVCHECK_SEQLENS);
+  if (s_bad && threadIdx.x == 0) {
+    atomicCAS(status, 0, GDR_DEVCHECK_SEQLENS);
+    atomicCAS(dev_status, 0, GDR_DEVCHECK_SEQLENS);
+  }
   for (int i = threadIdx.x; i < n_seqs; i += blockDim.x) {
     if (!sort) {
       order[i] = i;
@@ -101,9 +114,13 @@ gdr_status prefill_common(const gdr_shape* sh, const void* q, const void* k, con
     ring = (unsigned char*)ring_flags +
            WorkspaceLayout::flag_bytes(WorkspaceLayout::ring_pairs(*sh));
   }
+  int32_t* dev_status = nullptr;
+  if (cudaGetSymbolAddress((void**)&dev_status, g_device_status) != cudaSuccess) return GDR_ERR_CUDA;
   PrefillArgs a{sh->n_seqs, sh->H, sh->total_tokens, q, k, v, alpha, beta, S0, cu,
-                out, S_final, order, status, ring_flags, ring, og, prologue, z0, z_final, eps};
-  prep_kernel<<<1, kPrepThreads, 0, s>>>(cu, sh->n_seqs, sh->total_tokens, order, status);
+                out, S_final, order, status, ring_flags, ring, og, prologue, z0, z_final, eps,
+                dev_status};
+  prep_kernel<<<1, kPrepThreads, 0, s>>>(cu, sh->n_seqs, sh->total_tokens, order, status,
+                                         dev_status);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess)
     e = prefill_tc_supported(*sh) ? launch_prefill_tc(*sh, a, kind, s)
@@ -251,6 +268,19 @@ gdr_status gdr_workspace_status(void* workspace, void* stream, int32_t* code) {
   if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), s) != cudaSuccess) return GDR_ERR_CUDA;
   *code = h;
   return GDR_OK;
+}
+
+gdr_status gdr_query_device_status(void* stream) {
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return GDR_ERR_CUDA;
+  gdr::take_device_status_kernel<<<1, 1, 0, s>>>();
+  if (cudaGetLastError() != cudaSuccess) return GDR_ERR_CUDA;
+  int32_t h = 0;
+  if (cudaMemcpyFromSymbolAsync(&h, gdr::g_device_status_taken, sizeof(h), 0,
+                                cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return GDR_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return GDR_ERR_CUDA;
+  return h == GDR_DEVCHECK_OK ? GDR_OK : GDR_ERR_DEVICE_CHECK;
 }
 
 const char* gdr_status_string(gdr_status status) {

@@ -81,7 +81,21 @@ struct PrefillArgs {
   const float* z0 = nullptr;
   float* z_final = nullptr;
   float eps = 0.f;
+  // the library's per-device error word (gdr_query_device_status), written beside `status`
+  int32_t* dev_status = nullptr;
 };
+
+// Records the first device-check failure (0 -> code).
+__device__ __forceinline__ void report(int32_t* status, int32_t code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// Records a device-check failure of a prefill-like call in its workspace word and in the
+// library's per-device error word.
+__device__ __forceinline__ void report(const PrefillArgs& a, int32_t code) {
+  report(a.status, code);
+  report(a.dev_status, code);
+}
 
 // phi(x) = elu(x) + 1: x + 1 above zero, e^x at and below it.
 __device__ __forceinline__ float phi_f(float x) { return x > 0.f ? x + 1.f : __expf(x); }
@@ -98,11 +112,6 @@ __device__ __forceinline__ float inv_norm(float ss) { return ss >= 1e-24f ? rsqr
 // The output gate of one element: o * sigmoid(g).
 __device__ __forceinline__ float gate_out(float o, float g) { return o / (1.f + __expf(-g)); }
 
-// Records the first device-check failure (0 -> code).
-__device__ __forceinline__ void report(int32_t* status, int32_t code) {
-  if (status) atomicCAS(status, 0, code);
-}
-
 // Resolves (seq -> token range) with the bounds check every kernel performs before touching
 // memory.  Returns false (after recording the failure) if the range is invalid.
 __device__ __forceinline__ bool seq_range(const PrefillArgs& a, int seq, int64_t& t0,
@@ -115,7 +124,7 @@ __device__ __forceinline__ bool seq_range(const PrefillArgs& a, int seq, int64_t
     t1 = a.total_tokens;
   }
   if (t0 < 0 || t1 < t0 || t1 > a.total_tokens) {
-    report(a.status, GDR_DEVCHECK_SEQLENS);
+    report(a, GDR_DEVCHECK_SEQLENS);
     return false;
   }
   return true;

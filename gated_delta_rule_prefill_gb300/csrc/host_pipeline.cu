@@ -203,6 +203,7 @@ extern "C" gdr_status gdr_prefill_host(const gdr_shape* shape, const void* q, co
   }
   const std::vector<int64_t> cuts = piece_cuts(cu, T, p.piece);
   const int npieces = (int)cuts.size() - 1;
+  gdr_status launch_st = GDR_OK;  // the first failed piece launch, if any
   for (int i = 0; i < npieces && e == cudaSuccess; ++i) {
     const int b = i & 1;
     const int64_t a0 = cuts[i], a1 = cuts[i + 1], len = a1 - a0;
@@ -236,7 +237,10 @@ extern "C" gdr_status gdr_prefill_host(const gdr_shape* shape, const void* q, co
     st = prefill_launch(&ps, dst[0], dst[1], dst[2], reinterpret_cast<const float*>(dst[3]),
                         reinterpret_cast<const float*>(dst[4]), st_p, d_pcu, base + p.out[b],
                         st_p, base + p.ws, p.ws_bytes, s);
-    if (st != GDR_OK) return st;
+    if (st != GDR_OK) {
+      launch_st = st;
+      break;
+    }
     ok(cudaEventRecord(r.comp[i % kRing], s));
     // outputs of piece i back to the host
     ok(cudaStreamWaitEvent(r.out, r.comp[i % kRing], 0));
@@ -244,13 +248,19 @@ extern "C" gdr_status gdr_prefill_host(const gdr_shape* shape, const void* q, co
                        (size_t)len * p.o_tok, cudaMemcpyDeviceToHost, r.out));
     ok(cudaEventRecord(r.d2h[i % kRing], r.out));
   }
-  // the final states once every piece (and the copy-in of the entering states) is done
+  // The final states once every piece (and the copy-in of the entering states) is done.  This
+  // join also runs after a failed piece: copies of earlier pieces into the caller's host arrays
+  // may still be queued on the internal streams, and the caller's stream must not pass the
+  // call before they have finished.  (The `ok` calls still execute after an error; they only
+  // stop recording it.)
   ok(cudaEventRecord(r.in_done, r.in));
   ok(cudaEventRecord(r.last, s));
   ok(cudaStreamWaitEvent(r.out, r.in_done, 0));
   ok(cudaStreamWaitEvent(r.out, r.last, 0));
-  if (S_final) ok(cudaMemcpyAsync(S_final, d_states, states_bytes, cudaMemcpyDeviceToHost, r.out));
+  if (S_final && launch_st == GDR_OK)
+    ok(cudaMemcpyAsync(S_final, d_states, states_bytes, cudaMemcpyDeviceToHost, r.out));
   ok(cudaEventRecord(r.end, r.out));
   ok(cudaStreamWaitEvent(s, r.end, 0));
+  if (launch_st != GDR_OK) return launch_st;
   return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }

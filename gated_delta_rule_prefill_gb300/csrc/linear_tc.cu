@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (MODE == 1) {  // hand the run's sums on through the workspace
     if (failed) {
-      if (tid == 0) report(a.status, GDR_DEVCHECK_TIMEOUT);
+      if (tid == 0) report(a, GDR_DEVCHECK_TIMEOUT);
     } else {
       s_final<DH>(x, drun + (size_t)x.lrow * kD);
       if (NORM && warp < 4) drun[kD * kD + tid] = tmem_ld1(x.tm + x.lane_base + kColZ);
@@ -482,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     o_store(nloc - 1, tl, (int)(te - tl));
   }
   if (failed) {
-    if (tid == 0) report(a.status, GDR_DEVCHECK_TIMEOUT);
+    if (tid == 0) report(a, GDR_DEVCHECK_TIMEOUT);
     // let copies already in flight land before the shared memory is released
     mbar_wait(bar_ld, ph_ld[0], kWaitNs);
     mbar_wait(bar_ld + 1, ph_ld[1], kWaitNs);

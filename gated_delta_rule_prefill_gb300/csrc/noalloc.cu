@@ -13,8 +13,6 @@
 // word is cleared first, the order array fully written), so nothing carries over, but two calls
 // whose work overlaps on the GPU (different streams, or different host threads) race on it and
 // must be serialised by the caller.
-#include <mutex>
-
 #include "gdr_internal.cuh"
 
 namespace gdr {
@@ -24,29 +22,10 @@ constexpr size_t kNoAllocScratchBytes = WorkspaceLayout::kHeaderBytes +
                                         ((size_t)GDR_NOALLOC_MAX_SEQS * 4 + 255) / 256 * 256;
 
 // The shared scratch: a device-side symbol, so host code never uses its address directly; the
-// device address is looked up with cudaGetSymbolAddress, once per device.
+// device address is looked up with cudaGetSymbolAddress on every call, with the caller's device
+// current (a cached address would go stale if the caller reset the device and the module were
+// loaded again into a new context).
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
-
-constexpr int kMaxDevices = 64;
-std::mutex g_mutex;
-void* g_scratch_addr[kMaxDevices] = {nullptr};
-
-// Device address of the scratch array on the current device (looked up on first use).
-cudaError_t scratch_address(void** addr) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_mutex);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = p;
-  }
-  *addr = g_scratch_addr[dev];
-  return cudaSuccess;
-}
 
 }  // namespace
 }  // namespace gdr
@@ -58,7 +37,7 @@ extern "C" gdr_status gdr_prefill_noalloc(const gdr_shape* shape, const void* q,
   if (!shape) return GDR_ERR_INVALID_ARG;
   if (shape->n_seqs > GDR_NOALLOC_MAX_SEQS) return GDR_ERR_UNSUPPORTED;
   void* scratch = nullptr;
-  if (gdr::scratch_address(&scratch) != cudaSuccess) return GDR_ERR_CUDA;
+  if (cudaGetSymbolAddress(&scratch, gdr::g_noalloc_scratch) != cudaSuccess) return GDR_ERR_CUDA;
   return gdr::prefill_launch(shape, q, k, v, alpha, beta, S0, cu_seqlens, out, S_final, scratch,
                              gdr::kNoAllocScratchBytes, stream);
 }

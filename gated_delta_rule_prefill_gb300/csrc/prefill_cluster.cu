@@ -403,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       o_store(nch - 1, tl, (int)(t1 - tl));
     }
     if (failed) {
-      if (tid == 0) report(a.status, GDR_DEVCHECK_TIMEOUT);
+      if (tid == 0) report(a, GDR_DEVCHECK_TIMEOUT);
       mbar_wait(bar_v, ph_v, kWaitNs);
     } else if (valid && a.S_final) {
       s_final<DH>(x, a.S_final + sidx + (size_t)x.lrow * kD);
@@ -536,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (tid == 0) bulk_wait_all();  // every copy into the chain CTA has landed
     if (failed) {
-      if (tid == 0) report(a.status, GDR_DEVCHECK_TIMEOUT);
+      if (tid == 0) report(a, GDR_DEVCHECK_TIMEOUT);
       mbar_wait(bar_qk, ph_qk, kWaitNs);
       if (kAlphaTile) mbar_wait(bar_a, ph_a, kWaitNs);
     }

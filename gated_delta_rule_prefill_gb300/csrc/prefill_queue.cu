@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       o_store(nch - 1, tl, (int)(t1 - tl));
     }
     if (failed) {
-      if (tid == 0) report(a.status, GDR_DEVCHECK_TIMEOUT);
+      if (tid == 0) report(a, GDR_DEVCHECK_TIMEOUT);
       if (loader && issued > landed) {  // a ring load still in flight into shared memory
         const int cc = issued - 1;
         mbar_wait(full + (cc & 1), ph_full[cc & 1], kWaitNs);
@@ -468,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       cur = nxt;
     }
     if (failed) {
-      if (tid == 0) report(a.status, GDR_DEVCHECK_TIMEOUT);
+      if (tid == 0) report(a, GDR_DEVCHECK_TIMEOUT);
       mbar_wait(bar_qk, ph_qk, kWaitNs);
       if (kAlphaTile) mbar_wait(bar_a, ph_a, kWaitNs);
     } else {  // hand over the last chunk

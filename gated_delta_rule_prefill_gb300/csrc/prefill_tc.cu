@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (failed) {
-    if (tid == 0) report(a.status, GDR_DEVCHECK_TIMEOUT);
+    if (tid == 0) report(a, GDR_DEVCHECK_TIMEOUT);
     // let copies already in flight land before the shared memory is released
     mbar_wait(bar_qk, ph_qk, kWaitNs);
     if (kAlphaTile) mbar_wait(bar_a, ph_a, kWaitNs);

@@ -23,8 +23,8 @@
  * Conventions shared by every call
  *   - Pointers are DEVICE pointers unless stated otherwise; the caller owns every buffer.  The
  *     library allocates nothing, keeps no state between calls and never frees caller memory
- *     (two stated exceptions: gdr_prefill_noalloc's fixed scratch array and gdr_prefill_host's
- *     internal copy streams).
+ *     (three stated exceptions: the per-device error word of gdr_query_device_status,
+ *     gdr_prefill_noalloc's fixed scratch array and gdr_prefill_host's internal copy streams).
  *   - Layouts are packed and token-major, row-major, no padding:
  *       q, k            [T_total, H, d_k]   dtype = shape->dtype
  *       v, out          [T_total, H, d_v]   dtype = shape->dtype
@@ -41,7 +41,8 @@
  *     default stream).  Argument errors are returned synchronously, before any launch.  Launch
  *     failures return GDR_ERR_CUDA.  Checks that need device data (cu_seqlens monotone and within
  *     total_tokens) run on the device and record the first failure in the workspace status word,
- *     read with gdr_workspace_status(); sequences that fail the check are skipped.
+ *     read with gdr_workspace_status(), and in the library's error word on that device, read
+ *     with gdr_query_device_status(); sequences that fail the check are skipped.
  *   - 16-byte alignment is required for every pointer (GDR_ERR_INVALID_ARG otherwise).
  */
 #ifndef GDR_H_
@@ -59,7 +60,7 @@ typedef enum {
   GDR_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, bad size, bad enum, workspace too small */
   GDR_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. d_k != d_v, d not 64/128) */
   GDR_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
-  GDR_ERR_DEVICE_CHECK = 4  /* a device-side check failed (see gdr_workspace_status) */
+  GDR_ERR_DEVICE_CHECK = 4  /* a device-side check failed (gdr_query_device_status) */
 } gdr_status;
 
 typedef enum { GDR_F32 = 0, GDR_BF16 = 1 } gdr_dtype; /* dtype of q, k, v and out */
@@ -249,6 +250,19 @@ gdr_status gdr_gated_linear_attn(const gdr_shape* shape, const void* q, const vo
 gdr_status gdr_workspace_status(void* workspace, void* stream, int32_t* code);
 
 /*
+ * gdr_query_device_status -- synchronise `stream`, then take (read and clear, atomically) the
+ * library's error word on the current device: the first device-side check failure recorded by
+ * any prefill-like call on this device since the previous query (GDR_DEVCHECK_SEQLENS from the
+ * cu_seqlens check, GDR_DEVCHECK_TIMEOUT from a bounded wait that gave up).  The pages define no
+ * interface; this is the error path of the library.  The word is per device and shared by all
+ * calls on it (the one piece of state the library keeps besides the two listed above); the
+ * failing call's own code is also in its workspace word (gdr_workspace_status).
+ * Returns GDR_OK (no failure recorded), GDR_ERR_DEVICE_CHECK (a failure was recorded and is now
+ * cleared) or GDR_ERR_CUDA (the synchronisation, the exchange or the copy failed).
+ */
+gdr_status gdr_query_device_status(void* stream);
+
+/*
  * gdr_prefill_noalloc -- gdr_prefill for callers that cannot provide a workspace.  (The pages
  * have no counterpart: this is a property of the library interface, not of the method.)
  *
@@ -259,8 +273,9 @@ gdr_status gdr_workspace_status(void* workspace, void* stream, int32_t* code);
  * the library's device memory, sized for at most GDR_NOALLOC_MAX_SEQS sequences (larger n_seqs
  * returns GDR_ERR_UNSUPPORTED), held on every GPU that loads the library until the process
  * exits.
- *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress)
- *     with that device current; make that first call before any stream capture.
+ *   - Every call looks up the array's device address on the current device
+ *     (cudaGetSymbolAddress); the first call on a device may also load the library's device
+ *     code there, so make that first call before any stream capture.
  *   - Every call shares the array and leaves its contents behind; each call rewrites what it
  *     uses, but calls that overlap on the GPU (other streams, other host threads) race on it:
  *     serialise them.

@@ -234,3 +234,15 @@ def test_decode_variants_argument_errors(lib):
     sh2 = _shape(n_seqs=4, H=2, total_tokens=4)
     sh2.flags = GDR_FLAG_LAYER_PROLOGUE
     assert norm(shape=sh2) == 2
+
+
+def test_query_device_status_without_a_device(lib):
+    # the call synchronises the stream first; with no usable GPU that fails cleanly with
+    # GDR_ERR_CUDA instead of touching device memory, and on a GPU it returns a status
+    from gated_delta_rule_prefill_gb300 import _abi
+    import torch
+    rc = lib.gdr_query_device_status(None)
+    if torch.cuda.is_available():
+        assert rc in (_abi.GDR_OK, _abi.GDR_ERR_DEVICE_CHECK)
+    else:
+        assert rc == _abi.GDR_ERR_CUDA

@@ -9,7 +9,7 @@ import torch
 
 import gdr_inputs as gi
 import oracle
-from tests.parity import TOL, dev_inputs, host, rel_rows, rel_states, to_dev
+from tests.parity import TOL, dev_inputs, err_rows, err_states, host, rel_states, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -33,7 +33,7 @@ def _prefill(d, linear=False):
 
 
 def _check(name, got_o, got_s, ref_o, ref_s, tol):
-    eo, es = rel_rows(got_o, ref_o), rel_states(got_s, ref_s)
+    eo, es = err_rows(got_o, ref_o, tol), err_states(got_s, ref_s, tol)
     print("%s: output err %.3g, state err %.3g" % (name, eo, es))
     assert eo <= tol and es <= tol, (name, eo, es)
 

@@ -9,7 +9,7 @@ import torch
 
 import gdr_inputs as gi
 import oracle
-from tests.parity import TOL, dev_inputs, host, rel_rows, rel_states, to_dev
+from tests.parity import TOL, dev_inputs, err_rows, err_states, host, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -29,7 +29,7 @@ def check(a, dtype, force_simt=False, what="", no_cluster=False):
     torch.cuda.synchronize()
     ref = oracle.gated_linear(a["q"], a["k"], a["v"], a["alpha"], S0=a["S0"],
                               cu_seqlens=a["cu_seqlens"])
-    eo, es = rel_rows(host(out), ref[0]), rel_states(host(sf), ref[1])
+    eo, es = err_rows(host(out), ref[0], TOL[dtype]), err_states(host(sf), ref[1], TOL[dtype])
     print("%s: output err %.3g, state err %.3g" % (what, eo, es))
     assert eo <= TOL[dtype] and es <= TOL[dtype], (what, eo, es)
     assert np.isfinite(host(out)).all()
@@ -94,7 +94,7 @@ def test_gla_decode_step(dtype, d, gate):
                                              Sd)
         torch.cuda.synchronize()
         ro, rs = oracle.gated_linear(a["q"], a["k"], a["v"], a["alpha"], S0=S, cu_seqlens=cu)
-        eo, es = rel_rows(host(out), ro), rel_states(host(Sd), rs)
+        eo, es = err_rows(host(out), ro, TOL[dtype]), err_states(host(Sd), rs, TOL[dtype])
         print("gla decode %s %s step %d: out %.3g state %.3g" % (dtype, gate, step, eo, es))
         assert eo <= TOL[dtype] and es <= TOL[dtype], (eo, es)
         S = rs
@@ -114,5 +114,5 @@ def test_gla_decode_step_prologue():
     torch.cuda.synchronize()
     q, k, al, _ = oracle.layer_prologue(a["q"], a["k"], a["alpha"], a["beta"])
     ro, rs = oracle.gated_linear(q, k, a["v"], al, S0=S, cu_seqlens=np.arange(N + 1))
-    eo, es = rel_rows(host(out), ro), rel_states(host(Sd), rs)
+    eo, es = err_rows(host(out), ro, TOL["bf16"]), err_states(host(Sd), rs, TOL["bf16"])
     assert eo <= TOL["bf16"] and es <= TOL["bf16"], (eo, es)

@@ -9,7 +9,7 @@ import torch
 
 import gdr_inputs as gi
 import oracle
-from tests.parity import TOL, dev_inputs, host, rel_rows, rel_states
+from tests.parity import TOL, dev_inputs, err_rows, err_states, host, rel_rows, rel_states
 
 pytestmark = pytest.mark.gpu
 
@@ -43,10 +43,10 @@ def run_case(a, dtype, piece, pinned=True, with_s0=True, with_final=True):
     s0 = a["S0"] if with_s0 else None
     ref = oracle.gated_delta(a["q"], a["k"], a["v"], a["alpha"], a["beta"], S0=s0,
                              cu_seqlens=a["cu_seqlens"])
-    eo = rel_rows(out.float().numpy(), ref[0])
+    eo = err_rows(out.float().numpy(), ref[0], TOL[dtype])
     assert eo <= TOL[dtype], eo
     if with_final:
-        es = rel_states(sf.numpy(), ref[1])
+        es = err_states(sf.numpy(), ref[1], TOL[dtype])
         assert es <= TOL[dtype], es
     # the same prefill on device copies (one call): identical chunking, so the results agree
     d = dev_inputs(a, dtype)

@@ -9,7 +9,7 @@ import torch
 
 import gdr_inputs as gi
 import oracle
-from tests.parity import TOL, dev_inputs, host, rel_rows, rel_states, to_dev
+from tests.parity import TOL, dev_inputs, err_rows, err_states, host, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -34,8 +34,8 @@ def run(a, dtype, eps=0.0, with_state=True, force_simt=False, z0_scale=1.0):
     ro, rs, rz = oracle.normalized_linear(a["q"], a["k"], a["v"],
                                           a["S0"] if with_state else None,
                                           z0 if with_state else None, a["cu_seqlens"], eps)
-    eo, es = rel_rows(host(out), ro), rel_states(host(sf), rs)
-    ez = rel_rows(host(zf), rz)
+    eo, es = err_rows(host(out), ro, TOL[dtype]), err_states(host(sf), rs, TOL[dtype])
+    ez = err_rows(host(zf), rz, TOL[dtype])
     print("%s eps %g simt %s: out %.3g state %.3g z %.3g" % (dtype, eps, force_simt, eo, es, ez))
     assert eo <= TOL[dtype] and es <= TOL[dtype] and ez <= TOL[dtype], (eo, es, ez)
 
@@ -96,7 +96,8 @@ def test_normlinear_decode_step(dtype, d):
         out = g.gdr_normalized_linear_decode_step(d_["q"], d_["k"], d_["v"], Sd, zd, eps=1e-6)
         torch.cuda.synchronize()
         ro, rs, rz = oracle.normalized_linear(a["q"], a["k"], a["v"], S, z, cu, 1e-6)
-        eo, es, ez = rel_rows(host(out), ro), rel_states(host(Sd), rs), rel_rows(host(zd), rz)
+        eo, es = err_rows(host(out), ro, TOL[dtype]), err_states(host(Sd), rs, TOL[dtype])
+        ez = err_rows(host(zd), rz, TOL[dtype])
         print("norm decode %s step %d: out %.3g state %.3g z %.3g" % (dtype, step, eo, es, ez))
         assert eo <= TOL[dtype] and es <= TOL[dtype] and ez <= TOL[dtype], (eo, es, ez)
         S, z = rs, rz

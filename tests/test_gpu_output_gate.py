@@ -9,7 +9,7 @@ import torch
 
 import gdr_inputs as gi
 import oracle
-from tests.parity import TOL, dev_inputs, host, rel_rows, rel_states, to_dev
+from tests.parity import TOL, dev_inputs, err_rows, err_states, host, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -38,7 +38,7 @@ def run(a, dtype, path="default", seed=401):
     ref_o, ref_s = oracle.gated_delta(a["q"], a["k"], a["v"], a["alpha"], a["beta"], S0=a["S0"],
                                       cu_seqlens=a["cu_seqlens"])
     ref = oracle.output_gate(ref_o, gate)
-    eo, es = rel_rows(host(out), ref), rel_states(host(sf), ref_s)
+    eo, es = err_rows(host(out), ref, TOL[dtype]), err_states(host(sf), ref_s, TOL[dtype])
     print("%s %s: output err %.3g, state err %.3g" % (dtype, path, eo, es))
     assert eo <= TOL[dtype] and es <= TOL[dtype], (path, eo, es)
 

@@ -10,7 +10,7 @@ import torch
 
 import gdr_inputs as gi
 import oracle
-from tests.parity import TOL, dev_inputs, host, rel_rows, rel_states, to_dev
+from tests.parity import TOL, dev_inputs, err_rows, err_states, host, rel_rows, rel_states, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -27,8 +27,8 @@ def mapped(a):
 
 
 def check(name, out, sf, ref_o, ref_s, dtype):
-    eo = rel_rows(host(out), ref_o)
-    es = rel_states(host(sf), ref_s) if sf is not None else 0.0
+    eo = err_rows(host(out), ref_o, TOL[dtype])
+    es = err_states(host(sf), ref_s, TOL[dtype]) if sf is not None else 0.0
     print("%s: output err %.3g, state err %.3g" % (name, eo, es))
     assert eo <= TOL[dtype] and es <= TOL[dtype], (name, eo, es)
 

@@ -52,3 +52,22 @@ def test_named_workloads():
     assert gi.workload("kda_b1_h32_t32768").total_tokens == 32768
     d = gi.gen_decode_step(gi.workload("decode_n256_h32"), 3)
     assert d["q"].shape == (256, 32, 128) and d["alpha"].shape == (256, 32, 128)
+
+
+def test_parity_metrics():
+    # the element-wise metric sees a single wrong element that the row norm hides, and the
+    # fp32 bound asserts it; the bf16 bound keeps the row-normwise metric alone
+    from tests.parity import TOL, err_rows, rel_elem, rel_rows
+    rng = np.random.default_rng(0)
+    ref = rng.normal(size=(8, 128))
+    got = ref.copy()
+    got[3, 5] += 5e-4 * abs(ref[3, 5]) + 1e-12
+    assert rel_rows(got, ref) < 1e-4 < rel_elem(got, ref)
+    assert err_rows(got, ref, TOL["f32"]) > TOL["f32"]
+    assert err_rows(got, ref, TOL["bf16"]) == rel_rows(got, ref)
+    # elements near zero are judged against 1e-3 x the RMS, not their own size
+    ref2 = np.ones((2, 4))
+    ref2[0, 0] = 0.0
+    got2 = ref2.copy()
+    got2[0, 0] = 1e-8
+    assert rel_elem(got2, ref2) < 1e-4
