@@ -21,7 +21,11 @@
 // of S are independent (v and U enter column-wise), so the value dimension splits across CTAs
 // with no communication.  Each CTA walks its sequence's chunks in order; the state block lives
 // in shared memory for the whole walk.  All pair decays e^{G_r - G_j} are formed directly (no
-// factorisation), so any alpha in [0, 1] is exact to fp32 rounding.
+// factorisation) when the chunk's decay is strong; otherwise as the products of e^{G_r} and
+// e^{-G_j}, which are then far inside the fp32 range.  G is kept as an unevaluated sum hi + lo
+// (the error of every addition carried in lo), so a difference G_r - G_j is as accurate as its
+// own size allows, whatever the size of G after a reset; with the accurate logf and expf this
+// makes any alpha in [0, 1] exact to fp32 rounding.
 #include "gdr_internal.cuh"
 
 namespace gdr {
@@ -39,8 +43,9 @@ struct SimtSmem {
   static constexpr int off_Q = 0;
   static constexpr int off_K = off_Q + C * LD;
   static constexpr int off_Kh = off_K + C * LD;
-  static constexpr int off_G = off_Kh + C * LD;
-  static constexpr int off_X = off_G + C * LD;
+  static constexpr int off_G = off_Kh + C * LD;   // G, rounded part (hi)
+  static constexpr int off_Gl = off_G + C * LD;   // G, rounding error of hi (lo)
+  static constexpr int off_X = off_Gl + C * LD;
   static constexpr int off_A = off_X + C * LX;
   static constexpr int off_M = off_A + C * LC;
   static constexpr int off_S = off_M + C * LC;
@@ -49,7 +54,8 @@ struct SimtSmem {
   static constexpr int off_B = off_U + C * LV;
   static constexpr int off_Gam = off_B + C;
   static constexpr int off_Z = off_Gam + D;    // the normaliser z (normalised linear attention)
-  static constexpr int total_floats = off_Z + D;
+  static constexpr int off_Flag = off_Z + D;   // the chunk's decay is weak enough to factorise
+  static constexpr int total_floats = off_Flag + 4;
   static constexpr size_t bytes = (size_t)total_floats * 4;
 };
 
@@ -65,6 +71,8 @@ __global__ void __launch_bounds__(kSimtThreads) prefill_simt_kernel(PrefillArgs 
   float* sK = sm + L::off_K;
   float* sKh = sm + L::off_Kh;
   float* sG = sm + L::off_G;
+  float* sGl = sm + L::off_Gl;
+  int* sFlag = reinterpret_cast<int*>(sm + L::off_Flag);
   float* sX = sm + L::off_X;
   float* sA = sm + L::off_A;
   float* sM = sm + L::off_M;
@@ -118,7 +126,7 @@ __global__ void __launch_bounds__(kSimtThreads) prefill_simt_kernel(PrefillArgs 
         float g = 0.f;
         if (ok) {
           const float al = CHANNEL ? a.alpha[o] : a.alpha[(size_t)(tc + r) * H + h];
-          g = log_gate(a.prologue ? sigmoid_f(al) : al);
+          g = fmaxf(logf(a.prologue ? sigmoid_f(al) : al), kLogAlphaMin);
         }
         sG[r * L::LD + c] = g;
       }
@@ -148,14 +156,44 @@ __global__ void __launch_bounds__(kSimtThreads) prefill_simt_kernel(PrefillArgs 
       __syncthreads();
     }
 
+    bool factor = false;  // pair decays as e^{G_r} e^{-G_j} (weak decay) or directly
     if (!LINEAR) {
-      // ---- 2. in-chunk inclusive prefix sums of the log-gates, per key channel
+      // ---- 2. in-chunk inclusive prefix sums of the log-gates, per key channel, as hi + lo
+      // (two-sum: lo collects the rounding error of every addition)
+      if (tid == 0) *sFlag = 1;
+      __syncthreads();
       for (int c = tid; c < D; c += kSimtThreads) {
-        float acc = 0.f;
+        float hi = 0.f, lo = 0.f;
         for (int r = 0; r < C; ++r) {
-          acc += sG[r * L::LD + c];
-          sG[r * L::LD + c] = acc;
+          const float g = sG[r * L::LD + c];
+          const float s2 = hi + g;
+          const float bb = s2 - hi;
+          lo += (hi - (s2 - bb)) + (g - bb);
+          hi = s2;
+          sG[r * L::LD + c] = hi;
+          sGl[r * L::LD + c] = lo;
         }
+        if (hi + lo < -80.f) *sFlag = 0;  // e^{-G} would leave the comfortable fp32 range
+      }
+      __syncthreads();
+      factor = *sFlag != 0;
+    }
+    // e^{G_r} from its two parts: expf of the exact hi, times (1 + lo)
+    auto eG = [&](int r, int c, float sign) {
+      const float e = expf(sign * sG[r * L::LD + c]);
+      return fmaf(e, sign * sGl[r * L::LD + c], e);
+    };
+
+    if (factor) {
+      // ---- 3a. weak decay: the gate-scaled operands first (beta K~ into the solve's right-hand
+      // side, Q~ in place, Kr = K e^{-G} into the K^ tile), then plain products below
+      for (int i = tid; i < C * D; i += kSimtThreads) {
+        const int r = i / D, c = i % D;
+        const float e = eG(r, c, 1.f);
+        const float kv = sK[r * L::LD + c];
+        if (ERASE) sX[r * L::LX + c] = sB[r] * kv * e;  // beta K~
+        sKh[r * L::LD + c] = kv * eG(r, c, -1.f);
+        sQ[r * L::LD + c] *= e;
       }
       __syncthreads();
     }
@@ -172,11 +210,21 @@ __global__ void __launch_bounds__(kSimtThreads) prefill_simt_kernel(PrefillArgs 
       const float* qr = sQ + r * L::LD;
       if (LINEAR) {
         for (int c = 0; c < D; ++c) acc_m = fmaf(qr[c], kj[c], acc_m);
+      } else if (factor) {
+        const float* xr = sX + r * L::LX;   // beta_r K~_r
+        const float* krj = sKh + j * L::LD;  // Kr_j
+        for (int c = 0; c < D; ++c) {
+          if (ERASE) acc_a = fmaf(xr[c], krj[c], acc_a);
+          acc_m = fmaf(qr[c], krj[c], acc_m);  // qr is Q~_r here
+        }
+        if (ERASE) sA[r * L::LC + j] = (j < r) ? acc_a : 0.f;
       } else {
         const float* gr = sG + r * L::LD;
         const float* gj = sG + j * L::LD;
+        const float* glr = sGl + r * L::LD;
+        const float* glj = sGl + j * L::LD;
         for (int c = 0; c < D; ++c) {
-          const float w = kj[c] * __expf(gr[c] - gj[c]);
+          const float w = kj[c] * expf((gr[c] - gj[c]) + (glr[c] - glj[c]));
           acc_a = fmaf(kr[c], w, acc_a);
           acc_m = fmaf(qr[c], w, acc_m);
         }
@@ -202,15 +250,23 @@ __global__ void __launch_bounds__(kSimtThreads) prefill_simt_kernel(PrefillArgs 
     }
 
     if (!LINEAR) {
-      // ---- 4. gate-scaled operands and the right-hand sides of the solve
+      // ---- 4. gate-scaled operands and the right-hand sides of the solve (strong decay: here;
+      // weak decay: K^ = Kr gamma)
+      for (int c = tid; c < D; c += kSimtThreads) sGam[c] = eG(C - 1, c, 1.f);
+      if (factor) __syncthreads();
       for (int i = tid; i < C * D; i += kSimtThreads) {
         const int r = i / D, c = i % D;
-        const float g = sG[r * L::LD + c];
-        const float gam = __expf(g);
+        if (factor) {
+          sKh[r * L::LD + c] *= sGam[c];
+          continue;
+        }
         const float kv = sK[r * L::LD + c];
-        if (ERASE) sX[r * L::LX + c] = sB[r] * kv * gam;                    // beta K~
-        sKh[r * L::LD + c] = kv * __expf(sG[(C - 1) * L::LD + c] - g);      // K^
-        sQ[r * L::LD + c] *= gam;                                           // Q~
+        const float e = eG(r, c, 1.f);
+        if (ERASE) sX[r * L::LX + c] = sB[r] * kv * e;  // beta K~
+        sKh[r * L::LD + c] =
+            kv * expf((sG[(C - 1) * L::LD + c] - sG[r * L::LD + c]) +
+                      (sGl[(C - 1) * L::LD + c] - sGl[r * L::LD + c]));  // K^
+        sQ[r * L::LD + c] *= e;                                            // Q~
       }
       if (ERASE) {
         for (int i = tid; i < C * kDVB; i += kSimtThreads) {
@@ -218,7 +274,6 @@ __global__ void __launch_bounds__(kSimtThreads) prefill_simt_kernel(PrefillArgs 
           sX[r * L::LX + D + c] = sB[r] * sV[r * L::LV + c];  // beta V
         }
       }
-      for (int c = tid; c < D; c += kSimtThreads) sGam[c] = __expf(sG[(C - 1) * L::LD + c]);
       __syncthreads();
     }
     if (ERASE) {
