@@ -9,7 +9,7 @@ import torch
 
 import gdr_inputs as gi
 import oracle
-from tests.parity import TOL, dev_inputs, err_rows, err_states, host, rel_states, to_dev
+from tests.parity import TOL, dev_inputs, err_rows, err_states, host, rel_rows, rel_states, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -143,3 +143,30 @@ def test_varlen_full_sampled():
            np.stack(ref["s"]), TOL["bf16"])
     _check("varlen linear (64 pairs)", cat(got["lo"]), np.stack(got["ls"]), cat(ref["lo"]),
            np.stack(ref["ls"]), TOL["bf16"])
+
+
+@pytest.mark.parametrize("path", ["cluster", "one_cta"])
+def test_error_against_chain_length(path):
+    """One 65,536-token sequence (1,024 chunks, longer than any chain of the named workloads),
+    2 heads, bf16 q/k/v, per-channel gates drawn as in the workloads, S0 ~ N(0, 0.01): every
+    output and the final state against the oracle, with the output error reported per 8,192-token
+    segment.  The tensor-core chain feeds a bf16 copy of the fp32 state to its products each
+    chunk; the error must stay within the bf16 bound with margin (<= 1e-2) and must not grow
+    along the chain (the last segment within 2x of the first)."""
+    import gated_delta_rule_prefill_gb300 as g
+    wl = gi.custom(seed=4242, seqlens=[65536], H=2, d_k=128, d_v=128, dtype="bf16",
+                   gate="channel", s0="normal")
+    a = gi.gen_full(wl, threads=16)
+    d = dev_inputs(a, "bf16")
+    out, Sf = g.gdr_prefill(d["q"], d["k"], d["v"], d["alpha"], d["beta"], S0=d["S0"],
+                            cu_seqlens=d["cu_seqlens"], no_cluster=(path == "one_cta"))
+    torch.cuda.synchronize()
+    ro, rs = oracle.gated_delta(a["q"], a["k"], a["v"], a["alpha"], a["beta"], S0=a["S0"],
+                                cu_seqlens=a["cu_seqlens"])
+    got = host(out)
+    seg = [rel_rows(got[i:i + 8192], ro[i:i + 8192]) for i in range(0, 65536, 8192)]
+    es = rel_states(host(Sf), rs)
+    print("%s: output error per 8K segment %s, final state %.3g"
+          % (path, " ".join("%.3g" % e for e in seg), es))
+    assert max(seg) <= 1e-2 and es <= 1e-2, (seg, es)
+    assert seg[-1] <= 2 * seg[0], seg
