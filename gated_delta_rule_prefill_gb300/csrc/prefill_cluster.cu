@@ -36,9 +36,12 @@ struct ChainSmem {
   static constexpr uint32_t VIN = 2 * kSlotBytes;          // V [64 tok][128] SW128, 2 slabs
   static constexpr uint32_t UU = VIN + 16384;              // U [tok][128] (MN-major B)
   static constexpr uint32_t SS = UU + 16384;               // S [d_k][128] (MN-major B)
-  static constexpr uint32_t BARS = SS + 32768;             // full[2], v, mma, o, TMEM slot
-  static constexpr uint32_t END = BARS + 64;
+  static constexpr uint32_t OST = SS + 32768;              // output gate: O rows [64][256 B]
+  static constexpr uint32_t END = OST + 16384;
+  // full[2], v, mma, o, TMEM slot: in the second slot's tail, which no copy writes
+  static constexpr uint32_t BARS = kSlotBytes + kSlotGam + 512;
 };
+static_assert(ChainSmem::BARS + 64 <= 2 * kSlotBytes, "barriers inside the second slot's tail");
 
 struct HelperSmem {
   static constexpr uint32_t QIN = 0;              // [64][128] bf16 row-major
@@ -238,20 +241,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     // columns go through its own 4 KB of the bf16 state tile (the rows it rewrites itself in
     // s_update, free between the chunk's first MMA and that update), so that each global store
     // instruction writes four whole 128-byte row segments instead of 32 scattered pieces.
-    // the output gate's values for the O rows this thread stores next (lane -> 8 row segments of
-    // 16 bytes, the coalesced store pattern below), loaded ahead so their latency is hidden
-    uint4 gv[8];
-    auto load_gates = [&](int64_t tc, int n) {
-      if constexpr (OGATE) {
-        const __nv_bfloat16* og = static_cast<const __nv_bfloat16*>(a.og);
-        const int lane = tid & 31, row0 = (warp & 3) * 32 - 64;
+    // Output gate: the O rows of chunk c - 1 leave TMEM in chunk c's U window into the staging
+    // tile OST (the O warps, 8 KB-swizzled rows of 256 bytes); all eight warps then gate and store
+    // them during chunk c + 1's first MMAs, when every warp is idle, with the gate values each
+    // thread loaded a chunk earlier (the rows were prefetched into L2 a chunk before that).
+    uint4 gq[4];
+    auto stage_o = [&](int c) {  // O warps: rows 0-63 of the staged tile
+      float v[64];
+      tmem_ld64(x.tm + x.lane_base + d_col(c) + x.wh * 64, v);
+      const int r = (warp & 3) * 32 + (tid & 31) - 64;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int r = 4 * j + (lane >> 3), ch = lane & 7;
-          gv[j] = make_uint4(0u, 0u, 0u, 0u);
-          if (row0 + r < n)
-            gv[j] = *reinterpret_cast<const uint4*>(og + ((size_t)(tc + row0 + r) * H + h) * kD +
-                                                    x.wh * 64 + ch * 8);
+      for (int j = 0; j < 8; ++j) {
+        __align__(16) __nv_bfloat162 hv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          hv[i] = __floats2bfloat162_rn(v[8 * j + 2 * i], v[8 * j + 2 * i + 1]);
+        *reinterpret_cast<uint4*>(sm + L::OST + r * 256 + (((8 * x.wh + j) ^ (r & 15)) << 4)) =
+            *reinterpret_cast<const uint4*>(hv);
+      }
+    };
+    auto load_og = [&](int64_t tc, int n) {  // every thread: 4 of the tile's 16-byte chunks
+      const __nv_bfloat16* og = static_cast<const __nv_bfloat16*>(a.og);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int e = tid + kThreads * j, r = e >> 4, ch = e & 15;
+        gq[j] = r < n ? *reinterpret_cast<const uint4*>(og + ((size_t)(tc + r) * H + h) * kD + ch * 8)
+                      : make_uint4(0u, 0u, 0u, 0u);
+      }
+    };
+    auto store_gated = [&](int64_t tc, int n) {  // every thread: the same 4 chunks, gated
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int e = tid + kThreads * j, r = e >> 4, ch = e & 15;
+        if (r < n) {
+          uint4 w = *reinterpret_cast<const uint4*>(sm + L::OST + r * 256 + ((ch ^ (r & 15)) << 4));
+          __nv_bfloat162* hw = reinterpret_cast<__nv_bfloat162*>(&w);
+          const __nv_bfloat162* hg = reinterpret_cast<const __nv_bfloat162*>(&gq[j]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) hw[i] = gate2_bf16(hw[i], hg[i]);
+          *reinterpret_cast<uint4*>(out + ((size_t)(tc + r) * H + h) * kD + ch * 8) = w;
         }
       }
     };
@@ -270,33 +298,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       const int row0 = (warp & 3) * 32 - 64;  // this warp's first O row
-      if constexpr (OGATE) {
-        // the output gate (values in gv, loaded ahead), on the rounded output: one more rounding
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int r = 4 * j + (lane >> 3), ch = lane & 7;
-          uint4 w = *reinterpret_cast<const uint4*>(stage + r * 128 + ((ch ^ (r & 7)) << 4));
-          if (row0 + r < n) {
-            __nv_bfloat162* hw = reinterpret_cast<__nv_bfloat162*>(&w);
-            const __nv_bfloat162* hg = reinterpret_cast<const __nv_bfloat162*>(&gv[j]);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float2 o2 = __bfloat1622float2(hw[i]), g2 = __bfloat1622float2(hg[i]);
-              hw[i] = __floats2bfloat162_rn(gate_out_bf16(o2.x, g2.x), gate_out_bf16(o2.y, g2.y));
-            }
-            *reinterpret_cast<uint4*>(out + ((size_t)(tc + row0 + r) * H + h) * kD + x.wh * 64 +
-                                      ch * 8) = w;
-          }
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int r = 4 * j + (lane >> 3), ch = lane & 7;
-          const uint4 w = *reinterpret_cast<const uint4*>(stage + r * 128 + ((ch ^ (r & 7)) << 4));
-          if (row0 + r < n)
-            *reinterpret_cast<uint4*>(out + ((size_t)(tc + row0 + r) * H + h) * kD + x.wh * 64 +
-                                      ch * 8) = w;
-        }
+      for (int j = 0; j < 8; ++j) {
+        const int r = 4 * j + (lane >> 3), ch = lane & 7;
+        const uint4 w = *reinterpret_cast<const uint4*>(stage + r * 128 + ((ch ^ (r & 7)) << 4));
+        if (row0 + r < n)
+          *reinterpret_cast<uint4*>(out + ((size_t)(tc + row0 + r) * H + h) * kD + x.wh * 64 +
+                                    ch * 8) = w;
       }
       __syncwarp();
     };
@@ -353,7 +361,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_run<kD>(x.tm + d_col(c), opWQ, opS, id_d, true);
         mma_commit_elect(x.bar_mma);
       }
-      if (OGATE && !u_rows && c > 0) load_gates(tc - kC, kC);  // for o_store(c - 1) below
+      if constexpr (OGATE) {  // chunk c - 2's gated rows leave the staging tile
+        if (c >= 2) store_gated(tc - 2 * kC, kC);
+        if (c >= 1) load_og(tc - kC, kC);
+        __syncthreads();  // the staging tile is free for chunk c - 1's rows below
+      }
       bad |= !mbar_wait(x.bar_mma, x.ph_mma, kWaitNs);
       x.ph_mma ^= 1u;
       fence_after_sync();
@@ -377,7 +389,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit_elect(bar_o);
         }
       } else if (c > 0) {
-        o_store(c - 1, tc - kC, kC);  // the previous chunk's output rows, off the tensor pipe
+        if constexpr (OGATE) {
+          stage_o(c - 1);
+        } else {
+          o_store(c - 1, tc - kC, kC);  // the previous chunk's output rows, off the tensor pipe
+        }
       }
       bad |= !mbar_wait(x.bar_mma, x.ph_mma, kWaitNs);
       x.ph_mma ^= 1u;
@@ -397,9 +413,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r = 1; r < ncl; ++r) st_relaxed_remote(map_to(cons_local, r), (uint32_t)(c + 1));
       }
     }
-    if (!failed && nch > 0 && !u_rows) {
+    if constexpr (OGATE) {  // the last two chunks' rows
+      if (!failed && nch > 0) {
+        const int64_t tl = t0 + (int64_t)(nch - 1) * kC;
+        if (nch >= 2) store_gated(tl - kC, kC);
+        __syncthreads();
+        if (!u_rows) stage_o(nch - 1);
+        load_og(tl, (int)(t1 - tl));
+        __syncthreads();
+        store_gated(tl, (int)(t1 - tl));
+      }
+    } else if (!failed && nch > 0 && !u_rows) {
       const int64_t tl = t0 + (int64_t)(nch - 1) * kC;
-      load_gates(tl, (int)(t1 - tl));
       o_store(nch - 1, tl, (int)(t1 - tl));
     }
     if (failed) {
