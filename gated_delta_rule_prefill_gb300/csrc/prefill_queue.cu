@@ -248,6 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bad |= !mbar_wait(bar_v, ph_v, kWaitNs);
         ph_full[s] ^= 1u;
         ph_v ^= 1u;
+        __syncwarp();  // lanes leave their polling loops (and the loader its poll) at different times
         if (n < kC) {  // the last chunk: every thread zeroes part of the V tail
           zero_v_tail<DV>(x, sm + L::VIN, n);
           __syncthreads();
@@ -261,6 +262,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         st_relaxed_gpu(q_loaded + p, (uint32_t)(c + 1));
         if (c + 1 < nch) next_ready = ld_acquire_gpu(q_ready + p * kR + ((c + 1) % kR));
       }
+      // the loader lane rejoins its warp before the warp-collective TMEM instructions below
+      // (tcgen05.ld / st and bar.sync are .aligned: the whole warp must execute them together)
+      __syncwarp();
       // D = [T'; Z] V + [-W; Q~] S; meanwhile the state master is faded and the previous
       // chunk's output rows are stored
       if (warp == 0) {
@@ -283,6 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         issue_load(c + 1);
         issued = c + 2;
       }
+      __syncwarp();
       if (u_rows) {  // U rows -> bf16 [tok][DV] tile (MN-major B operand)
         float v[64];
         tmem_ld64(x.tm + x.lane_base + d_col(c) + x.wh * 64, v);
@@ -300,6 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       bad |= !mbar_wait(x.bar_mma, x.ph_mma, kWaitNs);
       x.ph_mma ^= 1u;
+      __syncwarp();
       fence_after_sync();
       s_epilogue<DH>(x, sm + L::SS);
       // the local slot is free for chunk c + 2 once O's MMA is complete (gamma was read before
@@ -525,12 +531,17 @@ int max_resident() {
 }  // namespace
 
 // CTAs of the work-queue launch for this shape (0: use another kernel).  It needs the ring in
-// the workspace and at least one helper CTA per two chains.
+// the workspace, at least one helper CTA per two chains, and at most two per chain: with more
+// (the 32-chain, 512-chunk KDA workload has 3.75) the helpers outpace the chains, the rings fill,
+// and on that workload most launches stopped in a bounded wait -- a helper waiting for its chain
+// to land the chunk six before its own -- whose cause was not found.  Where the helpers are
+// fewer the chains consume as fast as the helpers produce and the rings do not fill.
 int queue_grid_for(const gdr_shape& sh, const PrefillArgs& a) {
   if (!a.ring || !a.ring_flags) return 0;
   const long pairs = (long)sh.n_seqs * sh.H;
   const int g = max_resident();
   if (pairs < 1 || pairs > WorkspaceLayout::kRingMaxPairs || g < 3 * pairs / 2 + 1) return 0;
+  if (g - pairs > 2 * pairs) return 0;
   return g;
 }
 

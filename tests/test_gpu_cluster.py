@@ -5,7 +5,9 @@ helper taking chunks from a shared queue; needs the full workspace, chosen where
 give a chain one helper).  Every case runs the default dispatch, the work-queue kernel
 (GDR_FLAG_PREFER_QUEUE), the clustered kernel (minimum workspace) and the one-CTA-per-chain kernel
 (GDR_FLAG_NO_CLUSTER), and checks each against the oracle.  The pair counts below reach different
-helper counts."""
+helper counts.  The work-queue kernel runs only where it has at most two helper CTAs per chain
+(51-76 chains on 152 SMs: here the 72-chain case); elsewhere GDR_FLAG_PREFER_QUEUE falls back to
+the clustered kernel."""
 import numpy as np
 import pytest
 import torch
@@ -101,3 +103,26 @@ def test_cluster_two_calls_in_a_row():
     ref = oracle.gated_delta(b["q"], b["k"], b["v"], b["alpha"], b["beta"], S0=b["S0"],
                              cu_seqlens=b["cu_seqlens"])
     assert rel_rows(second[0], ref[0]) <= TOL["bf16"]
+
+
+def test_queue_repeated_calls():
+    """The work-queue kernel (72 chains: one helper CTA per chain or so) called back to back:
+    every call ends without a device-check failure and gives the same bits."""
+    import gated_delta_rule_prefill_gb300 as g
+    lens, H = CASES["chains_72"]
+    wl = gi.custom(seed=93, seqlens=lens, H=H, d_k=128, d_v=128, dtype="bf16", s0="normal")
+    a = gi.gen_full(wl)
+    d = dev_inputs(a, "bf16")
+    n = g.gdr_prefill_workspace_size(len(lens), H, 128, 128, "bf16")
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    first = None
+    for _ in range(6):
+        out, Sf = g.gdr_prefill(d["q"], d["k"], d["v"], d["alpha"], d["beta"], S0=d["S0"],
+                                cu_seqlens=d["cu_seqlens"], workspace=ws, prefer_queue=True)
+        assert g.gdr_workspace_status(ws) == 0
+        cur = (host(out), host(Sf))
+        if first is None:
+            first = cur
+        else:
+            np.testing.assert_array_equal(cur[0], first[0])
+            np.testing.assert_array_equal(cur[1], first[1])
