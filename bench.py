@@ -695,6 +695,52 @@ def run_gpu(args):
     return 0
 
 
+def run_profile(args):
+    """Profiler target: `--warmup` launches each of the step's three kernels on a smaller KDA
+    prefill (1 x `--profile-tokens` tokens, 32 heads, the KDA workload's distributions; the
+    linear pass on the same q/k/v) and one decode step on the decode workload's shape, then exit.
+    For ncu captures that must stay small; it prints no bench line."""
+    import torch
+
+    import gated_delta_rule_prefill_gb300 as g
+
+    torch.cuda.set_device(0)
+    wp = gi.custom(name="kda_profile", seed=1002, seqlens=[args.profile_tokens], H=32, d_k=128,
+                   d_v=128, dtype="bf16", gate="channel", s0="normal")
+    d = gi.device_full(wp, "cuda")
+    wd = gi.workload(DECODE)
+    x = gi.device_decode_steps(wd, 1, "cuda")[0]
+    S = torch.randn((wd.n_seqs, wd.H, wd.d_k, wd.d_v), dtype=torch.float32, device="cuda") * 0.1
+    n = max(1, args.warmup)
+    for _ in range(n):
+        g.gdr_prefill(d["q"], d["k"], d["v"], d["alpha"], d["beta"], S0=d["S0"],
+                      cu_seqlens=d["cu_seqlens"])
+        g.gdr_linear_attn(d["q"], d["k"], d["v"], S0=d["S0"], cu_seqlens=d["cu_seqlens"])
+        g.gdr_decode_step(x["q"], x["k"], x["v"], x["alpha"], x["beta"], S)
+    if args.profile_variants:  # then the rows timed outside the step, in the bench's order
+        gate_in = torch.randn(d["v"].shape, device="cuda").mul_(2.0).to(torch.bfloat16)
+        R = gi.device_full(wp, "cuda", seed_offset=7, raw=True)
+        M = {kk: torch.empty_like(R[kk]) for kk in ("q", "k", "alpha", "beta")}
+        Z = S.sum(dim=3).abs_().add_(1.0)
+        for _ in range(n):
+            g.gdr_gated_linear_attn(d["q"], d["k"], d["v"], d["alpha"], S0=d["S0"],
+                                    cu_seqlens=d["cu_seqlens"])
+            g.gdr_prefill_output_gate(d["q"], d["k"], d["v"], d["alpha"], d["beta"], gate_in,
+                                      S0=d["S0"], cu_seqlens=d["cu_seqlens"])
+            g.gdr_prefill(R["q"], R["k"], d["v"], R["alpha"], R["beta"], S0=d["S0"],
+                          cu_seqlens=d["cu_seqlens"], prologue=True)
+            g.gdr_layer_prologue(R["q"], R["k"], R["alpha"], R["beta"], q=M["q"], k=M["k"],
+                                 alpha=M["alpha"], beta=M["beta"])
+            g.gdr_normalized_linear_attn(d["q"], d["k"], d["v"], eps=1e-6, S0=d["S0"],
+                                         cu_seqlens=d["cu_seqlens"])
+            g.gdr_gated_linear_decode_step(x["q"], x["k"], x["v"], x["alpha"], S)
+            g.gdr_normalized_linear_decode_step(x["q"], x["k"], x["v"], S, Z, eps=1e-6)
+    torch.cuda.synchronize()
+    print("profile case done: 1 x %d tokens x 32 heads, %d launches of each kernel"
+          % (args.profile_tokens, n))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -702,7 +748,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-tokens", type=int, default=0,
+                    help="profiler target only: the step's kernels on 1 x T tokens, then exit")
+    ap.add_argument("--profile-variants", action="store_true",
+                    help="with --profile-tokens: also the rows timed outside the step")
     args = ap.parse_args()
+    if args.profile_tokens > 0:
+        return run_profile(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)
