@@ -361,6 +361,11 @@ def run_gpu(args):
     t_end.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
+    # every bounded wait in the timed launches completed (a wait that gave up records a status;
+    # its launch would have run ~2 s and its results would be invalid)
+    checks = {"workspace": g.gdr_workspace_status(ws), "device": g.gdr_query_device_status()}
+    if checks["workspace"] or checks["device"]:
+        print("bench: a device-side check failed in the timed region: %s" % checks, file=sys.stderr)
     if world > 1:
         dist.barrier()
     total_ms = t_start.elapsed_time(t_end)
@@ -686,6 +691,7 @@ def run_gpu(args):
                 "out and S_final back, copies pipelined with the kernels inside the call"},
         "gpu_launches": 6 * K,  # per step: prep + prefill, prep + linear run sums + linear runs, decode
         "clocks": clk,
+        "device_checks": checks,
     }
     if cpu:
         line["cpu_baseline"] = cpu

@@ -212,14 +212,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     x.prologue = PRO;
     uint32_t ph_v = 0, ph_full[2] = {0, 0};
     __nv_bfloat16* __restrict__ out = static_cast<__nv_bfloat16*>(a.out);
-    auto issue_v = [&](int64_t tc) {
-      if (tid == 0) {
-        mbar_expect_tx(bar_v, 16384);
-        tma_load_3d(sm + L::VIN, &maps.v, 0, h, (int)tc, bar_v);
-        tma_load_3d(sm + L::VIN + 8192, &maps.v, 64, h, (int)tc, bar_v);
-      }
+    auto issue_v = [&](int64_t tc) {  // one thread
+      mbar_expect_tx(bar_v, 16384);
+      tma_load_3d(sm + L::VIN, &maps.v, 0, h, (int)tc, bar_v);
+      tma_load_3d(sm + L::VIN + 8192, &maps.v, 64, h, (int)tc, bar_v);
     };
-    if (nch > 0) issue_v(t0);
+    if (tid == 0 && nch > 0) issue_v(t0);
     s_init<DH>(x, a.S0 ? a.S0 + sidx + (size_t)x.lrow * kD : nullptr, sm + L::SS);
     cta_sync_tc();  // every row of the bf16 state tile is written before the first MMA
     const Opnd opV{x.sb + L::VIN, 8192, true};
@@ -369,18 +367,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       bad |= !mbar_wait(x.bar_mma, x.ph_mma, kWaitNs);
       x.ph_mma ^= 1u;
       fence_after_sync();
-      if (c + 1 < nch) issue_v(tc + kC);  // V is consumed
       __syncwarp();
+      // Named barrier 1: the U warps wait at it, the O warps only arrive, each after its own
+      // waits for this chunk's V tile and first products.  So neither barrier can complete a
+      // phase again (V of the next chunk, the second products) while a thread is still polling
+      // the previous one -- a parity wait that slept through two phases would sleep on.
       if (u_rows) {
-        // U rows -> bf16 [tok][DV] tile (MN-major B operand); the four warps holding them meet
-        // at a named barrier, then K^^T U (on the chain's critical path) and O += M U are issued
+        // U rows -> bf16 [tok][DV] tile (MN-major B operand); then K^^T U (on the chain's
+        // critical path) and O += M U are issued
         float v[64];
         tmem_ld64(x.tm + x.lane_base + d_col(c) + x.wh * 64, v);
 #pragma unroll
         for (int j = 0; j < 64; j += 8) st_chunk8(sm + L::UU, 8192, drow, x.wh * 64 + j, v + j);
         fence_async_smem();
         fence_before_sync();
-        asm volatile("bar.sync 1, 128;" ::: "memory");
+        asm volatile("bar.sync 1, 256;" ::: "memory");
         fence_after_sync();
         if (warp == 0) {
           mma_run<kC>(x.tm + kColU, opKH, opU, id_s, false);
@@ -388,11 +389,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_run<kC>(x.tm + d_col(c), opZM, opU, id_d, true);
           mma_commit_elect(bar_o);
         }
-      } else if (c > 0) {
-        if constexpr (OGATE) {
-          stage_o(c - 1);
-        } else {
-          o_store(c - 1, tc - kC, kC);  // the previous chunk's output rows, off the tensor pipe
+        if (tid == 32 && c + 1 < nch) issue_v(tc + kC);  // V is consumed, on every thread
+      } else {
+        asm volatile("bar.arrive 1, 256;" ::: "memory");
+        if (c > 0) {
+          if constexpr (OGATE) {
+            stage_o(c - 1);
+          } else {
+            o_store(c - 1, tc - kC, kC);  // the previous chunk's output rows, off the tensor pipe
+          }
         }
       }
       bad |= !mbar_wait(x.bar_mma, x.ph_mma, kWaitNs);

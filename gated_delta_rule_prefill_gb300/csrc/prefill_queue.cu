@@ -187,14 +187,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t ph_v = 0, ph_full[2] = {0, 0}, ph_o = 0;
     bool failed = false;
     __nv_bfloat16* __restrict__ out = static_cast<__nv_bfloat16*>(a.out);
-    auto issue_v = [&](int64_t tc) {
-      if (tid == 0) {
-        mbar_expect_tx(bar_v, 16384);
-        tma_load_3d(sm + L::VIN, &maps.v, 0, h, (int)tc, bar_v);
-        tma_load_3d(sm + L::VIN + 8192, &maps.v, 64, h, (int)tc, bar_v);
-      }
+    auto issue_v = [&](int64_t tc) {  // one thread
+      mbar_expect_tx(bar_v, 16384);
+      tma_load_3d(sm + L::VIN, &maps.v, 0, h, (int)tc, bar_v);
+      tma_load_3d(sm + L::VIN + 8192, &maps.v, 64, h, (int)tc, bar_v);
     };
-    if (nch > 0) issue_v(t0);
+    if (tid == 0 && nch > 0) issue_v(t0);
     s_init<DH>(x, a.S0 ? a.S0 + sidx + (size_t)x.lrow * kD : nullptr, sm + L::SS);
     cta_sync_tc();  // every row of the bf16 state tile is written before the first MMA
     const Opnd opV{x.sb + L::VIN, 8192, true};
@@ -281,7 +279,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       bad |= !mbar_wait(x.bar_mma, x.ph_mma, kWaitNs);
       x.ph_mma ^= 1u;
       fence_after_sync();
-      if (c + 1 < nch) issue_v(tc + kC);  // V is consumed
       if (loader && issued == c + 1 && c + 1 < nch &&  // a second look (warp 2 is idle here)
           ld_acquire_gpu(q_ready + p * kR + ((c + 1) % kR)) >= (uint32_t)(c + 2)) {
         issue_load(c + 1);
@@ -303,6 +300,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_run<kC>(x.tm + d_col(c), opZM, opU, id_d, true);
         mma_commit_elect(bar_o);
       }
+      // V is consumed, and every thread has passed its wait for this chunk's tile: requested
+      // only now, the next tile cannot complete the V barrier's next phase while a thread still
+      // polls this one (a parity wait that slept through two phases would sleep on)
+      if (tid == 32 && c + 1 < nch) issue_v(tc + kC);
       bad |= !mbar_wait(x.bar_mma, x.ph_mma, kWaitNs);
       x.ph_mma ^= 1u;
       __syncwarp();

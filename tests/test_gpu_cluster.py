@@ -126,3 +126,33 @@ def test_queue_repeated_calls():
         else:
             np.testing.assert_array_equal(cur[0], first[0])
             np.testing.assert_array_equal(cur[1], first[1])
+
+
+def test_cluster_back_to_back_launches():
+    """Hundreds of clustered launches back to back on one stream (32 chains of 64 chunks, the
+    plain, output-gated and gated-linear chains in turn): no bounded wait gives up -- a chain
+    thread that slept through two phases of a barrier would -- and every repeat gives the same
+    bits."""
+    import gated_delta_rule_prefill_gb300 as g
+    wl = gi.custom(seed=94, seqlens=[4096], H=32, d_k=128, d_v=128, dtype="bf16", s0="normal")
+    d = gi.device_full(wl, "cuda")
+    gate_in = torch.randn_like(d["v"])
+    ws = torch.empty(g.gdr_prefill_workspace_size(1, 32, 128, 128, "bf16"), dtype=torch.uint8,
+                     device="cuda")
+    g.gdr_query_device_status()
+    outs = [torch.empty_like(d["v"]) for _ in range(3)]
+    firsts = []
+    for rep in range(100):
+        o = [g.gdr_prefill(d["q"], d["k"], d["v"], d["alpha"], d["beta"], S0=d["S0"],
+                           cu_seqlens=d["cu_seqlens"], out=outs[0], workspace=ws)[0],
+             g.gdr_prefill_output_gate(d["q"], d["k"], d["v"], d["alpha"], d["beta"], gate_in,
+                                       S0=d["S0"], cu_seqlens=d["cu_seqlens"], out=outs[1],
+                                       workspace=ws)[0],
+             g.gdr_gated_linear_attn(d["q"], d["k"], d["v"], d["alpha"], S0=d["S0"],
+                                     cu_seqlens=d["cu_seqlens"], out=outs[2], workspace=ws)[0]]
+        if rep == 0 or rep == 99:
+            firsts.append([x.clone() for x in o])
+    assert g.gdr_workspace_status(ws) == 0
+    assert g.gdr_query_device_status() == g._abi.GDR_OK
+    for x, y in zip(firsts[0], firsts[1]):
+        assert torch.equal(x, y)
