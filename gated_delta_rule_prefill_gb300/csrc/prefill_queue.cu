@@ -532,17 +532,12 @@ int max_resident() {
 }  // namespace
 
 // CTAs of the work-queue launch for this shape (0: use another kernel).  It needs the ring in
-// the workspace, at least one helper CTA per two chains, and at most two per chain: with more
-// (the 32-chain, 512-chunk KDA workload has 3.75) the helpers outpace the chains, the rings fill,
-// and on that workload most launches stopped in a bounded wait -- a helper waiting for its chain
-// to land the chunk six before its own -- whose cause was not found.  Where the helpers are
-// fewer the chains consume as fast as the helpers produce and the rings do not fill.
+// the workspace and at least one helper CTA per two chains.
 int queue_grid_for(const gdr_shape& sh, const PrefillArgs& a) {
   if (!a.ring || !a.ring_flags) return 0;
   const long pairs = (long)sh.n_seqs * sh.H;
   const int g = max_resident();
   if (pairs < 1 || pairs > WorkspaceLayout::kRingMaxPairs || g < 3 * pairs / 2 + 1) return 0;
-  if (g - pairs > 2 * pairs) return 0;
   return g;
 }
 

@@ -90,8 +90,8 @@ typedef struct {
 /* On the tensor-core path, run the one-CTA-per-chain kernel even where a kernel with helper CTAs
  * that prepare each chain's chunks (work queue or clusters) would be chosen (for cross-checks). */
 #define GDR_FLAG_NO_CLUSTER 2
-/* Run the work-queue kernel wherever the workspace holds its operand rings and it has at most
- * two helper CTAs per chain, also where the clustered kernel would be chosen (for cross-checks). */
+/* Run the work-queue kernel wherever the workspace holds its operand rings, also where the
+ * clustered kernel would be chosen (for cross-checks). */
 #define GDR_FLAG_PREFER_QUEUE 4
 /* The layer prologue on load (heqinghuang "gpt2-to-kimi" §09: unit-length silu queries and keys,
  * beta a sigmoid of its projection; engineermaxxing "From GPT-2 to Kimi K3" §05c and §06b: the

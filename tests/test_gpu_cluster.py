@@ -5,9 +5,7 @@ helper taking chunks from a shared queue; needs the full workspace, chosen where
 give a chain one helper).  Every case runs the default dispatch, the work-queue kernel
 (GDR_FLAG_PREFER_QUEUE), the clustered kernel (minimum workspace) and the one-CTA-per-chain kernel
 (GDR_FLAG_NO_CLUSTER), and checks each against the oracle.  The pair counts below reach different
-helper counts.  The work-queue kernel runs only where it has at most two helper CTAs per chain
-(51-76 chains on 152 SMs: here the 72-chain case); elsewhere GDR_FLAG_PREFER_QUEUE falls back to
-the clustered kernel."""
+helper counts."""
 import numpy as np
 import pytest
 import torch
@@ -129,10 +127,10 @@ def test_queue_repeated_calls():
 
 
 def test_cluster_back_to_back_launches():
-    """Hundreds of clustered launches back to back on one stream (32 chains of 64 chunks, the
-    plain, output-gated and gated-linear chains in turn): no bounded wait gives up -- a chain
-    thread that slept through two phases of a barrier would -- and every repeat gives the same
-    bits."""
+    """Hundreds of launches with helper CTAs back to back on one stream (32 chains of 64
+    chunks: the plain, output-gated and gated-linear clustered chains and the work-queue kernel
+    with 3.75 helpers per chain, in turn): no bounded wait gives up -- a chain thread that slept
+    through two phases of a barrier would -- and every repeat gives the same bits."""
     import gated_delta_rule_prefill_gb300 as g
     wl = gi.custom(seed=94, seqlens=[4096], H=32, d_k=128, d_v=128, dtype="bf16", s0="normal")
     d = gi.device_full(wl, "cuda")
@@ -140,7 +138,7 @@ def test_cluster_back_to_back_launches():
     ws = torch.empty(g.gdr_prefill_workspace_size(1, 32, 128, 128, "bf16"), dtype=torch.uint8,
                      device="cuda")
     g.gdr_query_device_status()
-    outs = [torch.empty_like(d["v"]) for _ in range(3)]
+    outs = [torch.empty_like(d["v"]) for _ in range(4)]
     firsts = []
     for rep in range(100):
         o = [g.gdr_prefill(d["q"], d["k"], d["v"], d["alpha"], d["beta"], S0=d["S0"],
@@ -149,7 +147,10 @@ def test_cluster_back_to_back_launches():
                                        S0=d["S0"], cu_seqlens=d["cu_seqlens"], out=outs[1],
                                        workspace=ws)[0],
              g.gdr_gated_linear_attn(d["q"], d["k"], d["v"], d["alpha"], S0=d["S0"],
-                                     cu_seqlens=d["cu_seqlens"], out=outs[2], workspace=ws)[0]]
+                                     cu_seqlens=d["cu_seqlens"], out=outs[2], workspace=ws)[0],
+             g.gdr_prefill(d["q"], d["k"], d["v"], d["alpha"], d["beta"], S0=d["S0"],
+                           cu_seqlens=d["cu_seqlens"], out=outs[3], workspace=ws,
+                           prefer_queue=True)[0]]
         if rep == 0 or rep == 99:
             firsts.append([x.clone() for x in o])
     assert g.gdr_workspace_status(ws) == 0
