@@ -581,9 +581,6 @@ __device__ bool gate_stage(const TcCtx& x, int n, Hook before_writes = Hook()) {
       // Per-channel gates: running products of the gates down the
       // thread's rows, then the carry of the earlier row blocks through shared memory.
       float p[4][8];  // prefix products Gam[4 rb + rr][8 g8 + cc]
-      float ga[4][8];  // the thread's gates (1 past the chunk's end), kept for the suffixes
-      uint4 kraw[4], qraw[4];  // the thread's k and q chunks, loaded with the gates: their
-                               // latency hides behind the carry scan
       float gn[8];    // Gam_n (= gamma) of the 8 channels
       float sufc[8];  // product of the gates of the later row blocks, per channel
       {
@@ -593,20 +590,18 @@ __device__ bool gate_stage(const TcCtx& x, int n, Hook before_writes = Hook()) {
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr) {
           const int r = 4 * rb + rr;
+          float a8[8];
 #pragma unroll
-          for (int cc = 0; cc < 8; ++cc) ga[rr][cc] = 1.f;
-          kraw[rr] = qraw[rr] = make_uint4(0u, 0u, 0u, 0u);
+          for (int cc = 0; cc < 8; ++cc) a8[cc] = 1.f;
           if (r < n) {
             const float4 u0 = *reinterpret_cast<const float4*>(sAin + r * kD + 8 * g8);
             const float4 u1 = *reinterpret_cast<const float4*>(sAin + r * kD + 8 * g8 + 4);
-            ga[rr][0] = u0.x, ga[rr][1] = u0.y, ga[rr][2] = u0.z, ga[rr][3] = u0.w;
-            ga[rr][4] = u1.x, ga[rr][5] = u1.y, ga[rr][6] = u1.z, ga[rr][7] = u1.w;
-            kraw[rr] = *reinterpret_cast<const uint4*>(sKin + r * kD + 8 * g8);
-            qraw[rr] = *reinterpret_cast<const uint4*>(sQin + r * kD + 8 * g8);
+            a8[0] = u0.x, a8[1] = u0.y, a8[2] = u0.z, a8[3] = u0.w;
+            a8[4] = u1.x, a8[5] = u1.y, a8[6] = u1.z, a8[7] = u1.w;
           }
 #pragma unroll
           for (int cc = 0; cc < 8; ++cc) {
-            run[cc] *= ga[rr][cc];
+            run[cc] *= a8[cc];
             p[rr][cc] = run[cc];
           }
         }
@@ -675,15 +670,12 @@ __device__ bool gate_stage(const TcCtx& x, int n, Hook before_writes = Hook()) {
         for (int rr = 3; rr >= 0; --rr) {
           const int r = 4 * rb + rr;
           float k8[8], q8[8];
-          {
-            const __nv_bfloat162* hk = reinterpret_cast<const __nv_bfloat162*>(&kraw[rr]);
-            const __nv_bfloat162* hq = reinterpret_cast<const __nv_bfloat162*>(&qraw[rr]);
+          if (r < n) {
+            ld_bf16x8(sKin + r * kD + 8 * g8, k8);
+            ld_bf16x8(sQin + r * kD + 8 * g8, q8);
+          } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float2 fk = __bfloat1622float2(hk[i]), fq = __bfloat1622float2(hq[i]);
-              k8[2 * i] = fk.x, k8[2 * i + 1] = fk.y;
-              q8[2 * i] = fq.x, q8[2 * i + 1] = fq.y;
-            }
+            for (int cc = 0; cc < 8; ++cc) k8[cc] = q8[cc] = 0.f;
           }
           float ke[8], qe[8], ki[8], kh[8], dq = 0.f;
 #pragma unroll
@@ -695,9 +687,11 @@ __device__ bool gate_stage(const TcCtx& x, int n, Hook before_writes = Hook()) {
             ki[cc] = kh[cc] * rgn[cc];
             dq = fmaf(q8[cc], k8[cc], dq);
           }
-          if (rr > 0) {  // the suffix of row r - 1 gains this row's gates (1 past the end)
-#pragma unroll
-            for (int cc = 0; cc < 8; ++cc) suf[cc] *= ga[rr][cc];
+          if (rr > 0 && r < n) {  // the suffix of row r - 1 gains this row's gates
+            const float4 u0 = *reinterpret_cast<const float4*>(sAin + r * kD + 8 * g8);
+            const float4 u1 = *reinterpret_cast<const float4*>(sAin + r * kD + 8 * g8 + 4);
+            suf[0] *= u0.x, suf[1] *= u0.y, suf[2] *= u0.z, suf[3] *= u0.w;
+            suf[4] *= u1.x, suf[5] *= u1.y, suf[6] *= u1.z, suf[7] *= u1.w;
           }
           sDiagP[r * 16 + g8] = dq;  // M's diagonal carries no decay: q_r . k_r
           st_chunk8(sm + L::KQ, 16384, r, 8 * g8, ke);       // K~
