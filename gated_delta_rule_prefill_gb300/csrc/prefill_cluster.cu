@@ -367,6 +367,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bad |= !mbar_wait(x.bar_mma, x.ph_mma, kWaitNs);
       x.ph_mma ^= 1u;
       fence_after_sync();
+      // (with the output gate every thread has passed its V wait at the barrier above)
+      if (OGATE && tid == 0 && c + 1 < nch) issue_v(tc + kC);  // V is consumed
       __syncwarp();
       // Named barrier 1: the U warps wait at it, the O warps only arrive, each after its own
       // waits for this chunk's V tile and first products.  So neither barrier can complete a
@@ -389,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_run<kC>(x.tm + d_col(c), opZM, opU, id_d, true);
           mma_commit_elect(bar_o);
         }
-        if (tid == 32 && c + 1 < nch) issue_v(tc + kC);  // V is consumed, on every thread
+        if (!OGATE && tid == 32 && c + 1 < nch) issue_v(tc + kC);  // V is consumed, on every thread
       } else {
         asm volatile("bar.arrive 1, 256;" ::: "memory");
         if (c > 0) {
