@@ -43,6 +43,22 @@ struct ChainSmem {
 };
 static_assert(ChainSmem::BARS + 64 <= 2 * kSlotBytes, "barriers inside the second slot's tail");
 
+// The chain CTA of the transposed state pass (no output gate): three operand slots without the
+// zero tile (M where Z was), their gammas apart, and two V buffers.
+struct ChainSmemT {
+  static constexpr uint32_t kSlots = 3;
+  static constexpr uint32_t SLOT_BYTES = 65536;    // -W / Q~ [WQ], K^ [KH], T' [T], M [Z]
+  static constexpr uint32_t VIN = kSlots * SLOT_BYTES;  // V [64 tok][128] SW128 x 2 buffers
+  static constexpr uint32_t GAM = VIN + 2 * 16384;  // gamma [128] fp32 per slot
+  static constexpr uint32_t BARS = GAM + kSlots * 512;  // full[3], v[2], mma, o, TMEM slot
+  static constexpr uint32_t END = BARS + 64;
+  static constexpr uint32_t kM = kSlotZ;  // M's offset in a slot
+};
+static_assert(ChainSmemT::END <= ChainSmem::END, "the transposed chain fits the cluster's CTAs");
+static_assert(kSlotWQ + 32768 <= kSlotKH && kSlotKH + 16384 <= kSlotT &&
+                  kSlotT + 8192 <= ChainSmemT::kM && ChainSmemT::kM + 8192 <= ChainSmemT::SLOT_BYTES,
+              "slot tiles of the transposed chain");
+
 struct HelperSmem {
   static constexpr uint32_t QIN = 0;              // [64][128] bf16 row-major
   static constexpr uint32_t KIN = QIN + 16384;
@@ -141,9 +157,199 @@ __device__ bool wait_consumed(const uint32_t* cons, uint32_t need) {
   return !__syncthreads_or(!ok);
 }
 
-// ERASE = false: gated linear attention.  The helpers skip the triangular solve and W; the chain
-// CTA's slots hold T' = I and W = 0 from the start, so its U is V itself and its code is
-// unchanged, and a chunk's hand-over shrinks from 66 KB to 41 KB.
+// The chain CTA of gated linear attention, with its state pass transposed.  The state is kept as
+// S^T -- TMEM lane v = value column v, column k = key channel k -- so that S enters the products
+// as an A operand read from tensor memory (a bf16 copy in TMEM: row m of A in lane m, two K
+// values per 32-bit column, the lower K index in the low half), and nothing of the state pass
+// goes through shared memory; the helpers' slot tiles (and V) serve as B operands.  U = V here
+// (no erase term), so per chunk, with D^T and X two accumulators of 128 columns:
+//   D^T[:, 64..127] = S^T Q~^T,  X = V^T K^,  D^T[:, 64..127] += V^T M^T   (O^T)
+//   S^T <- S^T Diag(gamma) + X, folded into the master while its bf16 copy is made.
+// X goes to the accumulator that held the previous chunk's D^T, whose O^T columns warps 4-7
+// store (one bf16 value per lane and token: 64 contiguous bytes per warp store) at the top of
+// the chunk.  The freed shared memory holds three operand slots, so a slot is refilled while the
+// two after it are consumed, and V is double-buffered, requested a chunk ahead.  (The same
+// arrangement for the gated rule -- U^T = V^T T'^T + S^T (-W)^T into D^T[:, 0..63] first, its
+// bf16 copy in TMEM as the A operand of X and O^T -- was parity-green but slower than the
+// untransposed chain: 1.12 against 1.08 ms on 32 heads x 32K tokens.)
+__device__ void chain_transposed(unsigned char* sm, const TcMaps& maps, const PrefillArgs& a,
+                                 int h, int64_t t0, int64_t t1, int nch, size_t sidx,
+                                 bool valid, int ncl) {
+  using L = ChainSmemT;
+  constexpr uint32_t kPayload = kSlotPayload - 16384 - 8192;  // no -W, no T'
+  // TMEM columns: S^T master (fp32), its bf16 copy, D^T (two)
+  constexpr uint32_t cMS = 0, cSB = 128, cD0 = 192, cD1 = 320;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int q4 = warp & 3, wh = warp >> 2;
+  const int vv = q4 * 32 + lane;  // the value column held in this thread's TMEM lane
+  const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+  const int H = a.H;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);
+  uint64_t* full = bars;       // [3]
+  uint64_t* bar_v = bars + 3;  // [2]
+  uint64_t* bar_mma = bars + 5;
+  uint64_t* bar_o = bars + 6;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 7);
+  if (warp == 0) tmem_alloc(tslot, kTmemCols);
+  if (tid == 0) {
+    for (int i = 0; i < 7; ++i) mbar_init(bars + i, 1);
+    fence_mbar_init();
+    prefetch_tmap(&maps.v);
+    for (int s = 0; s < (int)L::kSlots && s < nch; ++s) mbar_expect_tx(full + s, kPayload);
+  }
+  cta_sync_tc();
+  cluster_sync();  // every CTA's barriers and counters are initialised
+  const uint32_t tm = *tslot;
+  auto dcol = [](int c) { return (c & 1) ? cD1 : cD0; };
+  auto pack2 = [](float x, float y) {
+    const __nv_bfloat162 hv = __floats2bfloat162_rn(x, y);
+    return *reinterpret_cast<const uint32_t*>(&hv);
+  };
+  __nv_bfloat16* __restrict__ out = static_cast<__nv_bfloat16*>(a.out);
+  // phases: bit s of ph_full for slot s, bit b of ph_v for V buffer b
+  uint32_t ph_full = 0, ph_v = 0, ph_mma = 0, ph_o = 0;
+  auto issue_v = [&](int c) {  // one thread: chunk c's V tile into buffer c & 1
+    unsigned char* dst = sm + L::VIN + (c & 1) * 16384;
+    const int tc = (int)(t0 + (int64_t)c * kC);
+    mbar_expect_tx(bar_v + (c & 1), 16384);
+    tma_load_3d(dst, &maps.v, 0, h, tc, bar_v + (c & 1));
+    tma_load_3d(dst + 8192, &maps.v, 64, h, tc, bar_v + (c & 1));
+  };
+  if (tid == 0 && nch > 0) issue_v(0);
+  {  // S0^T (or zeros): lane v holds column v of S0; this thread's key channels 64 wh + [0, 64)
+    float sv[64];
+    const float* s0 = a.S0 ? a.S0 + sidx : nullptr;
+#pragma unroll
+    for (int j = 0; j < 64; ++j) sv[j] = s0 ? s0[(size_t)(64 * wh + j) * kD + vv] : 0.f;
+    tmem_st32(tm + lane_base + cMS + 64 * wh, *reinterpret_cast<const float(*)[32]>(sv));
+    tmem_st32(tm + lane_base + cMS + 64 * wh + 32, *reinterpret_cast<const float(*)[32]>(sv + 32));
+    float pv[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) pv[i] = __uint_as_float(pack2(sv[2 * i], sv[2 * i + 1]));
+    tmem_st32(tm + lane_base + cSB + 32 * wh, pv);
+    tmem_wait_st();
+  }
+  cta_sync_tc();
+  const uint32_t id_t64 = idesc_bf16(128, 64, false, false, false);  // TMEM A, K-major B, N = 64
+  const uint32_t id_vk = idesc_bf16(128, 128, false, true, true);    // V^T (smem) K^
+  const uint32_t id_vm = idesc_bf16(128, 64, false, true, false);    // V^T (smem) M^T
+  const uint32_t cons_local = smem_u32(sm + HelperSmem::CONS);
+  bool failed = false;
+  int c_fail = 0;
+  // warps 4-7: O^T of chunk c (columns 64-127 of its D^T) -> out rows [tc, tc + n) of head h
+  auto o_drain = [&](int c, int64_t tc, int n) {
+    float o[64];
+    tmem_ld64(tm + lane_base + dcol(c) + 64, o);
+    __nv_bfloat16* dst = out + ((size_t)tc * H + h) * kD + vv;
+#pragma unroll
+    for (int j = 0; j < 64; ++j)
+      if (j < n) dst[(size_t)j * H * kD] = __float2bfloat16_rn(o[j]);
+  };
+#pragma unroll 1
+  for (int c = 0; c < nch && !failed; ++c) {
+    const int s = c % (int)L::kSlots, vb = c & 1;
+    const int64_t tc = t0 + (int64_t)c * kC;
+    const int n = (int)((t1 - tc) < (int64_t)kC ? (t1 - tc) : (int64_t)kC);
+    const uint32_t slot = smem_u32(sm) + (uint32_t)s * L::SLOT_BYTES;
+    const Opnd opQ{slot + kSlotWQ + 8192, 16384, false};  // Q~ rows: K-major B, N = 64
+    const Opnd opKH{slot + kSlotKH, 8192, true};          // K^ [tok][ch]: MN-major B, N = 128
+    const Opnd opM{slot + L::kM, 8192, false};            // M rows: K-major B, N = 64
+    const Opnd opVa{smem_u32(sm + L::VIN) + (uint32_t)vb * 16384, 8192, true};  // V^T: A
+    const float* gam = reinterpret_cast<const float*>(sm + L::GAM + s * 512);
+    // the next V tile: its buffer's last readers, chunk c - 1's products, completed before that
+    // chunk's closing barrier, which every thread passed after its wait for the buffer
+    if (tid == 128 && c + 1 < nch) issue_v(c + 1);
+    if (c > 0 && wh == 1) o_drain(c - 1, tc - kC, kC);
+    // Waits are per thread; one that gave up is agreed on at the chunk's closing barrier.
+    bool bad = false;
+    bad |= !mbar_wait(full + s, (ph_full >> s) & 1u, kWaitNs);
+    bad |= !mbar_wait(bar_v + vb, (ph_v >> vb) & 1u, kWaitNs);
+    ph_full ^= 1u << s;
+    ph_v ^= 1u << vb;
+    __syncwarp();  // lanes leave their polling loops at different times
+    if (n < kC) {  // the last chunk: every thread zeroes part of the V tail
+      zero_v_tail<kD>(make_ctx(sm, tm, bar_mma), sm + L::VIN + vb * 16384, n);
+      __syncthreads();
+    }
+    fence_after_sync();
+    if (warp == 0) {  // S^T Q~^T
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        mma_bf16_tmem_a_elect(tm + dcol(c) + 64, tm + cSB + 8 * ks, opQ.at(16 * ks), id_t64,
+                              ks > 0 ? 1u : 0u);
+    }
+    fence_before_sync();
+    __syncthreads();  // the previous chunk's O^T has left
+    fence_after_sync();
+    if (warp == 0) {  // X = V^T K^, then O^T += V^T M^T
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16_elect(tm + dcol(c + 1), opVa.at(16 * ks), opKH.at(16 * ks), id_vk,
+                       ks > 0 ? 1u : 0u);
+      mma_commit_elect(bar_mma);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16_elect(tm + dcol(c) + 64, opVa.at(16 * ks), opM.at(16 * ks), id_vm, 1u);
+      mma_commit_elect(bar_o);
+    }
+    bad |= !mbar_wait(bar_mma, ph_mma, kWaitNs);
+    ph_mma ^= 1u;
+    __syncwarp();
+    fence_after_sync();
+    {  // S^T <- S^T Diag(gamma) + X on this thread's 64 key channels, and its bf16 copy
+      const uint32_t k0 = (uint32_t)(64 * wh);
+      float sv[128];
+      tmem_ld64x2(tm + lane_base + cMS + k0, tm + lane_base + dcol(c + 1) + k0, sv);
+#pragma unroll
+      for (int j = 0; j < 64; j += 4) {
+        const float4 g4 = *reinterpret_cast<const float4*>(gam + k0 + j);
+        sv[j] = fmaf(g4.x, sv[j], sv[64 + j]);
+        sv[j + 1] = fmaf(g4.y, sv[j + 1], sv[65 + j]);
+        sv[j + 2] = fmaf(g4.z, sv[j + 2], sv[66 + j]);
+        sv[j + 3] = fmaf(g4.w, sv[j + 3], sv[67 + j]);
+      }
+      tmem_st32(tm + lane_base + cMS + k0, *reinterpret_cast<const float(*)[32]>(sv));
+      tmem_st32(tm + lane_base + cMS + k0 + 32, *reinterpret_cast<const float(*)[32]>(sv + 32));
+      float pv[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) pv[i] = __uint_as_float(pack2(sv[2 * i], sv[2 * i + 1]));
+      tmem_st32(tm + lane_base + cSB + 32 * wh, pv);
+    }
+    tmem_wait_st();
+    // the slot is consumed once O's products are complete (gamma was read above, before the
+    // barrier below): re-arm it for chunk c + 3 and tell the helpers, one warp per helper
+    if (tid == 0) bad |= !mbar_wait(bar_o, ph_o, kWaitNs);
+    __syncwarp();
+    ph_o ^= 1u;
+    fence_before_sync();
+    if (__syncthreads_or(bad)) { failed = true; c_fail = c; break; }
+    fence_after_sync();
+    if (tid == 0 && c + (int)L::kSlots < nch) mbar_expect_tx(full + s, kPayload);
+    if (lane == 0 && warp >= 1 && warp < ncl)
+      st_relaxed_remote(map_to(cons_local, (uint32_t)warp), (uint32_t)(c + 1));
+  }
+  if (!failed && nch > 0 && wh == 1) {  // the last chunk's O rows
+    const int64_t tl = t0 + (int64_t)(nch - 1) * kC;
+    o_drain(nch - 1, tl, (int)(t1 - tl));
+  }
+  if (failed) {
+    if (tid == 0) report(a, GDR_DEVCHECK_TIMEOUT);
+    // the next chunk's V tile, requested at the top of the failed chunk, lands before the CTA
+    // exits
+    if (c_fail + 1 < nch)
+      mbar_wait(bar_v + ((c_fail + 1) & 1), (ph_v >> ((c_fail + 1) & 1)) & 1u, kWaitNs);
+  } else if (valid && a.S_final) {
+    float sv[64];
+    tmem_ld64(tm + lane_base + cMS + 64 * wh, sv);
+#pragma unroll
+    for (int j = 0; j < 64; ++j) a.S_final[sidx + (size_t)(64 * wh + j) * kD + vv] = sv[j];
+  }
+  cta_sync_tc();
+  if (warp == 0) tmem_dealloc(tm, kTmemCols);
+}
+
+// ERASE = false: gated linear attention.  The helpers skip the triangular solve and W (a chunk's
+// hand-over shrinks from 66 KB to 41 KB), and the chain CTA runs chain_transposed.
 // OGATE: the output gate out = o * sigmoid(g) on the stored output rows (a.og).
 // PRO: the layer prologue on load (a.prologue): the helpers map the staged raw q, k, alpha tiles
 // and the scalar gates before the gate stage.
@@ -173,8 +379,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // bytes a helper copies into a slot per chunk (gated linear attention: T' = I and W = 0 stay
   // in the slots from the start instead)
   constexpr uint32_t kPayload = ERASE ? kSlotPayload : kSlotPayload - 16384 - 8192;
-  if (crank == 0) {
+  if (crank == 0 && !ERASE) {
+    chain_transposed(sm, maps, a, h, t0, t1, nch, sidx, valid, ncl);
+  } else if (crank == 0) {
     // ===================================================================== chain CTA
+    // (the gated rule: S itself in TMEM, S and U as B operands in shared memory)
     using L = ChainSmem;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);
     uint64_t* full = bars;  // [2]
@@ -185,19 +394,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = tid; i < 2 * 8192 / 16; i += kThreads) {  // the Z tiles of both slots
       *reinterpret_cast<uint4*>(sm + L::SLOT + (i >> 9) * kSlotBytes + kSlotZ + (i & 511) * 16) =
           make_uint4(0, 0, 0, 0);
-    }
-    if (!ERASE) {  // T' = I and -W = 0 in both slots, for every chunk
-      for (int i = tid; i < 2 * 3 * 8192 / 16; i += kThreads) {
-        const int sl = i / (3 * 512), part = (i / 512) % 3, e = i % 512;
-        const uint32_t off = part == 0 ? kSlotWQ : (part == 1 ? kSlotWQ + 16384 : kSlotT);
-        *reinterpret_cast<uint4*>(sm + L::SLOT + sl * kSlotBytes + off + e * 16) =
-            make_uint4(0, 0, 0, 0);
-      }
-      __syncthreads();
-      if (tid < 2 * kC) {
-        const int sl = tid / kC, r = tid % kC;
-        st_bf16(sm + L::SLOT + sl * kSlotBytes + kSlotT, sw128_offset(r, r, 8192), 1.f);
-      }
     }
     fence_async_smem();
     if (tid == 0) {
@@ -468,7 +664,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     x.prologue = PRO;
     zero_upper_tp(sm + L::TT, tid);
     uint32_t ph_qk = 0, ph_a = 0;
-    const uint32_t chain_full = map_to(smem_u32(sm + ChainSmem::BARS), 0);
+    // the chain CTA's layout: three slots (gated linear attention's transposed state pass) or
+    // two (the gated rule)
+    constexpr bool kT = !ERASE;
+    constexpr int kNSlot = kT ? (int)ChainSmemT::kSlots : 2;
+    constexpr uint32_t kSlotStride = kT ? ChainSmemT::SLOT_BYTES : kSlotBytes;
+    const uint32_t chain_full = map_to(smem_u32(sm + (kT ? ChainSmemT::BARS : ChainSmem::BARS)), 0);
     const uint32_t chain_slots = map_to(smem_u32(sm + ChainSmem::SLOT), 0);
     auto issue_qk = [&](int64_t tc) {
       if (tid == 0) {
@@ -546,23 +747,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_async_smem();
       cta_sync_tc();
-      // hand the operands over: slot c & 1 is free once chunk c - 2 has been consumed
-      if (c >= 2 && !wait_consumed(cons, (uint32_t)(c - 1))) { failed = true; break; }
+      // hand the operands over: slot c mod kNSlot is free once chunk c - kNSlot has been consumed
+      if (c >= kNSlot && !wait_consumed(cons, (uint32_t)(c - kNSlot + 1))) { failed = true; break; }
       if (tid == 0) {
-        const uint32_t dst = chain_slots + (uint32_t)(c & 1) * kSlotBytes;
-        const uint32_t mbar = chain_full + (uint32_t)(c & 1) * 8u;
+        const int sl = c % kNSlot;
+        const uint32_t dst = chain_slots + (uint32_t)sl * kSlotStride;
+        const uint32_t mbar = chain_full + (uint32_t)sl * 8u;
+        const uint32_t gam = kT ? chain_slots + ChainSmemT::GAM + (uint32_t)sl * 512u : dst + kSlotGam;
         const uint32_t src = x.sb;
         bulk_copy_to(dst + kSlotWQ + 8192, src + L::KQ + 8192, 8192, mbar);    // Q~, channels 0-63
         bulk_copy_to(dst + kSlotWQ + 24576, src + L::KQ + 24576, 8192, mbar);  // Q~, 64-127
         bulk_copy_to(dst + kSlotKH, src + L::KH, 16384, mbar);
-        bulk_copy_to(dst + kSlotGam, src + L::GAM, 512, mbar);
+        bulk_copy_to(gam, src + L::GAM, 512, mbar);
         bulk_commit();
         if (ERASE) {
           bulk_copy_to(dst + kSlotWQ, src + L::WW, 8192, mbar);           // -W, channels 0-63
           bulk_copy_to(dst + kSlotWQ + 16384, src + L::WW + 8192, 8192, mbar);  // -W, 64-127
           bulk_copy_to(dst + kSlotT, src + L::TT, 8192, mbar);
         }
-        bulk_copy_to(dst + kSlotM, src + L::MM, 8192, mbar);
+        bulk_copy_to(dst + (kT ? ChainSmemT::kM : kSlotM), src + L::MM, 8192, mbar);
         bulk_commit();
       }
     }
