@@ -50,8 +50,8 @@ struct ChainSmemT {
   static constexpr uint32_t SLOT_BYTES = 65536;    // -W / Q~ [WQ], K^ [KH], T' [T], M [Z]
   static constexpr uint32_t VIN = kSlots * SLOT_BYTES;  // V [64 tok][128] SW128 x 2 buffers
   static constexpr uint32_t GAM = VIN + 2 * 16384;  // gamma [128] fp32 per slot
-  static constexpr uint32_t BARS = GAM + kSlots * 512;  // full[3], v[2], mma, o, TMEM slot
-  static constexpr uint32_t END = BARS + 64;
+  static constexpr uint32_t BARS = GAM + kSlots * 512;  // full[3], v[2], x, o; TMEM slot
+  static constexpr uint32_t END = BARS + 128;
   static constexpr uint32_t kM = kSlotZ;  // M's offset in a slot
 };
 static_assert(ChainSmemT::END <= ChainSmem::END, "the transposed chain fits the cluster's CTAs");
@@ -158,27 +158,29 @@ __device__ bool wait_consumed(const uint32_t* cons, uint32_t need) {
 }
 
 // The chain CTA of gated linear attention, with its state pass transposed.  The state is kept as
-// S^T -- TMEM lane v = value column v, column k = key channel k -- so that S enters the products
-// as an A operand read from tensor memory (a bf16 copy in TMEM: row m of A in lane m, two K
-// values per 32-bit column, the lower K index in the low half), and nothing of the state pass
-// goes through shared memory; the helpers' slot tiles (and V) serve as B operands.  U = V here
-// (no erase term), so per chunk, with D^T and X two accumulators of 128 columns:
-//   D^T[:, 64..127] = S^T Q~^T,  X = V^T K^,  D^T[:, 64..127] += V^T M^T   (O^T)
-//   S^T <- S^T Diag(gamma) + X, folded into the master while its bf16 copy is made.
-// X goes to the accumulator that held the previous chunk's D^T, whose O^T columns warps 4-7
-// store (one bf16 value per lane and token: 64 contiguous bytes per warp store) at the top of
-// the chunk.  The freed shared memory holds three operand slots, so a slot is refilled while the
-// two after it are consumed, and V is double-buffered, requested a chunk ahead.  (The same
-// arrangement for the gated rule -- U^T = V^T T'^T + S^T (-W)^T into D^T[:, 0..63] first, its
-// bf16 copy in TMEM as the A operand of X and O^T -- was parity-green but slower than the
-// untransposed chain: 1.12 against 1.08 ms on 32 heads x 32K tokens.)
+// S^T: the thread of TMEM lane v holds value column v, so S enters the products as an A operand
+// read from tensor memory (a bf16 copy in TMEM: row m of A in lane m, two K values per 32-bit
+// column, the lower K index in the low half), and the fp32 master stays in the registers of the
+// thread that owns the lane (64 key channels each, two threads per lane).  Nothing of the state
+// pass goes through shared memory; the helpers' slot tiles and V serve as B operands (U = V: no
+// erase term).  Per chunk:
+//   D^T = S^T Q~^T,  X = V^T K^,  D^T += V^T M^T   (O^T = D^T)
+//   S^T <- S^T Diag(gamma) + X  in registers, and its bf16 copy.
+// X has an accumulator of its own, so the previous chunk's O^T columns are stored by warps 4-7
+// (one bf16 value per lane and token: 64 contiguous bytes per warp store) while this chunk's
+// products run.  The freed shared memory holds three operand slots, so a slot is refilled while
+// the two after it are consumed, and V is double-buffered, requested a chunk ahead.
+// (The gated rule in the same arrangement -- U^T = V^T T'^T + S^T (-W)^T first, its bf16 copy in
+// TMEM as the A operand of X and O^T -- was parity-green but slower than its untransposed chain,
+// 1.12 against 1.08 ms on 32 heads x 32K tokens: its 66 KB hand-over per chunk, not the chain's
+// own work, sets that pace.)
 __device__ void chain_transposed(unsigned char* sm, const TcMaps& maps, const PrefillArgs& a,
                                  int h, int64_t t0, int64_t t1, int nch, size_t sidx,
                                  bool valid, int ncl) {
   using L = ChainSmemT;
   constexpr uint32_t kPayload = kSlotPayload - 16384 - 8192;  // no -W, no T'
-  // TMEM columns: S^T master (fp32), its bf16 copy, D^T (two)
-  constexpr uint32_t cMS = 0, cSB = 128, cD0 = 192, cD1 = 320;
+  // TMEM columns: the state's bf16 copy, D^T (O^T in 64-127; two), X
+  constexpr uint32_t cSB = 0, cD0 = 64, cD1 = 192, cX = 320;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int q4 = warp & 3, wh = warp >> 2;
   const int vv = q4 * 32 + lane;  // the value column held in this thread's TMEM lane
@@ -187,9 +189,9 @@ __device__ void chain_transposed(unsigned char* sm, const TcMaps& maps, const Pr
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);
   uint64_t* full = bars;       // [3]
   uint64_t* bar_v = bars + 3;  // [2]
-  uint64_t* bar_mma = bars + 5;
-  uint64_t* bar_o = bars + 6;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 7);
+  uint64_t* bar_x = bars + 5;  // X
+  uint64_t* bar_o = bars + 6;  // O^T
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::BARS + 64);
   if (warp == 0) tmem_alloc(tslot, kTmemCols);
   if (tid == 0) {
     for (int i = 0; i < 7; ++i) mbar_init(bars + i, 1);
@@ -207,7 +209,7 @@ __device__ void chain_transposed(unsigned char* sm, const TcMaps& maps, const Pr
   };
   __nv_bfloat16* __restrict__ out = static_cast<__nv_bfloat16*>(a.out);
   // phases: bit s of ph_full for slot s, bit b of ph_v for V buffer b
-  uint32_t ph_full = 0, ph_v = 0, ph_mma = 0, ph_o = 0;
+  uint32_t ph_full = 0, ph_v = 0, ph_x = 0, ph_o = 0;
   auto issue_v = [&](int c) {  // one thread: chunk c's V tile into buffer c & 1
     unsigned char* dst = sm + L::VIN + (c & 1) * 16384;
     const int tc = (int)(t0 + (int64_t)c * kC);
@@ -216,16 +218,15 @@ __device__ void chain_transposed(unsigned char* sm, const TcMaps& maps, const Pr
     tma_load_3d(dst + 8192, &maps.v, 64, h, tc, bar_v + (c & 1));
   };
   if (tid == 0 && nch > 0) issue_v(0);
-  {  // S0^T (or zeros): lane v holds column v of S0; this thread's key channels 64 wh + [0, 64)
-    float sv[64];
+  // the fp32 master: S^T[vv][64 wh + j] (S0, or zeros), and its bf16 copy in TMEM
+  float ms[64];
+  {
     const float* s0 = a.S0 ? a.S0 + sidx : nullptr;
 #pragma unroll
-    for (int j = 0; j < 64; ++j) sv[j] = s0 ? s0[(size_t)(64 * wh + j) * kD + vv] : 0.f;
-    tmem_st32(tm + lane_base + cMS + 64 * wh, *reinterpret_cast<const float(*)[32]>(sv));
-    tmem_st32(tm + lane_base + cMS + 64 * wh + 32, *reinterpret_cast<const float(*)[32]>(sv + 32));
+    for (int j = 0; j < 64; ++j) ms[j] = s0 ? s0[(size_t)(64 * wh + j) * kD + vv] : 0.f;
     float pv[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) pv[i] = __uint_as_float(pack2(sv[2 * i], sv[2 * i + 1]));
+    for (int i = 0; i < 32; ++i) pv[i] = __uint_as_float(pack2(ms[2 * i], ms[2 * i + 1]));
     tmem_st32(tm + lane_base + cSB + 32 * wh, pv);
     tmem_wait_st();
   }
@@ -260,7 +261,8 @@ __device__ void chain_transposed(unsigned char* sm, const TcMaps& maps, const Pr
     // chunk's closing barrier, which every thread passed after its wait for the buffer
     if (tid == 128 && c + 1 < nch) issue_v(c + 1);
     if (c > 0 && wh == 1) o_drain(c - 1, tc - kC, kC);
-    // Waits are per thread; one that gave up is agreed on at the chunk's closing barrier.
+    // Waits are per thread; one that gave up is agreed on at the chunk's closing barrier.  Each
+    // product barrier completes once per chunk, so no wait can see two of its phases pass.
     bool bad = false;
     bad |= !mbar_wait(full + s, (ph_full >> s) & 1u, kWaitNs);
     bad |= !mbar_wait(bar_v + vb, (ph_v >> vb) & 1u, kWaitNs);
@@ -268,51 +270,43 @@ __device__ void chain_transposed(unsigned char* sm, const TcMaps& maps, const Pr
     ph_v ^= 1u << vb;
     __syncwarp();  // lanes leave their polling loops at different times
     if (n < kC) {  // the last chunk: every thread zeroes part of the V tail
-      zero_v_tail<kD>(make_ctx(sm, tm, bar_mma), sm + L::VIN + vb * 16384, n);
+      zero_v_tail<kD>(make_ctx(sm, tm, bar_x), sm + L::VIN + vb * 16384, n);
       __syncthreads();
     }
     fence_after_sync();
-    if (warp == 0) {  // S^T Q~^T
+    if (warp == 0) {  // S^T Q~^T, X = V^T K^, then O^T += V^T M^T
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
         mma_bf16_tmem_a_elect(tm + dcol(c) + 64, tm + cSB + 8 * ks, opQ.at(16 * ks), id_t64,
                               ks > 0 ? 1u : 0u);
-    }
-    fence_before_sync();
-    __syncthreads();  // the previous chunk's O^T has left
-    fence_after_sync();
-    if (warp == 0) {  // X = V^T K^, then O^T += V^T M^T
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        mma_bf16_elect(tm + dcol(c + 1), opVa.at(16 * ks), opKH.at(16 * ks), id_vk,
-                       ks > 0 ? 1u : 0u);
-      mma_commit_elect(bar_mma);
+        mma_bf16_elect(tm + cX, opVa.at(16 * ks), opKH.at(16 * ks), id_vk, ks > 0 ? 1u : 0u);
+      mma_commit_elect(bar_x);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
         mma_bf16_elect(tm + dcol(c) + 64, opVa.at(16 * ks), opM.at(16 * ks), id_vm, 1u);
       mma_commit_elect(bar_o);
     }
-    bad |= !mbar_wait(bar_mma, ph_mma, kWaitNs);
-    ph_mma ^= 1u;
+    bad |= !mbar_wait(bar_x, ph_x, kWaitNs);
+    ph_x ^= 1u;
     __syncwarp();
     fence_after_sync();
     {  // S^T <- S^T Diag(gamma) + X on this thread's 64 key channels, and its bf16 copy
       const uint32_t k0 = (uint32_t)(64 * wh);
-      float sv[128];
-      tmem_ld64x2(tm + lane_base + cMS + k0, tm + lane_base + dcol(c + 1) + k0, sv);
+      float xv[64];
+      tmem_ld64(tm + lane_base + cX + k0, xv);
 #pragma unroll
       for (int j = 0; j < 64; j += 4) {
         const float4 g4 = *reinterpret_cast<const float4*>(gam + k0 + j);
-        sv[j] = fmaf(g4.x, sv[j], sv[64 + j]);
-        sv[j + 1] = fmaf(g4.y, sv[j + 1], sv[65 + j]);
-        sv[j + 2] = fmaf(g4.z, sv[j + 2], sv[66 + j]);
-        sv[j + 3] = fmaf(g4.w, sv[j + 3], sv[67 + j]);
+        ms[j] = fmaf(g4.x, ms[j], xv[j]);
+        ms[j + 1] = fmaf(g4.y, ms[j + 1], xv[j + 1]);
+        ms[j + 2] = fmaf(g4.z, ms[j + 2], xv[j + 2]);
+        ms[j + 3] = fmaf(g4.w, ms[j + 3], xv[j + 3]);
       }
-      tmem_st32(tm + lane_base + cMS + k0, *reinterpret_cast<const float(*)[32]>(sv));
-      tmem_st32(tm + lane_base + cMS + k0 + 32, *reinterpret_cast<const float(*)[32]>(sv + 32));
       float pv[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) pv[i] = __uint_as_float(pack2(sv[2 * i], sv[2 * i + 1]));
+      for (int i = 0; i < 32; ++i) pv[i] = __uint_as_float(pack2(ms[2 * i], ms[2 * i + 1]));
       tmem_st32(tm + lane_base + cSB + 32 * wh, pv);
     }
     tmem_wait_st();
@@ -339,10 +333,8 @@ __device__ void chain_transposed(unsigned char* sm, const TcMaps& maps, const Pr
     if (c_fail + 1 < nch)
       mbar_wait(bar_v + ((c_fail + 1) & 1), (ph_v >> ((c_fail + 1) & 1)) & 1u, kWaitNs);
   } else if (valid && a.S_final) {
-    float sv[64];
-    tmem_ld64(tm + lane_base + cMS + 64 * wh, sv);
 #pragma unroll
-    for (int j = 0; j < 64; ++j) a.S_final[sidx + (size_t)(64 * wh + j) * kD + vv] = sv[j];
+    for (int j = 0; j < 64; ++j) a.S_final[sidx + (size_t)(64 * wh + j) * kD + vv] = ms[j];
   }
   cta_sync_tc();
   if (warp == 0) tmem_dealloc(tm, kTmemCols);
