@@ -43,7 +43,8 @@ struct LinSmem {
   static constexpr uint32_t ZM = VIN + 32768;  // [Z; M]: zeros 8 KB, then M [64][64] K-major
   static constexpr uint32_t SS = ZM + 16384;   // S [d_k][128] (MN-major B) x 2 buffers, 32 KB each
   static constexpr uint32_t ONES = SS + 65536;  // NORM: 16 x 64 bf16 ones (K-major B, N = 16)
-  static constexpr uint32_t BARS = ONES + 2048;  // ld[2], s, q, m2, pf_full[4], pf_mma[4], TMEM
+  static constexpr uint32_t BARS = ONES + 2048;  // ld[2], s, q, m2, pf_full[4], pf_mma[4], TMEM,
+                                                 // ld (third buffer)
   static constexpr uint32_t ZB = BARS + 128;    // NORM: z entering chunk i at [i & 1] (2 x 128 fp32)
   static constexpr uint32_t DP = ZB + 1024;     // NORM: denominator halves [i & 1][half][64 rows]
   static constexpr uint32_t END = DP + 1024;
@@ -160,7 +161,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
   fence_async_smem();
   if (tid == 0) {
-    for (int i = 0; i < 13; ++i) mbar_init(bars + i, 1);
+    for (int i = 0; i < 15; ++i)
+      if (i != 13) mbar_init(bars + i, 1);
     fence_mbar_init();
     prefetch_tmap(&maps.q_sw);
     prefetch_tmap(&maps.k_sw);
@@ -354,6 +356,190 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool o_rows = (warp & 3) >= 2;  // TMEM lanes 64-127 (Q rows) of this warp
   const int qrow = (warp & 3) * 32 + (tid & 31) - 64;
   auto d_col = [](int i) { return (i & 1) ? kColD1 : kColD0; };
+
+  if constexpr (!NORM) {
+    // ---- The runs without the normaliser, transposed: the state is kept as S^T (the thread of
+    // TMEM lane v holds value column v; its fp32 master in registers, 64 key channels per thread,
+    // two threads per lane) so that its bf16 copy in TMEM is the A operand of O^T = S^T Q^T, and
+    // no state tile goes through shared memory.  Per chunk (one CTA, every product M = 128):
+    //   [K; Q] K^T (its rows 64-127: Q K^T) -> M = lower(Q K^T) in shared memory,
+    //   X = V^T K,   O^T = S^T Q^T,   then   O^T += V^T M^T,   S^T <- S^T + X (registers).
+    // The previous chunk's O^T columns are stored by warps 4-7 (one bf16 value per lane and
+    // token) while this chunk's tiles are awaited and its products run.  With no state tile in
+    // shared memory its room holds a third q, k, v buffer, so tiles are requested two chunks
+    // ahead.
+    constexpr uint32_t cSB = 0, cD0 = 64, cD1 = 192, cX = 320, cA = 448;
+    const int lane = tid & 31;
+    const int vv = (warp & 3) * 32 + lane;  // the value column of this thread's TMEM lane
+    float ms[64];                            // S^T[vv][64 wh + j]
+    {  // the entering state (TMEM [k][v] fp32) -> shared memory -> this thread's registers
+      float* sS = reinterpret_cast<float*>(sm + L::SS);  // [128][128] fp32, columns XOR-swizzled
+      if (!failed) {
+        float v[64];
+        tmem_ld64(x.tm + x.lane_base + kColS + x.wh * 64, v);
+#pragma unroll
+        for (int j = 0; j < 64; ++j) sS[x.lrow * kD + ((x.wh * 64 + j) ^ (x.lrow & 31))] = v[j];
+      }
+      cta_sync_tc();
+#pragma unroll
+      for (int j = 0; j < 64; ++j) {
+        const int k = x.wh * 64 + j;
+        ms[j] = sS[k * kD + (vv ^ (k & 31))];
+      }
+      float pv[32];
+#pragma unroll
+      for (int i2 = 0; i2 < 32; ++i2) {
+        const __nv_bfloat162 hv = __floats2bfloat162_rn(ms[2 * i2], ms[2 * i2 + 1]);
+        pv[i2] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&hv));
+      }
+      tmem_st32(x.tm + x.lane_base + cSB + 32 * x.wh, pv);
+      tmem_wait_st();
+      cta_sync_tc();
+    }
+    const uint32_t id_vk = idesc_bf16(128, kD, false, true, true);     // V^T (smem) K (MN-major)
+    const uint32_t id_t64 = idesc_bf16(128, kC, false, false, false);  // TMEM A, K-major B
+    const uint32_t id_vm = idesc_bf16(128, kC, false, true, false);    // V^T (smem) M^T
+    auto dcol = [](int i) { return (i & 1) ? cD1 : cD0; };
+    // warps 4-7: O^T of local chunk i (columns 64-127 of its D^T) -> out rows [tc, tc + n)
+    auto o_drain = [&](int i, int64_t tc, int n) {
+      float o[64];
+      tmem_ld64(x.tm + x.lane_base + dcol(i) + 64, o);
+      __nv_bfloat16* dst = out + ((size_t)tc * H + h) * kD + vv;
+#pragma unroll
+      for (int j = 0; j < 64; ++j)
+        if (j < n) dst[(size_t)j * H * kD] = __float2bfloat16_rn(o[j]);
+    };
+    // (bar_s continues from the run prefix's phase; the others are fresh)
+    uint32_t ph_ld3 = 0, ph_x = x.ph_mma, ph_a = 0, ph_o = 0;  // ph_ld3: bit b for buffer b
+    uint32_t ld_pending = 0;  // bit b: buffer b's tiles requested and not yet waited for
+    auto kq_of = [](int bb) -> uint32_t { return bb == 0 ? L::KQ : bb == 1 ? L::KQ + 32768 : L::SS; };
+    auto v_of = [](int bb) -> uint32_t {
+      return bb == 0 ? L::VIN : bb == 1 ? L::VIN + 16384 : L::SS + 32768;
+    };
+    auto ldbar = [&](int bb) { return bb == 2 ? bars + 14 : bar_ld + bb; };
+    auto issue_ld3 = [&](int i) {  // chunk c_begin + i into buffer i % 3
+      const int bb = i % 3;
+      if (tid == 0) {
+        const int tc = (int)(ts + (int64_t)i * kC);
+        unsigned char* kq = sm + kq_of(bb);
+        unsigned char* vt = sm + v_of(bb);
+        mbar_expect_tx(ldbar(bb), 32768 + 16384);
+        tma_load_3d(kq, &maps.k_sw, 0, h, tc, ldbar(bb));
+        tma_load_3d(kq + 8192, &maps.q_sw, 0, h, tc, ldbar(bb));
+        tma_load_3d(kq + 16384, &maps.k_sw, 64, h, tc, ldbar(bb));
+        tma_load_3d(kq + 24576, &maps.q_sw, 64, h, tc, ldbar(bb));
+        tma_load_3d(vt, &maps.v, 0, h, tc, ldbar(bb));
+        tma_load_3d(vt + 8192, &maps.v, 64, h, tc, ldbar(bb));
+      }
+      ld_pending |= 1u << bb;
+    };
+    if (!failed) {
+      for (int i = 0; i < 2 && i < nloc; ++i) issue_ld3(i);
+    }
+#pragma unroll 1
+    for (int i = 0; i < nloc && !failed; ++i) {
+      const int b = i % 3;
+      const int64_t tc = ts + (int64_t)i * kC;
+      const int n = (int)((te - tc) < (int64_t)kC ? (te - tc) : (int64_t)kC);
+      {
+        const bool ok = mbar_wait(ldbar(b), (ph_ld3 >> b) & 1u, kWaitNs);
+        ph_ld3 ^= 1u << b;
+        ld_pending &= ~(1u << b);
+        if (ok && n < kC) zero_v_tail<kD>(x, sm + v_of(b), n);  // padded rows: no V^T K
+        if (__syncthreads_or(!ok)) { failed = true; break; }
+        fence_after_sync();
+      }
+      // buffer (i + 2) % 3 held chunk i - 1, whose products are complete
+      if (i + 2 < nloc) issue_ld3(i + 2);
+      const uint32_t kqa = x.sb + kq_of(b);
+      const Opnd opKQ{kqa, 16384, false};         // [K; Q], K-major A
+      const Opnd opKb{kqa, 16384, false};         // K rows, K-major B
+      const Opnd opKm{kqa, 16384, true};          // K, MN-major B (N = d_k)
+      const Opnd opQ{kqa + 8192, 16384, false};   // Q rows, K-major B
+      const Opnd opVa{x.sb + v_of(b), 8192, true};  // V^T, MN-major A
+      const Opnd opM{x.sb + L::ZM + 8192, 8192, false};                // M rows, K-major B
+      bool bad = false;
+      if (warp == 0) {
+        mma_run<kD>(x.tm + cA, opKQ, opKb, id_a, false);  // [K; Q] K^T
+        mma_commit_elect(bar_q);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)  // X = V^T K
+          mma_bf16_elect(x.tm + cX, opVa.at(16 * ks), opKm.at(16 * ks), id_vk, ks > 0 ? 1u : 0u);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)  // O^T = S^T Q^T
+          mma_bf16_tmem_a_elect(x.tm + dcol(i) + 64, x.tm + cSB + 8 * ks, opQ.at(16 * ks), id_t64,
+                                ks > 0 ? 1u : 0u);
+        mma_commit_elect(bar_s);  // X and S^T Q^T: the state copy may be rewritten after it
+      }
+      // while those products run: warps 4-7 store the previous chunk's O^T columns; M =
+      // lower(Q K^T) (Q rows: TMEM lanes 64-127) becomes bf16 K-major rows, key columns 0-31 by
+      // warps 2-3 at once and 32-63 by warps 6-7 after their stores
+      if (i > 0 && x.wh == 1) o_drain(i - 1, tc - kC, kC);
+      if (o_rows) {
+        bad |= !mbar_wait(bar_q, ph_a, kWaitNs);
+        __syncwarp();
+        fence_after_sync();
+        float v[32];
+        tmem_ld32(x.tm + x.lane_base + cA + 32 * x.wh, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = (32 * x.wh + j <= qrow) ? v[j] : 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) st_chunk8(sm + L::ZM + 8192, 8192, qrow, 32 * x.wh + j, v + j);
+        fence_async_smem();
+      }
+      ph_a ^= 1u;
+      bad |= !mbar_wait(bar_s, ph_x, kWaitNs);
+      ph_x ^= 1u;
+      __syncwarp();
+      fence_after_sync();
+      {  // S^T <- S^T + X on this thread's 64 key channels, and its bf16 copy
+        float xv[64];
+        tmem_ld64(x.tm + x.lane_base + cX + x.wh * 64, xv);
+        float pv[32];
+#pragma unroll
+        for (int j = 0; j < 64; ++j) ms[j] += xv[j];
+#pragma unroll
+        for (int i2 = 0; i2 < 32; ++i2) {
+          const __nv_bfloat162 hv = __floats2bfloat162_rn(ms[2 * i2], ms[2 * i2 + 1]);
+          pv[i2] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&hv));
+        }
+        tmem_st32(x.tm + x.lane_base + cSB + 32 * x.wh, pv);
+        tmem_wait_st();
+      }
+      fence_before_sync();
+      __syncthreads();  // M and the state copy are written
+      fence_after_sync();
+      if (warp == 0) {
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)  // O^T += V^T M^T
+          mma_bf16_elect(x.tm + dcol(i) + 64, opVa.at(16 * ks), opM.at(16 * ks), id_vm, 1u);
+        mma_commit_elect(bar_m2);
+      }
+      // buffer b and M are reused only after that product completes
+      if (tid == 0) bad |= !mbar_wait(bar_m2, ph_o, kWaitNs);
+      __syncwarp();
+      ph_o ^= 1u;
+      fence_before_sync();
+      if (__syncthreads_or(bad)) { failed = true; break; }
+      fence_after_sync();
+    }
+    if (!failed && nloc > 0 && x.wh == 1) {
+      const int64_t tl = ts + (int64_t)(nloc - 1) * kC;
+      o_drain(nloc - 1, tl, (int)(te - tl));
+    }
+    if (failed) {
+      if (tid == 0) report(a, GDR_DEVCHECK_TIMEOUT);
+      // let copies already in flight land before the shared memory is released
+      for (int bb = 0; bb < 3; ++bb)
+        if ((ld_pending >> bb) & 1u) mbar_wait(ldbar(bb), (ph_ld3 >> bb) & 1u, kWaitNs);
+    } else if (a.S_final && c_end == nch) {  // the last run of the sequence hands the state on
+#pragma unroll
+      for (int j = 0; j < 64; ++j) a.S_final[sidx + (size_t)(x.wh * 64 + j) * kD + vv] = ms[j];
+    }
+    cta_sync_tc();
+    if (warp == 0) tmem_dealloc(x.tm, kTmemCols);
+    return;
+  }
   // O rows of local chunk i (lanes 64-127 of its D) -> out rows [tc, tc + n) of head h
   auto o_store = [&](int i, int64_t tc, int n) {
     float v[64];
