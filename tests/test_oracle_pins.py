@@ -202,7 +202,7 @@ def test_beta_zero_is_pure_decay():
 
 
 def test_idle_gates_coast():
-    """alpha = 1, beta = 0: the memory coasts untouched."""
+    """alpha = 1, beta = 0: neither fade nor write, so the state carries over unchanged."""
     rng = np.random.default_rng(6)
     q, k, v, a, _ = rand_inputs(rng, 7, 2, 4, 4)
     S0 = rng.standard_normal((1, 2, 4, 4))
