@@ -10,6 +10,7 @@ library's CUDA kernels; there is no Python or CPU fallback.
     gdr_gated_linear_attn(q, k, v, alpha, S0=None, cu_seqlens=None, out=None, S_final=None, ...)
     gdr_prefill_workspace_size(n_seqs, H, d_k, d_v, dtype)  /  gdr_workspace_status(workspace)
     gdr_query_device_status()  -- takes the library's error word on the current device
+    gdr_check_wait_timeout(workspace, limit_ns)  -- a bounded wait made to run out (error path)
     gdr_prefill_host(q, k, v, alpha, beta, ...)  -- host (CPU) tensors in and out, copies inside
     gdr_prefill_host_buffer_size(n_seqs, H, total_tokens, d_k, d_v, dtype, gate, piece_tokens)
     gdr_layer_prologue(xq, xk, a=None, b=None, q=None, k=None, alpha=None, beta=None)
@@ -35,7 +36,8 @@ __all__ = ["gdr_prefill", "gdr_prefill_output_gate", "gdr_decode_step", "gdr_lin
            "gdr_gated_linear_attn", "gdr_layer_prologue", "gdr_normalized_linear_attn",
            "gdr_gated_linear_decode_step", "gdr_normalized_linear_decode_step",
            "gdr_prefill_workspace_size",
-           "gdr_workspace_status", "gdr_query_device_status", "gdr_prefill_host",
+           "gdr_workspace_status", "gdr_query_device_status", "gdr_check_wait_timeout",
+           "gdr_prefill_host",
            "gdr_prefill_host_buffer_size",
            "make_shape", "GdrError"]
 
@@ -398,6 +400,17 @@ def gdr_query_device_status(stream=None) -> int:
     if rc not in (GDR_OK, GDR_ERR_DEVICE_CHECK):
         raise GdrError(rc, "gdr_query_device_status")
     return int(rc)
+
+
+def gdr_check_wait_timeout(workspace, limit_ns: int, stream=None) -> None:
+    """Launch the library's failure-detection check: one warp waits, with the kernels' bounded
+    wait, on a barrier that nothing completes and records GDR_DEVCHECK_TIMEOUT after limit_ns
+    in the workspace word and the per-device word (read them with gdr_workspace_status and
+    gdr_query_device_status).  Asynchronous on the stream."""
+    rc = _abi.load().gdr_check_wait_timeout(_ptr(workspace), ctypes.c_uint64(int(limit_ns)),
+                                            _stream(stream))
+    if rc != 0:
+        raise GdrError(rc, "gdr_check_wait_timeout")
 
 
 def compute_dtype(dtype: str, d: int, force_simt: bool = False) -> str:

@@ -22,7 +22,7 @@ EXPORTS = ("gdr_prefill", "gdr_prefill_workspace_size", "gdr_decode_step", "gdr_
            "gdr_prefill_host_buffer_size", "gdr_gated_linear_attn",
            "gdr_prefill_output_gate", "gdr_layer_prologue", "gdr_normalized_linear_attn",
            "gdr_gated_linear_decode_step", "gdr_normalized_linear_decode_step",
-           "gdr_query_device_status")
+           "gdr_query_device_status", "gdr_check_wait_timeout")
 GDR_NOALLOC_MAX_SEQS = 4096
 
 
@@ -71,6 +71,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.gdr_workspace_status.restype = ctypes.c_int
     lib.gdr_query_device_status.argtypes = [P]
     lib.gdr_query_device_status.restype = ctypes.c_int
+    lib.gdr_check_wait_timeout.argtypes = [P, ctypes.c_uint64, P]
+    lib.gdr_check_wait_timeout.restype = ctypes.c_int
     lib.gdr_prefill_noalloc.argtypes = [S, P, P, P, P, P, P, P, P, P, P]
     lib.gdr_prefill_noalloc.restype = ctypes.c_int
     lib.gdr_prefill_host.argtypes = [S, P, P, P, P, P, P, P, P, P, ctypes.c_int64, P,

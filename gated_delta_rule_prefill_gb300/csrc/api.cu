@@ -3,6 +3,7 @@
 #include <string.h>
 
 #include "gdr_internal.cuh"
+#include "umma.cuh"
 
 namespace gdr {
 namespace {
@@ -18,6 +19,23 @@ __device__ int32_t g_device_status_taken;
 
 __global__ void take_device_status_kernel() {
   g_device_status_taken = atomicExch(&g_device_status, 0);
+}
+
+// One warp waits on an mbarrier that nothing arrives on, with the kernels' bounded wait; each
+// lane gives up after limit_ns, and lane 0 records the timeout as a kernel would.
+__global__ void __launch_bounds__(32) wait_timeout_kernel(int32_t* status, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    umma::mbar_init(&bar, 1);
+    umma::fence_mbar_init();
+  }
+  __syncwarp();
+  const bool done = umma::mbar_wait(&bar, 0, limit_ns);
+  __syncwarp();
+  if (threadIdx.x == 0 && !done) {
+    report(status, GDR_DEVCHECK_TIMEOUT);
+    report(&g_device_status, GDR_DEVCHECK_TIMEOUT);
+  }
 }
 
 // One CTA: clears the status word, checks cu_seqlens, and writes the visiting order of the
@@ -281,6 +299,13 @@ gdr_status gdr_query_device_status(void* stream) {
     return GDR_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return GDR_ERR_CUDA;
   return h == GDR_DEVCHECK_OK ? GDR_OK : GDR_ERR_DEVICE_CHECK;
+}
+
+gdr_status gdr_check_wait_timeout(void* workspace, uint64_t limit_ns, void* stream) {
+  if (!workspace || ((uintptr_t)workspace & 255u)) return GDR_ERR_INVALID_ARG;
+  if (limit_ns == 0 || limit_ns > 10000000000ull) return GDR_ERR_INVALID_ARG;
+  gdr::wait_timeout_kernel<<<1, 32, 0, (cudaStream_t)stream>>>((int32_t*)workspace, limit_ns);
+  return cudaGetLastError() == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }
 
 const char* gdr_status_string(gdr_status status) {

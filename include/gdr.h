@@ -263,6 +263,22 @@ gdr_status gdr_workspace_status(void* workspace, void* stream, int32_t* code);
 gdr_status gdr_query_device_status(void* stream);
 
 /*
+ * gdr_check_wait_timeout -- exercises the library's failure detection without a GPU fault.  (The
+ * pages have no counterpart: this belongs to the library's error path.)  Launches one warp that
+ * waits on an mbarrier which nothing completes, with the bounded wait every tensor-core kernel
+ * uses for its MMA, copy and hand-over barriers, given up after `limit_ns` nanoseconds.  The
+ * timeout is recorded as a kernel's would be: GDR_DEVCHECK_TIMEOUT in the workspace word (if it
+ * was 0) and in the library's per-device error word, so gdr_workspace_status and
+ * gdr_query_device_status then report it; the kernel returns normally and the context stays
+ * usable.  Asynchronous on `stream`.
+ *   workspace  device, >= 256 bytes, 256-byte aligned (only its status word is written)
+ *   limit_ns   1 .. 10,000,000,000 (10 s)
+ * Returns GDR_OK, GDR_ERR_INVALID_ARG (null or unaligned workspace, limit out of range) or
+ * GDR_ERR_CUDA (the launch failed).
+ */
+gdr_status gdr_check_wait_timeout(void* workspace, uint64_t limit_ns, void* stream);
+
+/*
  * gdr_prefill_noalloc -- gdr_prefill for callers that cannot provide a workspace.  (The pages
  * have no counterpart: this is a property of the library interface, not of the method.)
  *

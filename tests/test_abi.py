@@ -246,3 +246,13 @@ def test_query_device_status_without_a_device(lib):
         assert rc in (_abi.GDR_OK, _abi.GDR_ERR_DEVICE_CHECK)
     else:
         assert rc == _abi.GDR_ERR_CUDA
+
+
+def test_check_wait_timeout_argument_errors(lib):
+    # rejected before any CUDA work: null or unaligned workspace, limit out of range
+    P = ctypes.c_void_p
+    INV = 1
+    assert lib.gdr_check_wait_timeout(None, 1000, None) == INV
+    assert lib.gdr_check_wait_timeout(P(FAKE * 2 + 16), 1000, None) == INV
+    assert lib.gdr_check_wait_timeout(P(FAKE * 2), 0, None) == INV
+    assert lib.gdr_check_wait_timeout(P(FAKE * 2), 10_000_000_001, None) == INV
