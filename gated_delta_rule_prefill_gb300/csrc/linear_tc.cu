@@ -10,12 +10,15 @@
 //   S master -> bf16 operand for the next chunk (double-buffered, so this waits only for the
 //   state MMA), lower(Q K^T) -> bf16 M,  then  D += [Z; M] V  (rows 64-127: O)
 // and the O rows leave TMEM while the next chunk's MMAs run.  q, k, v of the next chunk are
-// fetched one chunk ahead.  With few (sequence, head) pairs each sequence is split into runs of
-// whole chunks, one CTA each, run g starting from S0 + sum of K^T V over the chunks before it.
-// Where the workspace has room (it holds the work-queue rings for such shapes), that sum comes
-// from a first launch (MODE 1: every run but the last computes its own sum_c K_c^T V_c, once)
-// and the second launch (MODE 2) adds the sums of the runs before it to S0; without the room,
-// each run rebuilds it from the chunks before it (MODE 0).
+// fetched one chunk ahead.  That is the normalised form's loop; the plain form runs the same
+// products transposed (S^T in TMEM as the A operand of S^T Q^T, its fp32 master in registers,
+// no state tile in shared memory, whose room then holds a third q, k, v buffer: tiles two
+// chunks ahead; described at that loop).  With few (sequence, head) pairs each sequence is
+// split into runs of whole chunks, one CTA each, run g starting from S0 + sum of K^T V over the
+// chunks before it.  Where the workspace has room (it holds the work-queue rings for such
+// shapes), that sum comes from a first launch (MODE 1: every run but the last computes its own
+// sum_c K_c^T V_c, once) and the second launch (MODE 2) adds the sums of the runs before it to
+// S0; without the room, each run rebuilds it from the chunks before it (MODE 0).
 //
 // NORM: normalised phi-linear attention (heqinghuang "gpt2-to-kimi" §07, engineermaxxing §02g):
 // phi = elu + 1 is applied in place to the staged [K; Q] tile (elementwise, so the swizzle does
@@ -42,6 +45,7 @@ struct LinSmem {
   static constexpr uint32_t VIN = 65536;       // V [64 tok][128] SW128 x 2 buffers, 16 KB each
   static constexpr uint32_t ZM = VIN + 32768;  // [Z; M]: zeros 8 KB, then M [64][64] K-major
   static constexpr uint32_t SS = ZM + 16384;   // S [d_k][128] (MN-major B) x 2 buffers, 32 KB each
+                                                // (plain form: the third q, k, v buffer)
   static constexpr uint32_t ONES = SS + 65536;  // NORM: 16 x 64 bf16 ones (K-major B, N = 16)
   static constexpr uint32_t BARS = ONES + 2048;  // ld[2], s, q, m2, pf_full[4], pf_mma[4], TMEM,
                                                  // ld (third buffer)
