@@ -219,6 +219,19 @@ class ClockSampler:
 # ----------------------------------------------------------------------------------------------
 # the oracle leg (CPU)
 # ----------------------------------------------------------------------------------------------
+def workload_config(n_ranks):
+    """The `config` of the bench line (both arms): the prefill and decode workloads of a step."""
+    wp, wd = gi.workload(PREFILL), gi.workload(DECODE)
+    return {"workload": "%s + %s" % (PREFILL, DECODE),
+            "prefill": {"n_seqs": wp.n_seqs, "T": wp.total_tokens, "H": wp.H, "d_k": wp.d_k,
+                        "d_v": wp.d_v, "gate": "channel",
+                        "dtype": "bf16 q/k/v, fp32 alpha/beta/state"},
+            "decode": {"n_seqs": wd.n_seqs, "H": wd.H, "d": wd.d_k,
+                       "state_prefill_tokens": DECODE_PREFILL_LEN},
+            "l2": "no flush: every step's inputs exceed L2 (129 MB)",
+            "parallelism": "replicas" if n_ranks > 1 else "1 GPU"}
+
+
 def oracle_sample(cores):
     """Inputs of the bounded oracle sample: the first SAMPLE_TOKENS tokens of min(H, cores) heads of the
     prefill workload (work scales linearly in tokens and heads)."""
@@ -258,8 +271,7 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": PREFILL, "T": wl.total_tokens, "H": wl.H, "d": wl.d_k,
-                       "gate": "channel", "sample": desc},
+            "config": dict(workload_config(1), sample=desc),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
                              "kind": "oracle", "sample": desc},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -666,13 +678,7 @@ def run_gpu(args):
         "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": g.compute_dtype(wp.dtype, d),
         "data": "synthetic (seeded, drawn on the device; distributions of the workload spec)",
-        "config": {"workload": "%s + %s" % (PREFILL, DECODE),
-                   "prefill": {"n_seqs": wp.n_seqs, "T": T, "H": H, "d_k": d, "d_v": d,
-                               "gate": "channel", "dtype": "bf16 q/k/v, fp32 alpha/beta/state"},
-                   "decode": {"n_seqs": wd.n_seqs, "H": wd.H, "d": wd.d_k,
-                              "state_prefill_tokens": DECODE_PREFILL_LEN},
-                   "l2": "no flush: every step's inputs exceed L2 (129 MB)",
-                   "parallelism": "replicas" if n > 1 else "1 GPU"},
+        "config": workload_config(n),
         "decode_tokens_per_s": decode_tps,
         "linear_attn_tokens_per_s": linear_tps,
         "gated_linear_attn_tokens_per_s": job_tokens_per_s(n, T, gla_ms / 1e3),
